@@ -1,0 +1,151 @@
+"""fp64 CPU oracle for multi-head scaled dot-product attention -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package. The library's CUDA path never calls it and the
+two share no code. The arithmetic lives in ``attention_oracle.c`` (plain C,
+fp64, OpenMP over independent (batch, head) pairs); this module only builds
+that file with gcc and marshals numpy arrays into it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attention_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile attention_oracle.c into liboracle.so (gcc, OpenMP, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared", "-fno-fast-math",
+               "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.POINTER(ctypes.c_int32)
+            ci, cd = ctypes.c_int, ctypes.c_double
+            lib.oracle_attention.argtypes = [dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, ci, ci, ip, cd, ci]
+            lib.oracle_attention.restype = ci
+            lib.oracle_attention_rows.argtypes = [dp, ip, ci, dp, dp, ci, ci, ci, ci, ci, cd, dp, ci]
+            lib.oracle_attention_rows.restype = ci
+            lib.oracle_mha.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, ci, ci,
+                                       ci, ip, cd, ci]
+            lib.oracle_mha.restype = ci
+            lib.oracle_max_threads.argtypes = []
+            lib.oracle_max_threads.restype = ci
+            _lib = lib
+    return _lib
+
+
+def _dp(a):
+    if a is None:
+        return ctypes.POINTER(ctypes.c_double)()
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _ip(a):
+    if a is None:
+        return ctypes.POINTER(ctypes.c_int32)()
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _f64(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def default_scale(d_k: int) -> float:
+    """1/sqrt(d_k), the factor of eq. (1)."""
+    return 1.0 / np.sqrt(float(d_k))
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def attention(q, k, v, mask_kind: int = MASK_NONE, kv_lens=None, scale: float | None = None,
+              return_weights: bool = False, nthreads: int = 0):
+    """Attention(Q,K,V) for q [B,h,n_q,d_k], k [B,h,n_k,d_k], v [B,h,n_k,d_v].
+
+    Returns out [B,h,n_q,d_v] (and the weight matrix [B,h,n_q,n_k] when asked).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, h, n_q, d_k = q.shape
+    n_k, d_v = k.shape[2], v.shape[3]
+    assert k.shape == (B, h, n_k, d_k) and v.shape == (B, h, n_k, d_v)
+    if scale is None or scale == 0.0:
+        scale = default_scale(d_k)
+    lens = None
+    if mask_kind & MASK_KEY_PADDING:
+        lens = np.ascontiguousarray(np.asarray(kv_lens, dtype=np.int32))
+        assert lens.shape == (B,)
+    out = np.zeros((B, h, n_q, d_v), dtype=np.float64)
+    w = np.zeros((B, h, n_q, n_k), dtype=np.float64) if return_weights else None
+    rc = _load().oracle_attention(_dp(q), _dp(k), _dp(v), _dp(out), _dp(w), B, h, n_q, n_k, d_k,
+                                  d_v, int(mask_kind), _ip(lens), float(scale), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_attention rejected its arguments")
+    return (out, w) if return_weights else out
+
+
+def attention_rows(q_rows, row_pos, K, V, causal: bool, kv_len: int | None = None,
+                   scale: float | None = None, nthreads: int = 0):
+    """Selected query rows of one (batch, head): q_rows [R,d_k] at positions row_pos [R]."""
+    q_rows, K, V = _f64(q_rows), _f64(K), _f64(V)
+    R, d_k = q_rows.shape
+    n_k, d_v = V.shape
+    pos = np.ascontiguousarray(np.asarray(row_pos, dtype=np.int32))
+    if scale is None or scale == 0.0:
+        scale = default_scale(d_k)
+    out = np.zeros((R, d_v), dtype=np.float64)
+    rc = _load().oracle_attention_rows(_dp(q_rows), _ip(pos), R, _dp(K), _dp(V), n_k, d_k, d_v,
+                                       int(bool(causal)), -1 if kv_len is None else int(kv_len),
+                                       float(scale), _dp(out), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_attention_rows rejected its arguments")
+    return out
+
+
+def mha(x_q, x_kv, w_q, w_k, w_v, w_o, h: int, mask_kind: int = MASK_NONE, kv_lens=None,
+        scale: float | None = None, return_concat: bool = False, nthreads: int = 0):
+    """MultiHead(X_q, X_kv) = Concat(head_1..head_h) W_O (x.W convention, no biases)."""
+    x_q, x_kv = _f64(x_q), _f64(x_kv)
+    w_q, w_k, w_v, w_o = _f64(w_q), _f64(w_k), _f64(w_v), _f64(w_o)
+    B, n_q, d_model = x_q.shape
+    n_k = x_kv.shape[1]
+    d_k = w_q.shape[1] // h
+    d_v = w_v.shape[1] // h
+    assert w_q.shape == (d_model, h * d_k) and w_k.shape == (d_model, h * d_k)
+    assert w_v.shape == (d_model, h * d_v) and w_o.shape == (h * d_v, d_model)
+    if scale is None or scale == 0.0:
+        scale = default_scale(d_k)
+    lens = None
+    if mask_kind & MASK_KEY_PADDING:
+        lens = np.ascontiguousarray(np.asarray(kv_lens, dtype=np.int32))
+    out = np.zeros((B, n_q, d_model), dtype=np.float64)
+    concat = np.zeros((B, n_q, h * d_v), dtype=np.float64) if return_concat else None
+    rc = _load().oracle_mha(_dp(x_q), _dp(x_kv), _dp(w_q), _dp(w_k), _dp(w_v), _dp(w_o), _dp(out),
+                            _dp(concat), B, n_q, n_k, d_model, h, d_k, d_v, int(mask_kind),
+                            _ip(lens), float(scale), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_mha rejected its arguments")
+    return (out, concat) if return_concat else out

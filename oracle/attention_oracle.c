@@ -1,0 +1,275 @@
+/*
+ * Oracle for multi-head scaled dot-product attention -- TEST INFRASTRUCTURE.
+ *
+ * Plain, slow, obviously correct fp64 CPU code. Only the tests, the smoke
+ * check and the benchmark's CPU-baseline leg may load it; the library's CUDA
+ * path never calls it and shares no code, header or table with it.
+ *
+ * What it computes, and where the pages define it:
+ *   - eq. (1), Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V, in the element
+ *     form alpha_ij = exp(q_i.k_j/sqrt(d_k)) / sum_l exp(q_i.k_l/sqrt(d_k)),
+ *     y_i = sum_j alpha_ij v_j
+ *     ("Attention Is All You Need를 지금 다시 읽는 법" (eightmm.github.io),
+ *      section "Attention 수식");
+ *   - masks set the logit to -inf BEFORE the softmax so the weight is exactly 0
+ *     ("[논문 리뷰]Attention Is All You Need" (kimjiil.github.io), section 3.2.3;
+ *      "Attention Is All You Need 해부" (sj-techlog), section "mask는 softmax
+ *      **전**에 더해야 한다"); causal: query i sees keys j <= i; key padding:
+ *      keys j >= kv_len[b] are padding and receive no attention
+ *      ("Attention Is All You Need 해부", the three-uses table of attention);
+ *   - the max-subtraction ("pivot") before exp, which changes nothing
+ *     mathematically ("Attention Is All You Need 해부", section "직접 검증");
+ *   - MultiHead(Q,K,V) = Concat(head_1..head_h) W^O,
+ *     head_i = Attention(Q W_i^Q, K W_i^K, V W_i^V), with the per-head matrices
+ *     being column block i of one [d_model, h*d] matrix
+ *     ("[논문 리뷰]Attention Is All You Need", section 3.2.2).
+ *
+ * Readings where the pages are silent (listed with the design notes):
+ *   - a query row whose every key is masked (kv_len = 0) has output 0 and
+ *     weights 0;
+ *   - kv_len values are clamped to [0, n_k];
+ *   - causal masking is defined for n_q == n_k (query i vs key i).
+ *
+ * Parity pins: every function here is checked by the CPU tests against the
+ * pages' worked examples, closed forms and invariants, and against
+ * torch's fp64 scaled_dot_product_attention on small cases.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_MASK_CAUSAL 1
+#define ORACLE_MASK_KEY_PADDING 2
+
+static int clamp_len(int len, int n_k)
+{
+    if (len < 0) return 0;
+    if (len > n_k) return n_k;
+    return len;
+}
+
+/*
+ * One query row of eq. (1).
+ *   q_i [d_k], K [n_k, d_k], V [n_k, d_v] (row-major); i is the query position.
+ *   scores: scratch of n_k doubles. weights (nullable) receives alpha_i.
+ *   y_i [d_v] receives the output row.
+ */
+static void attend_row(const double *q_i, const double *K, const double *V,
+                       int n_k, int d_k, int d_v, int i, int causal, int kv_len,
+                       double scale, double *scores, double *weights, double *y_i)
+{
+    int j, c;
+    int any_allowed = 0;
+    double m = -INFINITY, total = 0.0;
+
+    /* logits s_j = (q_i . k_j) * scale, -inf where the connection is illegal */
+    for (j = 0; j < n_k; ++j) {
+        int allowed = (j < kv_len) && !(causal && j > i);
+        if (allowed) {
+            double dot = 0.0;
+            for (c = 0; c < d_k; ++c) dot += q_i[c] * K[(size_t)j * d_k + c];
+            scores[j] = dot * scale;
+            any_allowed = 1;
+            if (scores[j] > m) m = scores[j];
+        } else {
+            scores[j] = -INFINITY;
+        }
+    }
+
+    for (c = 0; c < d_v; ++c) y_i[c] = 0.0;
+    if (!any_allowed) {
+        if (weights)
+            for (j = 0; j < n_k; ++j) weights[j] = 0.0;
+        return;
+    }
+
+    /* softmax over keys: exp(s_j - m) / sum_l exp(s_l - m); exp(-inf) = 0 */
+    for (j = 0; j < n_k; ++j) {
+        scores[j] = (scores[j] == -INFINITY) ? 0.0 : exp(scores[j] - m);
+        total += scores[j];
+    }
+    for (j = 0; j < n_k; ++j) scores[j] /= total;
+    if (weights)
+        for (j = 0; j < n_k; ++j) weights[j] = scores[j];
+
+    /* y_i = sum_j alpha_ij v_j */
+    for (j = 0; j < n_k; ++j) {
+        double a = scores[j];
+        if (a == 0.0) continue;
+        for (c = 0; c < d_v; ++c) y_i[c] += a * V[(size_t)j * d_v + c];
+    }
+}
+
+/*
+ * Scaled dot-product attention for every (batch, head, query row).
+ * Layouts (row-major, contiguous): q [B,h,n_q,d_k], k [B,h,n_k,d_k],
+ * v [B,h,n_k,d_v], out [B,h,n_q,d_v], weights (nullable) [B,h,n_q,n_k].
+ * kv_lens: int32[B] or NULL (used only with the key-padding mask bit).
+ * Returns 0 on success, -1 on invalid arguments.
+ */
+int oracle_attention(const double *q, const double *k, const double *v, double *out,
+                     double *weights, int B, int h, int n_q, int n_k, int d_k, int d_v,
+                     int mask_kind, const int32_t *kv_lens, double scale, int nthreads)
+{
+    int bh;
+    int causal = (mask_kind & ORACLE_MASK_CAUSAL) != 0;
+    int padding = (mask_kind & ORACLE_MASK_KEY_PADDING) != 0;
+    if (B < 0 || h < 0 || n_q < 0 || n_k < 0 || d_k <= 0 || d_v <= 0) return -1;
+    if (padding && !kv_lens) return -1;
+    if (causal && n_q != n_k) return -1;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic)
+#endif
+    for (bh = 0; bh < B * h; ++bh) {
+        int b = bh / h, i;
+        int kv_len = padding ? clamp_len(kv_lens[b], n_k) : n_k;
+        const double *K = k + (size_t)bh * n_k * d_k;
+        const double *V = v + (size_t)bh * n_k * d_v;
+        double *scores = (double *)malloc(sizeof(double) * (size_t)(n_k > 0 ? n_k : 1));
+        for (i = 0; i < n_q; ++i) {
+            attend_row(q + ((size_t)bh * n_q + i) * d_k, K, V, n_k, d_k, d_v, i, causal,
+                       kv_len, scale,
+                       scores, weights ? weights + ((size_t)bh * n_q + i) * n_k : NULL,
+                       out + ((size_t)bh * n_q + i) * d_v);
+        }
+        free(scores);
+    }
+    return 0;
+}
+
+/*
+ * Selected query rows of one (batch, head): rows q_rows [R, d_k] sit at query
+ * positions row_pos[R]; K [n_k, d_k], V [n_k, d_v]; out [R, d_v].
+ * kv_len < 0 means "no padding". Rows are independent, so this equals the
+ * corresponding rows of oracle_attention.
+ */
+int oracle_attention_rows(const double *q_rows, const int32_t *row_pos, int R,
+                          const double *K, const double *V, int n_k, int d_k, int d_v,
+                          int causal, int kv_len, double scale, double *out, int nthreads)
+{
+    int r;
+    int len = kv_len < 0 ? n_k : clamp_len(kv_len, n_k);
+    if (R < 0 || n_k < 0 || d_k <= 0 || d_v <= 0) return -1;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel
+#endif
+    {
+        double *scores = (double *)malloc(sizeof(double) * (size_t)(n_k > 0 ? n_k : 1));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 4)
+#endif
+        for (r = 0; r < R; ++r)
+            attend_row(q_rows + (size_t)r * d_k, K, V, n_k, d_k, d_v, row_pos[r], causal, len,
+                       scale, scores, NULL, out + (size_t)r * d_v);
+        free(scores);
+    }
+    return 0;
+}
+
+/* C[M,N] = A[M,K] B[K,N], plain triple loop (row-major). */
+static void matmul(const double *A, const double *Bm, double *C, int M, int N, int K)
+{
+    int i;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (i = 0; i < M; ++i) {
+        int j, p;
+        double *c = C + (size_t)i * N;
+        for (j = 0; j < N; ++j) c[j] = 0.0;
+        for (p = 0; p < K; ++p) {
+            double a = A[(size_t)i * K + p];
+            const double *b = Bm + (size_t)p * N;
+            for (j = 0; j < N; ++j) c[j] += a * b[j];
+        }
+    }
+}
+
+/*
+ * Multi-head attention, section 3.2.2 of "[논문 리뷰]Attention Is All You Need":
+ *   Q = X_q W_Q, K = X_kv W_K, V = X_kv W_V            (x.W convention, no biases)
+ *   head_i = Attention(Q[:, i*d_k:(i+1)*d_k], K[:, i*d_k:...], V[:, i*d_v:...])
+ *   out = Concat(head_1..head_h) W_O
+ * Layouts: x_q [B,n_q,d_model], x_kv [B,n_k,d_model], w_q/w_k [d_model,h*d_k],
+ * w_v [d_model,h*d_v], w_o [h*d_v,d_model], out [B,n_q,d_model].
+ * concat_out (nullable) receives Concat(head_1..head_h) [B,n_q,h*d_v].
+ */
+int oracle_mha(const double *x_q, const double *x_kv, const double *w_q, const double *w_k,
+               const double *w_v, const double *w_o, double *out, double *concat_out,
+               int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
+               int mask_kind, const int32_t *kv_lens, double scale, int nthreads)
+{
+    int b, hh, i, c, rc = 0;
+    size_t qsz = (size_t)B * n_q * h * d_k, ksz = (size_t)B * n_k * h * d_k;
+    size_t vsz = (size_t)B * n_k * h * d_v, osz = (size_t)B * n_q * h * d_v;
+    double *Q, *Kp, *Vp, *Qh, *Kh, *Vh, *Oh, *concat;
+    if (B < 0 || n_q < 0 || n_k < 0 || d_model <= 0 || h <= 0 || d_k <= 0 || d_v <= 0) return -1;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+    Q = (double *)malloc(sizeof(double) * (qsz ? qsz : 1));
+    Kp = (double *)malloc(sizeof(double) * (ksz ? ksz : 1));
+    Vp = (double *)malloc(sizeof(double) * (vsz ? vsz : 1));
+    Qh = (double *)malloc(sizeof(double) * (qsz ? qsz : 1));
+    Kh = (double *)malloc(sizeof(double) * (ksz ? ksz : 1));
+    Vh = (double *)malloc(sizeof(double) * (vsz ? vsz : 1));
+    Oh = (double *)malloc(sizeof(double) * (osz ? osz : 1));
+    concat = (double *)malloc(sizeof(double) * (osz ? osz : 1));
+
+    /* projections of all positions at once */
+    matmul(x_q, w_q, Q, B * n_q, h * d_k, d_model);
+    matmul(x_kv, w_k, Kp, B * n_k, h * d_k, d_model);
+    matmul(x_kv, w_v, Vp, B * n_k, h * d_v, d_model);
+
+    /* head split: head hh takes column block hh of each projection */
+    for (b = 0; b < B; ++b)
+        for (hh = 0; hh < h; ++hh) {
+            for (i = 0; i < n_q; ++i)
+                for (c = 0; c < d_k; ++c)
+                    Qh[(((size_t)b * h + hh) * n_q + i) * d_k + c] =
+                        Q[((size_t)b * n_q + i) * h * d_k + (size_t)hh * d_k + c];
+            for (i = 0; i < n_k; ++i) {
+                for (c = 0; c < d_k; ++c)
+                    Kh[(((size_t)b * h + hh) * n_k + i) * d_k + c] =
+                        Kp[((size_t)b * n_k + i) * h * d_k + (size_t)hh * d_k + c];
+                for (c = 0; c < d_v; ++c)
+                    Vh[(((size_t)b * h + hh) * n_k + i) * d_v + c] =
+                        Vp[((size_t)b * n_k + i) * h * d_v + (size_t)hh * d_v + c];
+            }
+        }
+
+    rc = oracle_attention(Qh, Kh, Vh, Oh, NULL, B, h, n_q, n_k, d_k, d_v, mask_kind, kv_lens,
+                          scale, nthreads);
+
+    /* head merge: Concat(head_1..head_h) along the feature axis */
+    if (rc == 0) {
+        for (b = 0; b < B; ++b)
+            for (hh = 0; hh < h; ++hh)
+                for (i = 0; i < n_q; ++i)
+                    for (c = 0; c < d_v; ++c)
+                        concat[((size_t)b * n_q + i) * h * d_v + (size_t)hh * d_v + c] =
+                            Oh[(((size_t)b * h + hh) * n_q + i) * d_v + c];
+        if (concat_out)
+            for (size_t t = 0; t < osz; ++t) concat_out[t] = concat[t];
+        matmul(concat, w_o, out, B * n_q, d_model, h * d_v);
+    }
+
+    free(Q); free(Kp); free(Vp); free(Qh); free(Kh); free(Vh); free(Oh); free(concat);
+    return rc;
+}
+
+/* Number of threads an OpenMP parallel region would use (1 without OpenMP). */
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

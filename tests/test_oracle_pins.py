@@ -1,0 +1,352 @@
+"""Pins for the fp64 oracle: the pages' worked examples, closed forms,
+invariants and an independent library routine. CPU only.
+
+Each check is chosen so that a plausible mistake in the oracle (a wrong
+scale, masking after the softmax, a transposed operand, a wrong head block,
+an off-by-one in the causal or padding test) fails at least one of them.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import MASK_CAUSAL, MASK_KEY_PADDING, MASK_NONE
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        return json.load(f)
+
+
+def _one(q, k, v, mask=MASK_NONE, **kw):
+    """Wrap single-head [n, d] arrays as [1, 1, n, d]."""
+    q, k, v = (np.asarray(a, dtype=np.float64)[None, None] for a in (q, k, v))
+    out, w = oracle.attention(q, k, v, mask, return_weights=True, **kw)
+    return out[0, 0], w[0, 0]
+
+
+# ---------------------------------------------------------------- worked examples
+
+def test_three_token_unmasked_matches_printed_run():
+    g = _load("three_token_verification.json")
+    out, w = _one(g["q"], g["k"], g["v"])
+    tol = g["tolerance"]
+    assert np.sqrt(2.0) == pytest.approx(g["scale_sqrt_dk"], abs=tol)
+    np.testing.assert_allclose(w[0], g["unmasked_row0_weights"], atol=tol, rtol=0)
+    np.testing.assert_allclose(out[0], g["unmasked_row0_output"], atol=tol, rtol=0)
+
+
+def test_three_token_causal_matches_printed_run():
+    g = _load("three_token_verification.json")
+    out, w = _one(g["q"], g["k"], g["v"], MASK_CAUSAL)
+    tol = g["tolerance"]
+    np.testing.assert_allclose(w, g["causal_weights"], atol=tol, rtol=0)
+    np.testing.assert_allclose(out, g["causal_outputs"], atol=tol, rtol=0)
+
+
+def test_mask_goes_before_softmax_not_after():
+    """Zeroing future weights after the softmax leaves row 0 summing to 0.401112
+    (the page's negative example); the oracle must not do that."""
+    g = _load("three_token_verification.json")
+    _, w_unmasked = _one(g["q"], g["k"], g["v"])
+    wrong = np.array([w_unmasked[0, 0], 0.0, 0.0])
+    assert wrong.sum() == pytest.approx(g["wrong_post_softmax_mask_row0_sum"], abs=1e-6)
+    np.testing.assert_allclose(wrong @ np.asarray(g["v"]), g["wrong_post_softmax_mask_row0_output"],
+                               atol=1e-6)
+    out, w = _one(g["q"], g["k"], g["v"], MASK_CAUSAL)
+    assert w[0].sum() == pytest.approx(1.0, abs=1e-15)
+    assert not np.allclose(out[0], g["wrong_post_softmax_mask_row0_output"], atol=1e-3)
+
+
+def test_two_token_worked_example():
+    g = _load("two_token_worked_example.json")
+    q, k = np.asarray(g["q"]), np.asarray(g["k"])
+    # the page's step 2 (Q K^T) and step 3 (divide by sqrt(d_k)) on its own matrices
+    np.testing.assert_allclose(q @ k.T, g["scores_qkt"], atol=0)
+    np.testing.assert_allclose(q @ k.T / np.sqrt(2.0), g["scaled_scores"], atol=g["tolerance_scores"])
+    out, w = _one(g["q"], g["k"], g["v"])
+    np.testing.assert_allclose(w, g["weights"], atol=g["tolerance"])
+    np.testing.assert_allclose(out, g["output"], atol=g["tolerance"])
+    # exact values, re-derived from the closed form of a 2-key softmax (logistic function)
+    for i in range(2):
+        s = q[i] @ k.T / np.sqrt(2.0)
+        p0 = 1.0 / (1.0 + np.exp(s[1] - s[0]))
+        assert w[i, 0] == pytest.approx(p0, abs=1e-14)
+
+
+# ---------------------------------------------------------------- closed forms
+
+def test_scale_is_inverse_sqrt_dk():
+    """With two keys the log weight ratio is the scaled logit difference, which
+    pins the factor 1/sqrt(d_k) (not 1/d_k, not 1)."""
+    rng = np.random.default_rng(7)
+    for d_k in (2, 16, 64, 128):
+        q = rng.standard_normal((1, d_k))
+        k = rng.standard_normal((2, d_k))
+        v = rng.standard_normal((2, 3))
+        _, w = _one(q, k, v)
+        expect = (q[0] @ k[0] - q[0] @ k[1]) / np.sqrt(d_k)
+        assert np.log(w[0, 0] / w[0, 1]) == pytest.approx(expect, abs=1e-12)
+
+
+def test_explicit_scale_is_used():
+    rng = np.random.default_rng(8)
+    q, k, v = rng.standard_normal((1, 4)), rng.standard_normal((2, 4)), rng.standard_normal((2, 2))
+    _, w = _one(q, k, v, scale=0.3)
+    assert np.log(w[0, 0] / w[0, 1]) == pytest.approx(0.3 * (q[0] @ (k[0] - k[1])), abs=1e-12)
+
+
+def test_output_is_weights_times_v_and_q_k_not_transposed():
+    """Asymmetric shapes (n_q != n_k, d_k != d_v) catch a transposed operand."""
+    rng = np.random.default_rng(9)
+    q = rng.standard_normal((1, 1, 3, 5))
+    k = rng.standard_normal((1, 1, 7, 5))
+    v = rng.standard_normal((1, 1, 7, 2))
+    out, w = oracle.attention(q, k, v, return_weights=True)
+    assert out.shape == (1, 1, 3, 2) and w.shape == (1, 1, 3, 7)
+    np.testing.assert_allclose(out[0, 0], w[0, 0] @ v[0, 0], atol=1e-14)
+    # each weight row is a normalised exponential of that query's logits
+    s = q[0, 0] @ k[0, 0].T / np.sqrt(5.0)
+    e = np.exp(s - s.max(axis=1, keepdims=True))
+    np.testing.assert_allclose(w[0, 0], e / e.sum(axis=1, keepdims=True), atol=1e-14)
+
+
+# ---------------------------------------------------------------- invariants
+
+def _rand(seed, B=2, h=3, n_q=9, n_k=9, d_k=8, d_v=6):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((B, h, n_q, d_k)), rng.standard_normal((B, h, n_k, d_k)),
+            rng.standard_normal((B, h, n_k, d_v)))
+
+
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING,
+                                  MASK_CAUSAL | MASK_KEY_PADDING])
+def test_rows_sum_to_one_and_masked_weights_are_zero(mask):
+    q, k, v = _rand(11)
+    lens = np.array([4, 9], dtype=np.int32)
+    out, w = oracle.attention(q, k, v, mask, kv_lens=lens, return_weights=True)
+    n = q.shape[2]
+    i = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    for b in range(2):
+        allowed = np.ones((n, n), dtype=bool)
+        if mask & MASK_CAUSAL:
+            allowed &= j <= i
+        if mask & MASK_KEY_PADDING:
+            allowed &= j < lens[b]
+        assert np.all(w[b][:, ~allowed] == 0.0)          # future / pad weights exactly 0
+        assert np.all(w[b][:, allowed] > 0.0)
+        np.testing.assert_allclose(w[b].sum(axis=-1), 1.0, atol=1e-14)
+
+
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING,
+                                  MASK_CAUSAL | MASK_KEY_PADDING])
+def test_zero_query_gives_mean_of_allowed_values(mask):
+    _, k, v = _rand(12)
+    q = np.zeros((2, 3, 9, 8))
+    lens = np.array([5, 2], dtype=np.int32)
+    out = oracle.attention(q, k, v, mask, kv_lens=lens)
+    for b in range(2):
+        for i in range(9):
+            hi = 9
+            if mask & MASK_CAUSAL:
+                hi = min(hi, i + 1)
+            if mask & MASK_KEY_PADDING:
+                hi = min(hi, lens[b])
+            np.testing.assert_allclose(out[b, :, i], v[b, :, :hi].mean(axis=1), atol=1e-13)
+
+
+def test_causal_row_zero_is_v0():
+    q, k, v = _rand(13)
+    out = oracle.attention(q, k, v, MASK_CAUSAL)
+    np.testing.assert_array_equal(out[:, :, 0], v[:, :, 0])
+
+
+def test_joint_key_value_permutation_leaves_output_unchanged():
+    q, k, v = _rand(14, n_q=5, n_k=11)
+    perm = np.random.default_rng(0).permutation(11)
+    a = oracle.attention(q, k, v)
+    b = oracle.attention(q, k[:, :, perm], v[:, :, perm])
+    np.testing.assert_allclose(a, b, atol=1e-13)
+    # key padding: permuting within the valid prefix changes nothing either
+    lens = np.array([6, 11], dtype=np.int32)
+    p6 = np.concatenate([np.random.default_rng(1).permutation(6), np.arange(6, 11)])
+    a = oracle.attention(q, k, v, MASK_KEY_PADDING, kv_lens=lens)
+    b = oracle.attention(q, k[:, :, p6], v[:, :, p6], MASK_KEY_PADDING, kv_lens=lens)
+    np.testing.assert_allclose(a, b, atol=1e-13)
+
+
+def test_query_permutation_permutes_outputs():
+    q, k, v = _rand(15, n_q=7, n_k=5)
+    perm = np.random.default_rng(2).permutation(7)
+    a = oracle.attention(q, k, v)
+    b = oracle.attention(q[:, :, perm], k, v)
+    np.testing.assert_allclose(a[:, :, perm], b, atol=1e-13)
+
+
+def test_single_key_and_constant_values():
+    q, k, v = _rand(16, n_q=4, n_k=1)
+    np.testing.assert_allclose(oracle.attention(q, k, v), np.broadcast_to(v, (2, 3, 4, 6)), atol=0)
+    q, k, v = _rand(17, n_q=4, n_k=6)
+    c = np.broadcast_to(np.arange(6.0)[None, None, None, :] - 2.5, v.shape).copy()
+    np.testing.assert_allclose(oracle.attention(q, k, c), np.broadcast_to(c[:, :, :1], (2, 3, 4, 6)),
+                               atol=1e-13)
+
+
+def test_common_key_shift_leaves_output_unchanged():
+    """K + 1 u^T adds q.u to every logit of a row; the softmax ignores it."""
+    q, k, v = _rand(18)
+    u = np.random.default_rng(3).standard_normal(8)
+    for mask in (MASK_NONE, MASK_CAUSAL):
+        a = oracle.attention(q, k, v, mask)
+        b = oracle.attention(q, k + u, v, mask)
+        np.testing.assert_allclose(a, b, atol=1e-12)
+
+
+def test_empty_key_set_gives_zero_rows():
+    q, k, v = _rand(19)
+    out, w = oracle.attention(q, k, v, MASK_KEY_PADDING, kv_lens=np.array([0, 3], np.int32),
+                              return_weights=True)
+    assert np.all(out[0] == 0.0) and np.all(w[0] == 0.0)
+    assert np.all(np.isfinite(out))
+    # out-of-range lengths are clamped to [0, n_k]
+    a = oracle.attention(q, k, v, MASK_KEY_PADDING, kv_lens=np.array([-5, 100], np.int32))
+    assert np.all(a[0] == 0.0)
+    np.testing.assert_allclose(a[1], oracle.attention(q, k, v)[1], atol=0)
+
+
+def test_large_logits_do_not_overflow():
+    """The max-subtraction keeps exp finite for logits far beyond exp's range."""
+    q = np.full((1, 1, 2, 4), 300.0)
+    k = np.full((1, 1, 3, 4), 300.0)
+    k[0, 0, 1] = 299.0
+    v = np.eye(3)[None, None]
+    out, w = oracle.attention(q, k, v, return_weights=True)
+    assert np.all(np.isfinite(out))
+    np.testing.assert_allclose(w.sum(-1), 1.0, atol=1e-15)
+
+
+def test_rows_entry_equals_full_attention_rows():
+    q, k, v = _rand(20, n_q=12, n_k=12)
+    lens = np.array([7, 12], dtype=np.int32)
+    for mask in (MASK_NONE, MASK_CAUSAL, MASK_CAUSAL | MASK_KEY_PADDING):
+        full = oracle.attention(q, k, v, mask, kv_lens=lens)
+        rows = np.array([0, 5, 11, 3])
+        for b in range(2):
+            for hh in range(3):
+                got = oracle.attention_rows(q[b, hh, rows], rows, k[b, hh], v[b, hh],
+                                            causal=bool(mask & MASK_CAUSAL),
+                                            kv_len=int(lens[b]) if mask & MASK_KEY_PADDING else None)
+                np.testing.assert_allclose(got, full[b, hh, rows], atol=0)
+
+
+def test_variance_of_unscaled_logits_is_dk():
+    """Var(q.k) = d_k for iid unit-variance components; after 1/sqrt(d_k) it is 1
+    ("[논문 리뷰]Attention Is All You Need", section 3.2.1, the variance argument).
+    Checked on the generator's bf16 N(0,1) draws through two-key weight ratios."""
+    import synthetic
+    rng = np.random.default_rng(21)
+    d_k, n = 64, 20000
+    qb = synthetic.bf16_bits_to_f64(synthetic.normal_bf16(rng, (n, d_k)))
+    kb = synthetic.bf16_bits_to_f64(synthetic.normal_bf16(rng, (n, 2, d_k)))
+    q = qb[:, None, None, :].reshape(n, 1, 1, d_k)
+    k = kb.reshape(n, 1, 2, d_k)
+    v = np.zeros((n, 1, 2, 1))
+    _, w = oracle.attention(q, k, v, return_weights=True)
+    # log(w0/w1) = (q.k0 - q.k1)/sqrt(d_k) has variance 2 (difference of two unit-variance logits)
+    z = np.log(w[:, 0, 0, 0] / w[:, 0, 0, 1])
+    assert np.var(z) == pytest.approx(2.0, rel=0.05)
+
+
+# ---------------------------------------------------------------- library special case
+
+def _torch_sdpa(q, k, v, mask, lens):
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    B, h, n_q, _ = q.shape
+    n_k = k.shape[2]
+    allowed = torch.ones((B, 1, n_q, n_k), dtype=torch.bool)
+    if mask & MASK_CAUSAL:
+        allowed &= torch.tril(torch.ones((n_q, n_k), dtype=torch.bool))
+    if mask & MASK_KEY_PADDING:
+        allowed &= (torch.arange(n_k)[None, :] < torch.as_tensor(lens)[:, None])[:, None, None, :]
+    return F.scaled_dot_product_attention(torch.from_numpy(q), torch.from_numpy(k),
+                                          torch.from_numpy(v), attn_mask=allowed).numpy()
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 9, 9, 8, 8), (1, 2, 5, 13, 16, 4), (3, 1, 17, 17, 64, 64)])
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING,
+                                  MASK_CAUSAL | MASK_KEY_PADDING])
+def test_matches_torch_fp64_sdpa(shape, mask):
+    B, h, n_q, n_k, d_k, d_v = shape
+    if mask & MASK_CAUSAL and n_q != n_k:
+        pytest.skip("causal defined for n_q == n_k")
+    rng = np.random.default_rng(hash(shape) % 2**32)
+    q = rng.standard_normal((B, h, n_q, d_k))
+    k = rng.standard_normal((B, h, n_k, d_k))
+    v = rng.standard_normal((B, h, n_k, d_v))
+    lens = rng.integers(1, n_k + 1, size=B).astype(np.int32)
+    ours = oracle.attention(q, k, v, mask, kv_lens=lens)
+    ref = _torch_sdpa(q, k, v, mask, lens)
+    np.testing.assert_allclose(ours, ref, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- multi-head
+
+def _mha_case(seed, B=2, n_q=6, n_k=6, d_model=16, h=4, d=4):
+    rng = np.random.default_rng(seed)
+    x_q = rng.standard_normal((B, n_q, d_model))
+    x_kv = x_q if n_k == n_q else rng.standard_normal((B, n_k, d_model))
+    ws = [rng.standard_normal((d_model, h * d)) * 0.3 for _ in range(3)]
+    w_o = rng.standard_normal((h * d, d_model)) * 0.3
+    return x_q, x_kv, ws, w_o
+
+
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING])
+def test_mha_equals_independent_heads_then_output_projection(mask):
+    """MultiHead = Concat(head_1..head_h) W^O with head_i on column block i."""
+    x_q, x_kv, (w_q, w_k, w_v), w_o = _mha_case(31)
+    h, d = 4, 4
+    lens = np.array([3, 6], dtype=np.int32)
+    got, concat = oracle.mha(x_q, x_kv, w_q, w_k, w_v, w_o, h, mask, kv_lens=lens, return_concat=True)
+    heads = []
+    for i in range(h):
+        cols = slice(i * d, (i + 1) * d)
+        Qi, Ki, Vi = x_q @ w_q[:, cols], x_kv @ w_k[:, cols], x_kv @ w_v[:, cols]
+        heads.append(oracle.attention(Qi[:, None], Ki[:, None], Vi[:, None], mask, kv_lens=lens)[:, 0])
+    expect_concat = np.concatenate(heads, axis=-1)
+    np.testing.assert_allclose(concat, expect_concat, atol=1e-13)
+    np.testing.assert_allclose(got, expect_concat @ w_o, atol=1e-12)
+
+
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING])
+@pytest.mark.parametrize("cross", [False, True])
+def test_mha_matches_torch_multi_head_attention_forward(mask, cross):
+    """torch's fp64 multi_head_attention_forward (weights transposed into its
+    y = x W^T convention, no biases) is an independent implementation."""
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    if cross and mask & MASK_CAUSAL:
+        pytest.skip("causal defined for self-attention")
+    B, n_q, n_k, d_model, h = 2, 6, (9 if cross else 6), 16, 4
+    x_q, x_kv, (w_q, w_k, w_v), w_o = _mha_case(32, B=B, n_q=n_q, n_k=n_k, d_model=d_model, h=h)
+    lens = np.array([n_k - 2, n_k], dtype=np.int32)
+    ours = oracle.mha(x_q, x_kv, w_q, w_k, w_v, w_o, h, mask, kv_lens=lens)
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    attn_mask = None
+    if mask & MASK_CAUSAL:
+        attn_mask = ~torch.tril(torch.ones((n_q, n_k), dtype=torch.bool))  # True = not allowed
+    kpm = None
+    if mask & MASK_KEY_PADDING:
+        kpm = torch.arange(n_k)[None, :] >= T(lens)[:, None]
+    ref, _ = F.multi_head_attention_forward(
+        T(x_q.transpose(1, 0, 2)), T(x_kv.transpose(1, 0, 2)), T(x_kv.transpose(1, 0, 2)),
+        d_model, h, None, None, None, None, False, 0.0, T(w_o.T), None, training=False,
+        key_padding_mask=kpm, need_weights=False, attn_mask=attn_mask,
+        use_separate_proj_weight=True, q_proj_weight=T(w_q.T), k_proj_weight=T(w_k.T),
+        v_proj_weight=T(w_v.T))
+    np.testing.assert_allclose(ours, ref.numpy().transpose(1, 0, 2), rtol=1e-11, atol=1e-11)

@@ -1,0 +1,173 @@
+/*
+ * tsd_attention.h -- C ABI of the GB300 (sm_103a) multi-head scaled
+ * dot-product attention library (libtsd_attention.so).
+ *
+ * The operation is eq. (1) of "Attention Is All You Need",
+ *     Attention(Q, K, V) = softmax(Q K^T / sqrt(d_k)) V,
+ * a query mapped against a set of key/value pairs to a weighted sum of the
+ * values ("[논문 리뷰]Attention Is All You Need" (kimjiil.github.io),
+ * section 3.2 / 3.2.1), applied per head, and multi-head attention
+ *     MultiHead = Concat(head_1..head_h) W^O,
+ *     head_i = Attention(X_q W_i^Q, X_kv W_i^K, X_kv W_i^V)
+ * (same page, section 3.2.2). Masks set the illegal logits to -inf before
+ * the softmax so their weight is exactly 0 (same page, section 3.2.3;
+ * "Attention Is All You Need 해부" (sj-techlog), section "mask는 softmax
+ * **전**에 더해야 한다").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never frees, retains or allocates device memory on a call. Every call is
+ *    asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream) and returns before the GPU work finishes.
+ *  - Layouts are row-major and contiguous. bf16 tensors hold IEEE bfloat16
+ *    bit patterns (uint16); f32 tensors hold IEEE binary32.
+ *  - Host-detected argument errors return before anything is launched.
+ *  - kv_lens values are clamped on the device to [0, n_k]. A query row with
+ *    no allowed key (kv_len = 0) produces an all-zero output row.
+ *  - Kernels never trap or assert. Every wait inside a kernel is bounded;
+ *    a kernel that gives up sets a device error word and exits cleanly,
+ *    which attn_get_device_status() reports.
+ */
+#ifndef TSD_ATTENTION_H
+#define TSD_ATTENTION_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without pulling in the CUDA headers. */
+typedef struct CUstream_st *tsd_stream_t;
+
+typedef enum attn_status {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID = 1,        /* an argument is invalid; nothing was launched */
+    ATTN_ERR_UNSUPPORTED = 2,    /* valid for eq. (1) but outside what this build runs
+                                    (e.g. a head size the bf16 kernel has no variant for) */
+    ATTN_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed; see attn_last_cuda_error() */
+    ATTN_ERR_DEVICE_TIMEOUT = 4  /* a kernel's bounded wait ran out (attn_get_device_status) */
+} attn_status;
+
+/* mask_kind bit flags */
+enum {
+    ATTN_MASK_NONE = 0,
+    ATTN_MASK_CAUSAL = 1,       /* query i sees keys j <= i; requires n_q == n_k
+                                   (decoder masked self-attention, section 3.2.3) */
+    ATTN_MASK_KEY_PADDING = 2   /* keys j >= kv_lens[b] receive no attention
+                                   ("Attention Is All You Need 해부", three-uses table) */
+};
+
+/*
+ * attn_forward -- scaled dot-product attention, bf16 in/out, fp32 softmax and
+ * accumulation, on the tcgen05 tensor cores.
+ *
+ *   q    [B, h, n_q, d_k]  bf16, device, 16-byte aligned
+ *   k    [B, h, n_k, d_k]  bf16, device, 16-byte aligned
+ *   v    [B, h, n_k, d_v]  bf16, device, 16-byte aligned
+ *   out  [B, h, n_q, d_v]  bf16, device, 16-byte aligned, written in full
+ *   d_k == d_v, and d_k in {64, 128}         else ATTN_ERR_UNSUPPORTED
+ *   B, h >= 1; n_q, n_k >= 1                 else ATTN_ERR_INVALID
+ *   mask_kind: OR of ATTN_MASK_* bits; CAUSAL needs n_q == n_k
+ *   kv_lens: device int32[B]; required with ATTN_MASK_KEY_PADDING, ignored otherwise
+ *   scale: the logit factor; 0 selects 1/sqrt(d_k) (eq. (1))
+ * Errors: null/misaligned pointer, bad sizes or flags -> ATTN_ERR_INVALID;
+ * a failed launch -> ATTN_ERR_CUDA.
+ */
+attn_status attn_forward(const void *q, const void *k, const void *v, void *out,
+                         int B, int h, int n_q, int n_k, int d_k, int d_v,
+                         int mask_kind, const int32_t *kv_lens, float scale,
+                         tsd_stream_t stream);
+
+/*
+ * attn_forward_strided -- the same operation as attn_forward on tensors whose
+ * (batch, head, row) strides are given in ELEMENTS (the head dimension stays
+ * contiguous). This lets a caller read heads straight out of a [B, n, h*d]
+ * projection output (head i = column block i, section 3.2.2) and write the
+ * merged Concat(head_1..head_h) layout [B, n_q, h*d_v] without a copy.
+ * Every stride must be a multiple of 8 elements (16 bytes); rows may not
+ * overlap within a head. Other arguments and errors as attn_forward.
+ */
+attn_status attn_forward_strided(const void *q, int64_t q_sb, int64_t q_sh, int64_t q_sr,
+                                 const void *k, int64_t k_sb, int64_t k_sh, int64_t k_sr,
+                                 const void *v, int64_t v_sb, int64_t v_sh, int64_t v_sr,
+                                 void *out, int64_t o_sb, int64_t o_sh, int64_t o_sr,
+                                 int B, int h, int n_q, int n_k, int d_k, int d_v,
+                                 int mask_kind, const int32_t *kv_lens, float scale,
+                                 tsd_stream_t stream);
+
+/*
+ * attn_forward_f32 -- the same operation in fp32 throughout (FFMA, no TF32),
+ * for callers that need results within 1e-4 of exact.
+ *   q [B,h,n_q,d_k], k [B,h,n_k,d_k], v [B,h,n_k,d_v], out [B,h,n_q,d_v]: f32, device.
+ *   1 <= d_k, d_v <= 128. Other arguments and errors as attn_forward.
+ */
+attn_status attn_forward_f32(const float *q, const float *k, const float *v, float *out,
+                             int B, int h, int n_q, int n_k, int d_k, int d_v,
+                             int mask_kind, const int32_t *kv_lens, float scale,
+                             tsd_stream_t stream);
+
+/*
+ * mha_workspace_bytes -- size of the caller-owned device workspace that
+ * mha_forward needs for the head-split projections Q, K, V and the merged
+ * heads Concat(head_1..head_h) (bf16, each region 256-byte aligned).
+ * Returns 0 for invalid sizes.
+ */
+size_t mha_workspace_bytes(int B, int n_q, int n_k, int h, int d_k, int d_v);
+
+/*
+ * mha_forward -- multi-head attention, section 3.2.2 (x.W convention, no
+ * biases, as in the pages' formula):
+ *   Q = x_q W_Q, K = x_kv W_K, V = x_kv W_V        (tensor-core GEMMs)
+ *   head_i = Attention(Q_i, K_i, V_i)              (attn kernel; Q_i = column block i)
+ *   out = Concat(head_1..head_h) W_O               (tensor-core GEMM)
+ *
+ *   x_q  [B, n_q, d_model] bf16      x_kv [B, n_k, d_model] bf16 (may equal x_q)
+ *   w_q  [d_model, h*d_k]  bf16      w_k  [d_model, h*d_k]  bf16
+ *   w_v  [d_model, h*d_v]  bf16      w_o  [h*d_v, d_model]  bf16
+ *   out  [B, n_q, d_model] bf16
+ *   d_k == d_v in {64, 128}; d_model a multiple of 8 (16-byte rows), >= 8.
+ *   workspace: device, 256-byte aligned, >= mha_workspace_bytes(...) bytes;
+ *   its contents on return are the intermediate Q, K, V and merged heads.
+ *   mask_kind, kv_lens, scale: as attn_forward (the mask applies to every head).
+ * Errors: as attn_forward; a short workspace -> ATTN_ERR_INVALID.
+ */
+attn_status mha_forward(const void *x_q, const void *x_kv,
+                        const void *w_q, const void *w_k, const void *w_v, const void *w_o,
+                        void *out,
+                        int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
+                        int mask_kind, const int32_t *kv_lens, float scale,
+                        void *workspace, size_t workspace_bytes, tsd_stream_t stream);
+
+/*
+ * attn_get_device_status -- synchronises `stream`, then reads and clears the
+ * device error word the kernels set when a bounded wait runs out.
+ * Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT, or ATTN_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+attn_status attn_get_device_status(tsd_stream_t stream);
+
+/* The last CUDA error code (cudaError_t as int) seen by this library on the
+ * calling thread, 0 if none. */
+int attn_last_cuda_error(void);
+
+/* A static, human-readable name for a status code. */
+const char *attn_status_string(attn_status s);
+
+/*
+ * attn_selftest_wait_timeout -- failure-detection self test. Launches one
+ * small kernel whose bounded wait is on an mbarrier that nothing ever
+ * arrives on, with a limit of `limit_us` microseconds (1..2000000). The
+ * kernel records a timeout in the device error word and exits; the caller
+ * reads it with attn_get_device_status(), and the context stays usable.
+ * No tensor memory or asynchronous copy is involved.
+ */
+attn_status attn_selftest_wait_timeout(int limit_us, tsd_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSD_ATTENTION_H */

@@ -1,0 +1,128 @@
+"""The C-ABI library loads, exports every symbol the header declares, and
+rejects invalid arguments on the host before any launch (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import transformer_scaled_dot_gb300 as tsd
+from transformer_scaled_dot_gb300 import build as native_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    native_build.build()
+    return tsd.library()
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                            text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_functions()
+    assert set(tsd.EXPORTED_SYMBOLS) <= set(declared)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert tsd.attn_status_string(tsd.ATTN_OK) == "ATTN_OK"
+    assert tsd.attn_status_string(tsd.ATTN_ERR_DEVICE_TIMEOUT) == "ATTN_ERR_DEVICE_TIMEOUT"
+
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced: every call below fails validation
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (B, h, n_q, n_k, d_k, d_v, mask, kv_lens, scale)
+    ((1, 1, 16, 16, 96, 96, 0, None, 0.0), tsd.ATTN_ERR_UNSUPPORTED),
+    ((1, 1, 16, 16, 64, 128, 0, None, 0.0), tsd.ATTN_ERR_UNSUPPORTED),
+    ((-1, 1, 16, 16, 64, 64, 0, None, 0.0), tsd.ATTN_ERR_INVALID),
+    ((1, 1, 16, 8, 64, 64, 1, None, 0.0), tsd.ATTN_ERR_INVALID),      # causal, n_q != n_k
+    ((1, 1, 16, 16, 64, 64, 2, None, 0.0), tsd.ATTN_ERR_INVALID),     # padding without lengths
+    ((1, 1, 16, 16, 64, 64, 4, None, 0.0), tsd.ATTN_ERR_INVALID),     # unknown mask bit
+    ((1, 1, 16, 16, 64, 64, 0, None, -1.0), tsd.ATTN_ERR_INVALID),    # negative scale
+    ((1, 1, 16, 16, 64, 64, 0, None, float("nan")), tsd.ATTN_ERR_INVALID),
+    ((1, 70000, 16, 16, 64, 64, 0, None, 0.0), tsd.ATTN_ERR_INVALID),  # grid limit
+])
+def test_attn_forward_rejects_bad_arguments(lib, args, expect):
+    B, h, n_q, n_k, d_k, d_v, mask, lens, scale = args
+    st = lib.attn_forward(FAKE, FAKE, FAKE, FAKE, B, h, n_q, n_k, d_k, d_v, mask, lens, scale, None)
+    assert st == expect
+
+
+def test_attn_forward_rejects_null_and_misaligned(lib):
+    assert lib.attn_forward(None, FAKE, FAKE, FAKE, 1, 1, 16, 16, 64, 64, 0, None, 0.0, None) == \
+        tsd.ATTN_ERR_INVALID
+    assert lib.attn_forward(FAKE + 2, FAKE, FAKE, FAKE, 1, 1, 16, 16, 64, 64, 0, None, 0.0, None) == \
+        tsd.ATTN_ERR_INVALID
+    assert lib.attn_forward(FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 16, 64, 64, 2, FAKE + 2, 0.0, None) == \
+        tsd.ATTN_ERR_INVALID
+
+
+def test_empty_problems_are_no_ops(lib):
+    for B, h, n_q in ((0, 1, 16), (1, 0, 16), (1, 1, 0)):
+        assert lib.attn_forward(FAKE, FAKE, FAKE, FAKE, B, h, n_q, 16, 64, 64, 0, None, 0.0,
+                                None) == tsd.ATTN_OK
+
+
+def test_attn_forward_strided_rejects_bad_strides(lib):
+    good = (1 << 20, 8192, 64)
+    args = [FAKE, *good, FAKE, *good, FAKE, *good, FAKE, *good, 1, 1, 16, 16, 64, 64, 0, None, 0.0, None]
+    bad = list(args)
+    bad[3] = 60  # row stride not a multiple of 8 elements
+    assert lib.attn_forward_strided(*bad) == tsd.ATTN_ERR_INVALID
+    bad = list(args)
+    bad[15] = 32  # output row stride smaller than d_v
+    assert lib.attn_forward_strided(*bad) == tsd.ATTN_ERR_INVALID
+
+
+def test_attn_forward_f32_limits(lib):
+    assert lib.attn_forward_f32(FAKE, FAKE, FAKE, FAKE, 1, 1, 4, 4, 129, 64, 0, None, 0.0, None) == \
+        tsd.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_forward_f32(FAKE + 1, FAKE, FAKE, FAKE, 1, 1, 4, 4, 64, 64, 0, None, 0.0, None) == \
+        tsd.ATTN_ERR_INVALID
+
+
+def test_mha_workspace_bytes_layout(lib):
+    B, n_q, n_k, h, d = 32, 128, 160, 8, 64
+    got = tsd.mha_workspace_bytes(B, n_q, n_k, h, d, d)
+    align = lambda x: (x + 255) // 256 * 256
+    expect = align(B * n_q * h * d * 2) * 2 + align(B * n_k * h * d * 2) * 2
+    assert got == expect
+    assert tsd.mha_workspace_bytes(-1, 1, 1, 1, 64, 64) == 0
+
+
+def test_mha_forward_rejects_bad_arguments(lib):
+    B, n, dm, h, d = 2, 16, 128, 2, 64
+    wsb = tsd.mha_workspace_bytes(B, n, n, h, d, d)
+    base = [FAKE] * 7 + [B, n, n, dm, h, d, d, 0, None, 0.0, FAKE, wsb, None]
+    bad = list(base)
+    bad[18] = wsb - 1                      # short workspace
+    assert lib.mha_forward(*bad) == tsd.ATTN_ERR_INVALID
+    bad = list(base)
+    bad[17] = FAKE + 16                    # workspace not 256-byte aligned
+    assert lib.mha_forward(*bad) == tsd.ATTN_ERR_INVALID
+    bad = list(base)
+    bad[10] = 100                          # d_model not a multiple of 8
+    assert lib.mha_forward(*bad) == tsd.ATTN_ERR_INVALID
+    bad = list(base)
+    bad[12] = bad[13] = 32                 # head size without a bf16 kernel
+    assert lib.mha_forward(*bad) == tsd.ATTN_ERR_UNSUPPORTED
+
+
+def test_selftest_rejects_bad_limit(lib):
+    assert lib.attn_selftest_wait_timeout(0, None) == tsd.ATTN_ERR_INVALID
+    assert lib.attn_selftest_wait_timeout(3000000, None) == tsd.ATTN_ERR_INVALID

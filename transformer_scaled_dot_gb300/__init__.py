@@ -1,0 +1,157 @@
+"""GB300 (sm_103a) multi-head scaled dot-product attention.
+
+A thin Python binding over the C ABI of libtsd_attention.so
+(include/tsd_attention.h). Each function has the name and the parameters of
+its C entry point and only marshals arguments: tensor arguments may be
+torch tensors (their data_ptr() is passed) or raw device addresses (int);
+`stream` may be a torch.cuda.Stream, a raw cudaStream_t (int), or None for
+torch's current stream. A non-OK status raises AttnError.
+
+There is no fallback: if the native library is missing, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+__all__ = [
+    "ATTN_OK", "ATTN_ERR_INVALID", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA",
+    "ATTN_ERR_DEVICE_TIMEOUT", "ATTN_MASK_NONE", "ATTN_MASK_CAUSAL", "ATTN_MASK_KEY_PADDING",
+    "AttnError", "library", "library_path", "EXPORTED_SYMBOLS",
+    "attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_workspace_bytes",
+    "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
+    "attn_selftest_wait_timeout",
+]
+
+ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = range(5)
+ATTN_MASK_NONE, ATTN_MASK_CAUSAL, ATTN_MASK_KEY_PADDING = 0, 1, 2
+
+EXPORTED_SYMBOLS = (
+    "attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_workspace_bytes",
+    "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
+    "attn_selftest_wait_timeout",
+)
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        name = library().attn_status_string(status).decode()
+        extra = ""
+        if status == ATTN_ERR_CUDA:
+            extra = f" (cudaError {library().attn_last_cuda_error()})"
+        super().__init__(f"{where}: {name}{extra}")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def library():
+    """Loads libtsd_attention.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    vp, i, i64, f, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+    lib.attn_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, f, st]
+    lib.attn_forward_strided.argtypes = [vp, i64, i64, i64, vp, i64, i64, i64, vp, i64, i64, i64,
+                                         vp, i64, i64, i64, i, i, i, i, i, i, i, vp, f, st]
+    lib.attn_forward_f32.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, f, st]
+    lib.mha_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    lib.mha_workspace_bytes.restype = ctypes.c_size_t
+    lib.mha_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, f, vp,
+                                ctypes.c_size_t, st]
+    lib.attn_get_device_status.argtypes = [st]
+    lib.attn_last_cuda_error.argtypes = []
+    lib.attn_status_string.argtypes = [i]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_selftest_wait_timeout.argtypes = [i, st]
+    for name in ("attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_forward",
+                 "attn_get_device_status", "attn_last_cuda_error", "attn_selftest_wait_timeout"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != ATTN_OK:
+        raise AttnError(status, where)
+
+
+def attn_forward(q, k, v, out, B, h, n_q, n_k, d_k, d_v, mask_kind=ATTN_MASK_NONE, kv_lens=None,
+                 scale=0.0, stream=None):
+    _check(library().attn_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, h, n_q, n_k, d_k, d_v,
+                                  mask_kind, _ptr(kv_lens), scale, _stream(stream)), "attn_forward")
+
+
+def attn_forward_strided(q, q_sb, q_sh, q_sr, k, k_sb, k_sh, k_sr, v, v_sb, v_sh, v_sr,
+                         out, o_sb, o_sh, o_sr, B, h, n_q, n_k, d_k, d_v,
+                         mask_kind=ATTN_MASK_NONE, kv_lens=None, scale=0.0, stream=None):
+    _check(library().attn_forward_strided(
+        _ptr(q), q_sb, q_sh, q_sr, _ptr(k), k_sb, k_sh, k_sr, _ptr(v), v_sb, v_sh, v_sr,
+        _ptr(out), o_sb, o_sh, o_sr, B, h, n_q, n_k, d_k, d_v, mask_kind, _ptr(kv_lens), scale,
+        _stream(stream)), "attn_forward_strided")
+
+
+def attn_forward_f32(q, k, v, out, B, h, n_q, n_k, d_k, d_v, mask_kind=ATTN_MASK_NONE,
+                     kv_lens=None, scale=0.0, stream=None):
+    _check(library().attn_forward_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, h, n_q, n_k, d_k,
+                                      d_v, mask_kind, _ptr(kv_lens), scale, _stream(stream)),
+           "attn_forward_f32")
+
+
+def mha_workspace_bytes(B, n_q, n_k, h, d_k, d_v) -> int:
+    return int(library().mha_workspace_bytes(B, n_q, n_k, h, d_k, d_v))
+
+
+def mha_forward(x_q, x_kv, w_q, w_k, w_v, w_o, out, B, n_q, n_k, d_model, h, d_k, d_v,
+                mask_kind=ATTN_MASK_NONE, kv_lens=None, scale=0.0, workspace=None,
+                workspace_bytes=0, stream=None):
+    _check(library().mha_forward(_ptr(x_q), _ptr(x_kv), _ptr(w_q), _ptr(w_k), _ptr(w_v),
+                                 _ptr(w_o), _ptr(out), B, n_q, n_k, d_model, h, d_k, d_v,
+                                 mask_kind, _ptr(kv_lens), scale, _ptr(workspace),
+                                 workspace_bytes, _stream(stream)), "mha_forward")
+
+
+def attn_get_device_status(stream=None) -> int:
+    """Returns the status code (does not raise on ATTN_ERR_DEVICE_TIMEOUT)."""
+    return int(library().attn_get_device_status(_stream(stream)))
+
+
+def attn_last_cuda_error() -> int:
+    return int(library().attn_last_cuda_error())
+
+
+def attn_status_string(status: int) -> str:
+    return library().attn_status_string(status).decode()
+
+
+def attn_selftest_wait_timeout(limit_us: int, stream=None):
+    _check(library().attn_selftest_wait_timeout(limit_us, _stream(stream)),
+           "attn_selftest_wait_timeout")

@@ -1,0 +1,355 @@
+// api.cu -- the C ABI (include/tsd_attention.h): argument validation, TMA
+// descriptor encoding, and the launch sequence of multi-head attention.
+// Every host-detectable error returns before anything is launched.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "tsd_attention.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+attn_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return ATTN_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so the
+// library does not link libcuda directly.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder(cudaError_t* err) {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static cudaError_t status = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                              cudaEnableDefault, &q);
+    if (status == cudaSuccess && (q != cudaDriverEntryPointSuccess || p == nullptr))
+      status = cudaErrorNotSupported;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  *err = status;
+  return fn;
+}
+
+// bf16 tensor map, rank 2..4, dims innermost first, strides in elements
+// (dims 1..rank-1), 128-byte swizzle, zero fill out of bounds.
+cudaError_t encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                            const int64_t* strides_elems, const uint32_t* box) {
+  cudaError_t err;
+  auto enc = tensor_map_encoder(&err);
+  if (err != cudaSuccess) return err;
+  cuuint64_t gdim[5];
+  cuuint64_t gstride[4];
+  cuuint32_t bdim[5];
+  cuuint32_t estride[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    estride[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) gstride[i] = static_cast<cuuint64_t>(strides_elems[i]) * 2u;
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                   const_cast<void*>(base), gdim, gstride, bdim, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Q/K/V as a 4-D (d, rows, heads, batch) map with 64 x 128 boxes.
+cudaError_t encode_head_map(CUtensorMap* map, const void* base, int d, int rows, int h, int B,
+                            int64_t sr, int64_t sh, int64_t sb) {
+  const uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(rows < 1 ? 1 : rows),
+                            static_cast<uint64_t>(h), static_cast<uint64_t>(B)};
+  const int64_t strides[3] = {sr, sh, sb};
+  const uint32_t box[4] = {64, 128, 1, 1};
+  return encode_bf16_map(map, base, 4, dims, strides, box);
+}
+
+bool valid_scale(float s) { return std::isfinite(s) && s >= 0.f; }
+
+float resolve_scale(float s, int d_k) {
+  return s == 0.f ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k))) : s;
+}
+
+// Shared checks of attn_forward / attn_forward_strided / mha_forward.
+attn_status check_common(int B, int h, int n_q, int n_k, int d_k, int d_v, int mask_kind,
+                         const int32_t* kv_lens, float scale) {
+  if (B < 0 || h < 0 || n_q < 0 || n_k < 0 || d_k <= 0 || d_v <= 0) return ATTN_ERR_INVALID;
+  if (h > 65535 || B > 65535) return ATTN_ERR_INVALID;  // grid y / z limits
+  if (mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_KEY_PADDING)) return ATTN_ERR_INVALID;
+  if ((mask_kind & ATTN_MASK_CAUSAL) && n_q != n_k) return ATTN_ERR_INVALID;
+  if ((mask_kind & ATTN_MASK_KEY_PADDING) &&
+      (kv_lens == nullptr || (reinterpret_cast<uintptr_t>(kv_lens) & 3u)))
+    return ATTN_ERR_INVALID;
+  if (!valid_scale(scale)) return ATTN_ERR_INVALID;
+  return ATTN_OK;
+}
+
+attn_status check_bf16_head_dims(int d_k, int d_v) {
+  if (d_k != d_v || (d_k != 64 && d_k != 128)) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+attn_status run_attn_bf16(const void* q, int64_t q_sb, int64_t q_sh, int64_t q_sr, const void* k,
+                          int64_t k_sb, int64_t k_sh, int64_t k_sr, const void* v, int64_t v_sb,
+                          int64_t v_sh, int64_t v_sr, void* out, int64_t o_sb, int64_t o_sh,
+                          int64_t o_sr, int B, int h, int n_q, int n_k, int d, int mask_kind,
+                          const int32_t* kv_lens, float scale, cudaStream_t stream) {
+  CUtensorMap tm_q, tm_k, tm_v;
+  cudaError_t e = encode_head_map(&tm_q, q, d, n_q, h, B, q_sr, q_sh, q_sb);
+  if (e == cudaSuccess) e = encode_head_map(&tm_k, k, d, n_k, h, B, k_sr, k_sh, k_sb);
+  if (e == cudaSuccess) e = encode_head_map(&tm_v, v, d, n_k, h, B, v_sr, v_sh, v_sb);
+  if (e != cudaSuccess) return cuda_fail(e);
+  tsd::AttnProblem p;
+  p.B = B;
+  p.h = h;
+  p.n_q = n_q;
+  p.n_k = n_k;
+  p.d = d;
+  p.mask_kind = mask_kind;
+  p.kv_lens = kv_lens;
+  p.scale = resolve_scale(scale, d);
+  p.out = static_cast<uint16_t*>(out);
+  p.o_sb = o_sb;
+  p.o_sh = o_sh;
+  p.o_sr = o_sr;
+  e = tsd::launch_attn_bf16(p, tm_q, tm_k, tm_v, stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+size_t align256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
+
+struct MhaLayout {
+  size_t q_off, k_off, v_off, o_off, total;
+};
+
+bool mha_layout(int B, int n_q, int n_k, int h, int d_k, int d_v, MhaLayout* L) {
+  if (B < 0 || n_q < 0 || n_k < 0 || h <= 0 || d_k <= 0 || d_v <= 0) return false;
+  const size_t q = static_cast<size_t>(B) * n_q * h * d_k * 2;
+  const size_t k = static_cast<size_t>(B) * n_k * h * d_k * 2;
+  const size_t v = static_cast<size_t>(B) * n_k * h * d_v * 2;
+  const size_t o = static_cast<size_t>(B) * n_q * h * d_v * 2;
+  L->q_off = 0;
+  L->k_off = align256(q);
+  L->v_off = L->k_off + align256(k);
+  L->o_off = L->v_off + align256(v);
+  L->total = L->o_off + align256(o);
+  return true;
+}
+
+// One GEMM group: C[M, N] = A[M, K] B[K, N], all row-major bf16.
+cudaError_t make_gemm_group(tsd::GemmGroup* g, const void* a, const void* b, void* c, int M, int N,
+                            int K) {
+  const uint64_t adims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+  const int64_t astr[1] = {K};
+  const uint32_t abox[2] = {64, 128};
+  cudaError_t e = encode_bf16_map(&g->tm_a, a, 2, adims, astr, abox);
+  if (e != cudaSuccess) return e;
+  const uint64_t bdims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K)};
+  const int64_t bstr[1] = {N};
+  const uint32_t bbox[2] = {64, 64};
+  e = encode_bf16_map(&g->tm_b, b, 2, bdims, bstr, bbox);
+  if (e != cudaSuccess) return e;
+  g->c = static_cast<uint16_t*>(c);
+  g->ldc = N;
+  g->M = M;
+  g->N = N;
+  g->tiles_m = (M + 127) / 128;
+  g->tiles_n = (N + 127) / 128;
+  return cudaSuccess;
+}
+
+void finish_gemm_problem(tsd::GemmProblem* p) {
+  int t = 0;
+  for (int i = 0; i < p->num_groups; ++i) {
+    p->g[i].tile_begin = t;
+    t += p->g[i].tiles_m * p->g[i].tiles_n;
+  }
+  p->total_tiles = t;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_forward(const void* q, const void* k, const void* v, void* out, int B, int h,
+                         int n_q, int n_k, int d_k, int d_v, int mask_kind, const int32_t* kv_lens,
+                         float scale, tsd_stream_t stream) {
+  attn_status s = check_common(B, h, n_q, n_k, d_k, d_v, mask_kind, kv_lens, scale);
+  if (s != ATTN_OK) return s;
+  if (!q || !k || !v || !out) return ATTN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_INVALID;
+  s = check_bf16_head_dims(d_k, d_v);
+  if (s != ATTN_OK) return s;
+  if (B == 0 || h == 0 || n_q == 0) return ATTN_OK;  // nothing to write
+  const int64_t d = d_k;
+  return run_attn_bf16(q, int64_t(h) * n_q * d, int64_t(n_q) * d, d, k, int64_t(h) * n_k * d,
+                       int64_t(n_k) * d, d, v, int64_t(h) * n_k * d, int64_t(n_k) * d, d, out,
+                       int64_t(h) * n_q * d, int64_t(n_q) * d, d, B, h, n_q, n_k, d_k, mask_kind,
+                       kv_lens, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_forward_strided(const void* q, int64_t q_sb, int64_t q_sh, int64_t q_sr,
+                                 const void* k, int64_t k_sb, int64_t k_sh, int64_t k_sr,
+                                 const void* v, int64_t v_sb, int64_t v_sh, int64_t v_sr,
+                                 void* out, int64_t o_sb, int64_t o_sh, int64_t o_sr, int B,
+                                 int h, int n_q, int n_k, int d_k, int d_v, int mask_kind,
+                                 const int32_t* kv_lens, float scale, tsd_stream_t stream) {
+  attn_status s = check_common(B, h, n_q, n_k, d_k, d_v, mask_kind, kv_lens, scale);
+  if (s != ATTN_OK) return s;
+  if (!q || !k || !v || !out) return ATTN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_INVALID;
+  s = check_bf16_head_dims(d_k, d_v);
+  if (s != ATTN_OK) return s;
+  const int64_t strides[12] = {q_sb, q_sh, q_sr, k_sb, k_sh, k_sr, v_sb, v_sh, v_sr, o_sb, o_sh, o_sr};
+  for (int64_t st : strides)
+    if (st <= 0 || (st % 8) != 0 || st > (int64_t(1) << 38)) return ATTN_ERR_INVALID;
+  if (q_sr < d_k || k_sr < d_k || v_sr < d_v || o_sr < d_v) return ATTN_ERR_INVALID;
+  if (B == 0 || h == 0 || n_q == 0) return ATTN_OK;
+  return run_attn_bf16(q, q_sb, q_sh, q_sr, k, k_sb, k_sh, k_sr, v, v_sb, v_sh, v_sr, out, o_sb,
+                       o_sh, o_sr, B, h, n_q, n_k, d_k, mask_kind, kv_lens, scale,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_forward_f32(const float* q, const float* k, const float* v, float* out, int B,
+                             int h, int n_q, int n_k, int d_k, int d_v, int mask_kind,
+                             const int32_t* kv_lens, float scale, tsd_stream_t stream) {
+  attn_status s = check_common(B, h, n_q, n_k, d_k, d_v, mask_kind, kv_lens, scale);
+  if (s != ATTN_OK) return s;
+  if (!q || !k || !v || !out) return ATTN_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 3u)
+    return ATTN_ERR_INVALID;
+  if (d_k > 128 || d_v > 128) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || h == 0 || n_q == 0) return ATTN_OK;
+  tsd::AttnF32Problem p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.B = B;
+  p.h = h;
+  p.n_q = n_q;
+  p.n_k = n_k;
+  p.d_k = d_k;
+  p.d_v = d_v;
+  p.mask_kind = mask_kind;
+  p.kv_lens = kv_lens;
+  p.scale = resolve_scale(scale, d_k);
+  cudaError_t e = tsd::launch_attn_f32(p, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+size_t mha_workspace_bytes(int B, int n_q, int n_k, int h, int d_k, int d_v) {
+  MhaLayout L;
+  if (!mha_layout(B, n_q, n_k, h, d_k, d_v, &L)) return 0;
+  return L.total;
+}
+
+attn_status mha_forward(const void* x_q, const void* x_kv, const void* w_q, const void* w_k,
+                        const void* w_v, const void* w_o, void* out, int B, int n_q, int n_k,
+                        int d_model, int h, int d_k, int d_v, int mask_kind,
+                        const int32_t* kv_lens, float scale, void* workspace,
+                        size_t workspace_bytes, tsd_stream_t stream_) {
+  attn_status s = check_common(B, h, n_q, n_k, d_k, d_v, mask_kind, kv_lens, scale);
+  if (s != ATTN_OK) return s;
+  if (h <= 0 || d_model < 8 || (d_model % 8) != 0) return ATTN_ERR_INVALID;
+  const void* ptrs[8] = {x_q, x_kv, w_q, w_k, w_v, w_o, out, workspace};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID;
+  s = check_bf16_head_dims(d_k, d_v);
+  if (s != ATTN_OK) return s;
+  MhaLayout L;
+  if (!mha_layout(B, n_q, n_k, h, d_k, d_v, &L)) return ATTN_ERR_INVALID;
+  if (workspace_bytes < L.total) return ATTN_ERR_INVALID;
+  const int64_t Mq = int64_t(B) * n_q, Mk = int64_t(B) * n_k;
+  if (Mq > INT32_MAX || Mk > INT32_MAX) return ATTN_ERR_INVALID;
+  if (Mq == 0) return ATTN_OK;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* Q = ws + L.q_off;
+  void* K = ws + L.k_off;
+  void* V = ws + L.v_off;
+  void* O = ws + L.o_off;
+  const int hdk = h * d_k, hdv = h * d_v;
+
+  // 1. Q = X_q W_Q, K = X_kv W_K, V = X_kv W_V   (one grouped launch)
+  tsd::GemmProblem g1;
+  std::memset(&g1, 0, sizeof(g1));
+  g1.K = d_model;
+  g1.num_groups = 1;
+  cudaError_t e = make_gemm_group(&g1.g[0], x_q, w_q, Q, int(Mq), hdk, d_model);
+  if (e == cudaSuccess && Mk > 0) {
+    e = make_gemm_group(&g1.g[1], x_kv, w_k, K, int(Mk), hdk, d_model);
+    if (e == cudaSuccess) e = make_gemm_group(&g1.g[2], x_kv, w_v, V, int(Mk), hdv, d_model);
+    g1.num_groups = 3;
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  finish_gemm_problem(&g1);
+  e = tsd::launch_gemm_bf16(g1, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  // 2. head_i = Attention(Q_i, K_i, V_i): heads are column blocks of the
+  //    [B, n, h*d] projections; the output is written merged, [B, n_q, h*d_v]
+  s = run_attn_bf16(Q, int64_t(n_q) * hdk, d_k, hdk, K, int64_t(n_k) * hdk, d_k, hdk, V,
+                    int64_t(n_k) * hdv, d_v, hdv, O, int64_t(n_q) * hdv, d_v, hdv, B, h, n_q, n_k,
+                    d_k, mask_kind, kv_lens, scale, stream);
+  if (s != ATTN_OK) return s;
+
+  // 3. out = Concat(head_1..head_h) W_O
+  tsd::GemmProblem g2;
+  std::memset(&g2, 0, sizeof(g2));
+  g2.K = hdv;
+  g2.num_groups = 1;
+  e = make_gemm_group(&g2.g[0], O, w_o, out, int(Mq), d_model, hdv);
+  if (e != cudaSuccess) return cuda_fail(e);
+  finish_gemm_problem(&g2);
+  e = tsd::launch_gemm_bf16(g2, stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+attn_status attn_get_device_status(tsd_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned int a = 0, g = 0, f = 0;
+  e = tsd::take_device_error_attn(&a);
+  if (e == cudaSuccess) e = tsd::take_device_error_gemm(&g);
+  if (e == cudaSuccess) e = tsd::take_device_error_f32(&f);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return (a | g | f) ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
+}
+
+int attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID: return "ATTN_ERR_INVALID";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT";
+  }
+  return "ATTN_STATUS_UNKNOWN";
+}
+
+attn_status attn_selftest_wait_timeout(int limit_us, tsd_stream_t stream) {
+  if (limit_us < 1 || limit_us > 2000000) return ATTN_ERR_INVALID;
+  cudaError_t e = tsd::launch_wait_timeout_selftest(static_cast<unsigned long long>(limit_us) * 1000ull,
+                                                    reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// kernels.h -- internal launch interface between the C ABI layer (api.cu)
+// and the kernels. Not installed; the public surface is include/tsd_attention.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace tsd {
+
+constexpr int kMaskCausal = 1;
+constexpr int kMaskKeyPadding = 2;
+
+// One attention problem: Q/K/V/O addressed as (batch, head, row, col) with
+// element strides; the head dimension is contiguous.
+struct AttnProblem {
+  int B, h, n_q, n_k, d;
+  int mask_kind;
+  const int32_t* kv_lens;  // device, may be null without the padding bit
+  float scale;             // logit factor (already resolved: never 0)
+  uint16_t* out;
+  int64_t o_sb, o_sh, o_sr;
+};
+
+// bf16 tcgen05 attention; tensor maps describe Q, K, V as 4-D
+// (d, rows, heads, batch) bf16 tensors with 128-byte swizzled 64x128 boxes.
+cudaError_t launch_attn_bf16(const AttnProblem& p, const CUtensorMap& tm_q,
+                             const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                             cudaStream_t stream);
+
+struct AttnF32Problem {
+  const float* q;
+  const float* k;
+  const float* v;
+  float* out;
+  int B, h, n_q, n_k, d_k, d_v;
+  int mask_kind;
+  const int32_t* kv_lens;
+  float scale;
+};
+cudaError_t launch_attn_f32(const AttnF32Problem& p, cudaStream_t stream);
+
+// Grouped bf16 GEMM C_g[M_g, N_g] = A_g[M_g, K] * B_g[K, N_g] (fp32 accumulate,
+// bf16 out). A is K-major (row-major [M, K]); B is N-major (row-major [K, N],
+// the x.W weight layout). Up to 3 groups share K and run in one launch.
+struct GemmGroup {
+  CUtensorMap tm_a;  // 2-D (K, M), box 64 x 128
+  CUtensorMap tm_b;  // 2-D (N, K), box 64 x 64
+  uint16_t* c;
+  int64_t ldc;       // elements
+  int M, N;
+  int tiles_m, tiles_n, tile_begin;
+};
+constexpr int kMaxGemmGroups = 3;
+struct GemmProblem {
+  GemmGroup g[kMaxGemmGroups];
+  int num_groups;
+  int K;
+  int total_tiles;
+};
+cudaError_t launch_gemm_bf16(const GemmProblem& p, cudaStream_t stream);
+
+// Per-file device error words (read and cleared; see sm103.cuh).
+cudaError_t take_device_error_attn(unsigned int* value);
+cudaError_t take_device_error_gemm(unsigned int* value);
+cudaError_t take_device_error_f32(unsigned int* value);
+
+// Failure-detection self test: a bounded wait on a barrier nobody arrives on.
+cudaError_t launch_wait_timeout_selftest(unsigned long long limit_ns, cudaStream_t stream);
+
+}  // namespace tsd

@@ -1,0 +1,740 @@
+#!/usr/bin/env python3
+"""Benchmark of the multi-head scaled dot-product attention hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+for the multi-head workloads that is mha_forward (Q/K/V projections, masked
+attention per head, output projection); for the attention-only workloads it
+is attn_forward. The metric is attention TFLOP/s counted as
+4*B*h*n_q*n_k*d_k (halved for causal) per attention call, over the step time.
+
+Timing: W untimed warm-up steps, then exactly K steps between two CUDA
+events on the launching stream, bracketed by a barrier and a device
+synchronize; rotating input sets whose total exceeds L2 keep the working set
+out of cache; nvidia-smi samples the clocks during the timed region. The
+dominant kernel's duration is measured in a second event-timed loop where
+each kernel is launched through its own entry point, and is compared with
+its roofline (MEASURED_PEAKS.json). The CPU baseline is the fp64 oracle on a
+bounded sample of the same workload. `--impl reference` times that oracle as
+the reference arm.
+
+Multi-GPU: the path has no exchange step; N ranks run N independent replicas
+(one GPU each, weak scaling) and only the timing is reduced.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+from synthetic import MASK_CAUSAL, MASK_KEY_PADDING, MASK_NONE  # noqa: E402
+
+METRIC = "attention TFLOP/s (bf16) and % of dense BF16 peak / % of HBM BW, 1 GB300"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# --------------------------------------------------------------------------- workloads
+
+WORKLOADS = {
+    "base_encoder_mha": dict(
+        kind="mha", calls=[dict(B=32, n_q=128, n_k=128, d_model=512, h=8, d=64,
+                                mask=MASK_KEY_PADDING, kv_range=(64, 128), add_pe=True,
+                                self_attention=True, seed=1001)],
+        desc="Transformer-base encoder self-attention MHA: B=32, n=128, d_model=512, h=8, "
+             "d_k=d_v=64, key padding kv_len~U[64,128], x~N(0,1)+PE, Xavier-uniform W"),
+    "base_decoder_mha": dict(
+        kind="mha", calls=[
+            dict(B=32, n_q=128, n_k=128, d_model=512, h=8, d=64, mask=MASK_CAUSAL | MASK_KEY_PADDING,
+                 kv_range=(64, 128), add_pe=False, self_attention=True, seed=1002),
+            dict(B=32, n_q=128, n_k=160, d_model=512, h=8, d=64, mask=MASK_KEY_PADDING,
+                 kv_range=(80, 160), add_pe=False, self_attention=False, seed=1012)],
+        desc="Transformer-base decoder: masked self-attention MHA (n=128, causal + target "
+             "padding U[64,128]) then cross-attention MHA (n_q=128, n_k=160, source padding "
+             "U[80,160]); d_model=512, h=8, d_k=64, B=32, N(0,1) activations"),
+    "big_self": dict(kind="attn", B=8, h=16, n=1024, d=64, causal=False, seed=1003,
+                     desc="Transformer-big self-attention: B=8, h=16, n=1024, d_k=d_v=64"),
+    "big_self_causal": dict(kind="attn", B=8, h=16, n=1024, d=64, causal=True, seed=1003,
+                            desc="Transformer-big causal self-attention: B=8, h=16, n=1024, d=64"),
+    "long": dict(kind="attn", B=4, h=16, n=4096, d=64, causal=False, seed=1004,
+                 desc="long-context attention sweep point"),
+}
+
+
+def attn_flops(B, h, n_q, n_k, d, causal):
+    f = 4.0 * B * h * n_q * n_k * d
+    return f / 2 if causal else f
+
+
+# --------------------------------------------------------------------------- helpers
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+KERNEL_SOURCES = {
+    "attn_fwd_bf16": "transformer_scaled_dot_gb300/csrc/attn_bf16.cu",
+    "gemm_bf16": "transformer_scaled_dot_gb300/csrc/gemm_bf16.cu",
+}
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, or None when there is
+    none for this kernel and workload, or the kernel source changed since."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir) or kernel not in KERNEL_SOURCES:
+        return None
+    sha = source_sha(KERNEL_SOURCES[kernel])
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith((".txt", ".md")):
+            continue
+        fields = {}
+        with open(os.path.join(pdir, fn), encoding="utf-8") as f:
+            for line in f:
+                if ":" in line and line.strip().startswith(("kernel", "workload", "source_sha256",
+                                                            "dram_bytes_per_launch")):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if (fields.get("kernel") == kernel and fields.get("workload") == workload
+                and fields.get("source_sha256") == sha and "dram_bytes_per_launch" in fields):
+            try:
+                return float(fields["dram_bytes_per_launch"])
+            except ValueError:
+                return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid.lower()
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5:  # wait for the first sample
+            time.sleep(0.01)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t_start, t_end):
+        rows = []
+        gpus = set()
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            gpus.add(parts[0].lower())
+            rows.append((t, parts))
+        if self.uuid and any(g.endswith(self.uuid) for g in gpus):
+            rows = [r for r in rows if r[1][0].lower().endswith(self.uuid)]
+        elif len(gpus) > 1:
+            rows = []
+        inside = [r for r in rows if t_start <= r[0] <= t_end]
+        if not inside and rows:  # region shorter than the sampling period: nearest samples
+            inside = sorted(rows, key=lambda r: min(abs(r[0] - t_start), abs(r[0] - t_end)))[:2]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(p[1]) for _, p in inside if p[1].replace(".", "").isdigit()]
+        smax = [float(p[2]) for _, p in inside if p[2].replace(".", "").isdigit()]
+        reasons = set()
+        for _, p in inside:
+            for name, val in zip(self.REASONS, p[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        pw = [float(p[3]) for _, p in inside if p[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(inside),
+                "power_w_max": max(pw) if pw else None}
+
+
+# --------------------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local = _env_int("LOCAL_RANK", 0)
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("TSD_BENCH_BACKEND", "nccl")
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(x: float, world: int) -> float:
+    """Maximum of a per-rank scalar over all ranks (host logic; any backend)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_sum(x: float, world: int) -> float:
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+class MhaCall:
+    """Device buffers of one mha_forward call, replicated over rotating sets."""
+
+    def __init__(self, tsd, cfg, nsets, seed_offset):
+        import torch
+        self.tsd, self.cfg = tsd, cfg
+        c = cfg
+        self.m = synthetic.mha_inputs(c["seed"] + seed_offset, c["B"], c["n_q"], c["n_k"],
+                                      c["d_model"], c["h"], c["d"], c["d"], c["mask"],
+                                      c["kv_range"], add_pe=c["add_pe"],
+                                      self_attention=c["self_attention"])
+        m = self.m
+        dev = "cuda"
+        bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        host = [m.x_q] + ([] if m.self_attention else [m.x_kv]) + [m.w_q, m.w_k, m.w_v, m.w_o]
+        self.wsb = tsd.mha_workspace_bytes(m.B, m.n_q, m.n_k, m.h, m.d_k, m.d_v)
+        self.sets = []
+        for _ in range(nsets):
+            t = [bf(a) for a in host]
+            x_q = t[0]
+            x_kv = x_q if m.self_attention else t[1]
+            w = t[-4:]
+            s = dict(x_q=x_q, x_kv=x_kv, w=w,
+                     lens=torch.from_numpy(m.kv_lens).to(dev) if m.kv_lens is not None else None,
+                     out=torch.empty((m.B, m.n_q, m.d_model), dtype=torch.bfloat16, device=dev),
+                     ws=torch.empty(self.wsb, dtype=torch.uint8, device=dev))
+            self.sets.append(s)
+        hdk, hdv = m.h * m.d_k, m.h * m.d_v
+        # workspace regions (the layout mha_workspace_bytes describes)
+        al = lambda x: (x + 255) // 256 * 256
+        self.q_off = 0
+        self.k_off = al(m.B * m.n_q * hdk * 2)
+        self.v_off = self.k_off + al(m.B * m.n_k * hdk * 2)
+        self.o_off = self.v_off + al(m.B * m.n_k * hdv * 2)
+        # host copies for the end-to-end leg (pinned)
+        self.h_x_q = torch.from_numpy(np.ascontiguousarray(m.x_q).view(np.int16)).pin_memory()
+        self.h_x_kv = None if m.self_attention else \
+            torch.from_numpy(np.ascontiguousarray(m.x_kv).view(np.int16)).pin_memory()
+        self.h_lens = torch.from_numpy(m.kv_lens).pin_memory() if m.kv_lens is not None else None
+        self.h_out = torch.empty((m.B, m.n_q, m.d_model), dtype=torch.bfloat16).pin_memory()
+
+    def bytes_per_set(self):
+        m = self.m
+        n = m.x_q.nbytes + (0 if m.self_attention else m.x_kv.nbytes)
+        n += m.w_q.nbytes + m.w_k.nbytes + m.w_v.nbytes + m.w_o.nbytes
+        return n + self.wsb + m.B * m.n_q * m.d_model * 2
+
+    def run(self, i, stream):
+        m, s = self.m, self.sets[i % len(self.sets)]
+        self.tsd.mha_forward(s["x_q"], s["x_kv"], *s["w"], s["out"], m.B, m.n_q, m.n_k, m.d_model,
+                             m.h, m.d_k, m.d_v, m.mask_kind, s["lens"], 0.0, s["ws"], self.wsb,
+                             stream)
+
+    def run_stages(self, i, stream, events):
+        """The same three launches through their own entry points, an event after each."""
+        m, s = self.m, self.sets[i % len(self.sets)]
+        base = s["ws"].data_ptr()
+        Q, K, V, O = base + self.q_off, base + self.k_off, base + self.v_off, base + self.o_off
+        hdk, hdv = m.h * m.d_k, m.h * m.d_v
+        self.tsd.mha_project_qkv(s["x_q"], s["x_kv"], *s["w"][:3], Q, K, V, m.B, m.n_q, m.n_k,
+                                 m.d_model, m.h, m.d_k, m.d_v, stream)
+        events[0].record(stream)
+        self.tsd.attn_forward_strided(Q, m.n_q * hdk, m.d_k, hdk, K, m.n_k * hdk, m.d_k, hdk,
+                                      V, m.n_k * hdv, m.d_v, hdv, O, m.n_q * hdv, m.d_v, hdv,
+                                      m.B, m.h, m.n_q, m.n_k, m.d_k, m.d_v, m.mask_kind,
+                                      s["lens"], 0.0, stream)
+        events[1].record(stream)
+        self.tsd.mha_project_out(O, s["w"][3], s["out"], m.B, m.n_q, m.d_model, m.h, m.d_v, stream)
+        events[2].record(stream)
+
+    def stage_names(self):
+        return ["gemm_bf16", "attn_fwd_bf16", "gemm_bf16"]
+
+    def stage_work(self):
+        """(algorithmic flops, algorithmic bytes) of each stage launch."""
+        m = self.m
+        dm, hdk, hdv = m.d_model, m.h * m.d_k, m.h * m.d_v
+        Mq, Mk = m.B * m.n_q, m.B * m.n_k
+        qkv_f = 2.0 * dm * (Mq * hdk + Mk * hdk + Mk * hdv)
+        qkv_b = 2.0 * (Mq * dm + (0 if m.self_attention else Mk * dm) + dm * (2 * hdk + hdv)
+                       + Mq * hdk + Mk * (hdk + hdv))
+        kv = self.kv_effective()
+        causal = bool(m.mask_kind & MASK_CAUSAL)
+        att_f = attn_flops(m.B, m.h, m.n_q, m.n_k, m.d_k, causal)
+        att_b = 2.0 * m.h * sum(m.n_q * m.d_k + kv[b] * (m.d_k + m.d_v) + m.n_q * m.d_v
+                                for b in range(m.B))
+        out_f = 2.0 * Mq * hdv * dm
+        out_b = 2.0 * (Mq * hdv + hdv * dm + Mq * dm)
+        return [(qkv_f, qkv_b), (att_f, att_b), (out_f, out_b)]
+
+    def kv_effective(self):
+        m = self.m
+        if m.kv_lens is None:
+            return [m.n_k] * m.B
+        return [int(min(max(x, 0), m.n_k)) for x in m.kv_lens]
+
+    def metric_flops(self):
+        m = self.m
+        return attn_flops(m.B, m.h, m.n_q, m.n_k, m.d_k, bool(m.mask_kind & MASK_CAUSAL))
+
+    def launches(self):
+        return 3
+
+    def e2e_run(self, i, stream):
+        """Host inputs -> device, mha_forward, result -> host (pinned buffers)."""
+        m, s = self.m, self.sets[i % len(self.sets)]
+        s["x_q"].view(torch_int16()).copy_(self.h_x_q, non_blocking=True)
+        if self.h_x_kv is not None:
+            s["x_kv"].view(torch_int16()).copy_(self.h_x_kv, non_blocking=True)
+        if self.h_lens is not None:
+            s["lens"].copy_(self.h_lens, non_blocking=True)
+        self.run(i, stream)
+        self.h_out.copy_(s["out"], non_blocking=True)
+
+    def e2e_bytes(self):
+        m = self.m
+        h2d = m.x_q.nbytes + (0 if m.self_attention else m.x_kv.nbytes)
+        h2d += 0 if m.kv_lens is None else m.kv_lens.nbytes
+        return h2d, m.B * m.n_q * m.d_model * 2
+
+
+class AttnCall:
+    """Device buffers of one attn_forward call over rotating sets."""
+
+    def __init__(self, tsd, cfg, nsets, seed_offset):
+        import torch
+        self.tsd, self.cfg = tsd, cfg
+        c = cfg
+        mask = MASK_CAUSAL if c["causal"] else MASK_NONE
+        self.a = synthetic.attention_inputs(c["seed"] + seed_offset, c["B"], c["h"], c["n"], c["n"],
+                                            c["d"], c["d"], mask)
+        a = self.a
+        bf = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to("cuda").view(torch.bfloat16)
+        self.sets = []
+        for i in range(nsets):
+            q, k, v = (bf(x) for x in (a.q, a.k, a.v))
+            self.sets.append(dict(q=q, k=k, v=v, out=torch.empty_like(q)))
+        self.h_qkv = [torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory()
+                      for x in (a.q, a.k, a.v)]
+        self.h_out = torch.empty(a.q.shape, dtype=torch.bfloat16).pin_memory()
+
+    def bytes_per_set(self):
+        return 4 * self.a.q.nbytes
+
+    def run(self, i, stream):
+        a, s = self.a, self.sets[i % len(self.sets)]
+        self.tsd.attn_forward(s["q"], s["k"], s["v"], s["out"], a.B, a.h, a.n_q, a.n_k, a.d_k,
+                              a.d_v, a.mask_kind, None, 0.0, stream)
+
+    def run_stages(self, i, stream, events):
+        self.run(i, stream)
+        events[0].record(stream)
+
+    def stage_names(self):
+        return ["attn_fwd_bf16"]
+
+    def stage_work(self):
+        a = self.a
+        f = attn_flops(a.B, a.h, a.n_q, a.n_k, a.d_k, bool(a.mask_kind & MASK_CAUSAL))
+        b = 2.0 * a.B * a.h * (a.n_q * a.d_k + a.n_k * (a.d_k + a.d_v) + a.n_q * a.d_v)
+        return [(f, b)]
+
+    def metric_flops(self):
+        return self.stage_work()[0][0]
+
+    def launches(self):
+        return 1
+
+    def e2e_run(self, i, stream):
+        s = self.sets[i % len(self.sets)]
+        for dst, src in zip((s["q"], s["k"], s["v"]), self.h_qkv):
+            dst.view(torch_int16()).copy_(src, non_blocking=True)
+        self.run(i, stream)
+        self.h_out.copy_(s["out"], non_blocking=True)
+
+    def e2e_bytes(self):
+        return 3 * self.a.q.nbytes, self.a.q.nbytes
+
+
+def torch_int16():
+    import torch
+    return torch.int16
+
+
+def make_calls(tsd, wl, args, seed_offset):
+    spec = WORKLOADS[wl]
+    if spec["kind"] == "mha":
+        cfgs = spec["calls"]
+        probe = [MhaCall(tsd, c, 1, seed_offset) for c in cfgs]
+        per_set = sum(p.bytes_per_set() for p in probe)
+        nsets = max(2, math.ceil(2.2 * L2_BYTES / per_set))
+        return [MhaCall(tsd, c, nsets, seed_offset) for c in cfgs], nsets, per_set
+    cfg = dict(spec)
+    for k in ("B", "n", "d"):
+        if getattr(args, k, None):
+            cfg[k] = getattr(args, k)
+    if args.causal is not None:
+        cfg["causal"] = bool(args.causal)
+    per_set = 4 * cfg["B"] * cfg["h"] * cfg["n"] * cfg["d"] * 2
+    nsets = max(2, math.ceil(2.2 * L2_BYTES / per_set))
+    return [AttnCall(tsd, cfg, nsets, seed_offset)], nsets, per_set
+
+
+def workload_config(wl, calls, args, nsets, per_set):
+    spec = WORKLOADS[wl]
+    cfg = {"workload": wl, "description": spec["desc"]}
+    if spec["kind"] == "mha":
+        cfg["calls"] = [{k: v for k, v in c.cfg.items() if k not in ("seed",)} for c in calls]
+        for c in cfg["calls"]:
+            c["mask"] = {0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding"}[c["mask"]]
+            c["kv_range"] = list(c["kv_range"]) if c["kv_range"] else None
+    else:
+        a = calls[0].a
+        cfg.update(B=a.B, h=a.h, n=a.n_q, d=a.d_k, causal=bool(a.mask_kind & MASK_CAUSAL))
+    cfg["l2"] = f"{nsets} rotating input sets of {per_set / 2**20:.1f} MiB (total > L2)"
+    return cfg
+
+
+def run_gpu_arm(args, world, rank, local):
+    import torch
+    import transformer_scaled_dot_gb300 as tsd
+    from transformer_scaled_dot_gb300 import build as native_build
+
+    if rank == 0 and native_build.is_stale():
+        native_build.build()
+    dist_barrier(world)
+    tsd.library()
+    torch.cuda.set_device(local)
+    stream = torch.cuda.current_stream()
+    calls, nsets, per_set = make_calls(tsd, args.workload, args, seed_offset=rank)
+    peaks, peak_src = load_peaks()
+
+    def step(i):
+        for c in calls:
+            c.run(i, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if tsd.attn_get_device_status() != tsd.ATTN_OK:
+        raise RuntimeError("device error during warm-up")
+
+    # ---------------------------------------------------------------- timed region
+    props = torch.cuda.get_device_properties(local)
+    sampler = ClockSampler(str(getattr(props, "uuid", "") or ""))
+    sampler.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    t_start = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    dist_barrier(world)
+    sampler.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    ms_total_max = dist_max(ms_total, world)
+    ms_per_step = ms_total_max / args.steps
+    if tsd.attn_get_device_status() != tsd.ATTN_OK:
+        raise RuntimeError("device error during the timed region")
+    clocks = sampler.summary(t_start, t_end)
+
+    flops_step = sum(c.metric_flops() for c in calls)
+    total_flops = dist_sum(flops_step * args.steps, world)
+    value = total_flops / (ms_total_max * 1e-3) / 1e12
+
+    # ---------------------------------------------------------------- per-kernel loop
+    n_iter = max(args.steps, 20)
+    per_kernel = {}
+    rec = []
+    for it in range(n_iter + 2):
+        evs = []
+        for c in calls:
+            st = torch.cuda.Event(enable_timing=True)
+            st.record(stream)
+            e = [torch.cuda.Event(enable_timing=True) for _ in c.stage_names()]
+            c.run_stages(it, stream, e)
+            evs.append((c, st, e))
+        if it >= 2:
+            rec.append(evs)
+    torch.cuda.synchronize()
+    for evs in rec:
+        for c, st, e in evs:
+            prev = st
+            for name, work, ev in zip(c.stage_names(), c.stage_work(), e):
+                d = per_kernel.setdefault(name, {"ms": 0.0, "launches": 0, "flops": 0.0, "bytes": 0.0})
+                d["ms"] += prev.elapsed_time(ev)
+                d["launches"] += 1
+                d["flops"] += work[0]
+                d["bytes"] += work[1]
+                prev = ev
+    dominant = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
+    d = per_kernel[dominant]
+    avg_ms = d["ms"] / d["launches"]
+    f_per, b_per = d["flops"] / d["launches"], d["bytes"] / d["launches"]
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if f_per / max(b_per, 1.0) >= ridge:
+        achieved = f_per / (avg_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        achieved = b_per / (avg_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = round(achieved / roof["peak"], 4)
+    tr = profiled_traffic(dominant, args.workload)
+    roof["traffic"] = tr
+    roof["kernel"] = dominant
+    roof["kernel_ms"] = round(avg_ms, 5)
+    roof["algorithmic"] = {"flops": f_per, "bytes": b_per}
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" \
+        else "fallback"
+    kernel_table = {k: {"ms_per_launch": round(v["ms"] / v["launches"], 5),
+                        "share": round(v["ms"] / sum(x["ms"] for x in per_kernel.values()), 4),
+                        "tflops": round(v["flops"] / (v["ms"] * 1e-3) / 1e12, 2),
+                        "gbs": round(v["bytes"] / (v["ms"] * 1e-3) / 1e9, 1)}
+                    for k, v in per_kernel.items()}
+
+    # ---------------------------------------------------------------- end to end
+    e2e_iters = max(args.steps, 10)
+    for i in range(2):
+        for c in calls:
+            c.e2e_run(i, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier(world)
+    e0.record(stream)
+    for i in range(e2e_iters):
+        for c in calls:
+            c.e2e_run(i, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = dist_max(e0.elapsed_time(e1), world) / e2e_iters
+    h2d = sum(c.e2e_bytes()[0] for c in calls)
+    d2h = sum(c.e2e_bytes()[1] for c in calls)
+    e2e_value = dist_sum(flops_step * e2e_iters, world) / (e2e_ms * e2e_iters * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) / Xavier inputs of the workload's shapes)",
+        "config": dict(workload_config(args.workload, calls, args, nsets, per_set),
+                       parallelism=f"replicas x{world}" if world > 1 else "single GPU",
+                       launch="eager C-ABI calls on the current torch stream"),
+        "roofline": roof,
+        "kernels": kernel_table,
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 5)},
+        "clocks": clocks,
+        "gpu_launches": int(sum(c.launches() for c in calls) * args.steps),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args, calls, budget_s=args.cpu_seconds)
+    return line, rank
+
+
+# --------------------------------------------------------------------------- oracle (CPU)
+
+def oracle_sample_runner(args):
+    """A function running the oracle on a bounded sample of the workload, and
+    the metric FLOPs that sample represents."""
+    import oracle
+    spec = WORKLOADS[args.workload]
+    if spec["kind"] == "mha":
+        ms = []
+        for c in spec["calls"]:
+            m = synthetic.mha_inputs(c["seed"], c["B"], c["n_q"], c["n_k"], c["d_model"], c["h"],
+                                     c["d"], c["d"], c["mask"], c["kv_range"], add_pe=c["add_pe"],
+                                     self_attention=c["self_attention"])
+            ms.append((m, m.as_f64()))
+        flops = sum(attn_flops(m.B, m.h, m.n_q, m.n_k, m.d_k, bool(m.mask_kind & MASK_CAUSAL))
+                    for m, _ in ms)
+
+        def run():
+            for m, f64 in ms:
+                oracle.mha(*f64, m.h, m.mask_kind, kv_lens=m.kv_lens)
+        return run, flops, "the whole batch through oracle.mha (projections, attention, W_O)"
+    cfg = dict(spec)
+    for k in ("B", "n", "d"):
+        if getattr(args, k, None):
+            cfg[k] = getattr(args, k)
+    if args.causal is not None:
+        cfg["causal"] = bool(args.causal)
+    n, d, causal = cfg["n"], cfg["d"], cfg["causal"]
+    rng = np.random.default_rng(cfg["seed"])
+    # one head of the workload, a seeded subset of its query rows
+    q = synthetic.bf16_bits_to_f64(synthetic.normal_bf16(rng, (n, d)))
+    k = synthetic.bf16_bits_to_f64(synthetic.normal_bf16(rng, (n, d)))
+    v = synthetic.bf16_bits_to_f64(synthetic.normal_bf16(rng, (n, d)))
+    rows = np.sort(rng.choice(n, size=min(n, 256), replace=False)).astype(np.int32)
+    keys_seen = (rows + 1).sum() if causal else len(rows) * n
+    flops = 4.0 * keys_seen * d
+
+    def run():
+        oracle.attention_rows(q[rows], rows, k, v, causal=causal)
+    return run, flops, f"{len(rows)} query rows of one head (n={n}, d={d}) via oracle.attention_rows"
+
+
+def cpu_baseline(args, calls, budget_s=10.0):
+    import oracle
+    run, flops, what = oracle_sample_runner(args)
+    run()  # warm-up (also builds the oracle library)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        run()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 50:
+            break
+    tflops = flops * reps / el / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{what}; {reps} repetitions in {el:.1f} s"}
+
+
+def run_reference_arm(args, world, rank):
+    if rank != 0:
+        return None, rank
+    import oracle
+    run, flops, what = oracle_sample_runner(args)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    el = time.perf_counter() - t0
+    value = flops * args.steps / el / 1e12
+    cfg = {"workload": args.workload, "description": WORKLOADS[args.workload]["desc"]}
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": what},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    return line, rank
+
+
+# --------------------------------------------------------------------------- main
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="base_encoder_mha")
+    ap.add_argument("--B", type=int, default=None)
+    ap.add_argument("--n", type=int, default=None)
+    ap.add_argument("--d", type=int, default=None, choices=[64, 128])
+    ap.add_argument("--causal", type=int, default=None, choices=[0, 1])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3  # timing rule: at least 3 warm-up steps
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        line, rank = run_reference_arm(args, world, rank)
+    else:
+        line, rank = run_gpu_arm(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -142,6 +142,29 @@ attn_status mha_forward(const void *x_q, const void *x_kv,
                         void *workspace, size_t workspace_bytes, tsd_stream_t stream);
 
 /*
+ * mha_project_qkv -- the input projections of section 3.2.2, all positions at
+ * once, in one launch:
+ *   q_out = x_q W_Q  [B, n_q, h*d_k],  k_out = x_kv W_K  [B, n_k, h*d_k],
+ *   v_out = x_kv W_V [B, n_k, h*d_v]   (bf16, fp32 accumulation)
+ * Head i of each result is its column block i, so the outputs feed
+ * attn_forward_strided directly. Shapes, alignment and errors as mha_forward
+ * (every pointer device, 16-byte aligned; d_model a multiple of 8).
+ */
+attn_status mha_project_qkv(const void *x_q, const void *x_kv,
+                            const void *w_q, const void *w_k, const void *w_v,
+                            void *q_out, void *k_out, void *v_out,
+                            int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
+                            tsd_stream_t stream);
+
+/*
+ * mha_project_out -- the output projection of section 3.2.2:
+ *   out [B, n_q, d_model] = Concat(head_1..head_h) [B, n_q, h*d_v] . W_O [h*d_v, d_model]
+ * (bf16, fp32 accumulation). Errors as mha_forward.
+ */
+attn_status mha_project_out(const void *concat, const void *w_o, void *out,
+                            int B, int n_q, int d_model, int h, int d_v, tsd_stream_t stream);
+
+/*
  * attn_get_device_status -- synchronises `stream`, then reads and clears the
  * device error word the kernels set when a bounded wait runs out.
  * Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT, or ATTN_ERR_CUDA if the

@@ -22,7 +22,7 @@ __all__ = [
     "AttnError", "library", "library_path", "EXPORTED_SYMBOLS",
     "attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_workspace_bytes",
     "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
-    "attn_selftest_wait_timeout",
+    "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = range(5)
@@ -31,7 +31,7 @@ ATTN_MASK_NONE, ATTN_MASK_CAUSAL, ATTN_MASK_KEY_PADDING = 0, 1, 2
 EXPORTED_SYMBOLS = (
     "attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_workspace_bytes",
     "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
-    "attn_selftest_wait_timeout",
+    "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out",
 )
 
 _lib = None
@@ -70,13 +70,16 @@ def library():
     lib.mha_workspace_bytes.restype = ctypes.c_size_t
     lib.mha_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, f, vp,
                                 ctypes.c_size_t, st]
+    lib.mha_project_qkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, st]
+    lib.mha_project_out.argtypes = [vp, vp, vp, i, i, i, i, i, st]
     lib.attn_get_device_status.argtypes = [st]
     lib.attn_last_cuda_error.argtypes = []
     lib.attn_status_string.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_selftest_wait_timeout.argtypes = [i, st]
     for name in ("attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_forward",
-                 "attn_get_device_status", "attn_last_cuda_error", "attn_selftest_wait_timeout"):
+                 "attn_get_device_status", "attn_last_cuda_error", "attn_selftest_wait_timeout",
+                 "mha_project_qkv", "mha_project_out"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -137,6 +140,18 @@ def mha_forward(x_q, x_kv, w_q, w_k, w_v, w_o, out, B, n_q, n_k, d_model, h, d_k
                                  _ptr(w_o), _ptr(out), B, n_q, n_k, d_model, h, d_k, d_v,
                                  mask_kind, _ptr(kv_lens), scale, _ptr(workspace),
                                  workspace_bytes, _stream(stream)), "mha_forward")
+
+
+def mha_project_qkv(x_q, x_kv, w_q, w_k, w_v, q_out, k_out, v_out, B, n_q, n_k, d_model, h, d_k,
+                    d_v, stream=None):
+    _check(library().mha_project_qkv(_ptr(x_q), _ptr(x_kv), _ptr(w_q), _ptr(w_k), _ptr(w_v),
+                                     _ptr(q_out), _ptr(k_out), _ptr(v_out), B, n_q, n_k, d_model,
+                                     h, d_k, d_v, _stream(stream)), "mha_project_qkv")
+
+
+def mha_project_out(concat, w_o, out, B, n_q, d_model, h, d_v, stream=None):
+    _check(library().mha_project_out(_ptr(concat), _ptr(w_o), _ptr(out), B, n_q, d_model, h, d_v,
+                                     _stream(stream)), "mha_project_out")
 
 
 def attn_get_device_status(stream=None) -> int:

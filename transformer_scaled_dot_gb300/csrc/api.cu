@@ -180,6 +180,54 @@ void finish_gemm_problem(tsd::GemmProblem* p) {
   p->total_tiles = t;
 }
 
+
+// Checks shared by the projection entry points.
+attn_status check_projection(int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v) {
+  if (B < 0 || n_q < 0 || n_k < 0 || h <= 0 || d_k <= 0 || d_v <= 0) return ATTN_ERR_INVALID;
+  if (d_model < 8 || (d_model % 8) != 0) return ATTN_ERR_INVALID;
+  if ((int64_t(h) * d_k) % 8 != 0 || (int64_t(h) * d_v) % 8 != 0) return ATTN_ERR_INVALID;
+  if (int64_t(B) * n_q > INT32_MAX || int64_t(B) * n_k > INT32_MAX) return ATTN_ERR_INVALID;
+  if (int64_t(h) * d_k > INT32_MAX || int64_t(h) * d_v > INT32_MAX) return ATTN_ERR_INVALID;
+  return ATTN_OK;
+}
+
+attn_status launch_qkv(const void* x_q, const void* x_kv, const void* w_q, const void* w_k,
+                       const void* w_v, void* Q, void* K, void* V, int B, int n_q, int n_k,
+                       int d_model, int h, int d_k, int d_v, cudaStream_t stream) {
+  const int Mq = B * n_q, Mk = B * n_k;
+  tsd::GemmProblem g;
+  std::memset(&g, 0, sizeof(g));
+  g.K = d_model;
+  g.num_groups = 0;
+  cudaError_t e = cudaSuccess;
+  if (Mq > 0) e = make_gemm_group(&g.g[g.num_groups++], x_q, w_q, Q, Mq, h * d_k, d_model);
+  if (e == cudaSuccess && Mk > 0) {
+    e = make_gemm_group(&g.g[g.num_groups++], x_kv, w_k, K, Mk, h * d_k, d_model);
+    if (e == cudaSuccess)
+      e = make_gemm_group(&g.g[g.num_groups++], x_kv, w_v, V, Mk, h * d_v, d_model);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (g.num_groups == 0) return ATTN_OK;
+  finish_gemm_problem(&g);
+  e = tsd::launch_gemm_bf16(g, stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+attn_status launch_out_proj(const void* concat, const void* w_o, void* out, int B, int n_q,
+                            int d_model, int h, int d_v, cudaStream_t stream) {
+  const int Mq = B * n_q;
+  if (Mq == 0) return ATTN_OK;
+  tsd::GemmProblem g;
+  std::memset(&g, 0, sizeof(g));
+  g.K = h * d_v;
+  g.num_groups = 1;
+  cudaError_t e = make_gemm_group(&g.g[0], concat, w_o, out, Mq, d_model, h * d_v);
+  if (e != cudaSuccess) return cuda_fail(e);
+  finish_gemm_problem(&g);
+  e = tsd::launch_gemm_bf16(g, stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -287,20 +335,8 @@ attn_status mha_forward(const void* x_q, const void* x_kv, const void* w_q, cons
   const int hdk = h * d_k, hdv = h * d_v;
 
   // 1. Q = X_q W_Q, K = X_kv W_K, V = X_kv W_V   (one grouped launch)
-  tsd::GemmProblem g1;
-  std::memset(&g1, 0, sizeof(g1));
-  g1.K = d_model;
-  g1.num_groups = 1;
-  cudaError_t e = make_gemm_group(&g1.g[0], x_q, w_q, Q, int(Mq), hdk, d_model);
-  if (e == cudaSuccess && Mk > 0) {
-    e = make_gemm_group(&g1.g[1], x_kv, w_k, K, int(Mk), hdk, d_model);
-    if (e == cudaSuccess) e = make_gemm_group(&g1.g[2], x_kv, w_v, V, int(Mk), hdv, d_model);
-    g1.num_groups = 3;
-  }
-  if (e != cudaSuccess) return cuda_fail(e);
-  finish_gemm_problem(&g1);
-  e = tsd::launch_gemm_bf16(g1, stream);
-  if (e != cudaSuccess) return cuda_fail(e);
+  s = launch_qkv(x_q, x_kv, w_q, w_k, w_v, Q, K, V, B, n_q, n_k, d_model, h, d_k, d_v, stream);
+  if (s != ATTN_OK) return s;
 
   // 2. head_i = Attention(Q_i, K_i, V_i): heads are column blocks of the
   //    [B, n, h*d] projections; the output is written merged, [B, n_q, h*d_v]
@@ -310,15 +346,30 @@ attn_status mha_forward(const void* x_q, const void* x_kv, const void* w_q, cons
   if (s != ATTN_OK) return s;
 
   // 3. out = Concat(head_1..head_h) W_O
-  tsd::GemmProblem g2;
-  std::memset(&g2, 0, sizeof(g2));
-  g2.K = hdv;
-  g2.num_groups = 1;
-  e = make_gemm_group(&g2.g[0], O, w_o, out, int(Mq), d_model, hdv);
-  if (e != cudaSuccess) return cuda_fail(e);
-  finish_gemm_problem(&g2);
-  e = tsd::launch_gemm_bf16(g2, stream);
-  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+  return launch_out_proj(O, w_o, out, B, n_q, d_model, h, d_v, stream);
+}
+
+attn_status mha_project_qkv(const void* x_q, const void* x_kv, const void* w_q, const void* w_k,
+                            const void* w_v, void* q_out, void* k_out, void* v_out, int B, int n_q,
+                            int n_k, int d_model, int h, int d_k, int d_v, tsd_stream_t stream) {
+  attn_status s = check_projection(B, n_q, n_k, d_model, h, d_k, d_v);
+  if (s != ATTN_OK) return s;
+  const void* ptrs[8] = {x_q, x_kv, w_q, w_k, w_v, q_out, k_out, v_out};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID;
+  return launch_qkv(x_q, x_kv, w_q, w_k, w_v, q_out, k_out, v_out, B, n_q, n_k, d_model, h, d_k,
+                    d_v, reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status mha_project_out(const void* concat, const void* w_o, void* out, int B, int n_q,
+                            int d_model, int h, int d_v, tsd_stream_t stream) {
+  attn_status s = check_projection(B, n_q, 0, d_model, h, d_v, d_v);
+  if (s != ATTN_OK) return s;
+  const void* ptrs[3] = {concat, w_o, out};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID;
+  return launch_out_proj(concat, w_o, out, B, n_q, d_model, h, d_v,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 attn_status attn_get_device_status(tsd_stream_t stream) {

@@ -165,6 +165,45 @@ attn_status mha_project_out(const void *concat, const void *w_o, void *out,
                             int B, int n_q, int d_model, int h, int d_v, tsd_stream_t stream);
 
 /*
+ * mha_forward_noalloc -- mha_forward for callers that cannot allocate device
+ * memory. The pages have no counterpart: this is a deployment variant.
+ *
+ * Who needs it: a plugin whose host application owns the device-memory budget
+ * and forbids allocation inside the plugin; a serving loop whose memory is
+ * planned up front and must not call cudaMalloc/cudaFree on the request path
+ * (they synchronise the device and stall other streams); a plain C caller
+ * with no access to its framework's caching allocator. Such callers cannot
+ * provide mha_forward's workspace, so this entry point uses a fixed
+ * file-scope device array of TSD_MHA_NOALLOC_SCRATCH_BYTES instead and calls
+ * no cudaMalloc, cudaFree or other allocating routine. The caller still
+ * passes every input and output.
+ *
+ *   Arguments, layouts and errors as mha_forward, without the workspace.
+ *   mha_workspace_bytes(B, n_q, n_k, h, d_k, d_v) must not exceed
+ *   TSD_MHA_NOALLOC_SCRATCH_BYTES, else ATTN_ERR_UNSUPPORTED (before any
+ *   CUDA call).
+ *
+ * The array belongs to the library's device image: every GPU that loads the
+ * library holds it until the process exits. The first call on a device, with
+ * that device current, looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture. A failed look-up returns ATTN_ERR_CUDA.
+ *
+ * All calls on a device share the one array, which keeps the last call's
+ * contents; calls that overlap on the GPU (other streams or host threads
+ * without ordering between them) race on it. No clearing is needed between
+ * calls: every byte a call reads from the array is written by that call.
+ */
+#define TSD_MHA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+attn_status mha_forward_noalloc(const void *x_q, const void *x_kv,
+                                const void *w_q, const void *w_k, const void *w_v,
+                                const void *w_o, void *out,
+                                int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
+                                int mask_kind, const int32_t *kv_lens, float scale,
+                                tsd_stream_t stream);
+
+/*
  * attn_get_device_status -- synchronises `stream`, then reads and clears the
  * device error word the kernels set when a bounded wait runs out.
  * Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT, or ATTN_ERR_CUDA if the

@@ -22,7 +22,8 @@ __all__ = [
     "AttnError", "library", "library_path", "EXPORTED_SYMBOLS",
     "attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_workspace_bytes",
     "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
-    "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out",
+    "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out", "mha_forward_noalloc",
+    "MHA_NOALLOC_SCRATCH_BYTES",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = range(5)
@@ -31,8 +32,11 @@ ATTN_MASK_NONE, ATTN_MASK_CAUSAL, ATTN_MASK_KEY_PADDING = 0, 1, 2
 EXPORTED_SYMBOLS = (
     "attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_workspace_bytes",
     "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
-    "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out",
+    "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out", "mha_forward_noalloc",
 )
+
+# TSD_MHA_NOALLOC_SCRATCH_BYTES of the header: the fixed scratch of mha_forward_noalloc
+MHA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 _lib = None
 
@@ -72,6 +76,8 @@ def library():
                                 ctypes.c_size_t, st]
     lib.mha_project_qkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, st]
     lib.mha_project_out.argtypes = [vp, vp, vp, i, i, i, i, i, st]
+    lib.mha_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, f,
+                                        st]
     lib.attn_get_device_status.argtypes = [st]
     lib.attn_last_cuda_error.argtypes = []
     lib.attn_status_string.argtypes = [i]
@@ -79,7 +85,7 @@ def library():
     lib.attn_selftest_wait_timeout.argtypes = [i, st]
     for name in ("attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_forward",
                  "attn_get_device_status", "attn_last_cuda_error", "attn_selftest_wait_timeout",
-                 "mha_project_qkv", "mha_project_out"):
+                 "mha_project_qkv", "mha_project_out", "mha_forward_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -152,6 +158,16 @@ def mha_project_qkv(x_q, x_kv, w_q, w_k, w_v, q_out, k_out, v_out, B, n_q, n_k, 
 def mha_project_out(concat, w_o, out, B, n_q, d_model, h, d_v, stream=None):
     _check(library().mha_project_out(_ptr(concat), _ptr(w_o), _ptr(out), B, n_q, d_model, h, d_v,
                                      _stream(stream)), "mha_project_out")
+
+
+def mha_forward_noalloc(x_q, x_kv, w_q, w_k, w_v, w_o, out, B, n_q, n_k, d_model, h, d_k, d_v,
+                        mask_kind=ATTN_MASK_NONE, kv_lens=None, scale=0.0, stream=None):
+    """mha_forward on the library's fixed device scratch (no workspace argument;
+    for callers that cannot allocate device memory)."""
+    _check(library().mha_forward_noalloc(_ptr(x_q), _ptr(x_kv), _ptr(w_q), _ptr(w_k), _ptr(w_v),
+                                         _ptr(w_o), _ptr(out), B, n_q, n_k, d_model, h, d_k, d_v,
+                                         mask_kind, _ptr(kv_lens), scale, _stream(stream)),
+           "mha_forward_noalloc")
 
 
 def attn_get_device_status(stream=None) -> int:

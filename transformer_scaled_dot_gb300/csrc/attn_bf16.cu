@@ -3,23 +3,28 @@
 // (kimjiil.github.io), section 3.2.1, eq. (1)).
 //
 // One CTA owns NQT query tiles of 128 rows of one (batch, head) and streams
-// that head's key/value tiles (128 keys each) through a shared-memory ring:
+// that head's key/value tiles (128 keys each) through two shared-memory rings:
 //
 //   warp 0      TMA producer: Q tiles once, then K_0, K_1, V_0, K_2, V_1, ...
-//   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T into tensor memory,
-//               O_t += P_t V_j into tensor memory; owns the TMEM allocation
+//   warp 1      S issuer (one thread): S_t = Q_t K_j^T into tensor memory;
+//               owns the TMEM allocation
+//   warp 2      PV issuer (one thread): O_t += P_t V_j into tensor memory
 //   warps 4..7  softmax for query tile 0; warps 8..11 for query tile 1:
 //               one thread per query row (= one TMEM lane)
 //
-// The n_q x n_k weight matrix never leaves the chip: S lives in TMEM, P in
-// shared memory, one 128x128 tile at a time, with the online (running max and
-// running sum) form of the row softmax in fp32. Scores are turned into
-// base-2 exponents with the folded factor scale*log2(e); the max is
-// subtracted before the exponential, as the pages' reference run does
+// Two issuing threads keep the tensor pipe fed: each thread's barrier waits
+// and commits (tcgen05.commit tracks only the issuing thread's MMAs) overlap
+// the other thread's MMA issue.
+//
+// The n_q x n_k weight matrix never leaves the chip: S lives in TMEM, P (bf16)
+// in TMEM as the A operand of the PV MMA, one 128x128 tile at a time, with the
+// online (running max and running sum) form of the row softmax in fp32.
+// Scores become base-2 exponents with the folded factor scale*log2(e); the max
+// is subtracted before the exponential, as the pages' reference run does
 // ("Attention Is All You Need 해부" (sj-techlog), section "직접 검증").
-// Masks: whole key tiles past the causal diagonal or past kv_len are never
-// loaded; inside the boundary tile the masked logits become -inf before the
-// max and the exponential, so their weight is exactly 0 (section 3.2.3).
+// Masks: key tiles past the causal diagonal or past kv_len are never loaded;
+// inside the boundary tile the masked logits become -inf before the max and
+// the exponential, so their weight is exactly 0 (section 3.2.3).
 // The running max is only raised when it grows by more than 2^8 (exponents
 // stay <= 256, exact in the final division), so the O rescale is rare.
 #include <cuda_bf16.h>
@@ -31,24 +36,50 @@ namespace tsd {
 
 namespace {
 
-constexpr int kRows = 128;   // query rows per tile (MMA M) and keys per tile
+constexpr int kRows = 128;                 // query rows per tile (MMA M) and keys per tile
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D, int NQT, int NSLOT>
+template <int D, int NQT>
+struct AttnShape {
+  static constexpr int kThreads = 128 + 128 * NQT;  // 4 control warps + softmax warpgroups
+  // P (bf16, 64 columns per query tile) gets its own TMEM columns unless S and
+  // O of two 128-wide tiles already fill all 512; then it overwrites the first
+  // half of its S tile, and S_t(j+1) waits for PV_t(j) to have read it.
+  static constexpr bool kPAliasS = (D == 128 && NQT == 2);
+  static constexpr int kColsUsed = NQT * kRows + NQT * D + (kPAliasS ? 0 : NQT * 64);
+  static constexpr int kTmemCols = kColsUsed <= 256 ? 256 : 512;
+  __host__ __device__ static constexpr int s_col(int t) { return t * kRows; }
+  __host__ __device__ static constexpr int o_col(int t) { return NQT * kRows + t * D; }
+  __host__ __device__ static constexpr int p_col(int t) {
+    return kPAliasS ? s_col(t) : NQT * kRows + NQT * D + t * 64;
+  }
+  // register split of the paired variants: control warps give up registers
+  // to the softmax warpgroups (sum <= threads x registers at launch)
+  static constexpr uint32_t kLaunchRegs = 65536 / kThreads / 8 * 8;
+  static constexpr uint32_t kCtrlRegs = D == 64 ? 72 : 88;
+  static constexpr uint32_t kSoftmaxRegs =
+      (kLaunchRegs * kThreads - kCtrlRegs * 128) / (128 * NQT) / 8 * 8;
+  static_assert(kColsUsed <= 512, "tensor memory budget");
+  // setmaxnreg.inc waits for registers released by .dec: the split must fit
+  // in what the CTA was launched with, or the increase would never complete
+  static_assert(kCtrlRegs * 128 + kSoftmaxRegs * 128 * NQT <= kLaunchRegs * kThreads,
+                "register split exceeds the launch allocation");
+};
+
+template <int D, int NQT, int NK, int NV>
 struct AttnSmem {
-  static constexpr int kTileBytes = kRows * D * 2;        // one Q, K or V tile
-  static constexpr int kPBytes = kRows * kRows * 2;       // one P tile
+  static constexpr int kTileBytes = kRows * D * 2;  // one Q, K or V tile
   alignas(1024) uint8_t q[NQT][kTileBytes];
-  alignas(1024) uint8_t kv[NSLOT][kTileBytes];
-  alignas(1024) uint8_t p[NQT][kPBytes];
+  alignas(1024) uint8_t k[NK][kTileBytes];
+  alignas(1024) uint8_t v[NV][kTileBytes];
   uint64_t q_full;
-  uint64_t kv_full[NSLOT];
-  uint64_t kv_empty[NSLOT];
+  uint64_t k_full[NK], k_empty[NK];
+  uint64_t v_full[NV], v_empty[NV];
   uint64_t s_full[NQT];
   uint64_t s_free[NQT];
   uint64_t p_full[NQT];
   uint64_t pv_done[NQT];
-  uint64_t mma_drained;
+  uint64_t s_drained, pv_drained;
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -62,20 +93,14 @@ struct AttnArgs {
   int64_t o_sb, o_sh, o_sr;
 };
 
-template <int D, int NQT>
-struct AttnShape {
-  static constexpr int kThreads = 128 + 128 * NQT;      // 4 control warps + softmax warpgroups
-  static constexpr int kTmemCols = NQT == 2 ? 512 : 256;
-  __host__ __device__ static constexpr int kSCol(int t) { return t * kRows; }
-  __host__ __device__ static constexpr int kOCol(int t) { return NQT * kRows + t * D; }
-};
+constexpr unsigned long long kDrainLimitNs = 100ull * 1000ull * 1000ull;  // 0.1 s
 
-template <int D, int NQT, int NSLOT>
+template <int D, int NQT, int NK, int NV>
 __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const AttnArgs args) {
-  using Smem = AttnSmem<D, NQT, NSLOT>;
+  using Smem = AttnSmem<D, NQT, NK, NV>;
   using Shape = AttnShape<D, NQT>;
   constexpr int kKAtoms = D / 64;  // 128-byte swizzle atoms along the head dimension
 
@@ -98,24 +123,30 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, 1)
     int len = args.kv_lens[b];
     kv_eff = len < 0 ? 0 : (len > args.n_k ? args.n_k : len);
   }
+  // key tiles each query tile visits (kept in scalars: a runtime-indexed
+  // array would live in local memory)
   const int nkt = (kv_eff + kRows - 1) / kRows;
-  int nt[NQT];
-  int nt_all = 0;
-#pragma unroll
-  for (int t = 0; t < NQT; ++t) {
+  auto tiles_for = [&](int t) {
     const int row0 = q0 + t * kRows;
     int n = nkt;
     if (causal) n = min(n, row0 / kRows + 1);
     if (row0 >= args.n_q) n = 0;
-    nt[t] = n;
-    nt_all = max(nt_all, n);
-  }
+    return n;
+  };
+  const int nt0 = tiles_for(0);
+  const int nt1 = NQT > 1 ? tiles_for(1) : 0;
+  auto nt = [&](int t) { return t == 0 ? nt0 : nt1; };
+  const int nt_all = max(nt0, nt1);
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
-    for (int s = 0; s < NSLOT; ++s) {
-      mbar_init(&sm.kv_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
     }
     for (int t = 0; t < NQT; ++t) {
       mbar_init(&sm.s_full[t], 1);
@@ -123,7 +154,8 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, 1)
       mbar_init(&sm.p_full[t], kRows);
       mbar_init(&sm.pv_done[t], 1);
     }
-    mbar_init(&sm.mma_drained, 1);
+    mbar_init(&sm.s_drained, 1);
+    mbar_init(&sm.pv_drained, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -137,148 +169,155 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile uint32_t* abort_flag = &sm.abort_flag;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && nt_all > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&sm.q_full, NQT * Smem::kTileBytes);
-      for (int t = 0; t < NQT; ++t)
-        for (int a = 0; a < kKAtoms; ++a)
-          tma_load_4d(sm.q[t] + a * 16384, &tm_q, &sm.q_full, a * 64, q0 + t * kRows, hh, b);
+  // Descriptors are built once; each MMA only adds a compile-time offset to
+  // the start-address field (addresses stay below 256 KB, so the 14-bit field
+  // never carries into the next one).
+  constexpr uint64_t kTileStep = Smem::kTileBytes >> 4;
+  constexpr uint32_t kIdescS = idesc_bf16(kRows, kRows, false, false);
+  constexpr uint32_t kIdescPV = idesc_bf16(kRows, D, false, true);
 
-      int L = 0;
-      bool ok = true;
-      auto issue = [&](const CUtensorMap* map, int row0) {
-        const int slot = L % NSLOT;
-        const uint32_t ph = static_cast<uint32_t>(L / NSLOT) & 1u;
-        if (!mbar_wait(&sm.kv_empty[slot], ph ^ 1u, abort_flag)) return false;
-        mbar_arrive_expect_tx(&sm.kv_full[slot], Smem::kTileBytes);
-        for (int a = 0; a < kKAtoms; ++a)
-          tma_load_4d(sm.kv[slot] + a * 16384, map, &sm.kv_full[slot], a * 64, row0, hh, b);
-        ++L;
-        return true;
-      };
-      ok = issue(&tm_k, 0);
-      for (int j = 0; ok && j < nt_all; ++j) {
-        if (j + 1 < nt_all) ok = issue(&tm_k, (j + 1) * kRows);
-        if (ok) ok = issue(&tm_v, j * kRows);
-      }
-      if (!ok) {
-        // wait (bounded) for this thread's copies still in flight
-        volatile uint32_t never = 0;
-        mbar_wait(&sm.q_full, 0, &never, 100000000ull);
-        for (int i = max(0, L - NSLOT); i < L; ++i)
-          mbar_wait(&sm.kv_full[i % NSLOT], static_cast<uint32_t>(i / NSLOT) & 1u, &never,
-                    100000000ull);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nt_all > 0) {
-      constexpr uint32_t kIdescS = idesc_bf16(kRows, kRows, false, false);
-      constexpr uint32_t kIdescPV = idesc_bf16(kRows, D, false, true);
-      const uint32_t q_addr = smem_u32(sm.q[0]);
-      const uint32_t kv_addr = smem_u32(sm.kv[0]);
-      const uint32_t p_addr = smem_u32(sm.p[0]);
-      bool ok = mbar_wait(&sm.q_full, 0, abort_flag);
-
-      // S_t = Q_t K^T : K-major A and B, K = head dimension in steps of 16
-      auto issue_s = [&](int t, int slot) {
-        const uint32_t d_tmem = tmem + Shape::kSCol(t);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint64_t da =
-              sdesc_sw128(q_addr + t * Smem::kTileBytes + off, 16, 1024);
-          const uint64_t db =
-              sdesc_sw128(kv_addr + slot * Smem::kTileBytes + off, 16, 1024);
-          mma_bf16_ss(d_tmem, da, db, kIdescS, kk > 0 ? 1u : 0u);
-        }
-      };
-      // O_t (+)= P_t V : P K-major (keys = K), V N-major (head dim = N)
-      auto issue_pv = [&](int t, int slot, bool accumulate) {
-        const uint32_t d_tmem = tmem + Shape::kOCol(t);
-#pragma unroll
-        for (int kk = 0; kk < kRows / 16; ++kk) {
-          const uint64_t da = sdesc_sw128(
-              p_addr + t * Smem::kPBytes + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-          const uint64_t db =
-              sdesc_sw128(kv_addr + slot * Smem::kTileBytes + kk * 2048, 16384, 1024);
-          mma_bf16_ss(d_tmem, da, db, kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
-        }
-      };
-
-      int L = 0;
-      if (ok) ok = mbar_wait(&sm.kv_full[0], 0, abort_flag);
-      if (ok) {
-        tc_fence_after();
+  if (warp < 4) {
+    if constexpr (NQT == 2) regs_decrease<Shape::kCtrlRegs>();
+    if (warp == 0) {
+      // ---------------------------------------------------------- producer
+      if (lane == 0 && nt_all > 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        mbar_arrive_expect_tx(&sm.q_full, NQT * Smem::kTileBytes);
         for (int t = 0; t < NQT; ++t)
-          if (nt[t] > 0) {
-            issue_s(t, 0);
-            mma_commit(&sm.s_full[t]);
-          }
-        mma_commit(&sm.kv_empty[0]);
-        L = 1;
-      }
-      for (int j = 0; ok && j < nt_all; ++j) {
-        const bool have_next = j + 1 < nt_all;
-        int slot_k = -1;
-        if (have_next) {
-          slot_k = L % NSLOT;
-          ok = mbar_wait(&sm.kv_full[slot_k], static_cast<uint32_t>(L / NSLOT) & 1u, abort_flag);
-          ++L;
+          for (int a = 0; a < kKAtoms; ++a)
+            tma_load_4d(sm.q[t] + a * 16384, &tm_q, &sm.q_full, a * 64, q0 + t * kRows, hh, b);
+
+        int kn = 0, vn = 0;  // tiles issued into each ring
+        auto load_k = [&]() {
+          const int slot = kn % NK;
+          if (!mbar_wait(&sm.k_empty[slot], (static_cast<uint32_t>(kn / NK) & 1u) ^ 1u, abort_flag))
+            return false;
+          mbar_arrive_expect_tx(&sm.k_full[slot], Smem::kTileBytes);
+          for (int a = 0; a < kKAtoms; ++a)
+            tma_load_4d(sm.k[slot] + a * 16384, &tm_k, &sm.k_full[slot], a * 64, kn * kRows, hh, b);
+          ++kn;
+          return true;
+        };
+        auto load_v = [&]() {
+          const int slot = vn % NV;
+          if (!mbar_wait(&sm.v_empty[slot], (static_cast<uint32_t>(vn / NV) & 1u) ^ 1u, abort_flag))
+            return false;
+          mbar_arrive_expect_tx(&sm.v_full[slot], Smem::kTileBytes);
+          for (int a = 0; a < kKAtoms; ++a)
+            tma_load_4d(sm.v[slot] + a * 16384, &tm_v, &sm.v_full[slot], a * 64, vn * kRows, hh, b);
+          ++vn;
+          return true;
+        };
+        // keys run one tile ahead of values, the order the MMAs consume them
+        bool ok = load_k();
+        for (int j = 0; ok && j < nt_all; ++j) {
+          if (j + 1 < nt_all) ok = load_k();
+          if (ok) ok = load_v();
         }
-        const int slot_v = L % NSLOT;
-        if (ok)
-          ok = mbar_wait(&sm.kv_full[slot_v], static_cast<uint32_t>(L / NSLOT) & 1u, abort_flag);
-        ++L;
-        if (!ok) break;
-        tc_fence_after();
-        for (int t = 0; ok && t < NQT; ++t) {
-          if (have_next && j + 1 < nt[t]) {
-            ok = mbar_wait(&sm.s_free[t], static_cast<uint32_t>(j) & 1u, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(t, slot_k);
+        if (!ok) {
+          // wait (bounded) for this thread's copies still in flight
+          volatile uint32_t never = 0;
+          mbar_wait(&sm.q_full, 0, &never, kDrainLimitNs);
+          for (int i = max(0, kn - NK); i < kn; ++i)
+            mbar_wait(&sm.k_full[i % NK], static_cast<uint32_t>(i / NK) & 1u, &never, kDrainLimitNs);
+          for (int i = max(0, vn - NV); i < vn; ++i)
+            mbar_wait(&sm.v_full[i % NV], static_cast<uint32_t>(i / NV) & 1u, &never, kDrainLimitNs);
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- S issuer
+      if (lane == 0 && nt_all > 0) {
+        const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);  // K-major Q
+        const uint64_t dk0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);  // K-major K
+        bool ok = mbar_wait(&sm.q_full, 0, abort_flag);
+        for (int j = 0; ok && j < nt_all; ++j) {
+          const int slot = j % NK;
+          ok = mbar_wait(&sm.k_full[slot], static_cast<uint32_t>(j / NK) & 1u, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t bk = dk0 + static_cast<uint64_t>(slot) * kTileStep;
+          for (int t = 0; t < NQT; ++t) {
+            if (j >= nt(t)) continue;
+            if (j > 0) {
+              // S_t(j-1) has been read (or, when P overwrites S, consumed by PV)
+              ok = Shape::kPAliasS
+                       ? mbar_wait(&sm.pv_done[t], static_cast<uint32_t>(j - 1) & 1u, abort_flag)
+                       : mbar_wait(&sm.s_free[t], static_cast<uint32_t>(j - 1) & 1u, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            // S_t = Q_t K^T : K-major A and B, K = head dimension in steps of 16
+            const uint32_t d_tmem = tmem + Shape::s_col(t);
+            const uint64_t a = dq0 + static_cast<uint64_t>(t) * kTileStep;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+              mma_bf16_ss(d_tmem, a + off, bk + off, kIdescS, kk > 0 ? 1u : 0u);
+            }
             mma_commit(&sm.s_full[t]);
           }
-          if (j < nt[t]) {
+          mma_commit(&sm.k_empty[slot]);
+        }
+        // every issued MMA has completed before tensor memory is released
+        volatile uint32_t never = 0;
+        mma_commit(&sm.s_drained);
+        mbar_wait(&sm.s_drained, 0, &never, kDrainLimitNs);
+      }
+    } else if (warp == 2) {
+      // ---------------------------------------------------------- PV issuer
+      if (lane == 0 && nt_all > 0) {
+        const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[0]), 16384, 1024);  // N-major V
+        bool ok = true;
+        for (int j = 0; ok && j < nt_all; ++j) {
+          const int slot = j % NV;
+          ok = mbar_wait(&sm.v_full[slot], static_cast<uint32_t>(j / NV) & 1u, abort_flag);
+          if (!ok) break;
+          const uint64_t bv = dv0 + static_cast<uint64_t>(slot) * kTileStep;
+          for (int t = 0; t < NQT; ++t) {
+            if (j >= nt(t)) continue;
             ok = mbar_wait(&sm.p_full[t], static_cast<uint32_t>(j) & 1u, abort_flag);
             if (!ok) break;
             tc_fence_after();
-            issue_pv(t, slot_v, j > 0);
+            // O_t (+)= P_t V : P from TMEM (keys = K), V N-major, 16 keys per MMA
+            const uint32_t d_tmem = tmem + Shape::o_col(t);
+#pragma unroll
+            for (int kk = 0; kk < kRows / 16; ++kk)
+              mma_bf16_ts(d_tmem, tmem + Shape::p_col(t) + kk * 8,
+                          bv + static_cast<uint64_t>(kk * (2048 >> 4)), kIdescPV,
+                          (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&sm.pv_done[t]);
           }
+          mma_commit(&sm.v_empty[slot]);
         }
-        if (have_next) mma_commit(&sm.kv_empty[slot_k]);
-        mma_commit(&sm.kv_empty[slot_v]);
+        volatile uint32_t never = 0;
+        mma_commit(&sm.pv_drained);
+        mbar_wait(&sm.pv_drained, 0, &never, kDrainLimitNs);
       }
-      // every issued MMA has completed before tensor memory is released
-      volatile uint32_t never = 0;
-      mma_commit(&sm.mma_drained);
-      mbar_wait(&sm.mma_drained, 0, &never, 100000000ull);
     }
-  } else if (warp >= 4) {
+  } else {
     // ------------------------------------------------------------ softmax
+    if constexpr (NQT == 2) regs_increase<Shape::kSoftmaxRegs>();
     const int t = (warp - 4) >> 2;           // query tile of this warpgroup
     const int quarter = warp & 3;             // TMEM lane quarter of this warp
     const int r = quarter * 32 + static_cast<int>(lane);  // row within the tile
     const int row = q0 + t * kRows + r;       // query index
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t taddr_s = tmem + lane_base + Shape::kSCol(t);
-    const uint32_t taddr_o = tmem + lane_base + Shape::kOCol(t);
-    const uint32_t p_row = smem_u32(sm.p[t]) + r * 128;
+    const uint32_t taddr_s = tmem + lane_base + Shape::s_col(t);
+    const uint32_t taddr_o = tmem + lane_base + Shape::o_col(t);
+    const uint32_t taddr_p = tmem + lane_base + Shape::p_col(t);
     const float sl2 = args.scale_log2;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
     const int lim_row = causal ? min(kv_eff, row + 1) : kv_eff;  // keys [0, lim_row) allowed
 
     float m_used = -INFINITY;
     float l = 0.f;
     bool ok = true;
-    const int ntt = nt[t];
+    const int ntt = nt(t);
     for (int j = 0; j < ntt; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], static_cast<uint32_t>(j) & 1u, abort_flag));
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&sm.s_full[t], static_cast<uint32_t>(j) & 1u, abort_flag));
       if (!ok) break;
       tc_fence_after();
       float s[kRows];
@@ -299,9 +338,16 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, 1)
         for (int c = 0; c < kRows; ++c)
           if (c >= bound) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // row max: 8 independent chains of 3-input max
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < kRows; ++c) mx = fmaxf(mx, s[c]);
+      for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+      for (int c = 16; c < kRows; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], s[c + i], s[c + 8 + i]);
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                             fmaxf(mx8[6], mx8[7]));
       const float m_cand = fmaxf(m_used, mx * sl2);
       const bool raise = m_cand > m_used + kRescaleThreshold;
       float alpha = 1.f;
@@ -310,16 +356,22 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, 1)
         m_used = m_cand;
       }
       const float m_eff = m_used == -INFINITY ? 0.f : m_used;
+      const uint64_t negm2 = f2_pack(-m_eff, -m_eff);
 
+      // p = 2^(s*scale*log2e - m): packed FFMA2, two MUFU ex2, packed FADD2
       uint32_t pk[kRows / 2];
-      float rowsum = 0.f;
+      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < kRows / 2; ++c) {
-        const float p0 = ex2(fmaf(s[2 * c], sl2, -m_eff));
-        const float p1 = ex2(fmaf(s[2 * c + 1], sl2, -m_eff));
-        rowsum += p0 + p1;
+        float x0, x1;
+        f2_unpack(ffma2(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, negm2), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
         pk[c] = pack_bf16x2(p0, p1);
+        acc2[c & 3] = fadd2(acc2[c & 3], f2_pack(p0, p1));
       }
+      float r0, r1;
+      f2_unpack(fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3])), r0, r1);
+      const float rowsum = r0 + r1;
 
       if (j > 0) {
         // PV of the previous tile has finished: O is stable, P is free
@@ -342,14 +394,17 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, 1)
       }
       l = l * alpha + rowsum;
 
-      // P row -> shared memory in the 128-byte-swizzled K-major layout
+      // P row -> TMEM lane r, two bf16 per 32-bit column (the MMA's A layout)
+      {
+        uint32_t half[32];
 #pragma unroll
-      for (int c16 = 0; c16 < kRows / 8; ++c16) {
-        const int atom = c16 >> 3, cc = c16 & 7;
-        const uint32_t addr = p_row + atom * 16384 + ((cc ^ (r & 7)) << 4);
-        st_shared_v4(addr, pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+        for (int i = 0; i < 32; ++i) half[i] = pk[i];
+        tmem_st32(taddr_p, half);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) half[i] = pk[32 + i];
+        tmem_st32(taddr_p + 32, half);
+        tmem_wait_st();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.p_full[t]);
     }
@@ -396,13 +451,13 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, Shape::kTmemCols);
 }
 
-template <int D, int NQT, int NSLOT>
+template <int D, int NQT, int NK, int NV>
 cudaError_t launch_variant(const AttnProblem& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                            const CUtensorMap& tm_v, cudaStream_t stream) {
-  using Smem = AttnSmem<D, NQT, NSLOT>;
+  using Smem = AttnSmem<D, NQT, NK, NV>;
   using Shape = AttnShape<D, NQT>;
   const size_t smem_bytes = sizeof(Smem) + 1024;  // + alignment slack
-  auto kernel = attn_fwd_bf16_kernel<D, NQT, NSLOT>;
+  auto kernel = attn_fwd_bf16_kernel<D, NQT, NK, NV>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem_bytes));
@@ -428,16 +483,16 @@ cudaError_t launch_variant(const AttnProblem& p, const CUtensorMap& tm_q, const 
 cudaError_t launch_attn_bf16(const AttnProblem& p, const CUtensorMap& tm_q,
                              const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              cudaStream_t stream) {
-  // Short query sets use one query tile per CTA (two CTAs share an SM);
-  // longer ones pair two query tiles so each K/V tile feeds two MMAs.
+  // Short query sets use one query tile per CTA; longer ones pair two query
+  // tiles so each K/V tile feeds two MMAs.
   const bool pair = p.n_q > kRows;
   if (p.d == 64) {
-    return pair ? launch_variant<64, 2, 6>(p, tm_q, tm_k, tm_v, stream)
-                : launch_variant<64, 1, 3>(p, tm_q, tm_k, tm_v, stream);
+    return pair ? launch_variant<64, 2, 4, 4>(p, tm_q, tm_k, tm_v, stream)
+                : launch_variant<64, 1, 2, 2>(p, tm_q, tm_k, tm_v, stream);
   }
   if (p.d == 128) {
-    return pair ? launch_variant<128, 2, 3>(p, tm_q, tm_k, tm_v, stream)
-                : launch_variant<128, 1, 2>(p, tm_q, tm_k, tm_v, stream);
+    return pair ? launch_variant<128, 2, 2, 2>(p, tm_q, tm_k, tm_v, stream)
+                : launch_variant<128, 1, 2, 2>(p, tm_q, tm_k, tm_v, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -103,8 +103,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_bf16_kernel(const __grid_con
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_bf16(kBM, kBN, false, true);
-      const uint32_t a_addr = smem_u32(sm.a[0]);
-      const uint32_t b_addr = smem_u32(sm.b[0]);
+      // descriptors built once, advanced by constant start-address offsets
+      const uint64_t da0 = sdesc_sw128(smem_u32(sm.a[0]), 16, 1024);    // K-major A
+      const uint64_t db0 = sdesc_sw128(smem_u32(sm.b[0]), 8192, 1024);  // N-major B
+      constexpr uint64_t kAStep = (kBM * kBK * 2) >> 4, kBStep = (kBK * kBN * 2) >> 4;
       bool ok = true;
       for (int kb = 0; kb < kblocks; ++kb) {
         const int s = kb % kStages;
@@ -113,14 +115,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_bf16_kernel(const __grid_con
           break;
         }
         tc_fence_after();
+        const uint64_t da = da0 + static_cast<uint64_t>(s) * kAStep;
+        const uint64_t db = db0 + static_cast<uint64_t>(s) * kBStep;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
-          // A: K-major, 16-element K step = 32 bytes inside the swizzle atom
-          const uint64_t da = sdesc_sw128(a_addr + s * (kBM * kBK * 2) + kk * 32, 16, 1024);
-          // B: N-major, 16 K rows = 2048 bytes; the second 64-wide N chunk is 8 KB on
-          const uint64_t db =
-              sdesc_sw128(b_addr + s * (kBK * kBN * 2) + kk * 2048, 8192, 1024);
-          mma_bf16_ss(tmem, da, db, kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          // A: K-major, a 16-element K step is 32 bytes inside the swizzle atom;
+          // B: N-major, 16 K rows are 2048 bytes (second 64-wide N chunk 8 KB on)
+          mma_bf16_ss(tmem, da + static_cast<uint64_t>(kk * (32 >> 4)),
+                      db + static_cast<uint64_t>(kk * (2048 >> 4)), kIdesc,
+                      (kb > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&sm.empty[s]);
       }

@@ -6,15 +6,19 @@
 // that head's key/value tiles (128 keys each) through two shared-memory rings:
 //
 //   warp 0      TMA producer: Q tiles once, then K_0, K_1, V_0, K_2, V_1, ...
-//   warp 1      S issuer (one thread): S_t = Q_t K_j^T into tensor memory;
-//               owns the TMEM allocation
-//   warp 2      PV issuer (one thread): O_t += P_t V_j into tensor memory
+//   warps 1-3   MMA issuers (one thread each), S_t = Q_t K_j^T and
+//               O_t += P_t V_j into tensor memory. The busier product gets one
+//               issuer per query tile: at d = 128 (S: 8 MMAs of N=128 per
+//               tile, PV: 8 of N=128) warps 1, 2 issue S for tiles 0, 1 and
+//               warp 3 issues PV; at d = 64 (S: 4 MMAs, PV: 8 of N=64, the
+//               less efficient shape) warp 1 issues S and warps 2, 3 issue PV
+//               for tiles 0, 1. Warp 1 owns the TMEM allocation.
 //   warps 4..7  softmax for query tile 0; warps 8..11 for query tile 1:
 //               one thread per query row (= one TMEM lane)
 //
-// Two issuing threads keep the tensor pipe fed: each thread's barrier waits
-// and commits (tcgen05.commit tracks only the issuing thread's MMAs) overlap
-// the other thread's MMA issue.
+// Several issuing threads keep the tensor pipe fed: each thread's barrier
+// waits and commits (tcgen05.commit tracks only the issuing thread's MMAs)
+// overlap the other threads' MMA issue.
 //
 // The n_q x n_k weight matrix never leaves the chip: S lives in TMEM, P (bf16)
 // in TMEM as the A operand of the PV MMA, one 128x128 tile at a time, with the
@@ -59,6 +63,10 @@ struct AttnShape {
   static constexpr uint32_t kCtrlRegs = D == 64 ? 72 : 88;
   static constexpr uint32_t kSoftmaxRegs =
       (kLaunchRegs * kThreads - kCtrlRegs * 128) / (128 * NQT) / 8 * 8;
+  // one issuer per query tile for S (else for PV), see the role table above
+  static constexpr bool kSplitS = (D == 128);
+  static constexpr int kSIssuers = kSplitS ? NQT : 1;
+  static constexpr int kPVIssuers = kSplitS ? 1 : NQT;
   static_assert(kColsUsed <= 512, "tensor memory budget");
   // setmaxnreg.inc waits for registers released by .dec: the split must fit
   // in what the CTA was launched with, or the increase would never complete
@@ -79,7 +87,7 @@ struct AttnSmem {
   uint64_t s_free[NQT];
   uint64_t p_full[NQT];
   uint64_t pv_done[NQT];
-  uint64_t s_drained, pv_drained;
+  uint64_t s_drained[NQT], pv_drained[NQT];
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -142,11 +150,11 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, 1)
     mbar_init(&sm.q_full, 1);
     for (int s = 0; s < NK; ++s) {
       mbar_init(&sm.k_full[s], 1);
-      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.k_empty[s], Shape::kSIssuers);  // one release per S-issuing warp
     }
     for (int s = 0; s < NV; ++s) {
       mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.v_empty[s], 1);
+      mbar_init(&sm.v_empty[s], Shape::kPVIssuers);  // one release per PV-issuing warp
     }
     for (int t = 0; t < NQT; ++t) {
       mbar_init(&sm.s_full[t], 1);
@@ -154,8 +162,10 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, 1)
       mbar_init(&sm.p_full[t], kRows);
       mbar_init(&sm.pv_done[t], 1);
     }
-    mbar_init(&sm.s_drained, 1);
-    mbar_init(&sm.pv_drained, 1);
+    for (int t = 0; t < NQT; ++t) {
+      mbar_init(&sm.s_drained[t], 1);
+      mbar_init(&sm.pv_drained[t], 1);
+    }
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -169,10 +179,9 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile uint32_t* abort_flag = &sm.abort_flag;
 
-  // Descriptors are built once; each MMA only adds a compile-time offset to
-  // the start-address field (addresses stay below 256 KB, so the 14-bit field
-  // never carries into the next one).
-  constexpr uint64_t kTileStep = Smem::kTileBytes >> 4;
+  // Descriptors are built once; each MMA only advances the start-address
+  // field by a compile-time offset (sdesc_advance keeps the sum inside it).
+  constexpr uint32_t kTileStep = Smem::kTileBytes >> 4;
   constexpr uint32_t kIdescS = idesc_bf16(kRows, kRows, false, false);
   constexpr uint32_t kIdescPV = idesc_bf16(kRows, D, false, true);
 
@@ -226,19 +235,24 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, 1)
             mbar_wait(&sm.v_full[i % NV], static_cast<uint32_t>(i / NV) & 1u, &never, kDrainLimitNs);
         }
       }
-    } else if (warp == 1) {
-      // ---------------------------------------------------------- S issuer
+    } else if (warp - 1 < Shape::kSIssuers) {
+      // ---------------------------------------------------------- S issuer(s)
+      // tiles [t_lo, t_hi) of this issuer, in order within each key tile
+      const int t_lo = Shape::kSplitS ? warp - 1 : 0;
+      const int t_hi = Shape::kSplitS ? warp : NQT;
       if (lane == 0 && nt_all > 0) {
         const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);  // K-major Q
         const uint64_t dk0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);  // K-major K
         bool ok = mbar_wait(&sm.q_full, 0, abort_flag);
         for (int j = 0; ok && j < nt_all; ++j) {
           const int slot = j % NK;
+          // the slot holds K_j before this warp releases it, so a release for
+          // tiles this issuer skips never counts toward an older use
           ok = mbar_wait(&sm.k_full[slot], static_cast<uint32_t>(j / NK) & 1u, abort_flag);
           if (!ok) break;
-          tc_fence_after();
-          const uint64_t bk = dk0 + static_cast<uint64_t>(slot) * kTileStep;
-          for (int t = 0; t < NQT; ++t) {
+          const uint64_t bk = sdesc_advance(dk0, static_cast<uint32_t>(slot) * kTileStep);
+          bool issued = false;
+          for (int t = t_lo; ok && t < t_hi; ++t) {
             if (j >= nt(t)) continue;
             if (j > 0) {
               // S_t(j-1) has been read (or, when P overwrites S, consumed by PV)
@@ -246,54 +260,66 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, 1)
                        ? mbar_wait(&sm.pv_done[t], static_cast<uint32_t>(j - 1) & 1u, abort_flag)
                        : mbar_wait(&sm.s_free[t], static_cast<uint32_t>(j - 1) & 1u, abort_flag);
               if (!ok) break;
-              tc_fence_after();
             }
+            tc_fence_after();
             // S_t = Q_t K^T : K-major A and B, K = head dimension in steps of 16
             const uint32_t d_tmem = tmem + Shape::s_col(t);
-            const uint64_t a = dq0 + static_cast<uint64_t>(t) * kTileStep;
+            const uint64_t a = sdesc_advance(dq0, static_cast<uint32_t>(t) * kTileStep);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-              mma_bf16_ss(d_tmem, a + off, bk + off, kIdescS, kk > 0 ? 1u : 0u);
+              const uint32_t off = static_cast<uint32_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+              mma_bf16_ss(d_tmem, sdesc_advance(a, off), sdesc_advance(bk, off), kIdescS,
+                          kk > 0 ? 1u : 0u);
             }
             mma_commit(&sm.s_full[t]);
+            issued = true;
           }
-          mma_commit(&sm.k_empty[slot]);
+          if (!ok) break;
+          if (issued) mma_commit(&sm.k_empty[slot]);
+          else mbar_arrive(&sm.k_empty[slot]);
         }
         // every issued MMA has completed before tensor memory is released
         volatile uint32_t never = 0;
-        mma_commit(&sm.s_drained);
-        mbar_wait(&sm.s_drained, 0, &never, kDrainLimitNs);
+        mma_commit(&sm.s_drained[t_lo]);
+        mbar_wait(&sm.s_drained[t_lo], 0, &never, kDrainLimitNs);
       }
-    } else if (warp == 2) {
-      // ---------------------------------------------------------- PV issuer
+    } else if (warp - 1 - Shape::kSIssuers < Shape::kPVIssuers) {
+      // ---------------------------------------------------------- PV issuer(s)
+      const int w = warp - 1 - Shape::kSIssuers;
+      const int t_lo = Shape::kSplitS ? 0 : w;
+      const int t_hi = Shape::kSplitS ? NQT : w + 1;
       if (lane == 0 && nt_all > 0) {
         const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[0]), 16384, 1024);  // N-major V
         bool ok = true;
         for (int j = 0; ok && j < nt_all; ++j) {
           const int slot = j % NV;
+          // as for K: the slot holds V_j before any release by this warp
           ok = mbar_wait(&sm.v_full[slot], static_cast<uint32_t>(j / NV) & 1u, abort_flag);
           if (!ok) break;
-          const uint64_t bv = dv0 + static_cast<uint64_t>(slot) * kTileStep;
-          for (int t = 0; t < NQT; ++t) {
+          const uint64_t bv = sdesc_advance(dv0, static_cast<uint32_t>(slot) * kTileStep);
+          bool issued = false;
+          for (int t = t_lo; ok && t < t_hi; ++t) {
             if (j >= nt(t)) continue;
             ok = mbar_wait(&sm.p_full[t], static_cast<uint32_t>(j) & 1u, abort_flag);
             if (!ok) break;
             tc_fence_after();
             // O_t (+)= P_t V : P from TMEM (keys = K), V N-major, 16 keys per MMA
             const uint32_t d_tmem = tmem + Shape::o_col(t);
+            const uint32_t p_tmem = tmem + Shape::p_col(t);
 #pragma unroll
             for (int kk = 0; kk < kRows / 16; ++kk)
-              mma_bf16_ts(d_tmem, tmem + Shape::p_col(t) + kk * 8,
-                          bv + static_cast<uint64_t>(kk * (2048 >> 4)), kIdescPV,
+              mma_bf16_ts(d_tmem, p_tmem + kk * 8, sdesc_advance(bv, kk * (2048 >> 4)), kIdescPV,
                           (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&sm.pv_done[t]);
+            issued = true;
           }
-          mma_commit(&sm.v_empty[slot]);
+          if (!ok) break;
+          if (issued) mma_commit(&sm.v_empty[slot]);
+          else mbar_arrive(&sm.v_empty[slot]);
         }
         volatile uint32_t never = 0;
-        mma_commit(&sm.pv_drained);
-        mbar_wait(&sm.pv_drained, 0, &never, kDrainLimitNs);
+        mma_commit(&sm.pv_drained[t_lo]);
+        mbar_wait(&sm.pv_drained[t_lo], 0, &never, kDrainLimitNs);
       }
     }
   } else {
@@ -329,8 +355,6 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, 1)
         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(raw[i]);
       }
       tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&sm.s_free[t]);
 
       const int bound = lim_row - j * kRows;  // keys c >= bound of this tile are masked
       if (bound < kRows) {
@@ -348,6 +372,12 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, 1)
         for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], s[c + i], s[c + 8 + i]);
       const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                              fmaxf(mx8[6], mx8[7]));
+      // S_t is free for S_t(j+1) only now, after the row max: the tensor pipe
+      // executes MMAs in issue order, and PV_t(j-1), issued when P_t(j-1) was
+      // stored, should run before S_t(j+1) -- this tile's next P store waits
+      // for it, while the next S is not needed until this iteration ends.
+      tc_fence_before();
+      mbar_arrive(&sm.s_free[t]);
       const float m_cand = fmaxf(m_used, mx * sl2);
       const bool raise = m_cand > m_used + kRescaleThreshold;
       float alpha = 1.f;

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_bf16_kernel(const __grid_con
       // descriptors built once, advanced by constant start-address offsets
       const uint64_t da0 = sdesc_sw128(smem_u32(sm.a[0]), 16, 1024);    // K-major A
       const uint64_t db0 = sdesc_sw128(smem_u32(sm.b[0]), 8192, 1024);  // N-major B
-      constexpr uint64_t kAStep = (kBM * kBK * 2) >> 4, kBStep = (kBK * kBN * 2) >> 4;
+      constexpr uint32_t kAStep = (kBM * kBK * 2) >> 4, kBStep = (kBK * kBN * 2) >> 4;
       bool ok = true;
       for (int kb = 0; kb < kblocks; ++kb) {
         const int s = kb % kStages;
@@ -115,15 +115,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_bf16_kernel(const __grid_con
           break;
         }
         tc_fence_after();
-        const uint64_t da = da0 + static_cast<uint64_t>(s) * kAStep;
-        const uint64_t db = db0 + static_cast<uint64_t>(s) * kBStep;
+        const uint64_t da = sdesc_advance(da0, static_cast<uint32_t>(s) * kAStep);
+        const uint64_t db = sdesc_advance(db0, static_cast<uint32_t>(s) * kBStep);
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
           // A: K-major, a 16-element K step is 32 bytes inside the swizzle atom;
           // B: N-major, 16 K rows are 2048 bytes (second 64-wide N chunk 8 KB on)
-          mma_bf16_ss(tmem, da + static_cast<uint64_t>(kk * (32 >> 4)),
-                      db + static_cast<uint64_t>(kk * (2048 >> 4)), kIdesc,
-                      (kb > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ss(tmem, sdesc_advance(da, kk * (32 >> 4)), sdesc_advance(db, kk * (2048 >> 4)),
+                      kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&sm.empty[s]);
       }

@@ -176,6 +176,16 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Advances a descriptor's start address by `units` 16-byte units. The field
+// holds address bits [4, 18) only and shared-window addresses may exceed
+// 256 KB, so the sum wraps inside the field instead of carrying into the
+// reserved bits above it.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t units) {
+  const uint32_t lo = static_cast<uint32_t>(desc);
+  const uint32_t moved = (lo & ~0x3FFFu) | ((lo + units) & 0x3FFFu);
+  return (desc & 0xFFFFFFFF00000000ull) | moved;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
 //   bits 4-5 D format (1 = f32)   bits 7-9 A format (1 = bf16)
 //   bits 10-12 B format (1 = bf16) bit 15 A major (1 = MN)  bit 16 B major

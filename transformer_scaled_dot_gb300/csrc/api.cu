@@ -43,10 +43,72 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder(cudaError_t* err) {
   return fn;
 }
 
+// Encoded maps are memoised: an encoding costs microseconds of host time,
+// about as much as a short attention kernel runs. A map holds nothing but
+// its inputs (address, sizes, strides, box), so the key is all of them and
+// a hit returns exactly what a fresh encoding would.
+struct MapKey {
+  const void* base;
+  int rank;
+  uint64_t dims[4];
+  int64_t strides[3];
+  uint32_t box[4];
+};
+
+constexpr int kMapCacheSlots = 256;  // direct-mapped
+struct MapCacheEntry {
+  bool used;
+  MapKey key;
+  CUtensorMap map;
+};
+std::mutex g_map_cache_mutex;
+MapCacheEntry g_map_cache[kMapCacheSlots];
+
+uint32_t map_key_hash(const MapKey& k) {
+  const unsigned char* p = reinterpret_cast<const unsigned char*>(&k);
+  uint32_t h = 2166136261u;  // FNV-1a
+  for (size_t i = 0; i < sizeof(MapKey); ++i) h = (h ^ p[i]) * 16777619u;
+  return h;
+}
+
+cudaError_t encode_bf16_map_uncached(CUtensorMap* map, const void* base, int rank,
+                                     const uint64_t* dims, const int64_t* strides_elems,
+                                     const uint32_t* box);
+
 // bf16 tensor map, rank 2..4, dims innermost first, strides in elements
 // (dims 1..rank-1), 128-byte swizzle, zero fill out of bounds.
 cudaError_t encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                             const int64_t* strides_elems, const uint32_t* box) {
+  MapKey key;
+  std::memset(&key, 0, sizeof(key));  // padding bytes take part in hash and compare
+  key.base = base;
+  key.rank = rank;
+  for (int i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+  }
+  for (int i = 0; i < rank - 1; ++i) key.strides[i] = strides_elems[i];
+  MapCacheEntry& slot = g_map_cache[map_key_hash(key) % kMapCacheSlots];
+  {
+    std::lock_guard<std::mutex> lock(g_map_cache_mutex);
+    if (slot.used && std::memcmp(&slot.key, &key, sizeof(key)) == 0) {
+      *map = slot.map;
+      return cudaSuccess;
+    }
+  }
+  cudaError_t e = encode_bf16_map_uncached(map, base, rank, dims, strides_elems, box);
+  if (e == cudaSuccess) {
+    std::lock_guard<std::mutex> lock(g_map_cache_mutex);
+    slot.used = true;
+    slot.key = key;
+    slot.map = *map;
+  }
+  return e;
+}
+
+cudaError_t encode_bf16_map_uncached(CUtensorMap* map, const void* base, int rank,
+                                     const uint64_t* dims, const int64_t* strides_elems,
+                                     const uint32_t* box) {
   cudaError_t err;
   auto enc = tensor_map_encoder(&err);
   if (err != cudaSuccess) return err;
@@ -159,7 +221,7 @@ cudaError_t make_gemm_group(tsd::GemmGroup* g, const void* a, const void* b, voi
   if (e != cudaSuccess) return e;
   const uint64_t bdims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K)};
   const int64_t bstr[1] = {N};
-  const uint32_t bbox[2] = {64, 64};
+  const uint32_t bbox[2] = {64, 128};  // 64 N columns x 128 K rows
   e = encode_bf16_map(&g->tm_b, b, 2, bdims, bstr, bbox);
   if (e != cudaSuccess) return e;
   g->c = static_cast<uint16_t*>(c);

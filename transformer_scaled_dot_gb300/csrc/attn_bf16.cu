@@ -488,9 +488,8 @@ cudaError_t launch_variant(const AttnProblem& p, const CUtensorMap& tm_q, const 
   using Shape = AttnShape<D, NQT>;
   const size_t smem_bytes = sizeof(Smem) + 1024;  // + alignment slack
   auto kernel = attn_fwd_bf16_kernel<D, NQT, NK, NV>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem_bytes));
+  static unsigned long long configured = 0;
+  cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured);
   if (e != cudaSuccess) return e;
   AttnArgs a;
   a.n_q = p.n_q;

@@ -135,9 +135,13 @@ __global__ void __launch_bounds__(kWarps * 32) attn_fwd_f32_kernel(const AttnF32
 cudaError_t launch_attn_f32(const AttnF32Problem& p, cudaStream_t stream) {
   const size_t smem = sizeof(float) *
                       (static_cast<size_t>(kRowsPerCta) * p.d_k + kKeys * (p.d_k + 1) + kKeys * p.d_v);
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  // the limit is raised once, to what the largest head dimensions need
+  constexpr int kMaxSmem =
+      static_cast<int>(sizeof(float) * (kRowsPerCta * kMaxD + kKeys * (kMaxD + 1) + kKeys * kMaxD));
+  static unsigned long long configured = 0;
+  cudaError_t e = set_smem_once(attn_fwd_f32_kernel, kMaxSmem, &configured);
   if (e != cudaSuccess) return e;
+  if (smem > static_cast<size_t>(kMaxSmem)) return cudaErrorInvalidValue;
   dim3 grid((p.n_q + kRowsPerCta - 1) / kRowsPerCta, p.h, p.B);
   attn_fwd_f32_kernel<<<grid, kWarps * 32, smem, stream>>>(p);
   return cudaGetLastError();

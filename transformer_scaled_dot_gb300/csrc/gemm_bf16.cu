@@ -4,13 +4,17 @@
 // Need" (kimjiil.github.io), section 3.2.2; weights in the x.W layout,
 // [d_model, h*d], no biases).
 //
-// One CTA computes one 128 x 128 tile of C = A B with fp32 accumulation in
-// tensor memory:
-//   warp 0     TMA producer: A box (64 K x 128 M, K-major) and two B boxes
-//              (64 N x 64 K each, N-major) per 64-deep K block, STAGES deep
-//   warp 1     MMA issuer (one thread); owns the 128-column TMEM allocation
+// Persistent kernel: one CTA per SM walks the 128 x 128 output tiles of all
+// groups (C = A B, fp32 accumulation in tensor memory):
+//   warp 0     TMA producer: per 128-deep K block, two A boxes (64 K x 128 M,
+//              K-major) and two B boxes (64 N x 128 K, N-major), kStages deep,
+//              running ahead across tile boundaries
+//   warp 1     MMA issuer (one thread), 8 MMAs per K block; owns the TMEM
+//              allocation: two 128-column accumulators, so the epilogue of
+//              one tile overlaps the main loop of the next
 //   warps 2-5  epilogue: one thread per output row (TMEM lane), fp32 -> bf16,
-//              16-byte stores
+//              16-byte stores; the accumulator is released right after it is
+//              read into registers
 // The head split needs no data movement: head i of Q is column block i of
 // the [B*n, h*d] result, which the attention kernel reads through strides.
 #include "kernels.h"
@@ -22,45 +26,66 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kBK = 64;
+constexpr int kBK = 128;
 constexpr int kStages = 3;
 constexpr int kThreads = 192;
-constexpr int kTmemCols = 128;
+constexpr int kAccCols = 128;
+constexpr int kTmemCols = 2 * kAccCols;
+constexpr int kABytes = kBM * kBK * 2;  // 32 KB: two 128-row x 128-byte K atoms
+constexpr int kBBytes = kBK * kBN * 2;  // 32 KB: two 128-row (K) x 128-byte N chunks
+constexpr unsigned long long kDrainLimitNs = 100ull * 1000ull * 1000ull;
 
 struct GemmSmem {
-  alignas(1024) uint8_t a[kStages][kBM * kBK * 2];   // 16 KB: 128 rows x 128 B
-  alignas(1024) uint8_t b[kStages][kBK * kBN * 2];   // 16 KB: two 64x64 N-major boxes
+  alignas(1024) uint8_t a[kStages][kABytes];
+  alignas(1024) uint8_t b[kStages][kBBytes];
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t acc_full;
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drained;
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
 
-__global__ void __launch_bounds__(kThreads, 2) gemm_bf16_kernel(const __grid_constant__ GemmProblem p) {
+struct TileCoord {
+  const GemmGroup* g;
+  int m0, n0;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(const GemmProblem& p, int tile) {
+  int gi = 0;
+  for (int i = 1; i < p.num_groups; ++i)
+    if (tile >= p.g[i].tile_begin) gi = i;
+  const GemmGroup& G = p.g[gi];
+  const int local = tile - G.tile_begin;
+  TileCoord c;
+  c.g = &G;
+  c.m0 = (local % G.tiles_m) * kBM;  // m fastest: neighbouring CTAs share B
+  c.n0 = (local / G.tiles_m) * kBN;
+  return c;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_constant__ GemmProblem p) {
   extern __shared__ uint8_t smem_raw[];
   GemmSmem& sm = *reinterpret_cast<GemmSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = warp_id();
   const uint32_t lane = lane_id();
-
-  // tile -> (group, m tile, n tile); m varies fastest
-  const int tile = blockIdx.x;
-  int g = 0;
-  for (int i = 1; i < p.num_groups; ++i)
-    if (tile >= p.g[i].tile_begin) g = i;
-  const GemmGroup& G = p.g[g];
-  const int local = tile - G.tile_begin;
-  const int m0 = (local % G.tiles_m) * kBM;
-  const int n0 = (local / G.tiles_m) * kBN;
   const int kblocks = (p.K + kBK - 1) / kBK;
+  // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
+  const int first = blockIdx.x;
+  const int stride = gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
-    mbar_init(&sm.acc_full, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sm.acc_full[a], 1);
+      mbar_init(&sm.acc_empty[a], 128);
+    }
+    mbar_init(&sm.drained, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -75,90 +100,119 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_bf16_kernel(const __grid_con
   volatile uint32_t* abort_flag = &sm.abort_flag;
 
   if (warp == 0) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&G.tm_a);
-      tma_prefetch_desc(&G.tm_b);
+      for (int i = 0; i < p.num_groups; ++i) {
+        tma_prefetch_desc(&p.g[i].tm_a);
+        tma_prefetch_desc(&p.g[i].tm_b);
+      }
       int issued = 0;
       bool ok = true;
-      for (int kb = 0; kb < kblocks; ++kb) {
-        const int s = kb % kStages;
-        const uint32_t ph = static_cast<uint32_t>(kb / kStages) & 1u;
-        if (!mbar_wait(&sm.empty[s], ph ^ 1u, abort_flag)) {
-          ok = false;
-          break;
+      for (int tile = first; ok && tile < p.total_tiles; tile += stride) {
+        const TileCoord c = tile_coord(p, tile);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const int s = issued % kStages;
+          const uint32_t ph = static_cast<uint32_t>(issued / kStages) & 1u;
+          if (!mbar_wait(&sm.empty[s], ph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.full[s], kABytes + kBBytes);
+          const int k0 = kb * kBK;
+          tma_load_2d(sm.a[s], &c.g->tm_a, &sm.full[s], k0, c.m0);
+          tma_load_2d(sm.a[s] + 16384, &c.g->tm_a, &sm.full[s], k0 + 64, c.m0);
+          tma_load_2d(sm.b[s], &c.g->tm_b, &sm.full[s], c.n0, k0);
+          tma_load_2d(sm.b[s] + 16384, &c.g->tm_b, &sm.full[s], c.n0 + 64, k0);
+          ++issued;
         }
-        mbar_arrive_expect_tx(&sm.full[s], kBM * kBK * 2 + kBK * kBN * 2);
-        tma_load_2d(sm.a[s], &G.tm_a, &sm.full[s], kb * kBK, m0);
-        tma_load_2d(sm.b[s], &G.tm_b, &sm.full[s], n0, kb * kBK);
-        tma_load_2d(sm.b[s] + 8192, &G.tm_b, &sm.full[s], n0 + 64, kb * kBK);
-        ++issued;
       }
       if (!ok) {
         volatile uint32_t never = 0;
         for (int i = max(0, issued - kStages); i < issued; ++i)
           mbar_wait(&sm.full[i % kStages], static_cast<uint32_t>(i / kStages) & 1u, &never,
-                    100000000ull);
+                    kDrainLimitNs);
       }
     }
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_bf16(kBM, kBN, false, true);
-      // descriptors built once, advanced by constant start-address offsets
-      const uint64_t da0 = sdesc_sw128(smem_u32(sm.a[0]), 16, 1024);    // K-major A
-      const uint64_t db0 = sdesc_sw128(smem_u32(sm.b[0]), 8192, 1024);  // N-major B
-      constexpr uint32_t kAStep = (kBM * kBK * 2) >> 4, kBStep = (kBK * kBN * 2) >> 4;
+      // descriptors built once, advanced inside the start-address field
+      const uint64_t da0 = sdesc_sw128(smem_u32(sm.a[0]), 16, 1024);     // K-major A
+      const uint64_t db0 = sdesc_sw128(smem_u32(sm.b[0]), 16384, 1024);  // N-major B
+      int consumed = 0;
+      int it = 0;
       bool ok = true;
-      for (int kb = 0; kb < kblocks; ++kb) {
-        const int s = kb % kStages;
-        if (!mbar_wait(&sm.full[s], static_cast<uint32_t>(kb / kStages) & 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
+      for (int tile = first; ok && tile < p.total_tiles; tile += stride, ++it) {
+        const int acc = it & 1;
+        // the epilogue has read this accumulator's previous tile
+        ok = mbar_wait(&sm.acc_empty[acc], (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, abort_flag);
+        if (!ok) break;
         tc_fence_after();
-        const uint64_t da = sdesc_advance(da0, static_cast<uint32_t>(s) * kAStep);
-        const uint64_t db = sdesc_advance(db0, static_cast<uint32_t>(s) * kBStep);
+        const uint32_t d_tmem = tmem + acc * kAccCols;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const int s = consumed % kStages;
+          ok = mbar_wait(&sm.full[s], static_cast<uint32_t>(consumed / kStages) & 1u, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t da = sdesc_advance(da0, static_cast<uint32_t>(s) * (kABytes >> 4));
+          const uint64_t db = sdesc_advance(db0, static_cast<uint32_t>(s) * (kBBytes >> 4));
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          // A: K-major, a 16-element K step is 32 bytes inside the swizzle atom;
-          // B: N-major, 16 K rows are 2048 bytes (second 64-wide N chunk 8 KB on)
-          mma_bf16_ss(tmem, sdesc_advance(da, kk * (32 >> 4)), sdesc_advance(db, kk * (2048 >> 4)),
-                      kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // A: K-major, atom kk/4, 32 bytes per 16-element step inside it;
+            // B: N-major, 16 K rows = 2048 bytes; the second N chunk is 16 KB on
+            const uint32_t a_off = static_cast<uint32_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+            mma_bf16_ss(d_tmem, sdesc_advance(da, a_off), sdesc_advance(db, kk * (2048 >> 4)),
+                        kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&sm.empty[s]);
+          ++consumed;
         }
-        mma_commit(&sm.empty[s]);
+        if (ok) mma_commit(&sm.acc_full[acc]);
       }
-      mma_commit(&sm.acc_full);
-      if (!ok) {
-        volatile uint32_t never = 0;
-        mbar_wait(&sm.acc_full, 0, &never, 100000000ull);
-      }
+      volatile uint32_t never = 0;
+      mma_commit(&sm.drained);
+      mbar_wait(&sm.drained, 0, &never, kDrainLimitNs);
     }
   } else {
-    // epilogue warps 2..5 cover TMEM lane quarters 2, 3, 0, 1
+    // ------------------------------------------------------------ epilogue
+    // warps 2..5 cover TMEM lane quarters 2, 3, 0, 1
     const int quarter = warp & 3;
     const int r = quarter * 32 + static_cast<int>(lane);
-    const int row = m0 + r;
-    bool ok = mbar_wait(&sm.acc_full, 0, abort_flag);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok && kblocks > 0) {
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    int it = 0;
+    for (int tile = first; tile < p.total_tiles; tile += stride, ++it) {
+      const int acc = it & 1;
+      const TileCoord c = tile_coord(p, tile);
+      const bool ok = __all_sync(
+          0xffffffffu,
+          mbar_wait(&sm.acc_full[acc], static_cast<uint32_t>(it >> 1) & 1u, abort_flag));
+      if (!ok) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-      uint16_t* crow = G.c + static_cast<int64_t>(row) * G.ldc;
+      uint32_t v[kBN];
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(taddr + c * 32, v);
-        tmem_wait_ld();
-        uint32_t w[16];
+      for (int cc = 0; cc < kBN / 32; ++cc) {
+        uint32_t chunk[32];
+        tmem_ld32(tmem + lane_base + acc * kAccCols + cc * 32, chunk);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-        if (row < G.M) {
+        for (int i = 0; i < 32; ++i) v[cc * 32 + i] = chunk[i];
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&sm.acc_empty[acc]);  // the MMA warp may reuse this accumulator
+
+      const int row = c.m0 + r;
+      if (row < c.g->M) {
+        uint16_t* crow = c.g->c + static_cast<int64_t>(row) * c.g->ldc;
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            const int col = n0 + c * 32 + v4 * 8;
-            if (col < G.N)
-              st_global_v4(crow + col, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
-          }
+        for (int v8 = 0; v8 < kBN / 8; ++v8) {
+          const int col = c.n0 + v8 * 8;
+          if (col < c.g->N)
+            st_global_v4(crow + col,
+                         pack_bf16x2(__uint_as_float(v[8 * v8 + 0]), __uint_as_float(v[8 * v8 + 1])),
+                         pack_bf16x2(__uint_as_float(v[8 * v8 + 2]), __uint_as_float(v[8 * v8 + 3])),
+                         pack_bf16x2(__uint_as_float(v[8 * v8 + 4]), __uint_as_float(v[8 * v8 + 5])),
+                         pack_bf16x2(__uint_as_float(v[8 * v8 + 6]), __uint_as_float(v[8 * v8 + 7])));
         }
       }
     }
@@ -170,15 +224,27 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_bf16_kernel(const __grid_con
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  }
+  return n;
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_bf16(const GemmProblem& p, cudaStream_t stream) {
   if (p.total_tiles <= 0) return cudaSuccess;
   const size_t smem_bytes = sizeof(GemmSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem_bytes));
+  static unsigned long long configured = 0;
+  cudaError_t e = set_smem_once(gemm_bf16_kernel, static_cast<int>(smem_bytes), &configured);
   if (e != cudaSuccess) return e;
-  gemm_bf16_kernel<<<p.total_tiles, kThreads, smem_bytes, stream>>>(p);
+  const int grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
+  gemm_bf16_kernel<<<grid, kThreads, smem_bytes, stream>>>(p);
   return cudaGetLastError();
 }
 

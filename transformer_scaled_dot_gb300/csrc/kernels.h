@@ -45,7 +45,7 @@ cudaError_t launch_attn_f32(const AttnF32Problem& p, cudaStream_t stream);
 // the x.W weight layout). Up to 3 groups share K and run in one launch.
 struct GemmGroup {
   CUtensorMap tm_a;  // 2-D (K, M), box 64 x 128
-  CUtensorMap tm_b;  // 2-D (N, K), box 64 x 64
+  CUtensorMap tm_b;  // 2-D (N, K), box 64 x 128
   uint16_t* c;
   int64_t ldc;       // elements
   int M, N;
@@ -59,6 +59,22 @@ struct GemmProblem {
   int total_tiles;
 };
 cudaError_t launch_gemm_bf16(const GemmProblem& p, cudaStream_t stream);
+
+// Raises a kernel's dynamic shared-memory limit once per device: the
+// attribute belongs to the device's context, and setting it on every launch
+// costs host time comparable to a short kernel. `done` holds one bit per
+// device ordinal (ordinals past 63 set it every time).
+template <typename Kernel>
+inline cudaError_t set_smem_once(Kernel kernel, int bytes, unsigned long long* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0ull && (__atomic_load_n(done, __ATOMIC_ACQUIRE) & bit) != 0ull) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0ull) __atomic_fetch_or(done, bit, __ATOMIC_RELEASE);
+  return e;
+}
 
 // Per-file device error words (read and cleared; see sm103.cuh).
 cudaError_t take_device_error_attn(unsigned int* value);

@@ -169,10 +169,11 @@ attn_status run_attn_bf16(const void* q, int64_t q_sb, int64_t q_sh, int64_t q_s
                           int64_t v_sh, int64_t v_sr, void* out, int64_t o_sb, int64_t o_sh,
                           int64_t o_sr, int B, int h, int n_q, int n_k, int d, int mask_kind,
                           const int32_t* kv_lens, float scale, cudaStream_t stream) {
-  CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
   cudaError_t e = encode_head_map(&tm_q, q, d, n_q, h, B, q_sr, q_sh, q_sb);
   if (e == cudaSuccess) e = encode_head_map(&tm_k, k, d, n_k, h, B, k_sr, k_sh, k_sb);
   if (e == cudaSuccess) e = encode_head_map(&tm_v, v, d, n_k, h, B, v_sr, v_sh, v_sb);
+  if (e == cudaSuccess) e = encode_head_map(&tm_o, out, d, n_q, h, B, o_sr, o_sh, o_sb);
   if (e != cudaSuccess) return cuda_fail(e);
   tsd::AttnProblem p;
   p.B = B;
@@ -187,7 +188,7 @@ attn_status run_attn_bf16(const void* q, int64_t q_sb, int64_t q_sh, int64_t q_s
   p.o_sb = o_sb;
   p.o_sh = o_sh;
   p.o_sr = o_sr;
-  e = tsd::launch_attn_bf16(p, tm_q, tm_k, tm_v, stream);
+  e = tsd::launch_attn_bf16(p, tm_q, tm_k, tm_v, tm_o, stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
@@ -221,8 +222,13 @@ cudaError_t make_gemm_group(tsd::GemmGroup* g, const void* a, const void* b, voi
   if (e != cudaSuccess) return e;
   const uint64_t bdims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K)};
   const int64_t bstr[1] = {N};
-  const uint32_t bbox[2] = {64, 128};  // 64 N columns x 128 K rows
+  const uint32_t bbox[2] = {64, 64};  // 64 N columns x 64 K rows
   e = encode_bf16_map(&g->tm_b, b, 2, bdims, bstr, bbox);
+  if (e != cudaSuccess) return e;
+  const uint64_t cdims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+  const int64_t cstr[1] = {N};
+  const uint32_t cbox[2] = {64, 128};  // 64 columns x 128 rows, written by TMA stores
+  e = encode_bf16_map(&g->tm_c, c, 2, cdims, cstr, cbox);
   if (e != cudaSuccess) return e;
   g->c = static_cast<uint16_t*>(c);
   g->ldc = N;

@@ -21,7 +21,12 @@
 //               and commits (tcgen05.commit tracks only its own MMAs) overlap
 //               the others' MMA issue.
 //   warps 4..7  softmax for query tile 0; warps 8..11 for query tile 1:
-//               one thread per query row (= one TMEM lane), then the epilogue
+//               one thread per query row (= one TMEM lane), then the epilogue:
+//               O / l to bf16 into a 128-byte-swizzled staging tile and one
+//               TMA store per 64 columns (a row per thread written straight
+//               to global memory would scatter each warp store over 32 rows);
+//               the d = 128 paired variant has no shared memory left for the
+//               staging tile and stores rows directly
 //
 // The n_q x n_k weight matrix never leaves the chip: S lives in TMEM, P (bf16)
 // in TMEM as the A operand of the PV MMA, one 128x128 tile at a time, with the
@@ -86,12 +91,13 @@ struct AttnShape {
                 "register split exceeds the launch allocation");
 };
 
-template <int D, int NQT, int NK, int NV, int QB>
+template <int D, int NQT, int NK, int NV, int QB, bool STO>
 struct AttnSmem {
-  static constexpr int kTileBytes = kRows * D * 2;  // one Q, K or V tile
+  static constexpr int kTileBytes = kRows * D * 2;  // one Q, K, V or O tile
   alignas(1024) uint8_t q[QB][NQT][kTileBytes];
   alignas(1024) uint8_t k[NK][kTileBytes];
   alignas(1024) uint8_t v[NV][kTileBytes];
+  alignas(1024) uint8_t o[NQT][STO ? kTileBytes : 16];  // epilogue staging
   uint64_t q_full[QB], q_empty[QB];
   uint64_t k_full[NK], k_empty[NK];
   uint64_t v_full[NV], v_empty[NV];
@@ -158,12 +164,13 @@ __device__ __forceinline__ Item item_at(const AttnArgs& a, int w) {
   return it;
 }
 
-template <int D, int NQT, int NK, int NV, int QB>
+template <int D, int NQT, int NK, int NV, int QB, bool STO>
 __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>::kMinBlocks)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v, const AttnArgs args) {
-  using Smem = AttnSmem<D, NQT, NK, NV, QB>;
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_o, const AttnArgs args) {
+  using Smem = AttnSmem<D, NQT, NK, NV, QB, STO>;
   using Shape = AttnShape<D, NQT>;
   constexpr int kKAtoms = D / 64;  // 128-byte swizzle atoms along the head dimension
 
@@ -214,6 +221,9 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile uint32_t* abort_flag = &sm.abort_flag;
+  // the set-up above may overlap the previous kernel; global memory may not
+  griddep_launch_dependents();
+  griddep_wait();
 
   // Descriptors are built once; each MMA only advances the start-address
   // field by a compile-time offset (sdesc_advance keeps the sum inside it).
@@ -229,6 +239,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        if constexpr (STO) tma_prefetch_desc(&tm_o);
         int qn = 0, kn = 0, vn = 0;  // items / tiles issued into each ring
         bool ok = true;
         auto load_k = [&](const Item& it, int j) {
@@ -414,6 +425,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
     const uint32_t taddr_p = tmem + lane_base + Shape::p_col(t);
     const float sl2 = args.scale_log2;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
+    const bool leader = (quarter == 0 && lane == 0);  // issues the tile's TMA stores
     int c = 0;  // S / P tiles of this query tile so far (phase counter)
     bool ok = true;
     for (int i = 0, w = item_index(0); ok && w < args.num_items; w = item_index(++i)) {
@@ -521,15 +533,21 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
         tc_fence_before();
         mbar_arrive(&sm.p_full[t]);
       }
-      if (!ok) break;
+      if (!STO && !ok) break;
 
       // -------------------------------------------------------- epilogue
-      if (ntt > 0) {
+      if (ok && ntt > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.pv_done[t], static_cast<uint32_t>(c - 1) & 1u,
                                                abort_flag));
-        if (!ok) break;
-        tc_fence_after();
       }
+      if constexpr (STO) {
+        // the staging tile's previous store has finished reading it, and the
+        // warpgroup's four warps take one decision (none is left at a barrier)
+        if (leader) bulk_wait_group_read<0>();
+        ok = named_bar_and(1 + t, kRows, ok);
+      }
+      if (!ok) break;
+      if (ntt > 0) tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       uint16_t* dst = args.out + static_cast<int64_t>(it.b) * args.o_sb +
                       static_cast<int64_t>(it.hh) * args.o_sh + static_cast<int64_t>(row) * args.o_sr;
@@ -548,16 +566,38 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           wv[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-        if (store) {
+        if constexpr (STO) {
+          // 128-byte swizzle of the store's tensor map: 16-byte chunk jj of
+          // row r sits at chunk position jj ^ (r mod 8) of the row's 128 bytes
+          uint8_t* box = sm.o[t] + (cc >> 1) * 16384 + r * 128;
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const int jj = (cc & 1) * 4 + v4;
+            st_shared_v4(smem_u32(box + ((jj ^ (r & 7)) << 4)), wv[4 * v4], wv[4 * v4 + 1],
+                         wv[4 * v4 + 2], wv[4 * v4 + 3]);
+          }
+        } else if (store) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
             st_global_v4(dst + cc * 32 + v4 * 8, wv[4 * v4], wv[4 * v4 + 1], wv[4 * v4 + 2],
                          wv[4 * v4 + 3]);
         }
       }
+      if constexpr (STO) {
+        fence_proxy_async_smem();  // staged bytes visible to the TMA unit
+        named_bar_sync(1 + t, kRows);
+        const int row0 = it.q0 + t * kRows;
+        if (leader && row0 < args.n_q) {  // the map clips rows past n_q
+#pragma unroll
+          for (int bx = 0; bx < D / 64; ++bx)
+            tma_store_4d(&tm_o, sm.o[t] + bx * 16384, bx * 64, row0, it.hh, it.b);
+          bulk_commit_group();
+        }
+      }
       // the O reads above complete before this tile's next P store signals PV
       tc_fence_before();
     }
+    if (STO && leader) bulk_wait_group<0>();  // stores complete before the CTA exits
   }
 
   // ---------------------------------------------------------------- teardown
@@ -578,13 +618,13 @@ int num_sms() {
   return n;
 }
 
-template <int D, int NQT, int NK, int NV, int QB>
+template <int D, int NQT, int NK, int NV, int QB, bool STO>
 cudaError_t launch_variant(const AttnProblem& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                           const CUtensorMap& tm_v, cudaStream_t stream) {
-  using Smem = AttnSmem<D, NQT, NK, NV, QB>;
+                           const CUtensorMap& tm_v, const CUtensorMap& tm_o, cudaStream_t stream) {
+  using Smem = AttnSmem<D, NQT, NK, NV, QB, STO>;
   using Shape = AttnShape<D, NQT>;
   const size_t smem_bytes = sizeof(Smem) + 1024;  // + alignment slack
-  auto kernel = attn_fwd_bf16_kernel<D, NQT, NK, NV, QB>;
+  auto kernel = attn_fwd_bf16_kernel<D, NQT, NK, NV, QB, STO>;
   static unsigned long long configured = 0;
   cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured);
   if (e != cudaSuccess) return e;
@@ -614,25 +654,26 @@ cudaError_t launch_variant(const AttnProblem& p, const CUtensorMap& tm_q, const 
   a.o_sr = p.o_sr;
   const long long slots = static_cast<long long>(resident) * num_sms();
   const int grid = static_cast<int>(items < slots ? items : slots);
-  kernel<<<grid, Shape::kThreads, smem_bytes, stream>>>(tm_q, tm_k, tm_v, a);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(grid), dim3(Shape::kThreads), smem_bytes, stream, tm_q, tm_k, tm_v,
+                    tm_o, a);
 }
 
 }  // namespace
 
 cudaError_t launch_attn_bf16(const AttnProblem& p, const CUtensorMap& tm_q,
                              const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                             cudaStream_t stream) {
+                             const CUtensorMap& tm_o, cudaStream_t stream) {
   // Short query sets use one query tile per work item (two CTAs per SM at
-  // d = 64); longer ones pair two query tiles so each K/V tile feeds two MMAs.
+  // d = 64, with one Q buffer so two fit); longer ones pair two query tiles
+  // so each K/V tile feeds two MMAs.
   const bool pair = p.n_q > kRows;
   if (p.d == 64) {
-    return pair ? launch_variant<64, 2, 4, 4, 2>(p, tm_q, tm_k, tm_v, stream)
-                : launch_variant<64, 1, 2, 2, 2>(p, tm_q, tm_k, tm_v, stream);
+    return pair ? launch_variant<64, 2, 4, 4, 2, true>(p, tm_q, tm_k, tm_v, tm_o, stream)
+                : launch_variant<64, 1, 2, 2, 1, true>(p, tm_q, tm_k, tm_v, tm_o, stream);
   }
   if (p.d == 128) {
-    return pair ? launch_variant<128, 2, 2, 2, 1>(p, tm_q, tm_k, tm_v, stream)
-                : launch_variant<128, 1, 2, 2, 2>(p, tm_q, tm_k, tm_v, stream);
+    return pair ? launch_variant<128, 2, 2, 2, 1, false>(p, tm_q, tm_k, tm_v, tm_o, stream)
+                : launch_variant<128, 1, 2, 2, 2, true>(p, tm_q, tm_k, tm_v, tm_o, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -6,15 +6,19 @@
 //
 // Persistent kernel: one CTA per SM walks the 128 x 128 output tiles of all
 // groups (C = A B, fp32 accumulation in tensor memory):
-//   warp 0     TMA producer: per 128-deep K block, two A boxes (64 K x 128 M,
-//              K-major) and two B boxes (64 N x 128 K, N-major), kStages deep,
+//   warp 0     TMA producer: per 64-deep K block, one A box (64 K x 128 M,
+//              K-major) and two B boxes (64 N x 64 K, N-major), kStages deep,
 //              running ahead across tile boundaries
-//   warp 1     MMA issuer (one thread), 8 MMAs per K block; owns the TMEM
+//   warp 1     MMA issuer (one thread), 4 MMAs per K block; owns the TMEM
 //              allocation: two 128-column accumulators, so the epilogue of
 //              one tile overlaps the main loop of the next
-//   warps 2-5  epilogue: one thread per output row (TMEM lane), fp32 -> bf16,
-//              16-byte stores; the accumulator is released right after it is
-//              read into registers
+//   warps 2-5  epilogue: one thread per output row (TMEM lane) reads its
+//              accumulator row, releases the accumulator, converts to bf16
+//              into a 128-byte-swizzled staging tile in shared memory, and
+//              one thread writes the tile with two TMA stores. Row-per-thread
+//              global stores would leave each warp instruction scattered over
+//              32 rows; the TMA store writes whole lines. Two staging tiles
+//              alternate, so a store drains while the next tile is staged.
 // The head split needs no data movement: head i of Q is column block i of
 // the [B*n, h*d] result, which the attention kernel reads through strides.
 #include "kernels.h"
@@ -26,18 +30,22 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kBK = 128;
-constexpr int kStages = 3;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
 constexpr int kThreads = 192;
 constexpr int kAccCols = 128;
 constexpr int kTmemCols = 2 * kAccCols;
-constexpr int kABytes = kBM * kBK * 2;  // 32 KB: two 128-row x 128-byte K atoms
-constexpr int kBBytes = kBK * kBN * 2;  // 32 KB: two 128-row (K) x 128-byte N chunks
+constexpr int kABytes = kBM * kBK * 2;  // 16 KB: one 128-row x 128-byte K atom column
+constexpr int kBBytes = kBK * kBN * 2;  // 16 KB: two 64-row (K) x 128-byte N chunks
+constexpr int kBChunk = kBK * 128;      // bytes of one 64-wide N chunk
+constexpr int kCBytes = kBM * kBN * 2;  // 32 KB: one bf16 output tile (two 64-column boxes)
+constexpr uint32_t kEpiBarrier = 1;     // named barrier of the four epilogue warps
 constexpr unsigned long long kDrainLimitNs = 100ull * 1000ull * 1000ull;
 
 struct GemmSmem {
   alignas(1024) uint8_t a[kStages][kABytes];
   alignas(1024) uint8_t b[kStages][kBBytes];
+  alignas(1024) uint8_t c[2][kCBytes];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t acc_full[2];
@@ -98,6 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile uint32_t* abort_flag = &sm.abort_flag;
+  // the set-up above may overlap the previous kernel; global memory may not
+  griddep_launch_dependents();
+  griddep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -105,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       for (int i = 0; i < p.num_groups; ++i) {
         tma_prefetch_desc(&p.g[i].tm_a);
         tma_prefetch_desc(&p.g[i].tm_b);
+        tma_prefetch_desc(&p.g[i].tm_c);
       }
       int issued = 0;
       bool ok = true;
@@ -120,9 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
           mbar_arrive_expect_tx(&sm.full[s], kABytes + kBBytes);
           const int k0 = kb * kBK;
           tma_load_2d(sm.a[s], &c.g->tm_a, &sm.full[s], k0, c.m0);
-          tma_load_2d(sm.a[s] + 16384, &c.g->tm_a, &sm.full[s], k0 + 64, c.m0);
           tma_load_2d(sm.b[s], &c.g->tm_b, &sm.full[s], c.n0, k0);
-          tma_load_2d(sm.b[s] + 16384, &c.g->tm_b, &sm.full[s], c.n0 + 64, k0);
+          tma_load_2d(sm.b[s] + kBChunk, &c.g->tm_b, &sm.full[s], c.n0 + 64, k0);
           ++issued;
         }
       }
@@ -139,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       constexpr uint32_t kIdesc = idesc_bf16(kBM, kBN, false, true);
       // descriptors built once, advanced inside the start-address field
       const uint64_t da0 = sdesc_sw128(smem_u32(sm.a[0]), 16, 1024);     // K-major A
-      const uint64_t db0 = sdesc_sw128(smem_u32(sm.b[0]), 16384, 1024);  // N-major B
+      const uint64_t db0 = sdesc_sw128(smem_u32(sm.b[0]), kBChunk, 1024);  // N-major B
       int consumed = 0;
       int it = 0;
       bool ok = true;
@@ -159,10 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
           const uint64_t db = sdesc_advance(db0, static_cast<uint32_t>(s) * (kBBytes >> 4));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            // A: K-major, atom kk/4, 32 bytes per 16-element step inside it;
-            // B: N-major, 16 K rows = 2048 bytes; the second N chunk is 16 KB on
-            const uint32_t a_off = static_cast<uint32_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-            mma_bf16_ss(d_tmem, sdesc_advance(da, a_off), sdesc_advance(db, kk * (2048 >> 4)),
+            // A: K-major, 32 bytes per 16-element step inside the atom;
+            // B: N-major, 16 K rows = 2048 bytes; the second N chunk is kBChunk on
+            mma_bf16_ss(d_tmem, sdesc_advance(da, kk * (32 >> 4)), sdesc_advance(db, kk * (2048 >> 4)),
                         kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&sm.empty[s]);
@@ -180,13 +190,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
     const int quarter = warp & 3;
     const int r = quarter * 32 + static_cast<int>(lane);
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const bool leader = (warp == 2 && lane == 0);  // issues the tile's TMA stores
     int it = 0;
     for (int tile = first; tile < p.total_tiles; tile += stride, ++it) {
       const int acc = it & 1;
       const TileCoord c = tile_coord(p, tile);
-      const bool ok = __all_sync(
+      bool ok = __all_sync(
           0xffffffffu,
           mbar_wait(&sm.acc_full[acc], static_cast<uint32_t>(it >> 1) & 1u, abort_flag));
+      // staging tile it&1 was last written out two tiles ago: its store must
+      // have finished reading shared memory before it is overwritten
+      if (leader) bulk_wait_group_read<1>();
+      // one decision for all four warps: none is left waiting at a barrier
+      ok = named_bar_and(kEpiBarrier, 128, ok);
       if (!ok) break;
       tc_fence_after();
       uint32_t v[kBN];
@@ -201,21 +217,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       tc_fence_before();
       mbar_arrive(&sm.acc_empty[acc]);  // the MMA warp may reuse this accumulator
 
-      const int row = c.m0 + r;
-      if (row < c.g->M) {
-        uint16_t* crow = c.g->c + static_cast<int64_t>(row) * c.g->ldc;
+      uint8_t* stage = sm.c[it & 1];
+      // 128-byte swizzle of the store's tensor map: the 16-byte chunk j of
+      // row r sits at chunk position j ^ (r mod 8) of the row's 128 bytes
 #pragma unroll
-        for (int v8 = 0; v8 < kBN / 8; ++v8) {
-          const int col = c.n0 + v8 * 8;
-          if (col < c.g->N)
-            st_global_v4(crow + col,
-                         pack_bf16x2(__uint_as_float(v[8 * v8 + 0]), __uint_as_float(v[8 * v8 + 1])),
-                         pack_bf16x2(__uint_as_float(v[8 * v8 + 2]), __uint_as_float(v[8 * v8 + 3])),
-                         pack_bf16x2(__uint_as_float(v[8 * v8 + 4]), __uint_as_float(v[8 * v8 + 5])),
-                         pack_bf16x2(__uint_as_float(v[8 * v8 + 6]), __uint_as_float(v[8 * v8 + 7])));
+      for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t* e = v + half * 64 + j * 8;
+          st_shared_v4(smem_u32(stage + half * 16384 + r * 128 + ((j ^ (r & 7)) << 4)),
+                       pack_bf16x2(__uint_as_float(e[0]), __uint_as_float(e[1])),
+                       pack_bf16x2(__uint_as_float(e[2]), __uint_as_float(e[3])),
+                       pack_bf16x2(__uint_as_float(e[4]), __uint_as_float(e[5])),
+                       pack_bf16x2(__uint_as_float(e[6]), __uint_as_float(e[7])));
         }
       }
+      fence_proxy_async_smem();  // staged bytes visible to the TMA unit
+      named_bar_sync(kEpiBarrier, 128);
+      if (leader) {
+        // the map clips rows past M and columns past N
+        tma_store_2d(&c.g->tm_c, stage, c.n0, c.m0);
+        if (c.n0 + 64 < c.g->N) tma_store_2d(&c.g->tm_c, stage + 16384, c.n0 + 64, c.m0);
+        bulk_commit_group();
+      }
     }
+    if (leader) bulk_wait_group<0>();  // stores complete before the CTA exits
   }
 
   tc_fence_before();
@@ -244,8 +270,7 @@ cudaError_t launch_gemm_bf16(const GemmProblem& p, cudaStream_t stream) {
   cudaError_t e = set_smem_once(gemm_bf16_kernel, static_cast<int>(smem_bytes), &configured);
   if (e != cudaSuccess) return e;
   const int grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
-  gemm_bf16_kernel<<<grid, kThreads, smem_bytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(gemm_bf16_kernel, dim3(grid), dim3(kThreads), smem_bytes, stream, p);
 }
 
 TSD_DEFINE_ERROR_READER(take_device_error_gemm)

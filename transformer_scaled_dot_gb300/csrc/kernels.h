@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -22,11 +23,11 @@ struct AttnProblem {
   int64_t o_sb, o_sh, o_sr;
 };
 
-// bf16 tcgen05 attention; tensor maps describe Q, K, V as 4-D
-// (d, rows, heads, batch) bf16 tensors with 128-byte swizzled 64x128 boxes.
+// bf16 tcgen05 attention; tensor maps describe Q, K, V and the output O as
+// 4-D (d, rows, heads, batch) bf16 tensors with 128-byte swizzled 64x128 boxes.
 cudaError_t launch_attn_bf16(const AttnProblem& p, const CUtensorMap& tm_q,
                              const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                             cudaStream_t stream);
+                             const CUtensorMap& tm_o, cudaStream_t stream);
 
 struct AttnF32Problem {
   const float* q;
@@ -45,7 +46,8 @@ cudaError_t launch_attn_f32(const AttnF32Problem& p, cudaStream_t stream);
 // the x.W weight layout). Up to 3 groups share K and run in one launch.
 struct GemmGroup {
   CUtensorMap tm_a;  // 2-D (K, M), box 64 x 128
-  CUtensorMap tm_b;  // 2-D (N, K), box 64 x 128
+  CUtensorMap tm_b;  // 2-D (N, K), box 64 x 64
+  CUtensorMap tm_c;  // 2-D (N, M), box 64 x 128 (TMA store of the output tile)
   uint16_t* c;
   int64_t ldc;       // elements
   int M, N;
@@ -60,10 +62,12 @@ struct GemmProblem {
 };
 cudaError_t launch_gemm_bf16(const GemmProblem& p, cudaStream_t stream);
 
-// Raises a kernel's dynamic shared-memory limit once per device: the
-// attribute belongs to the device's context, and setting it on every launch
-// costs host time comparable to a short kernel. `done` holds one bit per
-// device ordinal (ordinals past 63 set it every time).
+// Raises a kernel's dynamic shared-memory limit once per device and asks
+// for the largest shared-memory carveout (else the occupancy query and the
+// launch may assume a smaller one, and fewer CTAs share an SM). The
+// attributes belong to the device's context, and setting them on every
+// launch costs host time comparable to a short kernel. `done` holds one bit
+// per device ordinal (ordinals past 63 set them every time).
 template <typename Kernel>
 inline cudaError_t set_smem_once(Kernel kernel, int bytes, unsigned long long* done) {
   int dev = 0;
@@ -72,8 +76,31 @@ inline cudaError_t set_smem_once(Kernel kernel, int bytes, unsigned long long* d
   const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
   if (bit != 0ull && (__atomic_load_n(done, __ATOMIC_ACQUIRE) & bit) != 0ull) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess && bit != 0ull) __atomic_fetch_or(done, bit, __ATOMIC_RELEASE);
   return e;
+}
+
+// Launches `kernel` on `stream` with programmatic stream serialization: it
+// may begin (prologue only: barrier set-up, tensor-memory allocation) while
+// the kernel ahead of it finishes. The kernels call griddep_wait() before
+// their first global-memory access.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Per-file device error words (read and cleared; see sm103.cuh).

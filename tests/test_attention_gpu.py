@@ -67,10 +67,12 @@ def test_attn_forward_matches_oracle(tsd, case):
     assert_bf16_close(got, ref, str(case))
 
 
-def test_attn_forward_key_lengths_zero_one_full(tsd):
-    """kv_len = 0 gives zero rows; 1 gives v_0 exactly; n_k is unmasked."""
-    a = synthetic.attention_inputs(2100, 3, 2, 200, 200, 64, 64, MASK_KEY_PADDING)
-    a.kv_lens = np.array([0, 1, 200], dtype=np.int32)
+@pytest.mark.parametrize("n,d", [(100, 64), (200, 64), (100, 128), (200, 128)])
+def test_attn_forward_key_lengths_zero_one_full(tsd, n, d):
+    """kv_len = 0 gives zero rows; 1 gives v_0 exactly; n_k is unmasked (one
+    and two query tiles per work item, both head sizes)."""
+    a = synthetic.attention_inputs(2100 + n + d, 3, 2, n, n, d, d, MASK_KEY_PADDING)
+    a.kv_lens = np.array([0, 1, n], dtype=np.int32)
     got = run_bf16(tsd, a)
     ref = oracle.attention(*a.as_f64(), MASK_KEY_PADDING, kv_lens=a.kv_lens)
     assert np.all(got[0] == 0.0)
@@ -82,6 +84,21 @@ def test_attn_forward_key_lengths_zero_one_full(tsd):
     got = run_bf16(tsd, a)
     ref = oracle.attention(*a.as_f64(), MASK_KEY_PADDING, kv_lens=a.kv_lens)
     assert_bf16_close(got, ref, "clamped lengths")
+
+
+@pytest.mark.parametrize("n_q,d", [(100, 64), (300, 64), (100, 128), (300, 128)])
+def test_attn_forward_no_keys_gives_zeros(tsd, n_q, d):
+    """n_k = 0: every row attends over an empty key set, whose result is 0.
+    K and V point at a small live buffer that must not be read."""
+    import torch
+    B, h = 2, 2
+    q = to_dev_bf16(synthetic.attention_inputs(2150, B, h, n_q, 1, d, d, MASK_NONE).q)
+    kv = torch.full((64,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = torch.full((B, h, n_q, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tsd.attn_forward(q, kv, kv, out, B, h, n_q, 0, d, d, MASK_NONE, None, 0.0)
+    torch.cuda.synchronize()
+    assert tsd.attn_get_device_status() == tsd.ATTN_OK
+    assert torch.all(out == 0).item()
 
 
 def test_attn_forward_explicit_scale(tsd):

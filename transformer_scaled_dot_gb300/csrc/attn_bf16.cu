@@ -34,7 +34,8 @@
 // Scores become base-2 exponents with the folded factor scale*log2(e); the max
 // is subtracted before the exponential, as the pages' reference run does
 // ("Attention Is All You Need 해부" (sj-techlog), section "직접 검증").
-// Masks: key tiles past the causal diagonal or past kv_len are never loaded;
+// Masks: key tiles past the causal diagonal or past kv_len are never loaded
+// (but for the first, loaded before kv_len is read, and unused if it is 0);
 // inside the boundary tile the masked logits become -inf before the max and
 // the exponential, so their weight is exactly 0 (section 3.2.3).
 // The running max is only raised when it grows by more than 2^8 (exponents
@@ -125,12 +126,18 @@ constexpr unsigned long long kDrainLimitNs = 100ull * 1000ull * 1000ull;  // 0.1
 struct Item {
   int b, hh, q0, kv_eff;
   int nt0, nt1;  // key tiles visited by query tile 0 / 1
+  int min_load;  // 1 if the key set is not empty by its shape (n_k > 0)
   __device__ int nt(int t) const { return t == 0 ? nt0 : nt1; }
   __device__ int nt_all() const { return nt0 > nt1 ? nt0 : nt1; }
+  // K/V tiles that pass through the rings: at least one when n_k > 0, so
+  // that the first key tile can be loaded before the key length is known
+  // (an item whose key length is 0 releases it unused)
+  __device__ int n_load() const { return nt_all() > min_load ? nt_all() : min_load; }
 };
 
+// Batch, head and first query row of item w (no memory access).
 template <int NQT>
-__device__ __forceinline__ Item item_at(const AttnArgs& a, int w) {
+__device__ __forceinline__ Item item_coords(const AttnArgs& a, int w) {
   const bool causal = (a.mask_kind & kMaskCausal) != 0;
   const int bh_count = a.B * a.h;
   int bh, qblk;
@@ -145,6 +152,17 @@ __device__ __forceinline__ Item item_at(const AttnArgs& a, int w) {
   it.b = bh / a.h;
   it.hh = bh % a.h;
   it.q0 = qblk * NQT * kRows;
+  it.kv_eff = 0;
+  it.nt0 = it.nt1 = 0;
+  it.min_load = a.n_k > 0 ? 1 : 0;
+  return it;
+}
+
+// The key range of an item (reads the key length).
+template <int NQT>
+__device__ __forceinline__ Item item_at(const AttnArgs& a, int w) {
+  const bool causal = (a.mask_kind & kMaskCausal) != 0;
+  Item it = item_coords<NQT>(a, w);
   int kv_eff = a.n_k;
   if (a.mask_kind & kMaskKeyPadding) {
     const int len = a.kv_lens[it.b];
@@ -221,6 +239,14 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile uint32_t* abort_flag = &sm.abort_flag;
+  if (warp == 0 && lane == 0) {
+    // descriptors live in the kernel parameters: fetched while the previous
+    // kernel finishes
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    if constexpr (STO) tma_prefetch_desc(&tm_o);
+  }
   // the set-up above may overlap the previous kernel; global memory may not
   griddep_launch_dependents();
   griddep_wait();
@@ -236,10 +262,6 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
     if (warp == 0) {
       // ---------------------------------------------------------- producer
       if (lane == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        if constexpr (STO) tma_prefetch_desc(&tm_o);
         int qn = 0, kn = 0, vn = 0;  // items / tiles issued into each ring
         bool ok = true;
         auto load_k = [&](const Item& it, int j) {
@@ -265,9 +287,9 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
           return true;
         };
         for (int i = 0, w = item_index(0); ok && w < args.num_items; w = item_index(++i)) {
-          const Item it = item_at<NQT>(args, w);
-          const int nt_all = it.nt_all();
-          if (nt_all == 0) continue;
+          // Q and the first key tile do not depend on the key length: both
+          // are on their way before it is read
+          const Item at = item_coords<NQT>(args, w);
           const int qs = qn % QB;
           ok = mbar_wait(&sm.q_empty[qs], (static_cast<uint32_t>(qn / QB) & 1u) ^ 1u, abort_flag);
           if (!ok) break;
@@ -275,13 +297,14 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
           for (int t = 0; t < NQT; ++t)
             for (int a = 0; a < kKAtoms; ++a)
               tma_load_4d(sm.q[qs][t] + a * 16384, &tm_q, &sm.q_full[qs], a * 64,
-                          it.q0 + t * kRows, it.hh, it.b);
+                          at.q0 + t * kRows, at.hh, at.b);
           ++qn;
+          if (at.min_load > 0) ok = load_k(at, 0);
+          const int n_load = item_at<NQT>(args, w).n_load();
           // keys run one tile ahead of values, the order the MMAs consume them
-          ok = load_k(it, 0);
-          for (int j = 0; ok && j < nt_all; ++j) {
-            if (j + 1 < nt_all) ok = load_k(it, j + 1);
-            if (ok) ok = load_v(it, j);
+          for (int j = 0; ok && j < n_load; ++j) {
+            if (j + 1 < n_load) ok = load_k(at, j + 1);
+            if (ok) ok = load_v(at, j);
           }
         }
         if (!ok) {
@@ -308,13 +331,12 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
         bool ok = true;
         for (int i = 0, w = item_index(0); ok && w < args.num_items; w = item_index(++i)) {
           const Item it = item_at<NQT>(args, w);
-          const int nt_all = it.nt_all();
-          if (nt_all == 0) continue;
+          const int n_load = it.n_load();
           const int qs = qc % QB;
           ok = mbar_wait(&sm.q_full[qs], static_cast<uint32_t>(qc / QB) & 1u, abort_flag);
           if (!ok) break;
           bool item_issued = false;
-          for (int j = 0; ok && j < nt_all; ++j) {
+          for (int j = 0; ok && j < n_load; ++j) {
             const int slot = kc % NK;
             // the slot holds K_j before this warp releases it, so a release for
             // tiles this issuer skips never counts toward an older use
@@ -377,8 +399,8 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
         bool ok = true;
         for (int i = 0, w = item_index(0); ok && w < args.num_items; w = item_index(++i)) {
           const Item it = item_at<NQT>(args, w);
-          const int nt_all = it.nt_all();
-          for (int j = 0; ok && j < nt_all; ++j) {
+          const int n_load = it.n_load();
+          for (int j = 0; ok && j < n_load; ++j) {
             const int slot = vc % NV;
             // as for K: the slot holds V_j before any release by this warp
             ok = mbar_wait(&sm.v_full[slot], static_cast<uint32_t>(vc / NV) & 1u, abort_flag);
@@ -544,7 +566,8 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
         // the staging tile's previous store has finished reading it, and the
         // warpgroup's four warps take one decision (none is left at a barrier)
         if (leader) bulk_wait_group_read<0>();
-        ok = named_bar_and(1 + t, kRows, ok);
+        // one named barrier per query tile (ids are immediates)
+        ok = t == 0 ? named_bar_and<1>(kRows, ok) : named_bar_and<2>(kRows, ok);
       }
       if (!ok) break;
       if (ntt > 0) tc_fence_after();
@@ -585,7 +608,8 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
       }
       if constexpr (STO) {
         fence_proxy_async_smem();  // staged bytes visible to the TMA unit
-        named_bar_sync(1 + t, kRows);
+        if (t == 0) named_bar_sync<1>(kRows);
+        else named_bar_sync<2>(kRows);
         const int row0 = it.q0 + t * kRows;
         if (leader && row0 < args.n_q) {  // the map clips rows past n_q
 #pragma unroll

@@ -4,21 +4,31 @@
 // Need" (kimjiil.github.io), section 3.2.2; weights in the x.W layout,
 // [d_model, h*d], no biases).
 //
-// Persistent kernel: one CTA per SM walks the 128 x 128 output tiles of all
-// groups (C = A B, fp32 accumulation in tensor memory):
-//   warp 0     TMA producer: per 64-deep K block, one A box (64 K x 128 M,
-//              K-major) and two B boxes (64 N x 64 K, N-major), kStages deep,
-//              running ahead across tile boundaries
-//   warp 1     MMA issuer (one thread), 4 MMAs per K block; owns the TMEM
-//              allocation: two 128-column accumulators, so the epilogue of
-//              one tile overlaps the main loop of the next
+// Persistent kernel, optionally in clusters of CM CTAs stacked along M: a
+// cluster walks groups of CM vertically adjacent 128 x 128 output tiles that
+// share their B (weight) tile, each B tile then read from L2 once per cluster.
+// The projections are bound by L2 -> SM traffic, not by the tensor cores, but
+// what limits them is the bytes each SM receives, which multicast does not
+// reduce (kGemmClusterM = 2 measured slower than 1 on the MHA shapes, the
+// pair waiting on each other's stage releases). Per CTA (C = A B, fp32
+// accumulation in tensor memory):
+//   warp 0     TMA producer: per 64-deep K block, its own A box (64 K x 128 M,
+//              K-major) and 1/CM of the K rows of the two B boxes (64 N each,
+//              N-major), multicast to every CTA of the cluster; kStages deep
+//              (as many bytes in flight as shared memory allows: the loads,
+//              not the MMAs, set the pace), running ahead across tiles
+//   warp 1     MMA issuer (one thread), 4 MMAs per K block, whose completion
+//              frees the stage in every CTA of the cluster (each stage holds
+//              bytes written by all of them); owns the TMEM allocation: two
+//              128-column accumulators, so the epilogue of one tile overlaps
+//              the main loop of the next
 //   warps 2-5  epilogue: one thread per output row (TMEM lane) reads its
 //              accumulator row, releases the accumulator, converts to bf16
 //              into a 128-byte-swizzled staging tile in shared memory, and
 //              one thread writes the tile with two TMA stores. Row-per-thread
 //              global stores would leave each warp instruction scattered over
-//              32 rows; the TMA store writes whole lines. Two staging tiles
-//              alternate, so a store drains while the next tile is staged.
+//              32 rows; the TMA store writes whole lines. The store drains
+//              while the next tile's main loop runs.
 // The head split needs no data movement: head i of Q is column block i of
 // the [B*n, h*d] result, which the attention kernel reads through strides.
 #include "kernels.h"
@@ -30,8 +40,8 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kBK = 64;
-constexpr int kStages = 4;
+constexpr int kBK = kGemmBK;
+constexpr int kStages = 6;
 constexpr int kThreads = 192;
 constexpr int kAccCols = 128;
 constexpr int kTmemCols = 2 * kAccCols;
@@ -39,13 +49,15 @@ constexpr int kABytes = kBM * kBK * 2;  // 16 KB: one 128-row x 128-byte K atom 
 constexpr int kBBytes = kBK * kBN * 2;  // 16 KB: two 64-row (K) x 128-byte N chunks
 constexpr int kBChunk = kBK * 128;      // bytes of one 64-wide N chunk
 constexpr int kCBytes = kBM * kBN * 2;  // 32 KB: one bf16 output tile (two 64-column boxes)
+constexpr int kCStages = 1;             // output staging tiles
 constexpr uint32_t kEpiBarrier = 1;     // named barrier of the four epilogue warps
 constexpr unsigned long long kDrainLimitNs = 100ull * 1000ull * 1000ull;
+static_assert(kGemmClusterM >= 1 && kBK % kGemmClusterM == 0, "B rows split over the cluster");
 
 struct GemmSmem {
   alignas(1024) uint8_t a[kStages][kABytes];
   alignas(1024) uint8_t b[kStages][kBBytes];
-  alignas(1024) uint8_t c[2][kCBytes];
+  alignas(1024) uint8_t c[kCStages][kCBytes];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t acc_full[2];
@@ -60,19 +72,23 @@ struct TileCoord {
   int m0, n0;
 };
 
-__device__ __forceinline__ TileCoord tile_coord(const GemmProblem& p, int tile) {
+// Cluster tile `ct` (CM row tiles x one column tile) -> this CTA's tile.
+template <int CM>
+__device__ __forceinline__ TileCoord tile_coord(const GemmProblem& p, int ct, int rank) {
   int gi = 0;
   for (int i = 1; i < p.num_groups; ++i)
-    if (tile >= p.g[i].tile_begin) gi = i;
+    if (ct >= p.g[i].tile_begin) gi = i;
   const GemmGroup& G = p.g[gi];
-  const int local = tile - G.tile_begin;
+  const int local = ct - G.tile_begin;
+  const int ctm = (G.tiles_m + CM - 1) / CM;
   TileCoord c;
   c.g = &G;
-  c.m0 = (local % G.tiles_m) * kBM;  // m fastest: neighbouring CTAs share B
-  c.n0 = (local / G.tiles_m) * kBN;
+  c.m0 = ((local % ctm) * CM + rank) * kBM;  // m fastest: neighbouring clusters share B
+  c.n0 = (local / ctm) * kBN;
   return c;
 }
 
+template <int CM>
 __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_constant__ GemmProblem p) {
   extern __shared__ uint8_t smem_raw[];
   GemmSmem& sm = *reinterpret_cast<GemmSmem*>(
@@ -80,14 +96,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
   const int warp = warp_id();
   const uint32_t lane = lane_id();
   const int kblocks = (p.K + kBK - 1) / kBK;
-  // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
-  const int first = blockIdx.x;
-  const int stride = gridDim.x;
+  const int rank = CM > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CM) - 1u);
+  constexpr int kBRows = kBK / CM;  // K rows of each B box this CTA loads
+  // cluster tiles of this CTA's cluster: cluster id, + number of clusters, ...
+  const int first = static_cast<int>(blockIdx.x) / CM;
+  const int stride = static_cast<int>(gridDim.x) / CM;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.empty[s], CM);  // released by the MMA warp of every CTA
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sm.acc_full[a], 1);
@@ -102,10 +121,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  // barriers of every CTA initialised before any peer multicasts into them
+  if constexpr (CM > 1) cluster_sync();
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile uint32_t* abort_flag = &sm.abort_flag;
+  if (warp == 0 && lane == 0) {
+    // descriptors live in the kernel parameters: fetched while the previous
+    // kernel finishes
+    for (int i = 0; i < p.num_groups; ++i) {
+      tma_prefetch_desc(&p.g[i].tm_a);
+      tma_prefetch_desc(&p.g[i].tm_b);
+      tma_prefetch_desc(&p.g[i].tm_c);
+    }
+  }
   // the set-up above may overlap the previous kernel; global memory may not
   griddep_launch_dependents();
   griddep_wait();
@@ -113,18 +143,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      for (int i = 0; i < p.num_groups; ++i) {
-        tma_prefetch_desc(&p.g[i].tm_a);
-        tma_prefetch_desc(&p.g[i].tm_b);
-        tma_prefetch_desc(&p.g[i].tm_c);
-      }
       int issued = 0;
       bool ok = true;
-      for (int tile = first; ok && tile < p.total_tiles; tile += stride) {
-        const TileCoord c = tile_coord(p, tile);
+      for (int ct = first; ok && ct < p.total_tiles; ct += stride) {
+        const TileCoord c = tile_coord<CM>(p, ct, rank);
         for (int kb = 0; kb < kblocks; ++kb) {
           const int s = issued % kStages;
           const uint32_t ph = static_cast<uint32_t>(issued / kStages) & 1u;
+          // stage free in every CTA of the cluster (this CTA writes into all)
           if (!mbar_wait(&sm.empty[s], ph ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -132,29 +158,38 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
           mbar_arrive_expect_tx(&sm.full[s], kABytes + kBBytes);
           const int k0 = kb * kBK;
           tma_load_2d(sm.a[s], &c.g->tm_a, &sm.full[s], k0, c.m0);
-          tma_load_2d(sm.b[s], &c.g->tm_b, &sm.full[s], c.n0, k0);
-          tma_load_2d(sm.b[s] + kBChunk, &c.g->tm_b, &sm.full[s], c.n0 + 64, k0);
+          const int kr = k0 + rank * kBRows;
+          uint8_t* bdst = sm.b[s] + rank * kBRows * 128;
+          if constexpr (CM > 1) {
+            tma_load_2d_multicast(bdst, &c.g->tm_b, &sm.full[s], c.n0, kr, kClusterMask);
+            tma_load_2d_multicast(bdst + kBChunk, &c.g->tm_b, &sm.full[s], c.n0 + 64, kr,
+                                  kClusterMask);
+          } else {
+            tma_load_2d(bdst, &c.g->tm_b, &sm.full[s], c.n0, kr);
+            tma_load_2d(bdst + kBChunk, &c.g->tm_b, &sm.full[s], c.n0 + 64, kr);
+          }
           ++issued;
         }
       }
-      if (!ok) {
-        volatile uint32_t never = 0;
-        for (int i = max(0, issued - kStages); i < issued; ++i)
-          mbar_wait(&sm.full[i % kStages], static_cast<uint32_t>(i / kStages) & 1u, &never,
-                    kDrainLimitNs);
-      }
+      // Every stage this CTA wrote has been released by all CTAs: no peer's
+      // release is still on its way here when the cluster leaves (and, after
+      // an abort, no copy of this CTA is in flight).
+      volatile uint32_t never = 0;
+      for (int i = max(0, issued - kStages); i < issued; ++i)
+        mbar_wait(&sm.empty[i % kStages], static_cast<uint32_t>(i / kStages) & 1u,
+                  ok ? abort_flag : &never, kDrainLimitNs);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_bf16(kBM, kBN, false, true);
       // descriptors built once, advanced inside the start-address field
-      const uint64_t da0 = sdesc_sw128(smem_u32(sm.a[0]), 16, 1024);     // K-major A
+      const uint64_t da0 = sdesc_sw128(smem_u32(sm.a[0]), 16, 1024);       // K-major A
       const uint64_t db0 = sdesc_sw128(smem_u32(sm.b[0]), kBChunk, 1024);  // N-major B
       int consumed = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = first; ok && tile < p.total_tiles; tile += stride, ++it) {
+      for (int ct = first; ok && ct < p.total_tiles; ct += stride, ++it) {
         const int acc = it & 1;
         // the epilogue has read this accumulator's previous tile
         ok = mbar_wait(&sm.acc_empty[acc], (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, abort_flag);
@@ -175,7 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
             mma_bf16_ss(d_tmem, sdesc_advance(da, kk * (32 >> 4)), sdesc_advance(db, kk * (2048 >> 4)),
                         kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&sm.empty[s]);
+          if constexpr (CM > 1) mma_commit_multicast(&sm.empty[s], kClusterMask);
+          else mma_commit(&sm.empty[s]);
           ++consumed;
         }
         if (ok) mma_commit(&sm.acc_full[acc]);
@@ -192,17 +228,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const bool leader = (warp == 2 && lane == 0);  // issues the tile's TMA stores
     int it = 0;
-    for (int tile = first; tile < p.total_tiles; tile += stride, ++it) {
+    for (int ct = first; ct < p.total_tiles; ct += stride, ++it) {
       const int acc = it & 1;
-      const TileCoord c = tile_coord(p, tile);
+      const TileCoord c = tile_coord<CM>(p, ct, rank);
       bool ok = __all_sync(
           0xffffffffu,
           mbar_wait(&sm.acc_full[acc], static_cast<uint32_t>(it >> 1) & 1u, abort_flag));
-      // staging tile it&1 was last written out two tiles ago: its store must
-      // have finished reading shared memory before it is overwritten
-      if (leader) bulk_wait_group_read<1>();
+      // this staging tile was last written out kCStages tiles ago: its store
+      // must have finished reading shared memory before it is overwritten
+      if (leader) bulk_wait_group_read<kCStages - 1>();
       // one decision for all four warps: none is left waiting at a barrier
-      ok = named_bar_and(kEpiBarrier, 128, ok);
+      ok = named_bar_and<kEpiBarrier>(128, ok);
       if (!ok) break;
       tc_fence_after();
       uint32_t v[kBN];
@@ -217,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       tc_fence_before();
       mbar_arrive(&sm.acc_empty[acc]);  // the MMA warp may reuse this accumulator
 
-      uint8_t* stage = sm.c[it & 1];
+      uint8_t* stage = sm.c[it % kCStages];
       // 128-byte swizzle of the store's tensor map: the 16-byte chunk j of
       // row r sits at chunk position j ^ (r mod 8) of the row's 128 bytes
 #pragma unroll
@@ -233,8 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
         }
       }
       fence_proxy_async_smem();  // staged bytes visible to the TMA unit
-      named_bar_sync(kEpiBarrier, 128);
-      if (leader) {
+      named_bar_sync<kEpiBarrier>(128);
+      // a cluster's last row tiles may lie past M: computed on zero rows, not stored
+      if (leader && c.m0 < c.g->M) {
         // the map clips rows past M and columns past N
         tma_store_2d(&c.g->tm_c, stage, c.n0, c.m0);
         if (c.n0 + 64 < c.g->N) tma_store_2d(&c.g->tm_c, stage + 16384, c.n0 + 64, c.m0);
@@ -245,7 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
   }
 
   tc_fence_before();
-  __syncthreads();
+  // no CTA leaves while a peer may still write into its shared memory
+  if constexpr (CM > 1) cluster_sync();
+  else __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
@@ -263,14 +302,48 @@ int num_sms() {
 
 }  // namespace
 
-cudaError_t launch_gemm_bf16(const GemmProblem& p, cudaStream_t stream) {
-  if (p.total_tiles <= 0) return cudaSuccess;
+cudaError_t launch_gemm_bf16(const GemmProblem& problem, cudaStream_t stream) {
+  constexpr int CM = kGemmClusterM;
+  // tiles counted per cluster: CM row tiles x one column tile
+  GemmProblem p = problem;
+  int t = 0;
+  for (int i = 0; i < p.num_groups; ++i) {
+    p.g[i].tile_begin = t;
+    t += ((p.g[i].tiles_m + CM - 1) / CM) * p.g[i].tiles_n;
+  }
+  p.total_tiles = t;
+  if (t <= 0) return cudaSuccess;
   const size_t smem_bytes = sizeof(GemmSmem) + 1024;
+  auto kernel = gemm_bf16_kernel<CM>;
   static unsigned long long configured = 0;
-  cudaError_t e = set_smem_once(gemm_bf16_kernel, static_cast<int>(smem_bytes), &configured);
+  cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured);
   if (e != cudaSuccess) return e;
-  const int grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
-  return launch_pdl(gemm_bf16_kernel, dim3(grid), dim3(kThreads), smem_bytes, stream, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CM;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  // persistent: as many clusters as can be resident at once (clusters stay
+  // inside one GPC, so this can be below SMs / CM)
+  static int max_clusters = 0;
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(num_sms() / CM * CM);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters = n > 0 ? n : 1;
+  }
+  const int clusters = t < max_clusters ? t : max_clusters;
+  cfg.gridDim = dim3(clusters * CM);
+  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 TSD_DEFINE_ERROR_READER(take_device_error_gemm)

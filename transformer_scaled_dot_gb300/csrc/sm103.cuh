@@ -156,6 +156,33 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// The same box delivered to the shared memory of every CTA in `cta_mask`
+// (same offsets), each destination's mbarrier at `bar`'s offset receiving
+// the bytes written there. Cluster launches only; this GPU's own memory.
+__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map,
+                                                      uint64_t* bar, int c0, int c1,
+                                                      uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask)
+      : "memory");
+}
+
+// ------------------------------------------------------------------ clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Whole-cluster barrier (every thread of every CTA of the cluster), with
+// release / acquire ordering of shared and global memory.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
 // Shared -> global tensor store of one box (clipped at the tensor's bounds),
 // tracked by this thread's bulk-group counter.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0,
@@ -188,14 +215,20 @@ __device__ __forceinline__ void bulk_wait_group() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Named barrier `id` (1..15) over `count` threads (a multiple of 32).
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+// Named barrier ID (1..15) over `count` threads (a multiple of 32). The id is
+// an immediate: with a register id the compiler must reserve all sixteen
+// barriers for the CTA, which keeps a second CTA off the SM.
+template <uint32_t ID>
+__device__ __forceinline__ void named_bar_sync(uint32_t count) {
+  static_assert(ID >= 1 && ID <= 15, "named barrier id");
+  asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(count) : "memory");
 }
 
 // Named barrier that also ANDs a predicate over the participating threads:
 // every thread gets the same answer, so all of them leave a loop together.
-__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool v) {
+template <uint32_t ID>
+__device__ __forceinline__ bool named_bar_and(uint32_t count, bool v) {
+  static_assert(ID >= 1 && ID <= 15, "named barrier id");
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
@@ -203,7 +236,7 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool 
       "barrier.cta.red.and.pred p, %2, %3, q;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(r)
-      : "r"(v ? 1u : 0u), "r"(id), "r"(count)
+      : "r"(v ? 1u : 0u), "n"(ID), "r"(count)
       : "memory");
   return r != 0u;
 }
@@ -294,6 +327,16 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
+      : "memory");
+}
+
+// As mma_commit, but the arrival lands on the mbarrier at `bar`'s offset in
+// every CTA of `cta_mask` (cluster launches).
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
       : "memory");
 }
 

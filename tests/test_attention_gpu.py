@@ -55,6 +55,9 @@ CASES = [
     (2, 2, 128, 160, 128, MASK_KEY_PADDING, (1, 160)),
     (1, 2, 600, 600, 128, MASK_CAUSAL | MASK_KEY_PADDING, (200, 600)),
     (1, 1, 384, 700, 128, MASK_NONE, None),
+    # more single-tile items than pipelines: every slot walks several items
+    (40, 16, 100, 100, 64, MASK_KEY_PADDING, (1, 100)),
+    (32, 16, 128, 128, 64, MASK_CAUSAL, None),
 ]
 
 

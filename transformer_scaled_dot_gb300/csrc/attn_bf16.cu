@@ -3,8 +3,12 @@
 // (kimjiil.github.io), section 3.2.1, eq. (1)).
 //
 // Persistent kernel. The work items are (batch, head, query block), a query
-// block being NQT tiles of 128 query rows; each CTA walks its share of them
-// (causal: largest blocks first). Per CTA:
+// block being NQT tiles of 128 query rows; each pipeline walks its share of
+// them (causal: largest blocks first). A CTA holds one pipeline, or two
+// ("slots", for single-tile items at d = 64: a CTA that allocates tensor
+// memory has its SM to itself, so two pipelines per SM share one CTA, each
+// with its own warps, shared memory, barriers and 256 TMEM columns). Per
+// pipeline (warp numbers within the slot):
 //
 //   warp 0      TMA producer: per item the Q tiles (double-buffered where
 //               shared memory allows, so the next item's Q loads during this
@@ -16,7 +20,7 @@
 //               tile, PV: 8 of N=128) warps 1, 2 issue S for tiles 0, 1 and
 //               warp 3 issues PV; at d = 64 (S: 4 MMAs, PV: 8 of N=64, the
 //               less efficient shape) warp 1 issues S and warps 2, 3 issue PV
-//               for tiles 0, 1. Warp 1 owns the TMEM allocation. Several
+//               for tiles 0, 1. Warp 1 allocates the TMEM of all slots. Several
 //               issuing threads keep the tensor pipe fed: each thread's waits
 //               and commits (tcgen05.commit tracks only its own MMAs) overlap
 //               the others' MMA issue.
@@ -55,9 +59,12 @@ namespace {
 constexpr int kRows = 128;                 // query rows per tile (MMA M) and keys per tile
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D, int NQT>
+template <int D, int NQT, int SL>
 struct AttnShape {
-  static constexpr int kThreads = 128 + 128 * NQT;  // 4 control warps + softmax warpgroups
+  // per slot: 4 control warps + NQT softmax warpgroups; SL slots per CTA
+  static constexpr int kSlotThreads = 128 + 128 * NQT;
+  static constexpr int kSlotWarps = kSlotThreads / 32;
+  static constexpr int kThreads = SL * kSlotThreads;
   // P (bf16, 64 columns per query tile) gets its own TMEM columns unless S and
   // O of two 128-wide tiles already fill all 512; then it overwrites the first
   // half of its S tile, and S_t(j+1) waits for PV_t(j) to have read it.
@@ -69,16 +76,15 @@ struct AttnShape {
   __host__ __device__ static constexpr int p_col(int t) {
     return kPAliasS ? s_col(t) : NQT * kRows + NQT * D + t * 64;
   }
-  // two CTAs share an SM when tensor memory allows (256 columns each)
-  static constexpr int kMinBlocks = kTmemCols <= 256 ? 2 : 1;
+  static_assert(SL == 1 || kTmemCols <= 256, "slots share the 512 tensor-memory columns");
   // control warps give up registers to the softmax warpgroups (the sum stays
-  // within what the CTA was launched with); a single-tile CTA alone on its
-  // SM needs no split
-  static constexpr bool kRegSplit = (NQT == 2) || (kMinBlocks == 2);
-  static constexpr uint32_t kLaunchRegs = 65536 / (kThreads * kMinBlocks) / 8 * 8;
+  // within what the CTA was launched with); a single-tile single-slot CTA
+  // has registers to spare and needs no split
+  static constexpr bool kRegSplit = (NQT == 2) || (SL == 2);
+  static constexpr uint32_t kLaunchRegs = 65536 / kThreads / 8 * 8;
   static constexpr uint32_t kCtrlRegs = NQT == 1 ? 56 : (D == 64 ? 72 : 104);
   static constexpr uint32_t kSoftmaxRegs =
-      (kLaunchRegs * kThreads - kCtrlRegs * 128) / (128 * NQT) / 8 * 8;
+      (kLaunchRegs * kSlotThreads - kCtrlRegs * 128) / (128 * NQT) / 8 * 8;
   // one issuer per query tile for S (else for PV), see the role table above
   static constexpr bool kSplitS = (D == 128);
   static constexpr int kSIssuers = kSplitS ? NQT : 1;
@@ -88,7 +94,7 @@ struct AttnShape {
   // in what the CTA was launched with, or the increase would never complete
   static_assert(!kRegSplit || kSoftmaxRegs <= 256, "register split");
   static_assert(!kRegSplit ||
-                    kCtrlRegs * 128 + kSoftmaxRegs * 128 * NQT <= kLaunchRegs * kThreads,
+                    SL * (kCtrlRegs * 128 + kSoftmaxRegs * 128 * NQT) <= kLaunchRegs * kThreads,
                 "register split exceeds the launch allocation");
 };
 
@@ -107,7 +113,6 @@ struct AttnSmem {
   uint64_t p_full[NQT];
   uint64_t pv_done[NQT];
   uint64_t s_drained[NQT], pv_drained[NQT];
-  uint32_t tmem_base;
   uint32_t abort_flag;
 };
 
@@ -182,31 +187,39 @@ __device__ __forceinline__ Item item_at(const AttnArgs& a, int w) {
   return it;
 }
 
-template <int D, int NQT, int NK, int NV, int QB, bool STO>
-__global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>::kMinBlocks)
+template <int D, int NQT, int NK, int NV, int QB, bool STO, int SL>
+__global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_o, const AttnArgs args) {
   using Smem = AttnSmem<D, NQT, NK, NV, QB, STO>;
-  using Shape = AttnShape<D, NQT>;
+  using Shape = AttnShape<D, NQT, SL>;
   constexpr int kKAtoms = D / 64;  // 128-byte swizzle atoms along the head dimension
 
-  extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-
-  const int warp = warp_id();
+  // Slots: SL independent pipelines in one CTA (a CTA that allocates tensor
+  // memory has an SM to itself, so a second pipeline per SM has to live in
+  // the same CTA). Each slot has its own warps, shared memory, barriers and
+  // tensor-memory columns, and walks its own items.
+  const int slot = SL > 1 ? warp_id() / Shape::kSlotWarps : 0;
+  const int warp = warp_id() - slot * Shape::kSlotWarps;  // warp within the slot
   const uint32_t lane = lane_id();
-  const bool causal = (args.mask_kind & kMaskCausal) != 0;
-  // Item i of this CTA: round i of the grid, taken in snake order (forward in
-  // even rounds, backward in odd ones), so that with causal items sorted
-  // longest first every CTA's total stays close to the others'.
-  const int cta = static_cast<int>(blockIdx.x);
-  const int grid = static_cast<int>(gridDim.x);
-  auto item_index = [&](int i) { return i * grid + ((i & 1) ? grid - 1 - cta : cta); };
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = reinterpret_cast<Smem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023))[slot];
+  __shared__ uint32_t tmem_all;
 
-  if (threadIdx.x == 0) {
+  const bool causal = (args.mask_kind & kMaskCausal) != 0;
+  // Item i of this slot: round i over all slots of the grid (slot 0 of every
+  // CTA before any slot 1, so that no SM holds two items while another is
+  // idle), taken in snake order (forward in even rounds, backward in odd
+  // ones), so that with causal items sorted longest first every slot's
+  // total stays close to the others'.
+  const int vcta = slot * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
+  const int vgrid = SL * static_cast<int>(gridDim.x);
+  auto item_index = [&](int i) { return i * vgrid + ((i & 1) ? vgrid - 1 - vcta : vcta); };
+
+  if (warp == 0 && lane == 0) {
     for (int s = 0; s < QB; ++s) {
       mbar_init(&sm.q_full[s], 1);
       mbar_init(&sm.q_empty[s], Shape::kSIssuers);  // one release per S-issuing warp
@@ -230,14 +243,14 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
     sm.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
-    tmem_alloc(&sm.tmem_base, Shape::kTmemCols);
+  if (warp_id() == 1) {  // one allocation for all slots (the permit is per CTA)
+    tmem_alloc(&tmem_all, SL * Shape::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = sm.tmem_base;
+  const uint32_t tmem = tmem_all + static_cast<uint32_t>(slot * Shape::kTmemCols);
   volatile uint32_t* abort_flag = &sm.abort_flag;
   if (warp == 0 && lane == 0) {
     // descriptors live in the kernel parameters: fetched while the previous
@@ -247,9 +260,9 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
     tma_prefetch_desc(&tm_v);
     if constexpr (STO) tma_prefetch_desc(&tm_o);
   }
-  // the set-up above may overlap the previous kernel; global memory may not
+  // Everything up to a role's first global-memory access may overlap the
+  // previous kernel: each role waits for it (griddep_wait) just before.
   griddep_launch_dependents();
-  griddep_wait();
 
   // Descriptors are built once; each MMA only advances the start-address
   // field by a compile-time offset (sdesc_advance keeps the sum inside it).
@@ -265,23 +278,23 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
         int qn = 0, kn = 0, vn = 0;  // items / tiles issued into each ring
         bool ok = true;
         auto load_k = [&](const Item& it, int j) {
-          const int slot = kn % NK;
-          if (!mbar_wait(&sm.k_empty[slot], (static_cast<uint32_t>(kn / NK) & 1u) ^ 1u, abort_flag))
+          const int rs = kn % NK;
+          if (!mbar_wait(&sm.k_empty[rs], (static_cast<uint32_t>(kn / NK) & 1u) ^ 1u, abort_flag))
             return false;
-          mbar_arrive_expect_tx(&sm.k_full[slot], Smem::kTileBytes);
+          mbar_arrive_expect_tx(&sm.k_full[rs], Smem::kTileBytes);
           for (int a = 0; a < kKAtoms; ++a)
-            tma_load_4d(sm.k[slot] + a * 16384, &tm_k, &sm.k_full[slot], a * 64, j * kRows, it.hh,
+            tma_load_4d(sm.k[rs] + a * 16384, &tm_k, &sm.k_full[rs], a * 64, j * kRows, it.hh,
                         it.b);
           ++kn;
           return true;
         };
         auto load_v = [&](const Item& it, int j) {
-          const int slot = vn % NV;
-          if (!mbar_wait(&sm.v_empty[slot], (static_cast<uint32_t>(vn / NV) & 1u) ^ 1u, abort_flag))
+          const int rs = vn % NV;
+          if (!mbar_wait(&sm.v_empty[rs], (static_cast<uint32_t>(vn / NV) & 1u) ^ 1u, abort_flag))
             return false;
-          mbar_arrive_expect_tx(&sm.v_full[slot], Smem::kTileBytes);
+          mbar_arrive_expect_tx(&sm.v_full[rs], Smem::kTileBytes);
           for (int a = 0; a < kKAtoms; ++a)
-            tma_load_4d(sm.v[slot] + a * 16384, &tm_v, &sm.v_full[slot], a * 64, j * kRows, it.hh,
+            tma_load_4d(sm.v[rs] + a * 16384, &tm_v, &sm.v_full[rs], a * 64, j * kRows, it.hh,
                         it.b);
           ++vn;
           return true;
@@ -294,6 +307,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
           ok = mbar_wait(&sm.q_empty[qs], (static_cast<uint32_t>(qn / QB) & 1u) ^ 1u, abort_flag);
           if (!ok) break;
           mbar_arrive_expect_tx(&sm.q_full[qs], NQT * Smem::kTileBytes);
+          if (qn == 0) griddep_wait();
           for (int t = 0; t < NQT; ++t)
             for (int a = 0; a < kKAtoms; ++a)
               tma_load_4d(sm.q[qs][t] + a * 16384, &tm_q, &sm.q_full[qs], a * 64,
@@ -329,6 +343,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
         int qc = 0, kc = 0;    // items / key tiles consumed
         int sc0 = 0, sc1 = 0;  // S tiles issued per query tile (phase counters)
         bool ok = true;
+        griddep_wait();  // the key lengths may come from the previous kernel
         for (int i = 0, w = item_index(0); ok && w < args.num_items; w = item_index(++i)) {
           const Item it = item_at<NQT>(args, w);
           const int n_load = it.n_load();
@@ -337,12 +352,12 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
           if (!ok) break;
           bool item_issued = false;
           for (int j = 0; ok && j < n_load; ++j) {
-            const int slot = kc % NK;
-            // the slot holds K_j before this warp releases it, so a release for
-            // tiles this issuer skips never counts toward an older use
-            ok = mbar_wait(&sm.k_full[slot], static_cast<uint32_t>(kc / NK) & 1u, abort_flag);
+            const int rs = kc % NK;
+            // the ring slot holds K_j before this warp releases it, so a release
+            // for tiles this issuer skips never counts toward an older use
+            ok = mbar_wait(&sm.k_full[rs], static_cast<uint32_t>(kc / NK) & 1u, abort_flag);
             if (!ok) break;
-            const uint64_t bk = sdesc_advance(dk0, static_cast<uint32_t>(slot) * kTileStep);
+            const uint64_t bk = sdesc_advance(dk0, static_cast<uint32_t>(rs) * kTileStep);
             bool issued = false;
             for (int t = t_lo; ok && t < t_hi; ++t) {
               if (j >= it.nt(t)) continue;
@@ -371,8 +386,8 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
               issued = true;
             }
             if (!ok) break;
-            if (issued) mma_commit(&sm.k_empty[slot]);
-            else mbar_arrive(&sm.k_empty[slot]);
+            if (issued) mma_commit(&sm.k_empty[rs]);
+            else mbar_arrive(&sm.k_empty[rs]);
             item_issued = item_issued || issued;
             ++kc;
           }
@@ -397,15 +412,16 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
         int vc = 0;            // value tiles consumed
         int pc0 = 0, pc1 = 0;  // PV products issued per query tile (phase counters)
         bool ok = true;
+        griddep_wait();
         for (int i = 0, w = item_index(0); ok && w < args.num_items; w = item_index(++i)) {
           const Item it = item_at<NQT>(args, w);
           const int n_load = it.n_load();
           for (int j = 0; ok && j < n_load; ++j) {
-            const int slot = vc % NV;
-            // as for K: the slot holds V_j before any release by this warp
-            ok = mbar_wait(&sm.v_full[slot], static_cast<uint32_t>(vc / NV) & 1u, abort_flag);
+            const int rs = vc % NV;
+            // as for K: the ring slot holds V_j before any release by this warp
+            ok = mbar_wait(&sm.v_full[rs], static_cast<uint32_t>(vc / NV) & 1u, abort_flag);
             if (!ok) break;
-            const uint64_t bv = sdesc_advance(dv0, static_cast<uint32_t>(slot) * kTileStep);
+            const uint64_t bv = sdesc_advance(dv0, static_cast<uint32_t>(rs) * kTileStep);
             bool issued = false;
             for (int t = t_lo; ok && t < t_hi; ++t) {
               if (j >= it.nt(t)) continue;
@@ -425,8 +441,8 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
               issued = true;
             }
             if (!ok) break;
-            if (issued) mma_commit(&sm.v_empty[slot]);
-            else mbar_arrive(&sm.v_empty[slot]);
+            if (issued) mma_commit(&sm.v_empty[rs]);
+            else mbar_arrive(&sm.v_empty[rs]);
             ++vc;
           }
         }
@@ -450,6 +466,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
     const bool leader = (quarter == 0 && lane == 0);  // issues the tile's TMA stores
     int c = 0;  // S / P tiles of this query tile so far (phase counter)
     bool ok = true;
+    griddep_wait();
     for (int i = 0, w = item_index(0); ok && w < args.num_items; w = item_index(++i)) {
       const Item it = item_at<NQT>(args, w);
       const int ntt = it.nt(t);
@@ -566,8 +583,13 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
         // the staging tile's previous store has finished reading it, and the
         // warpgroup's four warps take one decision (none is left at a barrier)
         if (leader) bulk_wait_group_read<0>();
-        // one named barrier per query tile (ids are immediates)
-        ok = t == 0 ? named_bar_and<1>(kRows, ok) : named_bar_and<2>(kRows, ok);
+        // one named barrier per (slot, query tile); ids are immediates
+        switch (slot * NQT + t) {
+          case 0: ok = named_bar_and<1>(kRows, ok); break;
+          case 1: ok = named_bar_and<2>(kRows, ok); break;
+          case 2: ok = named_bar_and<3>(kRows, ok); break;
+          default: ok = named_bar_and<4>(kRows, ok); break;
+        }
       }
       if (!ok) break;
       if (ntt > 0) tc_fence_after();
@@ -608,8 +630,12 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
       }
       if constexpr (STO) {
         fence_proxy_async_smem();  // staged bytes visible to the TMA unit
-        if (t == 0) named_bar_sync<1>(kRows);
-        else named_bar_sync<2>(kRows);
+        switch (slot * NQT + t) {
+          case 0: named_bar_sync<1>(kRows); break;
+          case 1: named_bar_sync<2>(kRows); break;
+          case 2: named_bar_sync<3>(kRows); break;
+          default: named_bar_sync<4>(kRows); break;
+        }
         const int row0 = it.q0 + t * kRows;
         if (leader && row0 < args.n_q) {  // the map clips rows past n_q
 #pragma unroll
@@ -621,14 +647,16 @@ __global__ void __launch_bounds__(AttnShape<D, NQT>::kThreads, AttnShape<D, NQT>
       // the O reads above complete before this tile's next P store signals PV
       tc_fence_before();
     }
-    if (STO && leader) bulk_wait_group<0>();  // stores complete before the CTA exits
+    // the stores have read the staging tiles before the CTA's shared memory
+    // goes; their global writes complete with the grid
+    if (STO && leader) bulk_wait_group_read<0>();
   }
 
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, Shape::kTmemCols);
+  if (warp_id() == 1) tmem_dealloc(tmem_all, SL * Shape::kTmemCols);
 }
 
 int num_sms() {
@@ -642,23 +670,16 @@ int num_sms() {
   return n;
 }
 
-template <int D, int NQT, int NK, int NV, int QB, bool STO>
+template <int D, int NQT, int NK, int NV, int QB, bool STO, int SL>
 cudaError_t launch_variant(const AttnProblem& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                            const CUtensorMap& tm_v, const CUtensorMap& tm_o, cudaStream_t stream) {
   using Smem = AttnSmem<D, NQT, NK, NV, QB, STO>;
-  using Shape = AttnShape<D, NQT>;
-  const size_t smem_bytes = sizeof(Smem) + 1024;  // + alignment slack
-  auto kernel = attn_fwd_bf16_kernel<D, NQT, NK, NV, QB, STO>;
+  using Shape = AttnShape<D, NQT, SL>;
+  const size_t smem_bytes = SL * sizeof(Smem) + 1024;  // + alignment slack
+  auto kernel = attn_fwd_bf16_kernel<D, NQT, NK, NV, QB, STO, SL>;
   static unsigned long long configured = 0;
   cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured);
   if (e != cudaSuccess) return e;
-  static int resident = 0;  // CTAs per SM: fixed by the kernel's resources
-  if (resident == 0) {
-    int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, Shape::kThreads, smem_bytes);
-    if (e != cudaSuccess) return e;
-    resident = n < 1 ? 1 : n;
-  }
   AttnArgs a;
   a.B = p.B;
   a.h = p.h;
@@ -676,8 +697,9 @@ cudaError_t launch_variant(const AttnProblem& p, const CUtensorMap& tm_q, const 
   a.o_sb = p.o_sb;
   a.o_sh = p.o_sh;
   a.o_sr = p.o_sr;
-  const long long slots = static_cast<long long>(resident) * num_sms();
-  const int grid = static_cast<int>(items < slots ? items : slots);
+  // one CTA per SM (tensor-memory kernels are not co-resident); slot 1 of
+  // each CTA takes the items beyond the first grid-full
+  const int grid = static_cast<int>(items < num_sms() ? items : num_sms());
   return launch_pdl(kernel, dim3(grid), dim3(Shape::kThreads), smem_bytes, stream, tm_q, tm_k, tm_v,
                     tm_o, a);
 }
@@ -687,17 +709,17 @@ cudaError_t launch_variant(const AttnProblem& p, const CUtensorMap& tm_q, const 
 cudaError_t launch_attn_bf16(const AttnProblem& p, const CUtensorMap& tm_q,
                              const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const CUtensorMap& tm_o, cudaStream_t stream) {
-  // Short query sets use one query tile per work item (two CTAs per SM at
-  // d = 64, with one Q buffer so two fit); longer ones pair two query tiles
-  // so each K/V tile feeds two MMAs.
+  // Short query sets use one query tile per work item (at d = 64 two
+  // pipelines per CTA, each with one Q buffer so both fit); longer ones pair
+  // two query tiles so each K/V tile feeds two MMAs.
   const bool pair = p.n_q > kRows;
   if (p.d == 64) {
-    return pair ? launch_variant<64, 2, 4, 4, 2, true>(p, tm_q, tm_k, tm_v, tm_o, stream)
-                : launch_variant<64, 1, 2, 2, 1, true>(p, tm_q, tm_k, tm_v, tm_o, stream);
+    return pair ? launch_variant<64, 2, 4, 4, 2, true, 1>(p, tm_q, tm_k, tm_v, tm_o, stream)
+                : launch_variant<64, 1, 2, 2, 1, true, 2>(p, tm_q, tm_k, tm_v, tm_o, stream);
   }
   if (p.d == 128) {
-    return pair ? launch_variant<128, 2, 2, 2, 1, false>(p, tm_q, tm_k, tm_v, tm_o, stream)
-                : launch_variant<128, 1, 2, 2, 2, true>(p, tm_q, tm_k, tm_v, tm_o, stream);
+    return pair ? launch_variant<128, 2, 2, 2, 1, false, 1>(p, tm_q, tm_k, tm_v, tm_o, stream)
+                : launch_variant<128, 1, 2, 2, 2, true, 1>(p, tm_q, tm_k, tm_v, tm_o, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -136,9 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       tma_prefetch_desc(&p.g[i].tm_c);
     }
   }
-  // the set-up above may overlap the previous kernel; global memory may not
+  // Everything up to a role's first global-memory access may overlap the
+  // previous kernel: the producer waits for it (griddep_wait) before its
+  // first load, the epilogue before its first store.
   griddep_launch_dependents();
-  griddep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -156,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
             break;
           }
           mbar_arrive_expect_tx(&sm.full[s], kABytes + kBBytes);
+          if (issued == 0) griddep_wait();
           const int k0 = kb * kBK;
           tma_load_2d(sm.a[s], &c.g->tm_a, &sm.full[s], k0, c.m0);
           const int kr = k0 + rank * kBRows;
@@ -227,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
     const int r = quarter * 32 + static_cast<int>(lane);
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const bool leader = (warp == 2 && lane == 0);  // issues the tile's TMA stores
+    if (leader) griddep_wait();
     int it = 0;
     for (int ct = first; ct < p.total_tiles; ct += stride, ++it) {
       const int acc = it & 1;
@@ -278,7 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
         bulk_commit_group();
       }
     }
-    if (leader) bulk_wait_group<0>();  // stores complete before the CTA exits
+    // the stores have read the staging tile before the CTA's shared memory
+    // goes; their global writes complete with the grid
+    if (leader) bulk_wait_group_read<0>();
   }
 
   tc_fence_before();

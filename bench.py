@@ -311,22 +311,24 @@ class MhaCall:
                              m.h, m.d_k, m.d_v, m.mask_kind, s["lens"], 0.0, s["ws"], self.wsb,
                              stream)
 
-    def run_stages(self, i, stream, events):
-        """The same three launches through their own entry points, an event after each."""
+    def run_stage(self, k, i, stream):
+        """Launch k of the three (QKV projection, attention, W_O projection)
+        through its own entry point, on input set i."""
         m, s = self.m, self.sets[i % len(self.sets)]
         base = s["ws"].data_ptr()
         Q, K, V, O = base + self.q_off, base + self.k_off, base + self.v_off, base + self.o_off
         hdk, hdv = m.h * m.d_k, m.h * m.d_v
-        self.tsd.mha_project_qkv(s["x_q"], s["x_kv"], *s["w"][:3], Q, K, V, m.B, m.n_q, m.n_k,
-                                 m.d_model, m.h, m.d_k, m.d_v, stream)
-        events[0].record(stream)
-        self.tsd.attn_forward_strided(Q, m.n_q * hdk, m.d_k, hdk, K, m.n_k * hdk, m.d_k, hdk,
-                                      V, m.n_k * hdv, m.d_v, hdv, O, m.n_q * hdv, m.d_v, hdv,
-                                      m.B, m.h, m.n_q, m.n_k, m.d_k, m.d_v, m.mask_kind,
-                                      s["lens"], 0.0, stream)
-        events[1].record(stream)
-        self.tsd.mha_project_out(O, s["w"][3], s["out"], m.B, m.n_q, m.d_model, m.h, m.d_v, stream)
-        events[2].record(stream)
+        if k == 0:
+            self.tsd.mha_project_qkv(s["x_q"], s["x_kv"], *s["w"][:3], Q, K, V, m.B, m.n_q, m.n_k,
+                                     m.d_model, m.h, m.d_k, m.d_v, stream)
+        elif k == 1:
+            self.tsd.attn_forward_strided(Q, m.n_q * hdk, m.d_k, hdk, K, m.n_k * hdk, m.d_k, hdk,
+                                          V, m.n_k * hdv, m.d_v, hdv, O, m.n_q * hdv, m.d_v, hdv,
+                                          m.B, m.h, m.n_q, m.n_k, m.d_k, m.d_v, m.mask_kind,
+                                          s["lens"], 0.0, stream)
+        else:
+            self.tsd.mha_project_out(O, s["w"][3], s["out"], m.B, m.n_q, m.d_model, m.h, m.d_v,
+                                     stream)
 
     def stage_names(self):
         return ["gemm_bf16", "attn_fwd_bf16", "gemm_bf16"]
@@ -407,9 +409,8 @@ class AttnCall:
         self.tsd.attn_forward(s["q"], s["k"], s["v"], s["out"], a.B, a.h, a.n_q, a.n_k, a.d_k,
                               a.d_v, a.mask_kind, None, 0.0, stream)
 
-    def run_stages(self, i, stream, events):
+    def run_stage(self, k, i, stream):
         self.run(i, stream)
-        events[0].record(stream)
 
     def stage_names(self):
         return ["attn_fwd_bf16"]
@@ -527,31 +528,36 @@ def run_gpu_arm(args, world, rank, local):
     total_flops = dist_sum(flops_step * args.steps, world)
     value = total_flops / (ms_total_max * 1e-3) / 1e12
 
-    # ---------------------------------------------------------------- per-kernel loop
-    n_iter = max(args.steps, 20)
+    # ---------------------------------------------------------------- per-kernel timing
+    # Each kernel on its own: a CUDA graph of back-to-back launches over the
+    # rotating input sets, replayed between two events on the launch stream.
+    # (Events between the eager launches of a step would time host launch
+    # gaps and break the programmatic overlap of consecutive kernels.)
     per_kernel = {}
-    rec = []
-    for it in range(n_iter + 2):
-        evs = []
-        for c in calls:
-            st = torch.cuda.Event(enable_timing=True)
-            st.record(stream)
-            e = [torch.cuda.Event(enable_timing=True) for _ in c.stage_names()]
-            c.run_stages(it, stream, e)
-            evs.append((c, st, e))
-        if it >= 2:
-            rec.append(evs)
-    torch.cuda.synchronize()
-    for evs in rec:
-        for c, st, e in evs:
-            prev = st
-            for name, work, ev in zip(c.stage_names(), c.stage_work(), e):
-                d = per_kernel.setdefault(name, {"ms": 0.0, "launches": 0, "flops": 0.0, "bytes": 0.0})
-                d["ms"] += prev.elapsed_time(ev)
-                d["launches"] += 1
-                d["flops"] += work[0]
-                d["bytes"] += work[1]
-                prev = ev
+    g_launches, g_reps = max(2 * nsets, 20), 5
+    for c in calls:
+        for k, (name, work) in enumerate(zip(c.stage_names(), c.stage_work())):
+            graph, cap = torch.cuda.CUDAGraph(), torch.cuda.Stream()
+            cap.wait_stream(stream)
+            with torch.cuda.graph(graph, stream=cap):
+                for i in range(g_launches):
+                    c.run_stage(k, i, cap)
+            stream.wait_stream(cap)
+            graph.replay()
+            ka, kb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ka.record(stream)
+            for _ in range(g_reps):
+                graph.replay()
+            kb.record(stream)
+            torch.cuda.synchronize()
+            d = per_kernel.setdefault(name, {"ms": 0.0, "launches": 0, "flops": 0.0, "bytes": 0.0})
+            d["ms"] += ka.elapsed_time(kb) / (g_reps * g_launches)
+            d["launches"] += 1
+            d["flops"] += work[0]
+            d["bytes"] += work[1]
+            del graph
+    if tsd.attn_get_device_status() != tsd.ATTN_OK:
+        raise RuntimeError("device error during the per-kernel timing")
     dominant = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
     d = per_kernel[dominant]
     avg_ms = d["ms"] / d["launches"]
@@ -573,6 +579,8 @@ def run_gpu_arm(args, world, rank, local):
     roof["algorithmic"] = {"flops": f_per, "bytes": b_per}
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" \
         else "fallback"
+    roof["timing"] = (f"each kernel alone: CUDA graph of {g_launches} back-to-back launches over "
+                      f"the rotating input sets, CUDA events around {g_reps} replays")
     kernel_table = {k: {"ms_per_launch": round(v["ms"] / v["launches"], 5),
                         "share": round(v["ms"] / sum(x["ms"] for x in per_kernel.values()), 4),
                         "tflops": round(v["flops"] / (v["ms"] * 1e-3) / 1e12, 2),

@@ -105,6 +105,7 @@ def source_sha(rel):
 KERNEL_SOURCES = {
     "attn_fwd_bf16": "transformer_scaled_dot_gb300/csrc/attn_bf16.cu",
     "gemm_bf16": "transformer_scaled_dot_gb300/csrc/gemm_bf16.cu",
+    "mha_fused": "transformer_scaled_dot_gb300/csrc/mha_fused.cu",
 }
 
 
@@ -311,13 +312,31 @@ class MhaCall:
                              m.h, m.d_k, m.d_v, m.mask_kind, s["lens"], 0.0, s["ws"], self.wsb,
                              stream)
 
+    def fused(self):
+        """Whether mha_forward takes the fused short-sequence kernel (the
+        library's rule: n_q, n_k <= 128, d_k = d_v = 64, h even, d_model a
+        multiple of 64)."""
+        m = self.m
+        return (m.d_k == 64 and m.d_v == 64 and 1 <= m.n_q <= 128 and 1 <= m.n_k <= 128
+                and m.h % 2 == 0 and m.d_model % 64 == 0)
+
     def run_stage(self, k, i, stream):
-        """Launch k of the three (QKV projection, attention, W_O projection)
-        through its own entry point, on input set i."""
+        """Launch k of the step's launches (fused path: heads, W_O projection;
+        otherwise QKV projection, attention, W_O projection) through its own
+        entry point, on input set i."""
         m, s = self.m, self.sets[i % len(self.sets)]
         base = s["ws"].data_ptr()
         Q, K, V, O = base + self.q_off, base + self.k_off, base + self.v_off, base + self.o_off
         hdk, hdv = m.h * m.d_k, m.h * m.d_v
+        if self.fused():
+            if k == 0:
+                self.tsd.mha_concat_heads(s["x_q"], s["x_kv"], *s["w"][:3], O, m.B, m.n_q, m.n_k,
+                                          m.d_model, m.h, m.d_k, m.d_v, m.mask_kind, s["lens"],
+                                          0.0, s["ws"], self.wsb, stream)
+            else:
+                self.tsd.mha_project_out(O, s["w"][3], s["out"], m.B, m.n_q, m.d_model, m.h,
+                                         m.d_v, stream)
+            return
         if k == 0:
             self.tsd.mha_project_qkv(s["x_q"], s["x_kv"], *s["w"][:3], Q, K, V, m.B, m.n_q, m.n_k,
                                      m.d_model, m.h, m.d_k, m.d_v, stream)
@@ -331,6 +350,8 @@ class MhaCall:
                                      stream)
 
     def stage_names(self):
+        if self.fused():
+            return ["mha_fused", "gemm_bf16"]
         return ["gemm_bf16", "attn_fwd_bf16", "gemm_bf16"]
 
     def stage_work(self):
@@ -339,8 +360,9 @@ class MhaCall:
         dm, hdk, hdv = m.d_model, m.h * m.d_k, m.h * m.d_v
         Mq, Mk = m.B * m.n_q, m.B * m.n_k
         qkv_f = 2.0 * dm * (Mq * hdk + Mk * hdk + Mk * hdv)
-        qkv_b = 2.0 * (Mq * dm + (0 if m.self_attention else Mk * dm) + dm * (2 * hdk + hdv)
-                       + Mq * hdk + Mk * (hdk + hdv))
+        x_b = 2.0 * (Mq * dm + (0 if m.self_attention else Mk * dm))
+        w_b = 2.0 * dm * (2 * hdk + hdv)
+        qkv_b = x_b + w_b + 2.0 * (Mq * hdk + Mk * (hdk + hdv))
         kv = self.kv_effective()
         causal = bool(m.mask_kind & MASK_CAUSAL)
         att_f = attn_flops(m.B, m.h, m.n_q, m.n_k, m.d_k, causal)
@@ -348,6 +370,9 @@ class MhaCall:
                                 for b in range(m.B))
         out_f = 2.0 * Mq * hdv * dm
         out_b = 2.0 * (Mq * hdv + hdv * dm + Mq * dm)
+        if self.fused():
+            # X, the weights and the merged heads cross HBM; Q/K/V stay on chip
+            return [(qkv_f + att_f, x_b + w_b + 2.0 * Mq * hdv), (out_f, out_b)]
         return [(qkv_f, qkv_b), (att_f, att_b), (out_f, out_b)]
 
     def kv_effective(self):
@@ -361,7 +386,7 @@ class MhaCall:
         return attn_flops(m.B, m.h, m.n_q, m.n_k, m.d_k, bool(m.mask_kind & MASK_CAUSAL))
 
     def launches(self):
-        return 3
+        return len(self.stage_names())
 
     def e2e_run(self, i, stream):
         """Host inputs -> device, mha_forward, result -> host (pinned buffers)."""

@@ -130,7 +130,10 @@ size_t mha_workspace_bytes(int B, int n_q, int n_k, int h, int d_k, int d_v);
  *   out  [B, n_q, d_model] bf16
  *   d_k == d_v in {64, 128}; d_model a multiple of 8 (16-byte rows), >= 8.
  *   workspace: device, 256-byte aligned, >= mha_workspace_bytes(...) bytes;
- *   its contents on return are the intermediate Q, K, V and merged heads.
+ *   on return its last region holds the merged heads; the Q, K, V regions
+ *   are scratch (short sequences -- n_q, n_k <= 128, d_k = d_v = 64, h even,
+ *   d_model a multiple of 64 -- are projected and attended in one kernel
+ *   and never write them).
  *   mask_kind, kv_lens, scale: as attn_forward (the mask applies to every head).
  * Errors: as attn_forward; a short workspace -> ATTN_ERR_INVALID.
  */
@@ -140,6 +143,25 @@ attn_status mha_forward(const void *x_q, const void *x_kv,
                         int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
                         int mask_kind, const int32_t *kv_lens, float scale,
                         void *workspace, size_t workspace_bytes, tsd_stream_t stream);
+
+/*
+ * mha_concat_heads -- Concat(head_1, ..., head_h), head_i =
+ * Attention(X_q W_i^Q, X_kv W_i^K, X_kv W_i^V): multi-head attention up to
+ * (not including) the output projection W_O ("[논문 리뷰]Attention Is All You
+ * Need" (kimjiil.github.io), section 3.2.2). mha_forward is this followed by
+ * mha_project_out.
+ *   Arguments and errors as mha_forward, with `concat` in place of w_o/out:
+ *   concat: device bf16 [B, n_q, h*d_v] (head i = column block i), 16-byte
+ *   aligned. The workspace (mha_workspace_bytes(...) bytes, 256-byte aligned)
+ *   is scratch for the Q, K, V projections; short sequences (n_q, n_k <= 128,
+ *   d_k = d_v = 64, h even, d_model a multiple of 64) run as one fused kernel
+ *   and leave it untouched.
+ */
+attn_status mha_concat_heads(const void *x_q, const void *x_kv,
+                             const void *w_q, const void *w_k, const void *w_v, void *concat,
+                             int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
+                             int mask_kind, const int32_t *kv_lens, float scale,
+                             void *workspace, size_t workspace_bytes, tsd_stream_t stream);
 
 /*
  * mha_project_qkv -- the input projections of section 3.2.2, all positions at

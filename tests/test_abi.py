@@ -123,6 +123,28 @@ def test_mha_forward_rejects_bad_arguments(lib):
     assert lib.mha_forward(*bad) == tsd.ATTN_ERR_UNSUPPORTED
 
 
+def test_mha_concat_heads_rejects_bad_arguments(lib):
+    B, n, dm, h, d = 2, 16, 128, 2, 64
+    wsb = tsd.mha_workspace_bytes(B, n, n, h, d, d)
+    # x_q, x_kv, w_q, w_k, w_v, concat, B, n_q, n_k, d_model, h, d_k, d_v, mask, lens, scale,
+    # workspace, bytes, stream
+    base = [FAKE] * 6 + [B, n, n, dm, h, d, d, 0, None, 0.0, FAKE, wsb, None]
+    bad = list(base)
+    bad[17] = wsb - 1                      # short workspace
+    assert lib.mha_concat_heads(*bad) == tsd.ATTN_ERR_INVALID
+    bad = list(base)
+    bad[5] = None                          # no output
+    assert lib.mha_concat_heads(*bad) == tsd.ATTN_ERR_INVALID
+    bad = list(base)
+    bad[13] = tsd.ATTN_MASK_KEY_PADDING    # padding without lengths
+    assert lib.mha_concat_heads(*bad) == tsd.ATTN_ERR_INVALID
+    bad = list(base)
+    bad[11] = bad[12] = 32                 # head size without a bf16 kernel
+    assert lib.mha_concat_heads(*bad) == tsd.ATTN_ERR_UNSUPPORTED
+    base[6] = 0                            # empty batch: nothing to do
+    assert lib.mha_concat_heads(*base) == tsd.ATTN_OK
+
+
 def test_selftest_rejects_bad_limit(lib):
     assert lib.attn_selftest_wait_timeout(0, None) == tsd.ATTN_ERR_INVALID
     assert lib.attn_selftest_wait_timeout(3000000, None) == tsd.ATTN_ERR_INVALID

@@ -82,17 +82,78 @@ def test_mha_small_shapes(tsd, shape):
     check(tsd, m, str(shape))
 
 
-def test_mha_intermediate_projections_and_heads(tsd):
-    """The workspace holds Q = X W_Q (head i = column block i) and the merged
-    heads; check both against the oracle's pieces."""
+@pytest.mark.parametrize("n", [96, 200])  # fused short-sequence path; projection GEMM path
+def test_mha_intermediate_projections_and_heads(tsd, n):
+    """The workspace's last region holds the merged heads; the projection
+    entry point gives Q = X W_Q (head i = column block i). Check both against
+    the oracle's pieces."""
     import torch
-    m = synthetic.mha_inputs(3100, 2, 96, 96, 128, 2, 64, 64, MASK_CAUSAL)
+    m = synthetic.mha_inputs(3100 + n, 2, n, n, 128, 2, 64, 64, MASK_CAUSAL)
     got, ws = run_mha(tsd, m)
     x, _, wq, _, _, wo = m.as_f64()
-    q_dev = ws[:2 * 96 * 128 * 2].view(torch.bfloat16).float().cpu().numpy().reshape(2, 96, 128)
-    assert_bf16_close(q_dev, x @ wq, "Q projection")
     ref, concat = oracle.mha(*m.as_f64(), 2, MASK_CAUSAL, return_concat=True)
-    off = tsd.mha_workspace_bytes(2, 96, 96, 2, 64, 64) - 2 * 96 * 128 * 2
-    o_dev = ws[off:].view(torch.bfloat16).float().cpu().numpy().reshape(2, 96, 128)
+    off = tsd.mha_workspace_bytes(2, n, n, 2, 64, 64) - 2 * n * 128 * 2
+    o_dev = ws[off:].view(torch.bfloat16).float().cpu().numpy().reshape(2, n, 128)
     assert_bf16_close(o_dev, concat, "merged heads")
     assert_bf16_close(got, ref, "output")
+    xd = to_dev_bf16(m.x_q)
+    wd = [to_dev_bf16(t) for t in (m.w_q, m.w_k, m.w_v)]
+    qkv = [torch.empty((2, n, 128), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    tsd.mha_project_qkv(xd, xd, *wd, *qkv, 2, n, n, 128, 2, 64, 64)
+    torch.cuda.synchronize()
+    q_dev = qkv[0].float().cpu().numpy()
+    assert_bf16_close(q_dev, x @ wq, "Q projection")
+
+
+@pytest.mark.parametrize("shape", [
+    # the fused short-sequence kernel: n_q, n_k <= 128, d = 64, h even, d_model % 64 == 0
+    # B, n_q, n_k, d_model, h, mask, self
+    (1, 1, 1, 64, 2, MASK_NONE, True),                          # one query, one key
+    (3, 77, 77, 64, 2, MASK_CAUSAL, True),                      # one 64-wide slice of d_model
+    (4, 100, 120, 256, 4, MASK_KEY_PADDING, False),             # cross-attention, x_kv != x_q
+    (2, 128, 33, 192, 6, MASK_NONE, False),                     # few keys
+    (2, 100, 100, 1024, 16, MASK_CAUSAL | MASK_KEY_PADDING, True),  # Transformer-big width
+    (40, 64, 64, 128, 16, MASK_KEY_PADDING, True),              # 320 head pairs: several per CTA
+])
+def test_mha_fused_short_sequences(tsd, shape):
+    B, n_q, n_k, dm, h, mask, self_attn = shape
+    m = synthetic.mha_inputs(3200 + B + n_q + dm, B, n_q, n_k, dm, h, 64, 64, mask, (1, n_k),
+                             self_attention=self_attn)
+    check(tsd, m, str(shape))
+
+
+def test_mha_fused_key_length_zero(tsd):
+    """A batch entry with no keys gives zero heads, so its output is 0 (the
+    projections carry no bias)."""
+    m = synthetic.mha_inputs(3300, 3, 64, 64, 128, 2, 64, 64, MASK_KEY_PADDING)
+    m.kv_lens = np.array([0, 64, 5], dtype=np.int32)
+    got, _ = run_mha(tsd, m)
+    ref = oracle.mha(*m.as_f64(), m.h, m.mask_kind, kv_lens=m.kv_lens)
+    assert np.all(got[0] == 0.0)
+    assert_bf16_close(got, ref, "kv_len 0")
+
+
+@pytest.mark.parametrize("shape", [
+    # B, n_q, n_k, d_model, h, mask, self  (fused short-sequence path, then the GEMM path)
+    (3, 90, 90, 256, 4, MASK_CAUSAL | MASK_KEY_PADDING, True),
+    (3, 90, 140, 256, 4, MASK_KEY_PADDING, False),
+])
+def test_mha_concat_heads_matches_oracle(tsd, shape):
+    """Concat(head_1..head_h) before W_O, through its own entry point."""
+    import torch
+    B, n_q, n_k, dm, h, mask, self_attn = shape
+    m = synthetic.mha_inputs(3400 + n_k, B, n_q, n_k, dm, h, 64, 64, mask, (1, n_k),
+                             self_attention=self_attn)
+    x_q = to_dev_bf16(m.x_q)
+    x_kv = x_q if self_attn else to_dev_bf16(m.x_kv)
+    w = [to_dev_bf16(t) for t in (m.w_q, m.w_k, m.w_v)]
+    concat = torch.full((B, n_q, h * 64), float("nan"), dtype=torch.bfloat16, device="cuda")
+    wsb = tsd.mha_workspace_bytes(B, n_q, n_k, h, 64, 64)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    lens = to_dev_i32(m.kv_lens) if m.kv_lens is not None else None
+    tsd.mha_concat_heads(x_q, x_kv, *w, concat, B, n_q, n_k, dm, h, 64, 64, mask, lens, 0.0,
+                         ws, wsb)
+    torch.cuda.synchronize()
+    assert tsd.attn_get_device_status() == tsd.ATTN_OK
+    _, ref = oracle.mha(*m.as_f64(), h, mask, kv_lens=m.kv_lens, return_concat=True)
+    assert_bf16_close(to_host_f64(concat), ref, "concat heads " + str(shape))

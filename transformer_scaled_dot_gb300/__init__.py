@@ -23,7 +23,7 @@ __all__ = [
     "attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_workspace_bytes",
     "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
     "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out", "mha_forward_noalloc",
-    "MHA_NOALLOC_SCRATCH_BYTES",
+    "mha_concat_heads", "MHA_NOALLOC_SCRATCH_BYTES",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = range(5)
@@ -33,6 +33,7 @@ EXPORTED_SYMBOLS = (
     "attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_workspace_bytes",
     "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
     "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out", "mha_forward_noalloc",
+    "mha_concat_heads",
 )
 
 # TSD_MHA_NOALLOC_SCRATCH_BYTES of the header: the fixed scratch of mha_forward_noalloc
@@ -75,6 +76,8 @@ def library():
     lib.mha_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, f, vp,
                                 ctypes.c_size_t, st]
     lib.mha_project_qkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, st]
+    lib.mha_concat_heads.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, f, vp,
+                                     ctypes.c_size_t, st]
     lib.mha_project_out.argtypes = [vp, vp, vp, i, i, i, i, i, st]
     lib.mha_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, f,
                                         st]
@@ -85,7 +88,7 @@ def library():
     lib.attn_selftest_wait_timeout.argtypes = [i, st]
     for name in ("attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_forward",
                  "attn_get_device_status", "attn_last_cuda_error", "attn_selftest_wait_timeout",
-                 "mha_project_qkv", "mha_project_out", "mha_forward_noalloc"):
+                 "mha_project_qkv", "mha_project_out", "mha_forward_noalloc", "mha_concat_heads"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -146,6 +149,15 @@ def mha_forward(x_q, x_kv, w_q, w_k, w_v, w_o, out, B, n_q, n_k, d_model, h, d_k
                                  _ptr(w_o), _ptr(out), B, n_q, n_k, d_model, h, d_k, d_v,
                                  mask_kind, _ptr(kv_lens), scale, _ptr(workspace),
                                  workspace_bytes, _stream(stream)), "mha_forward")
+
+
+def mha_concat_heads(x_q, x_kv, w_q, w_k, w_v, concat, B, n_q, n_k, d_model, h, d_k, d_v,
+                     mask_kind=ATTN_MASK_NONE, kv_lens=None, scale=0.0, workspace=None,
+                     workspace_bytes=0, stream=None):
+    _check(library().mha_concat_heads(_ptr(x_q), _ptr(x_kv), _ptr(w_q), _ptr(w_k), _ptr(w_v),
+                                      _ptr(concat), B, n_q, n_k, d_model, h, d_k, d_v, mask_kind,
+                                      _ptr(kv_lens), scale, _ptr(workspace), workspace_bytes,
+                                      _stream(stream)), "mha_concat_heads")
 
 
 def mha_project_qkv(x_q, x_kv, w_q, w_k, w_v, q_out, k_out, v_out, B, n_q, n_k, d_model, h, d_k,

@@ -282,6 +282,78 @@ attn_status launch_qkv(const void* x_q, const void* x_kv, const void* w_q, const
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
+// Shapes the fused short-sequence kernel takes (projections and attention
+// in one launch); others run the projection GEMM and the attention kernel.
+bool fused_eligible(int n_q, int n_k, int d_model, int h, int d_k, int d_v) {
+  return d_k == 64 && d_v == 64 && n_q >= 1 && n_q <= 128 && n_k >= 1 && n_k <= 128 &&
+         h % 2 == 0 && d_model >= 64 && d_model % 64 == 0;
+}
+
+// Q/K/V projections + attention of every (batch, head pair) -> the merged
+// heads, [B, n_q, h*64], in `concat`.
+attn_status launch_fused_core(const void* x_q, const void* x_kv, const void* w_q, const void* w_k,
+                              const void* w_v, void* concat, int B, int n_q, int n_k, int d_model,
+                              int h, int mask_kind, const int32_t* kv_lens, float scale,
+                              cudaStream_t stream) {
+  tsd::MhaFusedProblem p;
+  std::memset(&p, 0, sizeof(p));
+  p.self = (x_q == x_kv) && (n_q == n_k);
+  const uint32_t xbox[3] = {64, 128, 1};
+  const uint64_t xq_dims[3] = {static_cast<uint64_t>(d_model), static_cast<uint64_t>(n_q),
+                               static_cast<uint64_t>(B)};
+  const int64_t xq_str[2] = {d_model, int64_t(n_q) * d_model};
+  cudaError_t e = encode_bf16_map(&p.tm_xq, x_q, 3, xq_dims, xq_str, xbox);
+  if (e == cudaSuccess && !p.self) {
+    const uint64_t xkv_dims[3] = {static_cast<uint64_t>(d_model), static_cast<uint64_t>(n_k),
+                                  static_cast<uint64_t>(B)};
+    const int64_t xkv_str[2] = {d_model, int64_t(n_k) * d_model};
+    e = encode_bf16_map(&p.tm_xkv, x_kv, 3, xkv_dims, xkv_str, xbox);
+  } else {
+    p.tm_xkv = p.tm_xq;
+  }
+  const uint64_t w_dims[2] = {static_cast<uint64_t>(h) * 64, static_cast<uint64_t>(d_model)};
+  const int64_t w_str[1] = {int64_t(h) * 64};
+  const uint32_t wbox[2] = {64, 64};
+  if (e == cudaSuccess) e = encode_bf16_map(&p.tm_wq, w_q, 2, w_dims, w_str, wbox);
+  if (e == cudaSuccess) e = encode_bf16_map(&p.tm_wk, w_k, 2, w_dims, w_str, wbox);
+  if (e == cudaSuccess) e = encode_bf16_map(&p.tm_wv, w_v, 2, w_dims, w_str, wbox);
+  const uint64_t o_dims[3] = {static_cast<uint64_t>(h) * 64, static_cast<uint64_t>(n_q),
+                              static_cast<uint64_t>(B)};
+  const int64_t o_str[2] = {int64_t(h) * 64, int64_t(n_q) * h * 64};
+  if (e == cudaSuccess) e = encode_bf16_map(&p.tm_o, concat, 3, o_dims, o_str, xbox);
+  if (e != cudaSuccess) return cuda_fail(e);
+  p.B = B;
+  p.h = h;
+  p.n_q = n_q;
+  p.n_k = n_k;
+  p.d_model = d_model;
+  p.mask_kind = mask_kind;
+  p.kv_lens = kv_lens;
+  p.scale = resolve_scale(scale, 64);
+  e = tsd::launch_mha_fused(p, stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+// head_i = Attention(X_q W_Q,i, X_kv W_K,i, X_kv W_V,i), written merged,
+// [B, n_q, h*d_v]. Short sequences: one fused launch; else the grouped
+// projection GEMM into Q, K, V (column block i = head i) and the attention
+// kernel reading them through strides.
+attn_status concat_heads(const void* x_q, const void* x_kv, const void* w_q, const void* w_k,
+                         const void* w_v, void* concat, void* Q, void* K, void* V, int B, int n_q,
+                         int n_k, int d_model, int h, int d_k, int d_v, int mask_kind,
+                         const int32_t* kv_lens, float scale, cudaStream_t stream) {
+  if (fused_eligible(n_q, n_k, d_model, h, d_k, d_v))
+    return launch_fused_core(x_q, x_kv, w_q, w_k, w_v, concat, B, n_q, n_k, d_model, h,
+                             mask_kind, kv_lens, scale, stream);
+  const int hdk = h * d_k, hdv = h * d_v;
+  attn_status s =
+      launch_qkv(x_q, x_kv, w_q, w_k, w_v, Q, K, V, B, n_q, n_k, d_model, h, d_k, d_v, stream);
+  if (s != ATTN_OK) return s;
+  return run_attn_bf16(Q, int64_t(n_q) * hdk, d_k, hdk, K, int64_t(n_k) * hdk, d_k, hdk, V,
+                       int64_t(n_k) * hdv, d_v, hdv, concat, int64_t(n_q) * hdv, d_v, hdv, B, h,
+                       n_q, n_k, d_k, mask_kind, kv_lens, scale, stream);
+}
+
 attn_status launch_out_proj(const void* concat, const void* w_o, void* out, int B, int n_q,
                             int d_model, int h, int d_v, cudaStream_t stream) {
   const int Mq = B * n_q;
@@ -401,21 +473,38 @@ attn_status mha_forward(const void* x_q, const void* x_kv, const void* w_q, cons
   void* K = ws + L.k_off;
   void* V = ws + L.v_off;
   void* O = ws + L.o_off;
-  const int hdk = h * d_k, hdv = h * d_v;
-
-  // 1. Q = X_q W_Q, K = X_kv W_K, V = X_kv W_V   (one grouped launch)
-  s = launch_qkv(x_q, x_kv, w_q, w_k, w_v, Q, K, V, B, n_q, n_k, d_model, h, d_k, d_v, stream);
+  // 1-2. Concat(head_1..head_h) into the workspace's last region
+  s = concat_heads(x_q, x_kv, w_q, w_k, w_v, O, Q, K, V, B, n_q, n_k, d_model, h, d_k, d_v,
+                   mask_kind, kv_lens, scale, stream);
   if (s != ATTN_OK) return s;
-
-  // 2. head_i = Attention(Q_i, K_i, V_i): heads are column blocks of the
-  //    [B, n, h*d] projections; the output is written merged, [B, n_q, h*d_v]
-  s = run_attn_bf16(Q, int64_t(n_q) * hdk, d_k, hdk, K, int64_t(n_k) * hdk, d_k, hdk, V,
-                    int64_t(n_k) * hdv, d_v, hdv, O, int64_t(n_q) * hdv, d_v, hdv, B, h, n_q, n_k,
-                    d_k, mask_kind, kv_lens, scale, stream);
-  if (s != ATTN_OK) return s;
-
   // 3. out = Concat(head_1..head_h) W_O
   return launch_out_proj(O, w_o, out, B, n_q, d_model, h, d_v, stream);
+}
+
+attn_status mha_concat_heads(const void* x_q, const void* x_kv, const void* w_q, const void* w_k,
+                             const void* w_v, void* concat, int B, int n_q, int n_k, int d_model,
+                             int h, int d_k, int d_v, int mask_kind, const int32_t* kv_lens,
+                             float scale, void* workspace, size_t workspace_bytes,
+                             tsd_stream_t stream_) {
+  attn_status s = check_common(B, h, n_q, n_k, d_k, d_v, mask_kind, kv_lens, scale);
+  if (s != ATTN_OK) return s;
+  if (h <= 0 || d_model < 8 || (d_model % 8) != 0) return ATTN_ERR_INVALID;
+  const void* ptrs[7] = {x_q, x_kv, w_q, w_k, w_v, concat, workspace};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID;
+  s = check_bf16_head_dims(d_k, d_v);
+  if (s != ATTN_OK) return s;
+  MhaLayout L;
+  if (!mha_layout(B, n_q, n_k, h, d_k, d_v, &L)) return ATTN_ERR_INVALID;
+  if (workspace_bytes < L.total) return ATTN_ERR_INVALID;
+  const int64_t Mq = int64_t(B) * n_q, Mk = int64_t(B) * n_k;
+  if (Mq > INT32_MAX || Mk > INT32_MAX) return ATTN_ERR_INVALID;
+  if (Mq == 0) return ATTN_OK;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return concat_heads(x_q, x_kv, w_q, w_k, w_v, concat, ws + L.q_off, ws + L.k_off, ws + L.v_off,
+                      B, n_q, n_k, d_model, h, d_k, d_v, mask_kind, kv_lens, scale,
+                      reinterpret_cast<cudaStream_t>(stream_));
 }
 
 attn_status mha_project_qkv(const void* x_q, const void* x_kv, const void* w_q, const void* w_k,
@@ -444,12 +533,13 @@ attn_status mha_project_out(const void* concat, const void* w_o, void* out, int 
 attn_status attn_get_device_status(tsd_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
-  unsigned int a = 0, g = 0, f = 0;
+  unsigned int a = 0, g = 0, f = 0, m = 0;
   e = tsd::take_device_error_attn(&a);
   if (e == cudaSuccess) e = tsd::take_device_error_gemm(&g);
   if (e == cudaSuccess) e = tsd::take_device_error_f32(&f);
+  if (e == cudaSuccess) e = tsd::take_device_error_fused(&m);
   if (e != cudaSuccess) return cuda_fail(e);
-  return (a | g | f) ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
+  return (a | g | f | m) ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
 }
 
 int attn_last_cuda_error(void) { return g_last_cuda_error; }

@@ -107,10 +107,28 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Multi-head attention for short sequences in one kernel up to the merged
+// heads: the Q/K/V projections of each head pair, their attention, and the
+// merged [B, n_q, h*64] output. n_q, n_k <= 128, d_k = d_v = 64, h even,
+// d_model a multiple of 64.
+struct MhaFusedProblem {
+  CUtensorMap tm_xq;   // 3-D (d_model, n_q, B), box 64 x 128 x 1
+  CUtensorMap tm_xkv;  // 3-D (d_model, n_k, B) (unused when self)
+  CUtensorMap tm_wq, tm_wk, tm_wv;  // 2-D (h*64, d_model), box 64 x 64
+  CUtensorMap tm_o;    // 3-D (h*64, n_q, B), box 64 x 128 x 1 (TMA store)
+  int B, h, n_q, n_k, d_model;
+  bool self;           // x_kv is x_q (and n_k == n_q)
+  int mask_kind;
+  const int32_t* kv_lens;
+  float scale;
+};
+cudaError_t launch_mha_fused(const MhaFusedProblem& p, cudaStream_t stream);
+
 // Per-file device error words (read and cleared; see sm103.cuh).
 cudaError_t take_device_error_attn(unsigned int* value);
 cudaError_t take_device_error_gemm(unsigned int* value);
 cudaError_t take_device_error_f32(unsigned int* value);
+cudaError_t take_device_error_fused(unsigned int* value);
 
 // Failure-detection self test: a bounded wait on a barrier nobody arrives on.
 cudaError_t launch_wait_timeout_selftest(unsigned long long limit_ns, cudaStream_t stream);

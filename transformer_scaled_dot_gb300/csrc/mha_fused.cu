@@ -22,7 +22,8 @@
 //   warps 4..7  head 2p, warps 8..11 head 2p+1, one thread per row (= TMEM
 //               lane): (1) the head's projection accumulator row (fp32) ->
 //               bf16 rows of 128-byte-swizzled Q, K, V tiles written into the
-//               projection ring's memory (now free); (2) the softmax of the
+//               projection ring's memory (now free), Q and K first so the S
+//               MMA overlaps V's conversion; (2) the softmax of the
 //               single 128 x 128 score tile (masked logits -inf before max and
 //               exp2, scale*log2(e) folded); (3) O / l -> bf16 -> swizzled
 //               staging -> one TMA store into the merged [B, n_q, h*d] layout
@@ -61,7 +62,7 @@ struct FusedSmem {
   alignas(1024) uint8_t o[2][kTile];  // epilogue staging, one per head
   uint64_t full[kStages], empty[kStages];
   uint64_t proj_done, qkv_free, tmem_free;
-  uint64_t qkv_ready[2], s_full[2], p_full[2], pv_done[2];
+  uint64_t qk_ready[2], v_ready[2], s_full[2], p_full[2], pv_done[2];
   uint64_t drained;
   uint32_t tmem_base;
   uint32_t abort_flag;
@@ -102,7 +103,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.qkv_free, 1);
     mbar_init(&sm.tmem_free, 256);  // every softmax thread, after its last TMEM read
     for (int e = 0; e < 2; ++e) {
-      mbar_init(&sm.qkv_ready[e], 128);
+      mbar_init(&sm.qk_ready[e], 128);
+      mbar_init(&sm.v_ready[e], 128);
       mbar_init(&sm.s_full[e], 1);
       mbar_init(&sm.p_full[e], 128);
       mbar_init(&sm.pv_done[e], 1);
@@ -234,9 +236,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         mma_commit(&sm.proj_done);
-        // ---- S_e = Q_e K_e^T, once head e's Q/K/V tiles are written
+        // ---- S_e = Q_e K_e^T, once head e's Q and K tiles are written
         for (int e = 0; ok && e < 2; ++e) {
-          ok = mbar_wait(&sm.qkv_ready[e], static_cast<uint32_t>(ui) & 1u, abort_flag);
+          ok = mbar_wait(&sm.qk_ready[e], static_cast<uint32_t>(ui) & 1u, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint64_t a = sdesc_advance(dqk0, (3 * e + 0) * kTileStep);
@@ -249,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---- O_e = P_e V_e, P from tensor memory
         for (int e = 0; ok && e < 2; ++e) {
-          ok = mbar_wait(&sm.p_full[e], static_cast<uint32_t>(ui) & 1u, abort_flag);
+          ok = mbar_wait(&sm.v_ready[e], static_cast<uint32_t>(ui) & 1u, abort_flag) &&
+               mbar_wait(&sm.p_full[e], static_cast<uint32_t>(ui) & 1u, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint64_t bv = sdesc_advance(dv0, (3 * e + 2) * kTileStep);
@@ -299,31 +302,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       // four warps stop together (none is left waiting at it).
       bool okw = __all_sync(0xffffffffu, mbar_wait(&sm.proj_done, ph, abort_flag));
       if (okw) {
-        // ---- (1) this row of Q, K, V -> bf16 rows of the swizzled tiles
+        // ---- (1) this row of Q, K, V -> bf16 rows of the swizzled tiles;
+        // Q and K first, so that S runs while V is converted
         tc_fence_after();
-#pragma unroll
-        for (int part = 0; part < 3; ++part) {
+        auto convert = [&](int part) {
           uint8_t* row = ring + (3 * e + part) * kTile + r * 128;
+          uint32_t v[64];
+          tmem_ld32(taddr_acc + part * kD, *reinterpret_cast<uint32_t(*)[32]>(v));
+          tmem_ld32(taddr_acc + part * kD + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+          tmem_wait_ld();
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            uint32_t v[32];
-            tmem_ld32(taddr_acc + part * kD + cc * 32, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              const int j = cc * 4 + v4;  // 16-byte chunk of the 128-byte row
-              const uint32_t* x = v + 8 * v4;
-              st_shared_v4(smem_u32(row + ((j ^ (r & 7)) << 4)),
-                           pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
-                           pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
-                           pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
-                           pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
-            }
+          for (int j = 0; j < 8; ++j) {  // 16-byte chunk j of the 128-byte row
+            const uint32_t* x = v + 8 * j;
+            st_shared_v4(smem_u32(row + ((j ^ (r & 7)) << 4)),
+                         pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                         pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                         pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                         pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
           }
-        }
+        };
+        convert(0);
+        convert(1);
         fence_proxy_async_smem();  // the tiles are read by the tensor cores
         tc_fence_before();         // and S overwrites the accumulator just read
-        mbar_arrive(&sm.qkv_ready[e]);
+        mbar_arrive(&sm.qk_ready[e]);
+        convert(2);
+        fence_proxy_async_smem();
+        tc_fence_before();         // P overwrites V's accumulator columns
+        mbar_arrive(&sm.v_ready[e]);
       }
       // ---- (2) softmax of the single score tile
       okw = okw && __all_sync(0xffffffffu, mbar_wait(&sm.s_full[e], ph, abort_flag));

@@ -312,22 +312,32 @@ class MhaCall:
                              m.h, m.d_k, m.d_v, m.mask_kind, s["lens"], 0.0, s["ws"], self.wsb,
                              stream)
 
+    def n_launches(self):
+        """Kernels mha_forward launches for this shape, as the library plans
+        them: 1 (projections, attention and W_O in one kernel), 2 (that kernel
+        up to the merged heads, then the W_O GEMM) or 3 (QKV GEMM, attention,
+        W_O GEMM)."""
+        if not hasattr(self, "_n_launches"):
+            m = self.m
+            self._n_launches = self.tsd.mha_forward_launches(m.B, m.n_q, m.n_k, m.d_model, m.h,
+                                                             m.d_k, m.d_v, m.self_attention)
+            if self._n_launches not in (1, 2, 3):
+                raise RuntimeError(f"mha_forward_launches -> {self._n_launches}")
+        return self._n_launches
+
     def fused(self):
-        """Whether mha_forward takes the fused short-sequence kernel (the
-        library's rule: n_q, n_k <= 128, d_k = d_v = 64, h even, d_model a
-        multiple of 64)."""
-        m = self.m
-        return (m.d_k == 64 and m.d_v == 64 and 1 <= m.n_q <= 128 and 1 <= m.n_k <= 128
-                and m.h % 2 == 0 and m.d_model % 64 == 0)
+        return self.n_launches() < 3
 
     def run_stage(self, k, i, stream):
-        """Launch k of the step's launches (fused path: heads, W_O projection;
-        otherwise QKV projection, attention, W_O projection) through its own
-        entry point, on input set i."""
+        """Launch k of the step's launches through its own entry point, on
+        input set i."""
         m, s = self.m, self.sets[i % len(self.sets)]
         base = s["ws"].data_ptr()
         Q, K, V, O = base + self.q_off, base + self.k_off, base + self.v_off, base + self.o_off
         hdk, hdv = m.h * m.d_k, m.h * m.d_v
+        if self.n_launches() == 1:
+            self.run(i, stream)
+            return
         if self.fused():
             if k == 0:
                 self.tsd.mha_concat_heads(s["x_q"], s["x_kv"], *s["w"][:3], O, m.B, m.n_q, m.n_k,
@@ -350,6 +360,8 @@ class MhaCall:
                                      stream)
 
     def stage_names(self):
+        if self.n_launches() == 1:
+            return ["mha_fused"]
         if self.fused():
             return ["mha_fused", "gemm_bf16"]
         return ["gemm_bf16", "attn_fwd_bf16", "gemm_bf16"]
@@ -370,6 +382,10 @@ class MhaCall:
                                 for b in range(m.B))
         out_f = 2.0 * Mq * hdv * dm
         out_b = 2.0 * (Mq * hdv + hdv * dm + Mq * dm)
+        if self.n_launches() == 1:
+            # X, the four weights and out cross HBM; Q/K/V and the merged
+            # heads stay on chip or in L2
+            return [(qkv_f + att_f + out_f, x_b + w_b + 2.0 * (hdv * dm + Mq * dm))]
         if self.fused():
             # X, the weights and the merged heads cross HBM; Q/K/V stay on chip
             return [(qkv_f + att_f, x_b + w_b + 2.0 * Mq * hdv), (out_f, out_b)]

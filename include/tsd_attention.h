@@ -123,6 +123,7 @@ size_t mha_workspace_bytes(int B, int n_q, int n_k, int h, int d_k, int d_v);
  *   Q = x_q W_Q, K = x_kv W_K, V = x_kv W_V        (tensor-core GEMMs)
  *   head_i = Attention(Q_i, K_i, V_i)              (attn kernel; Q_i = column block i)
  *   out = Concat(head_1..head_h) W_O               (tensor-core GEMM)
+ * Short sequences run all three in one or two kernels (mha_forward_launches).
  *
  *   x_q  [B, n_q, d_model] bf16      x_kv [B, n_k, d_model] bf16 (may equal x_q)
  *   w_q  [d_model, h*d_k]  bf16      w_k  [d_model, h*d_k]  bf16
@@ -133,7 +134,9 @@ size_t mha_workspace_bytes(int B, int n_q, int n_k, int h, int d_k, int d_v);
  *   on return its last region holds the merged heads; the Q, K, V regions
  *   are scratch (short sequences -- n_q, n_k <= 128, d_k = d_v = 64, h even,
  *   d_model a multiple of 64 -- are projected and attended in one kernel
- *   and never write them).
+ *   and never write them). With thread-block clusters in flight, the
+ *   merged-heads region is how the CTAs of one batch entry share their
+ *   heads: calls running concurrently need distinct workspaces.
  *   mask_kind, kv_lens, scale: as attn_forward (the mask applies to every head).
  * Errors: as attn_forward; a short workspace -> ATTN_ERR_INVALID.
  */
@@ -143,6 +146,21 @@ attn_status mha_forward(const void *x_q, const void *x_kv,
                         int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
                         int mask_kind, const int32_t *kv_lens, float scale,
                         void *workspace, size_t workspace_bytes, tsd_stream_t stream);
+
+/*
+ * mha_forward_launches -- how many kernels mha_forward launches for these
+ * sizes on the current device (a planning query: no launch, no allocation;
+ * it may ask the runtime how many thread-block clusters fit):
+ *   1  short sequences, W_O applied in the same kernel (n_q, n_k <= 128,
+ *      d_k = d_v = 64, h even, h/2 <= 8, d_model / (h/2) = 64 or 128, and a
+ *      cluster of h/2 CTAs fits on the device);
+ *   2  short sequences, then the W_O GEMM;
+ *   3  the Q/K/V projection GEMM, the attention kernel, the W_O GEMM;
+ *   0  nothing to do (B * n_q == 0);  -1  sizes mha_forward rejects.
+ * self_attention: nonzero when x_kv will be passed equal to x_q.
+ */
+int mha_forward_launches(int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
+                         int self_attention);
 
 /*
  * mha_concat_heads -- Concat(head_1, ..., head_h), head_i =

@@ -122,6 +122,63 @@ def test_mha_fused_short_sequences(tsd, shape):
     check(tsd, m, str(shape))
 
 
+@pytest.mark.parametrize("shape", [
+    # the fused kernel applying W_O too (clusters of h/2 CTAs, d_model / (h/2)
+    # output columns each): B, n_q, n_k, d_model, h, mask, self
+    (80, 32, 32, 512, 8, MASK_KEY_PADDING, True),   # more batch entries than resident clusters
+    (5, 128, 96, 256, 8, MASK_NONE, False),         # 64 output columns per CTA; cross-attention
+    (3, 65, 65, 384, 6, MASK_CAUSAL, True),         # clusters of 3
+    (2, 1, 1, 128, 2, MASK_NONE, True),             # one CTA per cluster, one row
+])
+def test_mha_fused_output_projection(tsd, shape):
+    B, n_q, n_k, dm, h, mask, self_attn = shape
+    assert tsd.mha_forward_launches(B, n_q, n_k, dm, h, 64, 64, self_attn) == 1
+    m = synthetic.mha_inputs(3250 + B + n_q + dm, B, n_q, n_k, dm, h, 64, 64, mask, (1, n_k),
+                             self_attention=self_attn)
+    check(tsd, m, str(shape))
+
+
+def test_mha_forward_launch_plan(tsd):
+    """The launch counts mha_forward reports for the workload shapes."""
+    plan = tsd.mha_forward_launches
+    assert plan(32, 128, 128, 512, 8, 64, 64, True) == 1     # Transformer-base self-attention
+    assert plan(32, 128, 160, 512, 8, 64, 64, False) == 3    # decoder cross-attention, n_k > 128
+    assert plan(40, 64, 64, 128, 16, 64, 64, True) == 2      # 16 output columns per CTA: no
+    assert plan(8, 1024, 1024, 1024, 16, 64, 64, True) == 3  # Transformer-big, n = 1024
+    assert plan(0, 128, 128, 512, 8, 64, 64, True) == 0
+    assert plan(1, 16, 16, 512, 8, 32, 32, True) == -1
+
+
+def test_mha_fused_output_projection_matches_two_launch_path(tsd):
+    """The one-launch path (W_O inside the fused kernel) against the
+    two-launch one (merged heads, then the W_O GEMM) on the same inputs: the
+    merged heads are identical and out differs only by fp32 summation order
+    before the bf16 rounding."""
+    import torch
+    m = synthetic.mha_inputs(1001, 32, 128, 128, 512, 8, 64, 64, MASK_KEY_PADDING, (64, 128),
+                             add_pe=True)
+    got, ws = run_mha(tsd, m)
+    x = to_dev_bf16(m.x_q)
+    w = [to_dev_bf16(t) for t in (m.w_q, m.w_k, m.w_v, m.w_o)]
+    lens = to_dev_i32(m.kv_lens)
+    concat = torch.empty((32, 128, 512), dtype=torch.bfloat16, device="cuda")
+    out2 = torch.empty((32, 128, 512), dtype=torch.bfloat16, device="cuda")
+    wsb = tsd.mha_workspace_bytes(32, 128, 128, 8, 64, 64)
+    ws2 = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    tsd.mha_concat_heads(x, x, *w[:3], concat, 32, 128, 128, 512, 8, 64, 64, m.mask_kind, lens,
+                         0.0, ws2, wsb)
+    tsd.mha_project_out(concat, w[3], out2, 32, 128, 512, 8, 64)
+    torch.cuda.synchronize()
+    assert tsd.attn_get_device_status() == tsd.ATTN_OK
+    off = wsb - 32 * 128 * 512 * 2
+    merged = ws[off:].view(torch.bfloat16).view(32, 128, 512)
+    assert torch.equal(merged, concat)
+    two = to_host_f64(out2)
+    diff = np.abs(got - two)
+    # at most one bf16 step of the larger value apart
+    assert np.all(diff <= np.maximum(np.abs(got), np.abs(two)) * 2.0 ** -7 + 1e-6)
+
+
 def test_mha_fused_key_length_zero(tsd):
     """A batch entry with no keys gives zero heads, so its output is 0 (the
     projections carry no bias)."""

@@ -23,7 +23,7 @@ __all__ = [
     "attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_workspace_bytes",
     "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
     "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out", "mha_forward_noalloc",
-    "mha_concat_heads", "MHA_NOALLOC_SCRATCH_BYTES",
+    "mha_concat_heads", "mha_forward_launches", "MHA_NOALLOC_SCRATCH_BYTES",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = range(5)
@@ -33,7 +33,7 @@ EXPORTED_SYMBOLS = (
     "attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_workspace_bytes",
     "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
     "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out", "mha_forward_noalloc",
-    "mha_concat_heads",
+    "mha_concat_heads", "mha_forward_launches",
 )
 
 # TSD_MHA_NOALLOC_SCRATCH_BYTES of the header: the fixed scratch of mha_forward_noalloc
@@ -86,9 +86,11 @@ def library():
     lib.attn_status_string.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_selftest_wait_timeout.argtypes = [i, st]
+    lib.mha_forward_launches.argtypes = [i, i, i, i, i, i, i, i]
     for name in ("attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_forward",
                  "attn_get_device_status", "attn_last_cuda_error", "attn_selftest_wait_timeout",
-                 "mha_project_qkv", "mha_project_out", "mha_forward_noalloc", "mha_concat_heads"):
+                 "mha_project_qkv", "mha_project_out", "mha_forward_noalloc", "mha_concat_heads",
+                 "mha_forward_launches"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -149,6 +151,13 @@ def mha_forward(x_q, x_kv, w_q, w_k, w_v, w_o, out, B, n_q, n_k, d_model, h, d_k
                                  _ptr(w_o), _ptr(out), B, n_q, n_k, d_model, h, d_k, d_v,
                                  mask_kind, _ptr(kv_lens), scale, _ptr(workspace),
                                  workspace_bytes, _stream(stream)), "mha_forward")
+
+
+def mha_forward_launches(B, n_q, n_k, d_model, h, d_k, d_v, self_attention) -> int:
+    """Kernels mha_forward launches for these sizes (1, 2 or 3; 0 for no
+    work; -1 for sizes it rejects)."""
+    return int(library().mha_forward_launches(B, n_q, n_k, d_model, h, d_k, d_v,
+                                              1 if self_attention else 0))
 
 
 def mha_concat_heads(x_q, x_kv, w_q, w_k, w_v, concat, B, n_q, n_k, d_model, h, d_k, d_v,

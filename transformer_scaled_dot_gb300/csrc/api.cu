@@ -289,15 +289,29 @@ bool fused_eligible(int n_q, int n_k, int d_model, int h, int d_k, int d_v) {
          h % 2 == 0 && d_model >= 64 && d_model % 64 == 0;
 }
 
+// The fused kernel can apply W_O as well: h/2 <= 8 head pairs (one cluster
+// per batch entry), d_model / (h/2) output columns per CTA = 64 or 128, and
+// such a cluster fits on the device.
+bool fused_out_eligible(bool self, int d_model, int h) {
+  const int C = h / 2;
+  if (C < 1 || C > 8 || d_model % C != 0) return false;
+  const int n_slice = d_model / C;
+  if (n_slice != 64 && n_slice != 128) return false;
+  return tsd::mha_fused_out_clusters(h, self) > 0;
+}
+
 // Q/K/V projections + attention of every (batch, head pair) -> the merged
-// heads, [B, n_q, h*64], in `concat`.
+// heads, [B, n_q, h*64], in `concat`; with `w_o` also out = concat W_O in
+// the same launch (`concat` is then scratch).
 attn_status launch_fused_core(const void* x_q, const void* x_kv, const void* w_q, const void* w_k,
                               const void* w_v, void* concat, int B, int n_q, int n_k, int d_model,
                               int h, int mask_kind, const int32_t* kv_lens, float scale,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, const void* w_o = nullptr,
+                              void* out = nullptr) {
   tsd::MhaFusedProblem p;
   std::memset(&p, 0, sizeof(p));
   p.self = (x_q == x_kv) && (n_q == n_k);
+  p.out = w_o != nullptr;
   const uint32_t xbox[3] = {64, 128, 1};
   const uint64_t xq_dims[3] = {static_cast<uint64_t>(d_model), static_cast<uint64_t>(n_q),
                                static_cast<uint64_t>(B)};
@@ -321,6 +335,12 @@ attn_status launch_fused_core(const void* x_q, const void* x_kv, const void* w_q
                               static_cast<uint64_t>(B)};
   const int64_t o_str[2] = {int64_t(h) * 64, int64_t(n_q) * h * 64};
   if (e == cudaSuccess) e = encode_bf16_map(&p.tm_o, concat, 3, o_dims, o_str, xbox);
+  if (e == cudaSuccess && p.out) {
+    const uint64_t wo_dims[2] = {static_cast<uint64_t>(d_model), static_cast<uint64_t>(h) * 64};
+    const int64_t wo_str[1] = {d_model};
+    e = encode_bf16_map(&p.tm_wo, w_o, 2, wo_dims, wo_str, wbox);
+    if (e == cudaSuccess) e = encode_bf16_map(&p.tm_out, out, 3, xq_dims, xq_str, xbox);
+  }
   if (e != cudaSuccess) return cuda_fail(e);
   p.B = B;
   p.h = h;
@@ -473,12 +493,28 @@ attn_status mha_forward(const void* x_q, const void* x_kv, const void* w_q, cons
   void* K = ws + L.k_off;
   void* V = ws + L.v_off;
   void* O = ws + L.o_off;
+  // Short sequences: projections, attention and W_O in one launch (the
+  // merged heads pass through the workspace's last region)
+  if (fused_eligible(n_q, n_k, d_model, h, d_k, d_v) &&
+      fused_out_eligible(x_q == x_kv && n_q == n_k, d_model, h))
+    return launch_fused_core(x_q, x_kv, w_q, w_k, w_v, O, B, n_q, n_k, d_model, h, mask_kind,
+                             kv_lens, scale, stream, w_o, out);
   // 1-2. Concat(head_1..head_h) into the workspace's last region
   s = concat_heads(x_q, x_kv, w_q, w_k, w_v, O, Q, K, V, B, n_q, n_k, d_model, h, d_k, d_v,
                    mask_kind, kv_lens, scale, stream);
   if (s != ATTN_OK) return s;
   // 3. out = Concat(head_1..head_h) W_O
   return launch_out_proj(O, w_o, out, B, n_q, d_model, h, d_v, stream);
+}
+
+int mha_forward_launches(int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
+                         int self_attention) {
+  if (B < 0 || n_q < 0 || n_k < 0 || h <= 0 || d_model < 8 || (d_model % 8) != 0 ||
+      check_bf16_head_dims(d_k, d_v) != ATTN_OK)
+    return -1;
+  if (int64_t(B) * n_q == 0) return 0;
+  if (!fused_eligible(n_q, n_k, d_model, h, d_k, d_v)) return 3;
+  return fused_out_eligible(self_attention != 0 && n_q == n_k, d_model, h) ? 1 : 2;
 }
 
 attn_status mha_concat_heads(const void* x_q, const void* x_kv, const void* w_q, const void* w_k,

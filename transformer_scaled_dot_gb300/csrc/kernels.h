@@ -110,19 +110,27 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // Multi-head attention for short sequences in one kernel up to the merged
 // heads: the Q/K/V projections of each head pair, their attention, and the
 // merged [B, n_q, h*64] output. n_q, n_k <= 128, d_k = d_v = 64, h even,
-// d_model a multiple of 64.
+// d_model a multiple of 64. With `out`, the same launch also applies W_O
+// (clusters of h/2 CTAs, h/2 <= 8, d_model / (h/2) = 64 or 128), writing
+// `out` [B, n_q, d_model]; the merged buffer is then its scratch.
 struct MhaFusedProblem {
   CUtensorMap tm_xq;   // 3-D (d_model, n_q, B), box 64 x 128 x 1
   CUtensorMap tm_xkv;  // 3-D (d_model, n_k, B) (unused when self)
   CUtensorMap tm_wq, tm_wk, tm_wv;  // 2-D (h*64, d_model), box 64 x 64
-  CUtensorMap tm_o;    // 3-D (h*64, n_q, B), box 64 x 128 x 1 (TMA store)
+  CUtensorMap tm_o;    // 3-D (h*64, n_q, B), box 64 x 128 x 1 (TMA store, and load with out)
+  CUtensorMap tm_wo;   // 2-D (d_model, h*64), box 64 x 64 (out only)
+  CUtensorMap tm_out;  // 3-D (d_model, n_q, B), box 64 x 128 x 1 (out only)
   int B, h, n_q, n_k, d_model;
   bool self;           // x_kv is x_q (and n_k == n_q)
+  bool out;            // apply W_O too
   int mask_kind;
   const int32_t* kv_lens;
   float scale;
 };
 cudaError_t launch_mha_fused(const MhaFusedProblem& p, cudaStream_t stream);
+// Clusters of h/2 output-projecting CTAs that fit on the device at once (0:
+// the output projection cannot be fused).
+int mha_fused_out_clusters(int h, bool self);
 
 // Per-file device error words (read and cleared; see sm103.cuh).
 cudaError_t take_device_error_attn(unsigned int* value);

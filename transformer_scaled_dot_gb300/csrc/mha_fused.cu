@@ -3,8 +3,8 @@
 // of a head pair, their scaled dot-product attention, and the heads written
 // side by side ("[논문 리뷰]Attention Is All You Need" (kimjiil.github.io),
 // sections 3.2.1-3.2.2: head_i = Attention(Q W_i^Q, K W_i^K, V W_i^V);
-// weights in the x.W layout, [d_model, h*d], no biases). The output
-// projection W_O stays a separate GEMM.
+// weights in the x.W layout, [d_model, h*d], no biases), and optionally the
+// output projection of section 3.2.2 as well (MultiHead = Concat(heads) W_O).
 //
 // Why fuse: at these sizes the three-kernel path is latency-bound. The
 // projection GEMM's operand traffic from L2 is its limit, the attention
@@ -33,6 +33,24 @@
 // and P_e (bf16) its V part; O_e lives at [384 + 64e, 448 + 64e).
 // Rows past n_q / n_k are zero (the tensor maps clip them); they produce
 // nothing: keys past n_k are masked, query rows past n_q are not stored.
+//
+// With the output projection (OUT): the h/2 CTAs of one batch entry form a
+// cluster, CTA r owning head pair r and output columns [N r, N r + N),
+// N = d_model / (h/2) (64 or 128). Each CTA still stores its two heads into
+// the merged buffer; once a store has completed, its head leader signals
+// every peer (st.async of a word into the peer's shared memory, complete_tx
+// on the peer's mbarrier for this CTA, release at cluster scope). The
+// producer of each CTA, having acquired a peer's signals, loads its merged
+// tiles back from L2 into the space its own Q/K/V tiles used (6 slots of
+// 16 KB), and streams
+// the W_O rows of all h heads, columns [N r, N r + N), through the rest of
+// the ring (W_O's first chunks already during the attention). The MMA
+// warp accumulates out = sum_j head_j W_O[64 j : 64 j + 64, cols] over the
+// heads, its own two read straight from the epilogue's staging tiles, into
+// TMEM columns [0, N); the head warpgroups store it (bf16) to `out`.
+// Moving the merged tiles through L2 rather than distributed shared memory
+// is measured, not assumed: on GB300 a CTA receives about 155 GB/s from L2
+// by TMA but only about 20 GB/s from the other CTAs of its cluster.
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -50,6 +68,10 @@ constexpr uint32_t kCtrlRegs = 72;
 constexpr uint32_t kSoftmaxRegs = (kLaunchRegs * kThreads - kCtrlRegs * 128) / 256 / 8 * 8;
 static_assert(kCtrlRegs * 128 + kSoftmaxRegs * 256 <= kLaunchRegs * kThreads, "register split");
 constexpr unsigned long long kDrainLimitNs = 100ull * 1000ull * 1000ull;
+// output projection (OUT)
+constexpr int kSlot = 16384;    // a 128 x 64 merged-heads tile, or 64 rows of W_O x <= 128 columns
+constexpr int kOSlots = 6;      // peers' merged tiles, where the Q/K/V tiles were
+constexpr int kMaxCluster = 8;  // head pairs per batch entry (portable cluster size)
 
 template <bool SELF>
 struct FusedSmem {
@@ -64,9 +86,23 @@ struct FusedSmem {
   uint64_t proj_done, qkv_free, tmem_free;
   uint64_t qk_ready[2], v_ready[2], s_full[2], p_full[2], pv_done[2];
   uint64_t drained;
+  // output projection (OUT): peer tiles in ring slots [0, kOSlots), W_O
+  // chunks in the slots after them
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kWoSlots = (kRingBytes - kOSlots * kSlot) / kSlot;  // self 6, cross 4
+  uint64_t o_full[kOSlots], o_empty[kOSlots];
+  uint64_t wo_full[kWoSlots], wo_empty[kWoSlots];
+  uint64_t o_staged;   // this CTA's two merged tiles are in o[] (256 arrivals)
+  uint64_t out_done;   // every out-projection MMA of the item has completed
+  // peer slot s's merged tiles are in global memory (item parity): two 4-byte
+  // signals (one per head) into o_words
+  uint64_t o_ready[2][kMaxCluster - 1];
+  uint32_t o_words[2][kMaxCluster - 1][2];
   uint32_t tmem_base;
   uint32_t abort_flag;
   static_assert(kStages * kStageBytes >= 6 * kTile, "Q/K/V tiles fit in the ring");
+  static_assert(kOSlots * kSlot == 6 * kTile, "peer tiles take the Q/K/V tiles' place");
+  static_assert(kWoSlots >= 2, "W_O ring");
 };
 
 struct FusedArgs {
@@ -74,18 +110,22 @@ struct FusedArgs {
   int mask_kind;
   const int32_t* kv_lens;
   float scale_log2;
+  int n_slice;  // OUT: output columns per CTA (64 or 128)
 };
 
-template <bool SELF>
+template <bool SELF, bool OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     mha_fused_kernel(const __grid_constant__ CUtensorMap tm_xq,
                      const __grid_constant__ CUtensorMap tm_xkv,
                      const __grid_constant__ CUtensorMap tm_wq,
                      const __grid_constant__ CUtensorMap tm_wk,
                      const __grid_constant__ CUtensorMap tm_wv,
-                     const __grid_constant__ CUtensorMap tm_o, const FusedArgs args) {
+                     const __grid_constant__ CUtensorMap tm_o,
+                     const __grid_constant__ CUtensorMap tm_wo,
+                     const __grid_constant__ CUtensorMap tm_out, const FusedArgs args) {
   using Smem = FusedSmem<SELF>;
   constexpr int kStages = Smem::kStages;
+  constexpr int kWoSlots = Smem::kWoSlots;
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -110,6 +150,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.pv_done[e], 1);
     }
     mbar_init(&sm.drained, 1);
+    if constexpr (OUT) {
+      for (int i = 0; i < kOSlots; ++i) {
+        mbar_init(&sm.o_full[i], 1);
+        mbar_init(&sm.o_empty[i], 1);
+      }
+      for (int i = 0; i < kWoSlots; ++i) {
+        mbar_init(&sm.wo_full[i], 1);
+        mbar_init(&sm.wo_empty[i], 1);
+      }
+      mbar_init(&sm.o_staged, 256);
+      mbar_init(&sm.out_done, 1);
+      for (int p = 0; p < 2; ++p)
+        for (int i = 0; i < kMaxCluster - 1; ++i) mbar_init(&sm.o_ready[p][i], 1);
+    }
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -118,7 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  // peers arrive on this CTA's barriers: every CTA of the cluster has
+  // initialised its own first
+  if constexpr (OUT) cluster_sync();
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile uint32_t* abort_flag = &sm.abort_flag;
@@ -131,6 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_wk);
     tma_prefetch_desc(&tm_wv);
     tma_prefetch_desc(&tm_o);
+    if constexpr (OUT) {
+      tma_prefetch_desc(&tm_wo);
+      tma_prefetch_desc(&tm_out);
+    }
   }
   // Everything up to a role's first global-memory access may overlap the
   // previous kernel: each role waits for it (griddep_wait) just before.
@@ -140,15 +201,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_decrease<kCtrlRegs>();
     if (warp == 0 && lane == 0) {
       // ------------------------------------------------------------ producer
-      int issued = 0, ui = 0;
+      int issued = 0, ui = 0, wo_cnt = 0, o_cnt = 0, armed = -1;
       bool ok = true;
       for (int u = first; ok && u < args.num_units; u += stride, ++ui) {
         const int b = u / args.head_pairs;
-        const int h0 = 2 * (u % args.head_pairs);
-        // the previous item's Q/K/V tiles (in the ring) have been consumed
+        const int pair = u % args.head_pairs;
+        const int h0 = 2 * pair;
+        // the previous item's tiles in the ring (Q/K/V; with OUT also the
+        // peers' merged tiles and W_O) have been consumed
         if (ui > 0) {
-          ok = mbar_wait(&sm.qkv_free, static_cast<uint32_t>(ui - 1) & 1u, abort_flag);
+          ok = mbar_wait(OUT ? &sm.out_done : &sm.qkv_free, static_cast<uint32_t>(ui - 1) & 1u,
+                         abort_flag);
           if (!ok) break;
+        }
+        if constexpr (OUT) {
+          // expect the peers' signals for this item (2 x 4 bytes per peer);
+          // they may land before this, the phase completes with both
+          for (int s = 0; s < args.head_pairs - 1; ++s)
+            mbar_arrive_expect_tx(&sm.o_ready[ui & 1][s], 8);
+          armed = ui;
         }
         for (int kb = 0; kb < args.kblocks; ++kb) {
           const int s = issued % kStages;
@@ -170,6 +241,58 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++issued;
         }
+        if constexpr (OUT) {
+          if (!ok) break;
+          const int C = args.head_pairs;
+          // chunk j of the output projection: head 2 ((pair + j/2) mod C) + j%2
+          // (this CTA's own two heads first)
+          auto head_of = [&](int j) { return 2 * ((pair + (j >> 1)) % C) + (j & 1); };
+          auto issue_wo = [&](int j) -> bool {  // W_O rows of head j, this CTA's columns
+            const int s = wo_cnt % kWoSlots;
+            if (!mbar_wait(&sm.wo_empty[s], (static_cast<uint32_t>(wo_cnt / kWoSlots) & 1u) ^ 1u,
+                           abort_flag))
+              return false;
+            uint8_t* dst = sm.ring[0] + (kOSlots + s) * kSlot;
+            mbar_arrive_expect_tx(&sm.wo_full[s], static_cast<uint32_t>(args.n_slice) * 128u);
+            for (int c = 0; c < args.n_slice; c += 64)
+              tma_load_2d(dst + c * 128, &tm_wo, &sm.wo_full[s], pair * args.n_slice + c,
+                          head_of(j) * kD);
+            ++wo_cnt;
+            return true;
+          };
+          auto issue_o = [&](int j) -> bool {  // a peer's merged tile of head j
+            const int s = o_cnt % kOSlots;
+            if (!mbar_wait(&sm.o_empty[s], (static_cast<uint32_t>(o_cnt / kOSlots) & 1u) ^ 1u,
+                           abort_flag))
+              return false;
+            mbar_arrive_expect_tx(&sm.o_full[s], kTile);
+            tma_load_3d(sm.ring[0] + s * kSlot, &tm_o, &sm.o_full[s], head_of(j) * kD, 0, b);
+            ++o_cnt;
+            return true;
+          };
+          const uint32_t ph = static_cast<uint32_t>(ui) & 1u;
+          // W_O's first chunks while the attention runs: the projection
+          // stages are free once every projection MMA has completed
+          ok = mbar_wait(&sm.proj_done, ph, abort_flag);
+          int wj = 0;
+          for (; ok && wj < args.h && wj < kWoSlots; ++wj) ok = issue_wo(wj);
+          // the W_O chunks whose slots the own heads' MMAs free (those need
+          // nothing from the peers), then the peers' merged tiles, into the
+          // Q/K/V tiles' place once those are consumed, each peer's as soon
+          // as it has stored them
+          for (; ok && wj < args.h && wj < kWoSlots + 2; ++wj) ok = issue_wo(wj);
+          ok = ok && mbar_wait(&sm.qkv_free, ph, abort_flag);
+          for (int j = 2; ok && j < args.h; ++j) {
+            if ((j & 1) == 0) {
+              ok = mbar_wait_cluster(&sm.o_ready[ui & 1][(j >> 1) - 1],
+                                     static_cast<uint32_t>(ui >> 1) & 1u, abort_flag);
+              fence_proxy_async_global();  // before the TMA reads what the peer's TMA wrote
+            }
+            ok = ok && issue_o(j);
+            while (ok && wj <= j) ok = issue_wo(wj++);
+          }
+          while (ok && wj < args.h) ok = issue_wo(wj++);
+        }
       }
       if (!ok) {
         // wait (bounded) for this thread's copies still in flight
@@ -177,6 +300,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = max(0, issued - kStages); i < issued; ++i)
           mbar_wait(&sm.full[i % kStages], static_cast<uint32_t>(i / kStages) & 1u, &never,
                     kDrainLimitNs);
+        if constexpr (OUT) {
+          for (int i = max(0, wo_cnt - kWoSlots); i < wo_cnt; ++i)
+            mbar_wait(&sm.wo_full[i % kWoSlots], static_cast<uint32_t>(i / kWoSlots) & 1u, &never,
+                      kDrainLimitNs);
+          for (int i = max(0, o_cnt - kOSlots); i < o_cnt; ++i)
+            mbar_wait(&sm.o_full[i % kOSlots], static_cast<uint32_t>(i / kOSlots) & 1u, &never,
+                      kDrainLimitNs);
+        }
+      }
+      if constexpr (OUT) {
+        // the peers' signals this CTA expects have landed before it leaves
+        // (at once after a normal run; bounded when a peer gave up)
+        volatile uint32_t never = 0;
+        if (armed >= 0)
+          for (int s = 0; s < args.head_pairs - 1; ++s)
+            mbar_wait(&sm.o_ready[armed & 1][s], static_cast<uint32_t>(armed >> 1) & 1u, &never,
+                      ok ? kDrainLimitNs : 3 * kWaitLimitNs);
       }
     } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
@@ -195,10 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kStageStep = Smem::kStageBytes >> 4;
       constexpr uint32_t kTileStep = kTile >> 4;
       constexpr uint32_t kWStep = kWChunk >> 4;
-      int consumed = 0, ui = 0;
+      constexpr uint32_t kIdescOut128 = idesc_bf16(kRows, 128, false, true);
+      constexpr uint32_t kIdescOut64 = idesc_bf16(kRows, 64, false, true);
+      int consumed = 0, ui = 0, o_used = 0, wo_used = 0;
       bool ok = true;
       for (int u = first; ok && u < args.num_units; u += stride, ++ui) {
-        // the previous item's S, P and O have been read
+        // the previous item's S, P and O (and out) have been read
         if (ui > 0) {
           ok = mbar_wait(&sm.tmem_free, static_cast<uint32_t>(ui - 1) & 1u, abort_flag);
           if (!ok) break;
@@ -265,6 +407,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         mma_commit(&sm.qkv_free);  // every MMA reading this item's Q/K/V tiles has completed
+        if constexpr (OUT) {
+          // ---- out[:, cols] = sum_j head_j W_O[64 j : 64 j + 64, cols], into
+          // TMEM columns [0, n_slice) (S_0's, read long ago)
+          ok = mbar_wait(&sm.o_staged, static_cast<uint32_t>(ui) & 1u, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t idesc_out = args.n_slice == 128 ? kIdescOut128 : kIdescOut64;
+          for (int j = 0; ok && j < args.h; ++j) {
+            uint64_t a;
+            int os = -1;
+            if (j < 2) {  // this CTA's own heads, still in the epilogue's staging tiles
+              a = sdesc_sw128(smem_u32(sm.o[j]), 16, 1024);
+            } else {
+              os = o_used % kOSlots;
+              ok = mbar_wait(&sm.o_full[os], static_cast<uint32_t>(o_used / kOSlots) & 1u,
+                             abort_flag);
+              ++o_used;
+              a = sdesc_sw128(ring0 + os * kSlot, 16, 1024);
+            }
+            const int ws = wo_used % kWoSlots;
+            ok = ok && mbar_wait(&sm.wo_full[ws], static_cast<uint32_t>(wo_used / kWoSlots) & 1u,
+                                 abort_flag);
+            ++wo_used;
+            if (!ok) break;
+            tc_fence_after();
+            // W_O chunk: 64 rows x n_slice columns as 64-column blocks 8 KB apart
+            const uint64_t bw = sdesc_sw128(ring0 + (kOSlots + ws) * kSlot, kWChunk, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_bf16_ss(tmem, sdesc_advance(a, kk * 2), sdesc_advance(bw, kk * (2048 >> 4)),
+                          idesc_out, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&sm.wo_empty[ws]);
+            if (os >= 0) mma_commit(&sm.o_empty[os]);
+          }
+          if (!ok) break;
+          mma_commit(&sm.out_done);
+        }
       }
       // every issued MMA has completed before tensor memory is released
       volatile uint32_t never = 0;
@@ -291,7 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ui = 0;
     for (int u = first; ok && u < args.num_units; u += stride, ++ui) {
       const int b = u / args.head_pairs;
-      const int hh = 2 * (u % args.head_pairs) + e;
+      const int pair = u % args.head_pairs;
+      const int hh = 2 * pair + e;
       int kv_eff = args.n_k;
       if (args.mask_kind & kMaskKeyPadding) {
         const int len = args.kv_lens[b];
@@ -411,13 +591,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&sm.tmem_free);  // this thread's reads of S, P and O are done
-      fence_proxy_async_smem();    // staged bytes visible to the TMA unit
+      if constexpr (!OUT) mbar_arrive(&sm.tmem_free);  // this thread's reads of S, P and O are done
+      fence_proxy_async_smem();  // staged bytes visible to the TMA unit (and the tensor cores)
+      if constexpr (OUT) mbar_arrive(&sm.o_staged);
       if (e == 0) named_bar_sync<1>(128);
       else named_bar_sync<2>(128);
       if (leader) {  // the map clips rows past n_q
         tma_store_3d(&tm_o, sm.o[e], hh * kD, 0, b);
         bulk_commit_group();
+        if constexpr (OUT) {
+          if (args.head_pairs > 1) {
+            // the tile is in global memory: tell every peer of the cluster
+            // (CTA rank = head pair: the grid is a whole number of clusters);
+            // this CTA is peer slot (pair - q - 1) mod C of CTA q
+            bulk_wait_group<0>();
+            fence_proxy_async_global();
+            const int C = args.head_pairs;
+            for (int q = 0; q < C; ++q) {
+              if (q == pair) continue;
+              const int slot = (pair - q - 1 + C) % C;
+              signal_remote(cluster_map(&sm.o_words[ui & 1][slot][e], q),
+                            cluster_map(&sm.o_ready[ui & 1][slot], q));
+            }
+          }
+        }
+      }
+      if constexpr (OUT) {
+        // ---- (4) out[:, N pair + 64 e : + 64] (fp32 in TMEM) -> bf16 ->
+        // staging -> TMA store
+        okw = __all_sync(0xffffffffu, mbar_wait(&sm.out_done, ph, abort_flag));
+        if (leader) bulk_wait_group_read<0>();  // the merged tile's store has read the staging tile
+        ok = e == 0 ? named_bar_and<1>(128, okw) : named_bar_and<2>(128, okw);
+        if (!ok) break;
+        tc_fence_after();
+        const bool has_cols = e * 64 < args.n_slice;
+        if (has_cols) {
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_base + e * 64 + cc * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              const int j = cc * 4 + v4;
+              const uint32_t* x = o + 8 * v4;
+              st_shared_v4(smem_u32(sm.o[e] + r * 128 + ((j ^ (r & 7)) << 4)),
+                           pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                           pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                           pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                           pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&sm.tmem_free);  // this thread's reads of S, P, O and out are done
+        fence_proxy_async_smem();
+        if (e == 0) named_bar_sync<1>(128);
+        else named_bar_sync<2>(128);
+        if (leader && has_cols) {
+          tma_store_3d(&tm_out, sm.o[e], pair * args.n_slice + e * 64, 0, b);
+          bulk_commit_group();
+        }
       }
     }
     // the stores have read the staging tiles before the CTA's shared memory
@@ -430,6 +664,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
+  if constexpr (OUT) {
+    // After a normal run every signal a peer sends this CTA has landed (the
+    // producer waited for each), so it may leave at once. After a failure a
+    // peer might still signal it for a later item: then it stays until every
+    // CTA of the cluster has either left or come here too.
+    if (__syncthreads_or(*abort_flag != 0u)) cluster_sync();
+  }
 }
 
 int num_sms() {
@@ -443,11 +684,44 @@ int num_sms() {
   return n;
 }
 
+// Clusters of C CTAs of the output-projecting kernel that can be resident
+// at once (clusters stay inside one GPC); 0 if none fits. Asked once per C.
 template <bool SELF>
+int fused_out_max_clusters(int C) {
+  static int cache[kMaxCluster + 1] = {};  // 0: not asked yet, -1: none fits
+  if (C < 1 || C > kMaxCluster) return 0;
+  const int known = __atomic_load_n(&cache[C], __ATOMIC_ACQUIRE);
+  if (known != 0) return known > 0 ? known : 0;
+  using Smem = FusedSmem<SELF>;
+  const size_t smem_bytes = sizeof(Smem) + 1024;
+  auto kernel = mha_fused_kernel<SELF, true>;
+  static unsigned long long configured = 0;
+  if (set_smem_once(kernel, static_cast<int>(smem_bytes), &configured) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms() / C * C);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  __atomic_store_n(&cache[C], n > 0 ? n : -1, __ATOMIC_RELEASE);
+  return n > 0 ? n : 0;
+}
+
+template <bool SELF, bool OUT>
 cudaError_t launch_fused(const MhaFusedProblem& p, cudaStream_t stream) {
   using Smem = FusedSmem<SELF>;
   const size_t smem_bytes = sizeof(Smem) + 1024;  // + alignment slack
-  auto kernel = mha_fused_kernel<SELF>;
+  auto kernel = mha_fused_kernel<SELF, OUT>;
   static unsigned long long configured = 0;
   cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured);
   if (e != cudaSuccess) return e;
@@ -464,18 +738,55 @@ cudaError_t launch_fused(const MhaFusedProblem& p, cudaStream_t stream) {
   a.mask_kind = p.mask_kind;
   a.kv_lens = p.kv_lens;
   a.scale_log2 = p.scale * 1.4426950408889634f;
-  const int grid = static_cast<int>(units < num_sms() ? units : num_sms());
-  return launch_pdl(kernel, dim3(grid), dim3(kThreads), smem_bytes, stream, p.tm_xq, p.tm_xkv,
-                    p.tm_wq, p.tm_wk, p.tm_wv, p.tm_o, a);
+  a.n_slice = OUT ? p.d_model / a.head_pairs : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int grid = static_cast<int>(units < num_sms() ? units : num_sms());
+  if (OUT) {
+    // one cluster per batch entry, CTA rank = head pair; persistent over
+    // batch entries when more than the resident clusters
+    const int C = a.head_pairs;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = C;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+    const int max_clusters = fused_out_max_clusters<SELF>(C);
+    if (max_clusters <= 0) return cudaErrorInvalidConfiguration;
+    grid = (p.B < max_clusters ? p.B : max_clusters) * C;
+  }
+  cfg.gridDim = dim3(grid);
+  return cudaLaunchKernelEx(&cfg, kernel, p.tm_xq, p.tm_xkv, p.tm_wq, p.tm_wk, p.tm_wv, p.tm_o,
+                            p.tm_wo, p.tm_out, a);
 }
 
 }  // namespace
+
+int mha_fused_out_clusters(int h, bool self) {
+  const int C = h / 2;
+  if (h % 2 != 0 || C < 1 || C > kMaxCluster) return 0;
+  return self ? fused_out_max_clusters<true>(C) : fused_out_max_clusters<false>(C);
+}
 
 cudaError_t launch_mha_fused(const MhaFusedProblem& p, cudaStream_t stream) {
   if (p.h % 2 != 0 || p.d_model % 64 != 0 || p.d_model <= 0 || p.n_q < 1 || p.n_q > kRows ||
       p.n_k < 1 || p.n_k > kRows)
     return cudaErrorInvalidValue;
-  return p.self ? launch_fused<true>(p, stream) : launch_fused<false>(p, stream);
+  if (p.out) {
+    const int C = p.h / 2;
+    if (C > kMaxCluster || p.d_model % C != 0) return cudaErrorInvalidValue;
+    const int n_slice = p.d_model / C;
+    if (n_slice != 64 && n_slice != 128) return cudaErrorInvalidValue;
+    return p.self ? launch_fused<true, true>(p, stream) : launch_fused<false, true>(p, stream);
+  }
+  return p.self ? launch_fused<true, false>(p, stream) : launch_fused<false, false>(p, stream);
 }
 
 TSD_DEFINE_ERROR_READER(take_device_error_fused)

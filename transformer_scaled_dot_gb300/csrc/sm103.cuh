@@ -116,12 +116,50 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// mbar_wait whose completion also acquires what other CTAs of the cluster
+// released with their signals (signal_remote).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  volatile uint32_t* abort_flag,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
+  auto try_acq = [&]() {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+  };
+  if (try_acq()) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (try_acq()) return true;
+    if ((it & 31u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        *abort_flag = 1u;
+        atomicOr(&g_device_error, kErrWaitTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ fences
 
 // Generic-proxy writes to shared memory -> visible to the async proxy
 // (tensor-core operand reads, TMA stores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy accesses to global memory with its
+// async-proxy (TMA) accesses, e.g. a TMA load of data another CTA's TMA store
+// wrote, after acquiring that CTA's signal.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -184,6 +222,23 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
+}
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+// Signal another CTA of the cluster: an asynchronous 4-byte store into its
+// shared memory (`cluster_word`, from cluster_map) whose complete_tx (4
+// bytes) lands on its mbarrier `cluster_bar`, with release semantics at
+// cluster scope. It does not wait for the round trip that a remote
+// mbarrier.arrive takes (about 0.2 us each on GB300, issued one after
+// another by a thread).
+__device__ __forceinline__ void signal_remote(uint32_t cluster_word, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];"
+               ::"r"(cluster_word), "r"(1u), "r"(cluster_bar)
+               : "memory");
 }
 // Whole-cluster barrier (every thread of every CTA of the cluster), with
 // release / acquire ordering of shared and global memory.

@@ -49,6 +49,8 @@
 // the exact phase it needs; no wait can see a barrier two phases ahead of it.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -187,7 +189,7 @@ __device__ __forceinline__ Item item_at(const AttnArgs& a, int w) {
   return it;
 }
 
-template <int D, int NQT, int NK, int NV, int QB, bool STO, int SL>
+template <int D, int NQT, int NK, int NV, int QB, bool STO, int SL, bool MS>
 __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -480,31 +482,42 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         float s[kRows];
-#pragma unroll
-        for (int cc = 0; cc < kRows / 32; ++cc) {
-          uint32_t raw[32];
-          tmem_ld32(taddr_s + cc * 32, raw);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(raw[e]);
-        }
-        tmem_wait_ld();
-
         const int bound = lim_row - j * kRows;  // keys >= bound of this tile are masked
-        if (bound < kRows) {
+        // S row -> registers (masked keys -> -inf) -> row max. With MS there
+        // are two copies, and the tiles inside every row's key limit take the
+        // one without the masking code: at d = 64 with long rows its mere
+        // presence slows the loop by several percent (measured; with the
+        // causal mask the single copy measures faster).
+        auto load_max = [&](auto masked) -> float {
 #pragma unroll
-          for (int e = 0; e < kRows; ++e)
-            if (e >= bound) s[e] = -INFINITY;
-        }
-        // row max: 8 independent chains of 3-input max
-        float mx8[8];
+          for (int cc = 0; cc < kRows / 32; ++cc) {
+            uint32_t raw[32];
+            tmem_ld32(taddr_s + cc * 32, raw);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(s[e], s[e + 8]);
+            for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(raw[e]);
+          }
+          tmem_wait_ld();
+          if constexpr (decltype(masked)::value) {
+            if (MS || bound < kRows) {
 #pragma unroll
-        for (int e0 = 16; e0 < kRows; e0 += 16)
+              for (int e = 0; e < kRows; ++e)
+                if (e >= bound) s[e] = -INFINITY;
+            }
+          }
+          // row max: 8 independent chains of 3-input max
+          float mx8[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) mx8[e] = fmax3(mx8[e], s[e0 + e], s[e0 + 8 + e]);
-        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                               fmaxf(mx8[6], mx8[7]));
+          for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(s[e], s[e + 8]);
+#pragma unroll
+          for (int e0 = 16; e0 < kRows; e0 += 16)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = fmax3(mx8[e], s[e0 + e], s[e0 + 8 + e]);
+          return fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                       fmaxf(mx8[6], mx8[7]));
+        };
+        const float mx = (MS && __all_sync(0xffffffffu, bound >= kRows))
+                             ? load_max(std::false_type{})
+                             : load_max(std::true_type{});
         // S_t is free for the next S_t only now, after the row max: the tensor
         // pipe executes MMAs in issue order, and PV_t of the previous tile,
         // issued when its P was stored, should run before the next S_t -- this
@@ -670,13 +683,13 @@ int num_sms() {
   return n;
 }
 
-template <int D, int NQT, int NK, int NV, int QB, bool STO, int SL>
+template <int D, int NQT, int NK, int NV, int QB, bool STO, int SL, bool MS = false>
 cudaError_t launch_variant(const AttnProblem& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                            const CUtensorMap& tm_v, const CUtensorMap& tm_o, cudaStream_t stream) {
   using Smem = AttnSmem<D, NQT, NK, NV, QB, STO>;
   using Shape = AttnShape<D, NQT, SL>;
   const size_t smem_bytes = SL * sizeof(Smem) + 1024;  // + alignment slack
-  auto kernel = attn_fwd_bf16_kernel<D, NQT, NK, NV, QB, STO, SL>;
+  auto kernel = attn_fwd_bf16_kernel<D, NQT, NK, NV, QB, STO, SL, MS>;
   static unsigned long long configured = 0;
   cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured);
   if (e != cudaSuccess) return e;
@@ -714,8 +727,10 @@ cudaError_t launch_attn_bf16(const AttnProblem& p, const CUtensorMap& tm_q,
   // two query tiles so each K/V tile feeds two MMAs.
   const bool pair = p.n_q > kRows;
   if (p.d == 64) {
-    return pair ? launch_variant<64, 2, 4, 4, 2, true, 1>(p, tm_q, tm_k, tm_v, tm_o, stream)
-                : launch_variant<64, 1, 2, 2, 1, true, 2>(p, tm_q, tm_k, tm_v, tm_o, stream);
+    if (!pair) return launch_variant<64, 1, 2, 2, 1, true, 2>(p, tm_q, tm_k, tm_v, tm_o, stream);
+    return (p.mask_kind & kMaskCausal)
+               ? launch_variant<64, 2, 4, 4, 2, true, 1, false>(p, tm_q, tm_k, tm_v, tm_o, stream)
+               : launch_variant<64, 2, 4, 4, 2, true, 1, true>(p, tm_q, tm_k, tm_v, tm_o, stream);
   }
   if (p.d == 128) {
     return pair ? launch_variant<128, 2, 2, 2, 1, false, 1>(p, tm_q, tm_k, tm_v, tm_o, stream)

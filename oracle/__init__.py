@@ -46,8 +46,14 @@ def _load():
             ci, cd = ctypes.c_int, ctypes.c_double
             lib.oracle_attention.argtypes = [dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, ci, ci, ip, cd, ci]
             lib.oracle_attention.restype = ci
+            lib.oracle_attention_window.argtypes = [dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, ci, ci,
+                                                    ip, ci, ci, cd, ci]
+            lib.oracle_attention_window.restype = ci
             lib.oracle_attention_rows.argtypes = [dp, ip, ci, dp, dp, ci, ci, ci, ci, ci, cd, dp, ci]
             lib.oracle_attention_rows.restype = ci
+            lib.oracle_attention_rows_window.argtypes = [dp, ip, ci, dp, dp, ci, ci, ci, ci, ci,
+                                                         ci, ci, cd, dp, ci]
+            lib.oracle_attention_rows_window.restype = ci
             lib.oracle_mha.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, ci, ci,
                                        ci, ip, cd, ci]
             lib.oracle_mha.restype = ci
@@ -82,10 +88,21 @@ def max_threads() -> int:
     return int(_load().oracle_max_threads())
 
 
+def _window(window):
+    """(left, right) of a restricted window; None or a negative side = no bound."""
+    if window is None:
+        return -1, -1
+    left, right = window
+    return (-1 if left is None or left < 0 else int(left)), \
+           (-1 if right is None or right < 0 else int(right))
+
+
 def attention(q, k, v, mask_kind: int = MASK_NONE, kv_lens=None, scale: float | None = None,
-              return_weights: bool = False, nthreads: int = 0):
+              return_weights: bool = False, nthreads: int = 0, window=None):
     """Attention(Q,K,V) for q [B,h,n_q,d_k], k [B,h,n_k,d_k], v [B,h,n_k,d_v].
 
+    window = (left, right): restricted self-attention, query i sees only keys
+    j in [i - left, i + right] (n_q == n_k); None = unrestricted.
     Returns out [B,h,n_q,d_v] (and the weight matrix [B,h,n_q,n_k] when asked).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -100,15 +117,17 @@ def attention(q, k, v, mask_kind: int = MASK_NONE, kv_lens=None, scale: float | 
         assert lens.shape == (B,)
     out = np.zeros((B, h, n_q, d_v), dtype=np.float64)
     w = np.zeros((B, h, n_q, n_k), dtype=np.float64) if return_weights else None
-    rc = _load().oracle_attention(_dp(q), _dp(k), _dp(v), _dp(out), _dp(w), B, h, n_q, n_k, d_k,
-                                  d_v, int(mask_kind), _ip(lens), float(scale), int(nthreads))
+    wl, wr = _window(window)
+    rc = _load().oracle_attention_window(_dp(q), _dp(k), _dp(v), _dp(out), _dp(w), B, h, n_q, n_k,
+                                         d_k, d_v, int(mask_kind), _ip(lens), wl, wr, float(scale),
+                                         int(nthreads))
     if rc != 0:
         raise ValueError("oracle_attention rejected its arguments")
     return (out, w) if return_weights else out
 
 
 def attention_rows(q_rows, row_pos, K, V, causal: bool, kv_len: int | None = None,
-                   scale: float | None = None, nthreads: int = 0):
+                   scale: float | None = None, nthreads: int = 0, window=None):
     """Selected query rows of one (batch, head): q_rows [R,d_k] at positions row_pos [R]."""
     q_rows, K, V = _f64(q_rows), _f64(K), _f64(V)
     R, d_k = q_rows.shape
@@ -117,9 +136,11 @@ def attention_rows(q_rows, row_pos, K, V, causal: bool, kv_len: int | None = Non
     if scale is None or scale == 0.0:
         scale = default_scale(d_k)
     out = np.zeros((R, d_v), dtype=np.float64)
-    rc = _load().oracle_attention_rows(_dp(q_rows), _ip(pos), R, _dp(K), _dp(V), n_k, d_k, d_v,
-                                       int(bool(causal)), -1 if kv_len is None else int(kv_len),
-                                       float(scale), _dp(out), int(nthreads))
+    wl, wr = _window(window)
+    rc = _load().oracle_attention_rows_window(_dp(q_rows), _ip(pos), R, _dp(K), _dp(V), n_k, d_k,
+                                              d_v, int(bool(causal)),
+                                              -1 if kv_len is None else int(kv_len), wl, wr,
+                                              float(scale), _dp(out), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_attention_rows rejected its arguments")
     return out

@@ -19,6 +19,12 @@
  *      ("Attention Is All You Need 해부", the three-uses table of attention);
  *   - the max-subtraction ("pivot") before exp, which changes nothing
  *     mathematically ("Attention Is All You Need 해부", section "직접 검증");
+ *   - restricted self-attention: query i considers only the keys around its
+ *     own position, j in [i - window_left, i + window_right] (O(r n d) work
+ *     instead of O(n^2 d); "[논문 리뷰]Attention Is All You Need"
+ *     (kimjiil.github.io), section "[4] Why Self-Attention", Table 1, row
+ *     "Self-Attention (restricted)"); a negative bound means "no limit on
+ *     that side", so (-1, -1) is eq. (1) itself;
  *   - MultiHead(Q,K,V) = Concat(head_1..head_h) W^O,
  *     head_i = Attention(Q W_i^Q, K W_i^K, V W_i^V), with the per-head matrices
  *     being column block i of one [d_model, h*d] matrix
@@ -28,7 +34,12 @@
  *   - a query row whose every key is masked (kv_len = 0) has output 0 and
  *     weights 0;
  *   - kv_len values are clamped to [0, n_k];
- *   - causal masking is defined for n_q == n_k (query i vs key i).
+ *   - causal masking is defined for n_q == n_k (query i vs key i), and so is
+ *     the restricted window (query i and key i share a position);
+ *   - Table 1 sizes the neighbourhood by r; the bounds are taken per side, so
+ *     a neighbourhood of size r centred on the query is
+ *     window_left = window_right = (r - 1) / 2 and a radius-r window is
+ *     window_left = window_right = r.
  *
  * Parity pins: every function here is checked by the CPU tests against the
  * pages' worked examples, closed forms and invariants, and against
@@ -60,6 +71,7 @@ static int clamp_len(int len, int n_k)
  */
 static void attend_row(const double *q_i, const double *K, const double *V,
                        int n_k, int d_k, int d_v, int i, int causal, int kv_len,
+                       int win_left, int win_right,
                        double scale, double *scores, double *weights, double *y_i)
 {
     int j, c;
@@ -68,7 +80,9 @@ static void attend_row(const double *q_i, const double *K, const double *V,
 
     /* logits s_j = (q_i . k_j) * scale, -inf where the connection is illegal */
     for (j = 0; j < n_k; ++j) {
-        int allowed = (j < kv_len) && !(causal && j > i);
+        int allowed = (j < kv_len) && !(causal && j > i) &&
+                      !(win_left >= 0 && j < i - win_left) &&
+                      !(win_right >= 0 && j > i + win_right);
         if (allowed) {
             double dot = 0.0;
             for (c = 0; c < d_k; ++c) dot += q_i[c] * K[(size_t)j * d_k + c];
@@ -105,22 +119,26 @@ static void attend_row(const double *q_i, const double *K, const double *V,
 }
 
 /*
- * Scaled dot-product attention for every (batch, head, query row).
+ * Scaled dot-product attention for every (batch, head, query row), optionally
+ * restricted to the keys j in [i - win_left, i + win_right] (a negative bound
+ * is no bound).
  * Layouts (row-major, contiguous): q [B,h,n_q,d_k], k [B,h,n_k,d_k],
  * v [B,h,n_k,d_v], out [B,h,n_q,d_v], weights (nullable) [B,h,n_q,n_k].
  * kv_lens: int32[B] or NULL (used only with the key-padding mask bit).
  * Returns 0 on success, -1 on invalid arguments.
  */
-int oracle_attention(const double *q, const double *k, const double *v, double *out,
-                     double *weights, int B, int h, int n_q, int n_k, int d_k, int d_v,
-                     int mask_kind, const int32_t *kv_lens, double scale, int nthreads)
+int oracle_attention_window(const double *q, const double *k, const double *v, double *out,
+                            double *weights, int B, int h, int n_q, int n_k, int d_k, int d_v,
+                            int mask_kind, const int32_t *kv_lens, int win_left, int win_right,
+                            double scale, int nthreads)
 {
     int bh;
     int causal = (mask_kind & ORACLE_MASK_CAUSAL) != 0;
     int padding = (mask_kind & ORACLE_MASK_KEY_PADDING) != 0;
+    int windowed = win_left >= 0 || win_right >= 0;
     if (B < 0 || h < 0 || n_q < 0 || n_k < 0 || d_k <= 0 || d_v <= 0) return -1;
     if (padding && !kv_lens) return -1;
-    if (causal && n_q != n_k) return -1;
+    if ((causal || windowed) && n_q != n_k) return -1;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #pragma omp parallel for schedule(dynamic)
@@ -133,7 +151,7 @@ int oracle_attention(const double *q, const double *k, const double *v, double *
         double *scores = (double *)malloc(sizeof(double) * (size_t)(n_k > 0 ? n_k : 1));
         for (i = 0; i < n_q; ++i) {
             attend_row(q + ((size_t)bh * n_q + i) * d_k, K, V, n_k, d_k, d_v, i, causal,
-                       kv_len, scale,
+                       kv_len, win_left, win_right, scale,
                        scores, weights ? weights + ((size_t)bh * n_q + i) * n_k : NULL,
                        out + ((size_t)bh * n_q + i) * d_v);
         }
@@ -142,15 +160,25 @@ int oracle_attention(const double *q, const double *k, const double *v, double *
     return 0;
 }
 
+/* eq. (1) with the optional masks and no window. */
+int oracle_attention(const double *q, const double *k, const double *v, double *out,
+                     double *weights, int B, int h, int n_q, int n_k, int d_k, int d_v,
+                     int mask_kind, const int32_t *kv_lens, double scale, int nthreads)
+{
+    return oracle_attention_window(q, k, v, out, weights, B, h, n_q, n_k, d_k, d_v, mask_kind,
+                                   kv_lens, -1, -1, scale, nthreads);
+}
+
 /*
  * Selected query rows of one (batch, head): rows q_rows [R, d_k] sit at query
  * positions row_pos[R]; K [n_k, d_k], V [n_k, d_v]; out [R, d_v].
  * kv_len < 0 means "no padding". Rows are independent, so this equals the
  * corresponding rows of oracle_attention.
  */
-int oracle_attention_rows(const double *q_rows, const int32_t *row_pos, int R,
-                          const double *K, const double *V, int n_k, int d_k, int d_v,
-                          int causal, int kv_len, double scale, double *out, int nthreads)
+int oracle_attention_rows_window(const double *q_rows, const int32_t *row_pos, int R,
+                                 const double *K, const double *V, int n_k, int d_k, int d_v,
+                                 int causal, int kv_len, int win_left, int win_right,
+                                 double scale, double *out, int nthreads)
 {
     int r;
     int len = kv_len < 0 ? n_k : clamp_len(kv_len, n_k);
@@ -166,10 +194,18 @@ int oracle_attention_rows(const double *q_rows, const int32_t *row_pos, int R,
 #endif
         for (r = 0; r < R; ++r)
             attend_row(q_rows + (size_t)r * d_k, K, V, n_k, d_k, d_v, row_pos[r], causal, len,
-                       scale, scores, NULL, out + (size_t)r * d_v);
+                       win_left, win_right, scale, scores, NULL, out + (size_t)r * d_v);
         free(scores);
     }
     return 0;
+}
+
+int oracle_attention_rows(const double *q_rows, const int32_t *row_pos, int R,
+                          const double *K, const double *V, int n_k, int d_k, int d_v,
+                          int causal, int kv_len, double scale, double *out, int nthreads)
+{
+    return oracle_attention_rows_window(q_rows, row_pos, R, K, V, n_k, d_k, d_v, causal, kv_len,
+                                        -1, -1, scale, out, nthreads);
 }
 
 /* C[M,N] = A[M,K] B[K,N], plain triple loop (row-major). */

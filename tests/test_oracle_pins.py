@@ -350,3 +350,114 @@ def test_mha_matches_torch_multi_head_attention_forward(mask, cross):
         use_separate_proj_weight=True, q_proj_weight=T(w_q.T), k_proj_weight=T(w_k.T),
         v_proj_weight=T(w_v.T))
     np.testing.assert_allclose(ours, ref.numpy().transpose(1, 0, 2), rtol=1e-11, atol=1e-11)
+
+
+# ---------------------------------------------------------------- restricted self-attention
+# "[논문 리뷰]Attention Is All You Need" (kimjiil.github.io), section "[4] Why
+# Self-Attention", Table 1: restricted self-attention considers only the r
+# positions around each query (O(r n d)). The oracle takes the window per
+# side: keys j in [i - left, i + right].
+
+def _rand_self(seed, B=2, h=2, n=11, d_k=5, d_v=3):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((B, h, n, d_k)), rng.standard_normal((B, h, n, d_k)),
+            rng.standard_normal((B, h, n, d_v)), rng)
+
+
+def test_window_of_zero_width_returns_each_query_its_own_value():
+    q, k, v, _ = _rand_self(1)
+    out = oracle.attention(q, k, v, window=(0, 0))
+    np.testing.assert_allclose(out, v, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING])
+def test_window_covering_every_key_is_unrestricted_attention(mask):
+    q, k, v, rng = _rand_self(2)
+    lens = rng.integers(1, 12, size=2).astype(np.int32)
+    full = oracle.attention(q, k, v, mask, kv_lens=lens)
+    for window in [(10, 10), (50, 50), (None, 10), (10, None)]:
+        np.testing.assert_array_equal(oracle.attention(q, k, v, mask, kv_lens=lens, window=window),
+                                      full)
+
+
+@pytest.mark.parametrize("left,right", [(0, 0), (1, 1), (2, 0), (0, 3), (3, 1), (4, 4)])
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING])
+def test_window_zero_query_gives_mean_of_window_values(left, right, mask):
+    """Q = 0 makes every allowed logit 0, so each output row is the plain mean
+    of v_j over j in [i - left, i + right] (clipped to the keys, the causal
+    limit and the key length): an off-by-one in either bound changes it."""
+    n = 13
+    _, k, v, _ = _rand_self(3, B=2, h=1, n=n)
+    q = np.zeros_like(k)
+    lens = np.array([n, 7], dtype=np.int32)
+    out = oracle.attention(q, k, v, mask, kv_lens=lens, window=(left, right))
+    for b in range(2):
+        klen = lens[b] if mask & MASK_KEY_PADDING else n
+        for i in range(n):
+            lo = max(0, i - left)
+            hi = min(i + right, klen - 1, i if mask & MASK_CAUSAL else n - 1)
+            want = v[b, 0, lo:hi + 1].mean(axis=0) if hi >= lo else np.zeros(v.shape[-1])
+            np.testing.assert_allclose(out[b, 0, i], want, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("n,r", [(16, 2), (40, 5), (9, 0), (7, 3)])
+def test_radius_window_visits_the_table_1_number_of_pairs(n, r):
+    """A radius-r window over n positions connects sum_i (min(n-1, i+r) -
+    max(0, i-r) + 1) pairs, which is (2r+1) n - r (r+1) when n > 2r: the
+    O(r n) count of Table 1. The nonzero weights of the oracle count them."""
+    q, k, v, _ = _rand_self(4, B=1, h=1, n=n)
+    _, w = oracle.attention(q, k, v, return_weights=True, window=(r, r))
+    pairs = int(np.count_nonzero(w))
+    assert pairs == sum(min(n - 1, i + r) - max(0, i - r) + 1 for i in range(n))
+    if n > 2 * r:
+        assert pairs == (2 * r + 1) * n - r * (r + 1)
+    np.testing.assert_allclose(w.sum(axis=-1), 1.0, rtol=0, atol=1e-14)
+
+
+def test_causal_window_equals_left_only_window():
+    q, k, v, _ = _rand_self(5)
+    np.testing.assert_array_equal(oracle.attention(q, k, v, MASK_CAUSAL, window=(3, 5)),
+                                  oracle.attention(q, k, v, MASK_NONE, window=(3, 0)))
+
+
+def test_window_rows_entry_matches_full_window_attention():
+    q, k, v, _ = _rand_self(6, B=1, h=1, n=21)
+    full = oracle.attention(q, k, v, window=(4, 2))
+    rows = np.array([0, 5, 20, 13], dtype=np.int32)
+    got = oracle.attention_rows(q[0, 0, rows], rows, k[0, 0], v[0, 0], causal=False,
+                                window=(4, 2))
+    np.testing.assert_array_equal(got, full[0, 0, rows])
+
+
+def test_window_needs_equal_query_and_key_lengths():
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal((1, 1, 4, 3))
+    kv = rng.standard_normal((1, 1, 5, 3))
+    with pytest.raises(ValueError):
+        oracle.attention(q, kv, kv, window=(1, 1))
+
+
+@pytest.mark.parametrize("left,right,mask", [(2, 2, MASK_NONE), (0, 4, MASK_NONE),
+                                             (3, 0, MASK_CAUSAL), (5, 1, MASK_KEY_PADDING),
+                                             (1, 6, MASK_CAUSAL | MASK_KEY_PADDING)])
+def test_window_matches_torch_fp64_sdpa_with_band_mask(left, right, mask):
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    B, h, n = 3, 2, 19
+    q, k, v, rng = _rand_self(8 + left * 7 + right, B=B, h=h, n=n, d_k=8, d_v=6)
+    lens = rng.integers(1, n + 1, size=B).astype(np.int32)
+    i = torch.arange(n)[:, None]
+    j = torch.arange(n)[None, :]
+    allowed = ((j >= i - left) & (j <= i + right))[None, None].expand(B, 1, n, n).clone()
+    if mask & MASK_CAUSAL:
+        allowed &= (j <= i)[None, None]
+    if mask & MASK_KEY_PADDING:
+        allowed &= (torch.arange(n)[None, :] < torch.as_tensor(lens)[:, None])[:, None, None, :]
+    ref = F.scaled_dot_product_attention(torch.from_numpy(q), torch.from_numpy(k),
+                                         torch.from_numpy(v), attn_mask=allowed).numpy()
+    ours = oracle.attention(q, k, v, mask, kv_lens=lens, window=(left, right))
+    live = allowed.any(dim=-1).numpy()[:, 0]          # rows with at least one key
+    np.testing.assert_allclose(ours[np.broadcast_to(live[:, None], ours.shape[:3])],
+                               ref[np.broadcast_to(live[:, None], ref.shape[:3])],
+                               rtol=1e-12, atol=1e-12)
+    assert np.all(ours[np.broadcast_to(~live[:, None], ours.shape[:3])] == 0.0)

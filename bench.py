@@ -70,12 +70,29 @@ WORKLOADS = {
                             desc="Transformer-big causal self-attention: B=8, h=16, n=1024, d=64"),
     "long": dict(kind="attn", B=4, h=16, n=4096, d=64, causal=False, seed=1004,
                  desc="long-context attention sweep point"),
+    "window": dict(kind="attn", B=4, h=16, n=16384, d=64, causal=False, window=(256, 256),
+                   seed=1005,
+                   desc="restricted self-attention (Table 1, restricted row): B=4, h=16, n=16384, "
+                        "d=64, each query sees the keys within 256 positions of it; TFLOP/s "
+                        "counted over the allowed (query, key) pairs"),
 }
 
 
 def attn_flops(B, h, n_q, n_k, d, causal):
     f = 4.0 * B * h * n_q * n_k * d
     return f / 2 if causal else f
+
+
+def window_pairs(n, left, right, causal):
+    """(query, key) pairs of a restricted window over n positions: query i
+    sees keys [i - left, i + right] (a negative bound is none), and only j <= i
+    when causal."""
+    i = np.arange(n, dtype=np.int64)
+    lo = np.maximum(0, i - left) if left >= 0 else np.zeros_like(i)
+    hi = np.minimum(n - 1, i + right) if right >= 0 else np.full_like(i, n - 1)
+    if causal:
+        hi = np.minimum(hi, i)
+    return int(np.maximum(hi - lo + 1, 0).sum())
 
 
 # --------------------------------------------------------------------------- helpers
@@ -441,12 +458,18 @@ class AttnCall:
         self.h_qkv = [torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory()
                       for x in (a.q, a.k, a.v)]
         self.h_out = torch.empty(a.q.shape, dtype=torch.bfloat16).pin_memory()
+        self.window = cfg.get("window")
 
     def bytes_per_set(self):
         return 4 * self.a.q.nbytes
 
     def run(self, i, stream):
         a, s = self.a, self.sets[i % len(self.sets)]
+        if self.window is not None:
+            self.tsd.attn_forward_window(s["q"], s["k"], s["v"], s["out"], a.B, a.h, a.n_q, a.n_k,
+                                         a.d_k, a.d_v, self.window[0], self.window[1],
+                                         a.mask_kind, None, 0.0, stream)
+            return
         self.tsd.attn_forward(s["q"], s["k"], s["v"], s["out"], a.B, a.h, a.n_q, a.n_k, a.d_k,
                               a.d_v, a.mask_kind, None, 0.0, stream)
 
@@ -458,7 +481,11 @@ class AttnCall:
 
     def stage_work(self):
         a = self.a
-        f = attn_flops(a.B, a.h, a.n_q, a.n_k, a.d_k, bool(a.mask_kind & MASK_CAUSAL))
+        causal = bool(a.mask_kind & MASK_CAUSAL)
+        if self.window is not None:  # useful FLOPs: the allowed pairs only
+            f = 4.0 * a.B * a.h * a.d_k * window_pairs(a.n_q, *self.window, causal)
+        else:
+            f = attn_flops(a.B, a.h, a.n_q, a.n_k, a.d_k, causal)
         b = 2.0 * a.B * a.h * (a.n_q * a.d_k + a.n_k * (a.d_k + a.d_v) + a.n_q * a.d_v)
         return [(f, b)]
 
@@ -514,6 +541,8 @@ def workload_config(wl, calls, args, nsets, per_set):
     else:
         a = calls[0].a
         cfg.update(B=a.B, h=a.h, n=a.n_q, d=a.d_k, causal=bool(a.mask_kind & MASK_CAUSAL))
+        if calls[0].window is not None:
+            cfg["window"] = {"left": calls[0].window[0], "right": calls[0].window[1]}
     cfg["l2"] = f"{nsets} rotating input sets of {per_set / 2**20:.1f} MiB (total > L2)"
     return cfg
 
@@ -695,17 +724,25 @@ def oracle_sample_runner(args):
     if args.causal is not None:
         cfg["causal"] = bool(args.causal)
     n, d, causal = cfg["n"], cfg["d"], cfg["causal"]
+    window = cfg.get("window")
     rng = np.random.default_rng(cfg["seed"])
     # one head of the workload, a seeded subset of its query rows
     q = synthetic.bf16_bits_to_f64(synthetic.normal_bf16(rng, (n, d)))
     k = synthetic.bf16_bits_to_f64(synthetic.normal_bf16(rng, (n, d)))
     v = synthetic.bf16_bits_to_f64(synthetic.normal_bf16(rng, (n, d)))
     rows = np.sort(rng.choice(n, size=min(n, 256), replace=False)).astype(np.int32)
-    keys_seen = (rows + 1).sum() if causal else len(rows) * n
+    if window is not None:  # keys each sampled row is allowed to see
+        lo = np.maximum(0, rows - window[0]) if window[0] >= 0 else np.zeros_like(rows)
+        hi = np.minimum(n - 1, rows + window[1]) if window[1] >= 0 else np.full_like(rows, n - 1)
+        if causal:
+            hi = np.minimum(hi, rows)
+        keys_seen = int(np.maximum(hi - lo + 1, 0).sum())
+    else:
+        keys_seen = (rows + 1).sum() if causal else len(rows) * n
     flops = 4.0 * keys_seen * d
 
     def run():
-        oracle.attention_rows(q[rows], rows, k, v, causal=causal)
+        oracle.attention_rows(q[rows], rows, k, v, causal=causal, window=window)
     return run, flops, f"{len(rows)} query rows of one head (n={n}, d={d}) via oracle.attention_rows"
 
 

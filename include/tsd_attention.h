@@ -82,6 +82,29 @@ attn_status attn_forward(const void *q, const void *k, const void *v, void *out,
                          tsd_stream_t stream);
 
 /*
+ * attn_forward_window -- restricted self-attention: query i considers only
+ * the keys j with i - window_left <= j <= i + window_right ("[논문 리뷰]
+ * Attention Is All You Need" (kimjiil.github.io), section "[4] Why
+ * Self-Attention", Table 1, row "Self-Attention (restricted)": O(r n d) work
+ * for a neighbourhood of r positions instead of O(n^2 d)). Table 1 sizes the
+ * neighbourhood by r only; the bounds here are per side, so a neighbourhood
+ * of size r centred on the query is window_left = window_right = (r - 1) / 2
+ * and a radius-r window is window_left = window_right = r.
+ *   Arguments, layouts, masks and errors as attn_forward, plus:
+ *   window_left, window_right: >= 0, or -1 for no bound on that side
+ *   (-1, -1 is attn_forward); < -1 -> ATTN_ERR_INVALID. A window needs
+ *   n_q == n_k (query i and key i share a position), else ATTN_ERR_INVALID.
+ *   The causal bit and key padding combine with the window; a row left with
+ *   no key gets output 0. Key tiles outside every row's window are never
+ *   loaded.
+ */
+attn_status attn_forward_window(const void *q, const void *k, const void *v, void *out,
+                                int B, int h, int n_q, int n_k, int d_k, int d_v,
+                                int mask_kind, const int32_t *kv_lens,
+                                int window_left, int window_right,
+                                float scale, tsd_stream_t stream);
+
+/*
  * attn_forward_strided -- the same operation as attn_forward on tensors whose
  * (batch, head, row) strides are given in ELEMENTS (the head dimension stays
  * contiguous). This lets a caller read heads straight out of a [B, n, h*d]

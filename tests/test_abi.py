@@ -148,3 +148,24 @@ def test_mha_concat_heads_rejects_bad_arguments(lib):
 def test_selftest_rejects_bad_limit(lib):
     assert lib.attn_selftest_wait_timeout(0, None) == tsd.ATTN_ERR_INVALID
     assert lib.attn_selftest_wait_timeout(3000000, None) == tsd.ATTN_ERR_INVALID
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (n_q, n_k, window_left, window_right, mask)
+    ((16, 16, -2, 3, 0), tsd.ATTN_ERR_INVALID),   # a bound below -1
+    ((16, 16, 3, -5, 0), tsd.ATTN_ERR_INVALID),
+    ((16, 20, 2, 2, 0), tsd.ATTN_ERR_INVALID),    # a window needs n_q == n_k
+    ((16, 20, 0, -1, 0), tsd.ATTN_ERR_INVALID),
+    ((16, 16, 2, 2, 4), tsd.ATTN_ERR_INVALID),    # unknown mask bit
+    ((16, 16, 2, 2, 2), tsd.ATTN_ERR_INVALID),    # padding without lengths
+])
+def test_attn_forward_window_rejects_bad_arguments(lib, args, expect):
+    n_q, n_k, wl, wr, mask = args
+    st = lib.attn_forward_window(FAKE, FAKE, FAKE, FAKE, 1, 1, n_q, n_k, 64, 64, mask, None, wl, wr,
+                                 0.0, None)
+    assert st == expect
+
+
+def test_attn_forward_window_empty_problem_is_a_no_op(lib):
+    assert lib.attn_forward_window(FAKE, FAKE, FAKE, FAKE, 0, 1, 16, 16, 64, 64, 0, None, 3, 3,
+                                   0.0, None) == tsd.ATTN_OK

@@ -197,3 +197,57 @@ def test_bounded_wait_reports_timeout_and_context_survives(tsd):
     assert_bf16_close(run_bf16(tsd, a), ref, "after timeout")
     x = torch.ones(4, device="cuda")
     assert float(x.sum()) == 4.0
+
+
+# ---------------------------------------------------------------- restricted self-attention
+
+def run_window(tsd, a, left, right):
+    import torch
+    q, k, v = (to_dev_bf16(t) for t in (a.q, a.k, a.v))
+    out = torch.full((a.B, a.h, a.n_q, a.d_v), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lens = to_dev_i32(a.kv_lens) if a.kv_lens is not None else None
+    tsd.attn_forward_window(q, k, v, out, a.B, a.h, a.n_q, a.n_k, a.d_k, a.d_v, left, right,
+                            a.mask_kind, lens)
+    torch.cuda.synchronize()
+    assert tsd.attn_get_device_status() == tsd.ATTN_OK
+    return to_host_f64(out)
+
+
+WINDOW_CASES = [
+    # B, h, n, d, mask, kv_len_range, left, right
+    (2, 2, 100, 64, MASK_NONE, None, 0, 0),            # each query only its own key
+    (2, 2, 100, 64, MASK_NONE, None, 7, 3),            # one query tile per item
+    (1, 2, 1000, 64, MASK_NONE, None, 128, 128),       # tile-aligned radius, paired tiles
+    (1, 2, 1000, 64, MASK_NONE, None, 200, 57),        # ragged bounds on both sides
+    (2, 2, 777, 64, MASK_CAUSAL, None, 300, -1),       # causal sliding window
+    (2, 2, 777, 64, MASK_KEY_PADDING, (1, 777), 90, 250),
+    (1, 2, 1500, 64, MASK_CAUSAL | MASK_KEY_PADDING, (400, 1500), 129, 0),
+    (1, 2, 600, 64, MASK_NONE, None, -1, 100),         # bound on one side only
+    (1, 2, 600, 64, MASK_NONE, None, 5000, 5000),      # window wider than the sequence
+    (2, 2, 300, 128, MASK_NONE, None, 40, 40),
+    (1, 2, 1000, 128, MASK_CAUSAL, None, 256, -1),
+    (40, 8, 128, 64, MASK_KEY_PADDING, (1, 128), 16, 16),
+]
+
+
+@pytest.mark.parametrize("case", WINDOW_CASES,
+                         ids=lambda c: "B{}h{}n{}d{}m{}w{}_{}".format(*c[:5], c[6], c[7]))
+def test_attn_forward_window_matches_oracle(tsd, case):
+    B, h, n, d, mask, rng, left, right = case
+    a = synthetic.attention_inputs(2500 + B + n + d + max(left, 0), B, h, n, n, d, d, mask, rng)
+    got = run_window(tsd, a, left, right)
+    ref = oracle.attention(*a.as_f64(), mask, kv_lens=a.kv_lens, window=(left, right))
+    assert_bf16_close(got, ref, str(case))
+
+
+def test_attn_forward_window_unbounded_equals_attn_forward(tsd):
+    a = synthetic.attention_inputs(2600, 2, 2, 700, 700, 64, 64, MASK_CAUSAL)
+    np.testing.assert_array_equal(run_window(tsd, a, -1, -1), run_bf16(tsd, a))
+
+
+def test_attn_forward_window_zero_width_returns_values(tsd):
+    """A (0, 0) window leaves each query its own key: output = v_i rounded to
+    bf16 (one weight of exactly 1)."""
+    a = synthetic.attention_inputs(2601, 1, 2, 300, 300, 64, 64, MASK_NONE)
+    got = run_window(tsd, a, 0, 0)
+    np.testing.assert_array_equal(got, a.as_f64()[2])

@@ -23,7 +23,8 @@ __all__ = [
     "attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_workspace_bytes",
     "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
     "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out", "mha_forward_noalloc",
-    "mha_concat_heads", "mha_forward_launches", "MHA_NOALLOC_SCRATCH_BYTES",
+    "mha_concat_heads", "mha_forward_launches", "attn_forward_window",
+    "MHA_NOALLOC_SCRATCH_BYTES",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = range(5)
@@ -33,7 +34,7 @@ EXPORTED_SYMBOLS = (
     "attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_workspace_bytes",
     "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
     "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out", "mha_forward_noalloc",
-    "mha_concat_heads", "mha_forward_launches",
+    "mha_concat_heads", "mha_forward_launches", "attn_forward_window",
 )
 
 # TSD_MHA_NOALLOC_SCRATCH_BYTES of the header: the fixed scratch of mha_forward_noalloc
@@ -87,10 +88,11 @@ def library():
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_selftest_wait_timeout.argtypes = [i, st]
     lib.mha_forward_launches.argtypes = [i, i, i, i, i, i, i, i]
+    lib.attn_forward_window.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, i, i, f, st]
     for name in ("attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_forward",
                  "attn_get_device_status", "attn_last_cuda_error", "attn_selftest_wait_timeout",
                  "mha_project_qkv", "mha_project_out", "mha_forward_noalloc", "mha_concat_heads",
-                 "mha_forward_launches"):
+                 "mha_forward_launches", "attn_forward_window"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -122,6 +124,16 @@ def attn_forward(q, k, v, out, B, h, n_q, n_k, d_k, d_v, mask_kind=ATTN_MASK_NON
                  scale=0.0, stream=None):
     _check(library().attn_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, h, n_q, n_k, d_k, d_v,
                                   mask_kind, _ptr(kv_lens), scale, _stream(stream)), "attn_forward")
+
+
+def attn_forward_window(q, k, v, out, B, h, n_q, n_k, d_k, d_v, window_left, window_right,
+                        mask_kind=ATTN_MASK_NONE, kv_lens=None, scale=0.0, stream=None):
+    """Restricted self-attention: query i sees keys [i - window_left, i + window_right]
+    (-1 = no bound on that side)."""
+    _check(library().attn_forward_window(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, h, n_q, n_k,
+                                         d_k, d_v, mask_kind, _ptr(kv_lens), window_left,
+                                         window_right, scale, _stream(stream)),
+           "attn_forward_window")
 
 
 def attn_forward_strided(q, q_sb, q_sh, q_sr, k, k_sb, k_sh, k_sr, v, v_sb, v_sh, v_sr,

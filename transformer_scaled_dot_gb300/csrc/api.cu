@@ -168,7 +168,8 @@ attn_status run_attn_bf16(const void* q, int64_t q_sb, int64_t q_sh, int64_t q_s
                           int64_t k_sb, int64_t k_sh, int64_t k_sr, const void* v, int64_t v_sb,
                           int64_t v_sh, int64_t v_sr, void* out, int64_t o_sb, int64_t o_sh,
                           int64_t o_sr, int B, int h, int n_q, int n_k, int d, int mask_kind,
-                          const int32_t* kv_lens, float scale, cudaStream_t stream) {
+                          const int32_t* kv_lens, float scale, cudaStream_t stream,
+                          int win_left = -1, int win_right = -1) {
   CUtensorMap tm_q, tm_k, tm_v, tm_o;
   cudaError_t e = encode_head_map(&tm_q, q, d, n_q, h, B, q_sr, q_sh, q_sb);
   if (e == cudaSuccess) e = encode_head_map(&tm_k, k, d, n_k, h, B, k_sr, k_sh, k_sb);
@@ -188,6 +189,8 @@ attn_status run_attn_bf16(const void* q, int64_t q_sb, int64_t q_sh, int64_t q_s
   p.o_sb = o_sb;
   p.o_sh = o_sh;
   p.o_sr = o_sr;
+  p.win_left = win_left;
+  p.win_right = win_right;
   e = tsd::launch_attn_bf16(p, tm_q, tm_k, tm_v, tm_o, stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -408,6 +411,28 @@ attn_status attn_forward(const void* q, const void* k, const void* v, void* out,
                        int64_t(n_k) * d, d, v, int64_t(h) * n_k * d, int64_t(n_k) * d, d, out,
                        int64_t(h) * n_q * d, int64_t(n_q) * d, d, B, h, n_q, n_k, d_k, mask_kind,
                        kv_lens, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_forward_window(const void* q, const void* k, const void* v, void* out, int B,
+                                int h, int n_q, int n_k, int d_k, int d_v, int mask_kind,
+                                const int32_t* kv_lens, int window_left, int window_right,
+                                float scale, tsd_stream_t stream) {
+  attn_status s = check_common(B, h, n_q, n_k, d_k, d_v, mask_kind, kv_lens, scale);
+  if (s != ATTN_OK) return s;
+  if (window_left < -1 || window_right < -1) return ATTN_ERR_INVALID;
+  const bool windowed = window_left >= 0 || window_right >= 0;
+  if (windowed && n_q != n_k) return ATTN_ERR_INVALID;
+  if (!q || !k || !v || !out) return ATTN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_INVALID;
+  s = check_bf16_head_dims(d_k, d_v);
+  if (s != ATTN_OK) return s;
+  if (B == 0 || h == 0 || n_q == 0) return ATTN_OK;  // nothing to write
+  const int64_t d = d_k;
+  return run_attn_bf16(q, int64_t(h) * n_q * d, int64_t(n_q) * d, d, k, int64_t(h) * n_k * d,
+                       int64_t(n_k) * d, d, v, int64_t(h) * n_k * d, int64_t(n_k) * d, d, out,
+                       int64_t(h) * n_q * d, int64_t(n_q) * d, d, B, h, n_q, n_k, d_k, mask_kind,
+                       kv_lens, scale, reinterpret_cast<cudaStream_t>(stream), window_left,
+                       window_right);
 }
 
 attn_status attn_forward_strided(const void* q, int64_t q_sb, int64_t q_sh, int64_t q_sr,

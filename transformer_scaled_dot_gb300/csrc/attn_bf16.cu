@@ -125,6 +125,7 @@ struct AttnArgs {
   float scale_log2;
   uint16_t* out;
   int64_t o_sb, o_sh, o_sr;
+  int win_left, win_right;  // restricted window (WIN): keys [i - left, i + right]; < 0: no bound
 };
 
 constexpr unsigned long long kDrainLimitNs = 100ull * 1000ull * 1000ull;  // 0.1 s
@@ -132,18 +133,32 @@ constexpr unsigned long long kDrainLimitNs = 100ull * 1000ull * 1000ull;  // 0.1
 // One work item: a block of NQT query tiles of one (batch, head).
 struct Item {
   int b, hh, q0, kv_eff;
-  int nt0, nt1;  // key tiles visited by query tile 0 / 1
+  int nt0, nt1;  // query tile 0 / 1 visits key tiles [lo, nt)
+  int lo0, lo1;  // 0 unless a restricted window cuts the keys before the query
+  int lo_spec;   // first key tile through the rings (known before the key length)
   int min_load;  // 1 if the key set is not empty by its shape (n_k > 0)
   __device__ int nt(int t) const { return t == 0 ? nt0 : nt1; }
+  __device__ int lo(int t) const { return t == 0 ? lo0 : lo1; }
   __device__ int nt_all() const { return nt0 > nt1 ? nt0 : nt1; }
-  // K/V tiles that pass through the rings: at least one when n_k > 0, so
-  // that the first key tile can be loaded before the key length is known
-  // (an item whose key length is 0 releases it unused)
-  __device__ int n_load() const { return nt_all() > min_load ? nt_all() : min_load; }
+  // K/V tiles that pass through the rings, from lo_spec: at least one when
+  // n_k > 0, so that the first key tile can be loaded before the key length
+  // is known (an item whose key set turns out empty releases it unused)
+  __device__ int n_load() const {
+    const int n = nt_all() - lo_spec;
+    return n > min_load ? n : min_load;
+  }
 };
 
+// First key tile of a query tile whose first row is row0 (restricted window).
+template <bool WIN>
+__device__ __forceinline__ int window_lo_tile(const AttnArgs& a, int row0) {
+  if (!WIN || a.win_left < 0) return 0;
+  const int k0 = row0 - a.win_left;
+  return k0 > 0 ? k0 / kRows : 0;
+}
+
 // Batch, head and first query row of item w (no memory access).
-template <int NQT>
+template <int NQT, bool WIN>
 __device__ __forceinline__ Item item_coords(const AttnArgs& a, int w) {
   const bool causal = (a.mask_kind & kMaskCausal) != 0;
   const int bh_count = a.B * a.h;
@@ -161,15 +176,18 @@ __device__ __forceinline__ Item item_coords(const AttnArgs& a, int w) {
   it.q0 = qblk * NQT * kRows;
   it.kv_eff = 0;
   it.nt0 = it.nt1 = 0;
+  it.lo_spec = window_lo_tile<WIN>(a, it.q0);
+  it.lo0 = it.lo_spec;
+  it.lo1 = NQT > 1 ? window_lo_tile<WIN>(a, it.q0 + kRows) : it.lo_spec;
   it.min_load = a.n_k > 0 ? 1 : 0;
   return it;
 }
 
 // The key range of an item (reads the key length).
-template <int NQT>
+template <int NQT, bool WIN>
 __device__ __forceinline__ Item item_at(const AttnArgs& a, int w) {
   const bool causal = (a.mask_kind & kMaskCausal) != 0;
-  Item it = item_coords<NQT>(a, w);
+  Item it = item_coords<NQT, WIN>(a, w);
   int kv_eff = a.n_k;
   if (a.mask_kind & kMaskKeyPadding) {
     const int len = a.kv_lens[it.b];
@@ -181,6 +199,7 @@ __device__ __forceinline__ Item item_at(const AttnArgs& a, int w) {
     const int row0 = it.q0 + t * kRows;
     int n = nkt;
     if (causal) n = min(n, row0 / kRows + 1);
+    if (WIN && a.win_right >= 0) n = min(n, (row0 + kRows + a.win_right + kRows - 1) / kRows);
     if (row0 >= a.n_q) n = 0;
     return n;
   };
@@ -189,7 +208,7 @@ __device__ __forceinline__ Item item_at(const AttnArgs& a, int w) {
   return it;
 }
 
-template <int D, int NQT, int NK, int NV, int QB, bool STO, int SL, bool MS>
+template <int D, int NQT, int NK, int NV, int QB, bool STO, int SL, bool MS, bool WIN>
 __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -304,7 +323,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
         for (int i = 0, w = item_index(0); ok && w < args.num_items; w = item_index(++i)) {
           // Q and the first key tile do not depend on the key length: both
           // are on their way before it is read
-          const Item at = item_coords<NQT>(args, w);
+          const Item at = item_coords<NQT, WIN>(args, w);
           const int qs = qn % QB;
           ok = mbar_wait(&sm.q_empty[qs], (static_cast<uint32_t>(qn / QB) & 1u) ^ 1u, abort_flag);
           if (!ok) break;
@@ -315,12 +334,12 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
               tma_load_4d(sm.q[qs][t] + a * 16384, &tm_q, &sm.q_full[qs], a * 64,
                           at.q0 + t * kRows, at.hh, at.b);
           ++qn;
-          if (at.min_load > 0) ok = load_k(at, 0);
-          const int n_load = item_at<NQT>(args, w).n_load();
+          if (at.min_load > 0) ok = load_k(at, at.lo_spec);
+          const int n_load = item_at<NQT, WIN>(args, w).n_load();
           // keys run one tile ahead of values, the order the MMAs consume them
-          for (int j = 0; ok && j < n_load; ++j) {
-            if (j + 1 < n_load) ok = load_k(at, j + 1);
-            if (ok) ok = load_v(at, j);
+          for (int jj = 0; ok && jj < n_load; ++jj) {
+            if (jj + 1 < n_load) ok = load_k(at, at.lo_spec + jj + 1);
+            if (ok) ok = load_v(at, at.lo_spec + jj);
           }
         }
         if (!ok) {
@@ -347,13 +366,14 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
         bool ok = true;
         griddep_wait();  // the key lengths may come from the previous kernel
         for (int i = 0, w = item_index(0); ok && w < args.num_items; w = item_index(++i)) {
-          const Item it = item_at<NQT>(args, w);
+          const Item it = item_at<NQT, WIN>(args, w);
           const int n_load = it.n_load();
           const int qs = qc % QB;
           ok = mbar_wait(&sm.q_full[qs], static_cast<uint32_t>(qc / QB) & 1u, abort_flag);
           if (!ok) break;
           bool item_issued = false;
-          for (int j = 0; ok && j < n_load; ++j) {
+          for (int jj = 0; ok && jj < n_load; ++jj) {
+            const int j = it.lo_spec + jj;  // key tile
             const int rs = kc % NK;
             // the ring slot holds K_j before this warp releases it, so a release
             // for tiles this issuer skips never counts toward an older use
@@ -362,7 +382,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
             const uint64_t bk = sdesc_advance(dk0, static_cast<uint32_t>(rs) * kTileStep);
             bool issued = false;
             for (int t = t_lo; ok && t < t_hi; ++t) {
-              if (j >= it.nt(t)) continue;
+              if (j >= it.nt(t) || j < it.lo(t)) continue;
               int& sc = t == 0 ? sc0 : sc1;
               if (sc > 0) {
                 // the previous S_t has been read (or, when P overwrites S,
@@ -416,9 +436,10 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
         bool ok = true;
         griddep_wait();
         for (int i = 0, w = item_index(0); ok && w < args.num_items; w = item_index(++i)) {
-          const Item it = item_at<NQT>(args, w);
+          const Item it = item_at<NQT, WIN>(args, w);
           const int n_load = it.n_load();
-          for (int j = 0; ok && j < n_load; ++j) {
+          for (int jj = 0; ok && jj < n_load; ++jj) {
+            const int j = it.lo_spec + jj;  // key tile
             const int rs = vc % NV;
             // as for K: the ring slot holds V_j before any release by this warp
             ok = mbar_wait(&sm.v_full[rs], static_cast<uint32_t>(vc / NV) & 1u, abort_flag);
@@ -426,7 +447,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
             const uint64_t bv = sdesc_advance(dv0, static_cast<uint32_t>(rs) * kTileStep);
             bool issued = false;
             for (int t = t_lo; ok && t < t_hi; ++t) {
-              if (j >= it.nt(t)) continue;
+              if (j >= it.nt(t) || j < it.lo(t)) continue;
               int& pc = t == 0 ? pc0 : pc1;
               ok = mbar_wait(&sm.p_full[t], static_cast<uint32_t>(pc) & 1u, abort_flag);
               if (!ok) break;
@@ -437,7 +458,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
 #pragma unroll
               for (int kk = 0; kk < kRows / 16; ++kk)
                 mma_bf16_ts(d_tmem, p_tmem + kk * 8, sdesc_advance(bv, kk * (2048 >> 4)), kIdescPV,
-                            (j > 0 || kk > 0) ? 1u : 0u);
+                            (j > it.lo(t) || kk > 0) ? 1u : 0u);
               mma_commit(&sm.pv_done[t]);
               ++pc;
               issued = true;
@@ -470,19 +491,28 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
     bool ok = true;
     griddep_wait();
     for (int i = 0, w = item_index(0); ok && w < args.num_items; w = item_index(++i)) {
-      const Item it = item_at<NQT>(args, w);
+      const Item it = item_at<NQT, WIN>(args, w);
       const int ntt = it.nt(t);
+      const int lot = it.lo(t);                // key tiles [lot, ntt) of this query tile
+      const bool has_tiles = ntt > lot;
       const int row = it.q0 + t * kRows + r;  // query index
-      const int lim_row = causal ? min(it.kv_eff, row + 1) : it.kv_eff;  // keys [0, lim_row)
+      // keys [low_row, lim_row) of this row
+      int lim_row = causal ? min(it.kv_eff, row + 1) : it.kv_eff;
+      int low_row = 0;
+      if constexpr (WIN) {
+        if (args.win_right >= 0) lim_row = min(lim_row, row + args.win_right + 1);
+        if (args.win_left >= 0) low_row = max(0, row - args.win_left);
+      }
       float m_used = -INFINITY;
       float l = 0.f;
-      for (int j = 0; j < ntt; ++j, ++c) {
+      for (int j = lot; j < ntt; ++j, ++c) {
         ok = __all_sync(0xffffffffu,
                         mbar_wait(&sm.s_full[t], static_cast<uint32_t>(c) & 1u, abort_flag));
         if (!ok) break;
         tc_fence_after();
         float s[kRows];
-        const int bound = lim_row - j * kRows;  // keys >= bound of this tile are masked
+        const int bound = lim_row - j * kRows;   // keys >= bound of this tile are masked
+        const int lbound = low_row - j * kRows;  // and (WIN) keys < lbound
         // S row -> registers (masked keys -> -inf) -> row max. With MS there
         // are two copies, and the tiles inside every row's key limit take the
         // one without the masking code: at d = 64 with long rows its mere
@@ -498,10 +528,10 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
           }
           tmem_wait_ld();
           if constexpr (decltype(masked)::value) {
-            if (MS || bound < kRows) {
+            if (MS || bound < kRows || (WIN && lbound > 0)) {
 #pragma unroll
               for (int e = 0; e < kRows; ++e)
-                if (e >= bound) s[e] = -INFINITY;
+                if (e >= bound || (WIN && e < lbound)) s[e] = -INFINITY;
             }
           }
           // row max: 8 independent chains of 3-input max
@@ -515,7 +545,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
           return fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                        fmaxf(mx8[6], mx8[7]));
         };
-        const float mx = (MS && __all_sync(0xffffffffu, bound >= kRows))
+        const float mx = (MS && __all_sync(0xffffffffu, bound >= kRows && (!WIN || lbound <= 0)))
                              ? load_max(std::false_type{})
                              : load_max(std::true_type{});
         // S_t is free for the next S_t only now, after the row max: the tensor
@@ -550,7 +580,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
         f2_unpack(fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3])), r0, r1);
         const float rowsum = r0 + r1;
 
-        if (j > 0) {
+        if (j > lot) {
           // PV of the previous tile has finished: O is stable, P is free
           ok = __all_sync(0xffffffffu, mbar_wait(&sm.pv_done[t], static_cast<uint32_t>(c - 1) & 1u,
                                                  abort_flag));
@@ -588,7 +618,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
       if (!STO && !ok) break;
 
       // -------------------------------------------------------- epilogue
-      if (ok && ntt > 0) {
+      if (ok && has_tiles) {
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.pv_done[t], static_cast<uint32_t>(c - 1) & 1u,
                                                abort_flag));
       }
@@ -605,7 +635,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
         }
       }
       if (!ok) break;
-      if (ntt > 0) tc_fence_after();
+      if (has_tiles) tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       uint16_t* dst = args.out + static_cast<int64_t>(it.b) * args.o_sb +
                       static_cast<int64_t>(it.hh) * args.o_sh + static_cast<int64_t>(row) * args.o_sr;
@@ -613,7 +643,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
-        if (ntt > 0) {
+        if (has_tiles) {
           tmem_ld32(taddr_o + cc * 32, o);
           tmem_wait_ld();
         } else {
@@ -683,13 +713,14 @@ int num_sms() {
   return n;
 }
 
-template <int D, int NQT, int NK, int NV, int QB, bool STO, int SL, bool MS = false>
+template <int D, int NQT, int NK, int NV, int QB, bool STO, int SL, bool MS = false,
+          bool WIN = false>
 cudaError_t launch_variant(const AttnProblem& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                            const CUtensorMap& tm_v, const CUtensorMap& tm_o, cudaStream_t stream) {
   using Smem = AttnSmem<D, NQT, NK, NV, QB, STO>;
   using Shape = AttnShape<D, NQT, SL>;
   const size_t smem_bytes = SL * sizeof(Smem) + 1024;  // + alignment slack
-  auto kernel = attn_fwd_bf16_kernel<D, NQT, NK, NV, QB, STO, SL, MS>;
+  auto kernel = attn_fwd_bf16_kernel<D, NQT, NK, NV, QB, STO, SL, MS, WIN>;
   static unsigned long long configured = 0;
   cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured);
   if (e != cudaSuccess) return e;
@@ -710,6 +741,8 @@ cudaError_t launch_variant(const AttnProblem& p, const CUtensorMap& tm_q, const 
   a.o_sb = p.o_sb;
   a.o_sh = p.o_sh;
   a.o_sr = p.o_sr;
+  a.win_left = WIN ? p.win_left : -1;
+  a.win_right = WIN ? p.win_right : -1;
   // one CTA per SM (tensor-memory kernels are not co-resident); slot 1 of
   // each CTA takes the items beyond the first grid-full
   const int grid = static_cast<int>(items < num_sms() ? items : num_sms());
@@ -726,9 +759,31 @@ cudaError_t launch_attn_bf16(const AttnProblem& p, const CUtensorMap& tm_q,
   // pipelines per CTA, each with one Q buffer so both fit); longer ones pair
   // two query tiles so each K/V tile feeds two MMAs.
   const bool pair = p.n_q > kRows;
+  const bool causal = (p.mask_kind & kMaskCausal) != 0;
+  // restricted windows run separate instances: the unrestricted loops carry
+  // no window code
+  if (p.win_left >= 0 || p.win_right >= 0) {
+    if (p.n_q != p.n_k) return cudaErrorInvalidValue;
+    if (p.d == 64) {
+      if (!pair)
+        return launch_variant<64, 1, 2, 2, 1, true, 2, false, true>(p, tm_q, tm_k, tm_v, tm_o,
+                                                                     stream);
+      return causal ? launch_variant<64, 2, 4, 4, 2, true, 1, false, true>(p, tm_q, tm_k, tm_v,
+                                                                          tm_o, stream)
+                    : launch_variant<64, 2, 4, 4, 2, true, 1, true, true>(p, tm_q, tm_k, tm_v,
+                                                                         tm_o, stream);
+    }
+    if (p.d == 128) {
+      return pair ? launch_variant<128, 2, 2, 2, 1, false, 1, false, true>(p, tm_q, tm_k, tm_v,
+                                                                          tm_o, stream)
+                  : launch_variant<128, 1, 2, 2, 2, true, 1, false, true>(p, tm_q, tm_k, tm_v,
+                                                                         tm_o, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (p.d == 64) {
     if (!pair) return launch_variant<64, 1, 2, 2, 1, true, 2>(p, tm_q, tm_k, tm_v, tm_o, stream);
-    return (p.mask_kind & kMaskCausal)
+    return causal
                ? launch_variant<64, 2, 4, 4, 2, true, 1, false>(p, tm_q, tm_k, tm_v, tm_o, stream)
                : launch_variant<64, 2, 4, 4, 2, true, 1, true>(p, tm_q, tm_k, tm_v, tm_o, stream);
   }

@@ -21,6 +21,9 @@ struct AttnProblem {
   float scale;             // logit factor (already resolved: never 0)
   uint16_t* out;
   int64_t o_sb, o_sh, o_sr;
+  // restricted self-attention: query i sees keys [i - win_left, i + win_right]
+  // (n_q == n_k); a negative bound is no bound
+  int win_left = -1, win_right = -1;
 };
 
 // bf16 tcgen05 attention; tensor maps describe Q, K, V and the output O as

@@ -57,6 +57,8 @@ def _load():
             lib.oracle_mha.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, ci, ci,
                                        ci, ip, cd, ci]
             lib.oracle_mha.restype = ci
+            lib.oracle_decode.argtypes = [dp, dp, dp, dp, ci, ci, ci, ci, ci, ci, ip, cd, ci]
+            lib.oracle_decode.restype = ci
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ci
             _lib = lib
@@ -143,6 +145,33 @@ def attention_rows(q_rows, row_pos, K, V, causal: bool, kv_len: int | None = Non
                                               float(scale), _dp(out), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_attention_rows rejected its arguments")
+    return out
+
+
+def decode(q, k_cache, v_cache, cache_lens=None, scale: float | None = None, nthreads: int = 0):
+    """One decoding step against a key/value cache.
+
+    q [B,h,n_q,d_k]: the n_q newest tokens' queries; k_cache [B,h,n_max,d_k],
+    v_cache [B,h,n_max,d_v]: every position so far, the new tokens included;
+    cache_lens [B] (None = n_max): valid rows L per batch entry. Query t sits
+    at position L - n_q + t and sees the keys at positions <= its own.
+    Returns out [B,h,n_q,d_v].
+    """
+    q, k_cache, v_cache = _f64(q), _f64(k_cache), _f64(v_cache)
+    B, h, n_q, d_k = q.shape
+    n_max, d_v = k_cache.shape[2], v_cache.shape[3]
+    assert k_cache.shape == (B, h, n_max, d_k) and v_cache.shape == (B, h, n_max, d_v)
+    if scale is None or scale == 0.0:
+        scale = default_scale(d_k)
+    lens = None
+    if cache_lens is not None:
+        lens = np.ascontiguousarray(np.asarray(cache_lens, dtype=np.int32))
+        assert lens.shape == (B,)
+    out = np.zeros((B, h, n_q, d_v), dtype=np.float64)
+    rc = _load().oracle_decode(_dp(q), _dp(k_cache), _dp(v_cache), _dp(out), B, h, n_q, n_max,
+                               d_k, d_v, _ip(lens), float(scale), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_decode rejected its arguments")
     return out
 
 

@@ -25,6 +25,13 @@
  *     (kimjiil.github.io), section "[4] Why Self-Attention", Table 1, row
  *     "Self-Attention (restricted)"); a negative bound means "no limit on
  *     that side", so (-1, -1) is eq. (1) itself;
+ *   - incremental decoding with a key/value cache: the new tokens' queries
+ *     only, against the cached keys and values of every earlier position
+ *     plus their own ("Attention Is All You Need 해부" (sj-techlog), section
+ *     "KV cache는 추론의 같은 계산을 반복하지 않게 한다"; "[논문 리뷰]Attention
+ *     Is All You Need", section 3.7 "Inference — auto-regressive 디코딩"):
+ *     with L valid cache rows the n_q new tokens sit at positions
+ *     L - n_q .. L - 1, and the causal rule (key j <= query position) applies;
  *   - MultiHead(Q,K,V) = Concat(head_1..head_h) W^O,
  *     head_i = Attention(Q W_i^Q, K W_i^K, V W_i^V), with the per-head matrices
  *     being column block i of one [d_model, h*d] matrix
@@ -206,6 +213,41 @@ int oracle_attention_rows(const double *q_rows, const int32_t *row_pos, int R,
 {
     return oracle_attention_rows_window(q_rows, row_pos, R, K, V, n_k, d_k, d_v, causal, kv_len,
                                         -1, -1, scale, out, nthreads);
+}
+
+/*
+ * Decoding step against a key/value cache. q [B,h,n_q,d_k] are the queries of
+ * the n_q newest tokens; k_cache [B,h,n_max,d_k], v_cache [B,h,n_max,d_v]
+ * hold every position so far (the new tokens' own keys and values included);
+ * cache_lens int32[B] (NULL = n_max) gives the valid rows L of each batch
+ * entry (clamped to [0, n_max]). Query t sits at position L - n_q + t and
+ * sees the keys j <= that position (j < L); a query at a negative position
+ * sees none and gets 0. out [B,h,n_q,d_v].
+ */
+int oracle_decode(const double *q, const double *k_cache, const double *v_cache, double *out,
+                  int B, int h, int n_q, int n_max, int d_k, int d_v, const int32_t *cache_lens,
+                  double scale, int nthreads)
+{
+    int bh;
+    if (B < 0 || h < 0 || n_q < 0 || n_max < 0 || d_k <= 0 || d_v <= 0) return -1;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic)
+#endif
+    for (bh = 0; bh < B * h; ++bh) {
+        int b = bh / h, t;
+        int L = cache_lens ? clamp_len(cache_lens[b], n_max) : n_max;
+        const double *K = k_cache + (size_t)bh * n_max * d_k;
+        const double *V = v_cache + (size_t)bh * n_max * d_v;
+        double *scores = (double *)malloc(sizeof(double) * (size_t)(n_max > 0 ? n_max : 1));
+        for (t = 0; t < n_q; ++t) {
+            int pos = L - n_q + t;
+            attend_row(q + ((size_t)bh * n_q + t) * d_k, K, V, n_max, d_k, d_v, pos, 1, L, -1, -1,
+                       scale, scores, NULL, out + ((size_t)bh * n_q + t) * d_v);
+        }
+        free(scores);
+    }
+    return 0;
 }
 
 /* C[M,N] = A[M,K] B[K,N], plain triple loop (row-major). */

@@ -461,3 +461,78 @@ def test_window_matches_torch_fp64_sdpa_with_band_mask(left, right, mask):
                                ref[np.broadcast_to(live[:, None], ref.shape[:3])],
                                rtol=1e-12, atol=1e-12)
     assert np.all(ours[np.broadcast_to(~live[:, None], ours.shape[:3])] == 0.0)
+
+
+# ---------------------------------------------------------------- incremental decoding (KV cache)
+# "Attention Is All You Need 해부" (sj-techlog), section "KV cache는 추론의 같은
+# 계산을 반복하지 않게 한다": the new token's query only, against the cached
+# keys/values of all earlier positions and its own.
+
+def test_decode_one_token_at_a_time_reproduces_the_printed_causal_run():
+    """Feeding the page's 3 tokens one at a time through the cache gives the
+    printed causal outputs row by row ([10, 0], [3.302385, 6.697615],
+    [7.517449, 7.517449])."""
+    g = _load("three_token_verification.json")
+    q = np.asarray(g["q"], dtype=np.float64)[None, None]
+    k = np.asarray(g["k"], dtype=np.float64)[None, None]
+    v = np.asarray(g["v"], dtype=np.float64)[None, None]
+    tol = g["tolerance"]
+    for t in range(3):
+        out = oracle.decode(q[:, :, t:t + 1], k, v, cache_lens=[t + 1])
+        np.testing.assert_allclose(out[0, 0, 0], g["causal_outputs"][t], atol=tol, rtol=0)
+
+
+@pytest.mark.parametrize("n_q", [1, 3, 8])
+def test_decode_equals_the_last_rows_of_causal_attention(n_q):
+    """With L cached rows, the n_q newest tokens' outputs are rows L - n_q ..
+    L - 1 of causal self-attention over the first L positions (bottom-right
+    alignment); rows past L in the cache are never read."""
+    rng = np.random.default_rng(11 + n_q)
+    B, h, n_max, d = 3, 2, 23, 6
+    q_all = rng.standard_normal((B, h, n_max, d))
+    k = rng.standard_normal((B, h, n_max, d))
+    v = rng.standard_normal((B, h, n_max, d))
+    lens = np.array([23, 15, n_q], dtype=np.int32)
+    q = np.stack([q_all[b, :, lens[b] - n_q:lens[b]] for b in range(B)])
+    k_junk, v_junk = k.copy(), v.copy()
+    for b in range(B):  # garbage past each entry's length must not matter
+        k_junk[b, :, lens[b]:] = 1e6
+        v_junk[b, :, lens[b]:] = -1e6
+    out = oracle.decode(q, k_junk, v_junk, cache_lens=lens)
+    for b in range(B):
+        L = lens[b]
+        full = oracle.attention(q_all[b:b + 1, :, :L], k[b:b + 1, :, :L], v[b:b + 1, :, :L],
+                                MASK_CAUSAL)
+        np.testing.assert_allclose(out[b], full[0, :, L - n_q:L], rtol=0, atol=1e-12)
+
+
+def test_decode_more_queries_than_cached_rows_gives_zero_rows_first():
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((2, 1, 4, 5))
+    k = rng.standard_normal((2, 1, 6, 5))
+    v = rng.standard_normal((2, 1, 6, 5))
+    out = oracle.decode(q, k, v, cache_lens=[2, 0])
+    assert np.all(out[0, 0, :2] == 0.0) and np.all(out[1] == 0.0)
+    np.testing.assert_allclose(out[0, 0, 2], v[0, 0, 0], rtol=0, atol=1e-15)  # position 0
+    assert np.all(np.abs(out[0, 0, 3]) > 0)
+
+
+def test_decode_matches_torch_fp64_sdpa_with_bottom_right_causal_mask():
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    rng = np.random.default_rng(31)
+    B, h, n_q, n_max, d = 2, 3, 5, 37, 8
+    q = rng.standard_normal((B, h, n_q, d))
+    k = rng.standard_normal((B, h, n_max, d))
+    v = rng.standard_normal((B, h, n_max, d))
+    lens = np.array([37, 20], dtype=np.int32)
+    ours = oracle.decode(q, k, v, cache_lens=lens)
+    for b in range(B):
+        L = int(lens[b])
+        pos = torch.arange(L - n_q, L)[:, None]
+        allowed = (torch.arange(L)[None, :] <= pos)[None, None]
+        ref = F.scaled_dot_product_attention(torch.from_numpy(q[b:b + 1]),
+                                             torch.from_numpy(k[b:b + 1, :, :L]),
+                                             torch.from_numpy(v[b:b + 1, :, :L]),
+                                             attn_mask=allowed).numpy()
+        np.testing.assert_allclose(ours[b:b + 1], ref, rtol=1e-12, atol=1e-12)

@@ -70,6 +70,11 @@ WORKLOADS = {
                             desc="Transformer-big causal self-attention: B=8, h=16, n=1024, d=64"),
     "long": dict(kind="attn", B=4, h=16, n=4096, d=64, causal=False, seed=1004,
                  desc="long-context attention sweep point"),
+    "decode": dict(kind="decode", B=16, h=16, n_q=1, n_max=8192, d=64, len_range=(4096, 8192),
+                   seed=1006,
+                   desc="one decoding step against a key/value cache: B=16, h=16, d=64, one new "
+                        "token per sequence, cache lengths U[4096, 8192] of 8192 rows; TFLOP/s "
+                        "counted over the visible (query, key) pairs, the cache read from HBM"),
     "window": dict(kind="attn", B=4, h=16, n=16384, d=64, causal=False, window=(256, 256),
                    seed=1005,
                    desc="restricted self-attention (Table 1, restricted row): B=4, h=16, n=16384, "
@@ -123,6 +128,7 @@ KERNEL_SOURCES = {
     "attn_fwd_bf16": "transformer_scaled_dot_gb300/csrc/attn_bf16.cu",
     "gemm_bf16": "transformer_scaled_dot_gb300/csrc/gemm_bf16.cu",
     "mha_fused": "transformer_scaled_dot_gb300/csrc/mha_fused.cu",
+    "attn_decode": "transformer_scaled_dot_gb300/csrc/attn_decode.cu",
 }
 
 
@@ -506,6 +512,80 @@ class AttnCall:
         return 3 * self.a.q.nbytes, self.a.q.nbytes
 
 
+class DecodeCall:
+    """Device buffers of one attn_decode call (queries, the cache, lengths,
+    workspace) over rotating sets."""
+
+    def __init__(self, tsd, cfg, nsets, seed_offset):
+        import torch
+        self.tsd, self.cfg = tsd, cfg
+        c = cfg
+        B, h, n_q, n_max, d = c["B"], c["h"], c["n_q"], c["n_max"], c["d"]
+        self.shape = (B, h, n_q, n_max, d)
+        rng = np.random.default_rng(c["seed"] + seed_offset)
+        self.lens = synthetic.uniform_lengths(rng, B, *c["len_range"])
+        a = synthetic.attention_inputs(c["seed"] + seed_offset, B, h, n_q, n_max, d, d)
+        self.a = a
+        bf = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to("cuda").view(torch.bfloat16)
+        self.wsb = tsd.attn_decode_workspace_bytes(B, h, n_q, n_max, d)
+        self.sets = []
+        for _ in range(nsets):
+            self.sets.append(dict(q=bf(a.q), k=bf(a.k), v=bf(a.v),
+                                  lens=torch.from_numpy(self.lens).to("cuda"),
+                                  out=torch.empty((B, h, n_q, d), dtype=torch.bfloat16, device="cuda"),
+                                  ws=torch.empty(self.wsb, dtype=torch.uint8, device="cuda")))
+        self.h_q = torch.from_numpy(np.ascontiguousarray(a.q).view(np.int16)).pin_memory()
+        self.h_lens = torch.from_numpy(self.lens).pin_memory()
+        self.h_out = torch.empty((B, h, n_q, d), dtype=torch.bfloat16).pin_memory()
+
+    @staticmethod
+    def set_bytes(cfg):
+        return 2 * cfg["B"] * cfg["h"] * cfg["n_max"] * cfg["d"] * 2
+
+    def run(self, i, stream):
+        B, h, n_q, n_max, d = self.shape
+        s = self.sets[i % len(self.sets)]
+        self.tsd.attn_decode(s["q"], s["k"], s["v"], s["out"], B, h, n_q, n_max, d, d, s["lens"],
+                             0.0, s["ws"], self.wsb, stream)
+
+    def run_stage(self, k, i, stream):
+        self.run(i, stream)
+
+    def stage_names(self):
+        return ["attn_decode"]
+
+    def visible_pairs(self):
+        B, h, n_q, n_max, d = self.shape
+        n = 0
+        for L in self.lens:
+            L = int(min(max(L, 0), n_max))
+            n += sum(max(0, min(L, L - n_q + t + 1)) for t in range(n_q))
+        return n * h
+
+    def stage_work(self):
+        B, h, n_q, n_max, d = self.shape
+        f = 4.0 * d * self.visible_pairs()
+        rows = sum(int(min(max(L, 0), n_max)) for L in self.lens) * h  # cache rows read
+        b = 2.0 * (2 * rows * d + 2 * B * h * n_q * d)
+        return [(f, b)]
+
+    def metric_flops(self):
+        return self.stage_work()[0][0]
+
+    def launches(self):
+        return 2
+
+    def e2e_run(self, i, stream):
+        s = self.sets[i % len(self.sets)]
+        s["q"].view(torch_int16()).copy_(self.h_q, non_blocking=True)
+        s["lens"].copy_(self.h_lens, non_blocking=True)
+        self.run(i, stream)
+        self.h_out.copy_(s["out"], non_blocking=True)
+
+    def e2e_bytes(self):
+        return self.a.q.nbytes + self.lens.nbytes, self.a.q.nbytes
+
+
 def torch_int16():
     import torch
     return torch.int16
@@ -513,6 +593,10 @@ def torch_int16():
 
 def make_calls(tsd, wl, args, seed_offset):
     spec = WORKLOADS[wl]
+    if spec["kind"] == "decode":
+        per_set = DecodeCall.set_bytes(spec)
+        nsets = max(2, math.ceil(2.2 * L2_BYTES / per_set))
+        return [DecodeCall(tsd, spec, nsets, seed_offset)], nsets, per_set
     if spec["kind"] == "mha":
         cfgs = spec["calls"]
         probe = [MhaCall(tsd, c, 1, seed_offset) for c in cfgs]
@@ -538,6 +622,9 @@ def workload_config(wl, calls, args, nsets, per_set):
         for c in cfg["calls"]:
             c["mask"] = {0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding"}[c["mask"]]
             c["kv_range"] = list(c["kv_range"]) if c["kv_range"] else None
+    elif spec["kind"] == "decode":
+        cfg.update({k: spec[k] for k in ("B", "h", "n_q", "n_max", "d")})
+        cfg["len_range"] = list(spec["len_range"])
     else:
         a = calls[0].a
         cfg.update(B=a.B, h=a.h, n=a.n_q, d=a.d_k, causal=bool(a.mask_kind & MASK_CAUSAL))
@@ -717,6 +804,20 @@ def oracle_sample_runner(args):
             for m, f64 in ms:
                 oracle.mha(*f64, m.h, m.mask_kind, kv_lens=m.kv_lens)
         return run, flops, "the whole batch through oracle.mha (projections, attention, W_O)"
+    if spec["kind"] == "decode":
+        B, h, n_q, n_max, d = (spec[k] for k in ("B", "h", "n_q", "n_max", "d"))
+        nb = 2  # every head of the first two sequences
+        a = synthetic.attention_inputs(spec["seed"], nb, h, n_q, n_max, d, d)
+        rng = np.random.default_rng(spec["seed"])
+        lens = synthetic.uniform_lengths(rng, B, *spec["len_range"])[:nb]
+        q, k, v = (synthetic.bf16_bits_to_f64(x) for x in (a.q, a.k, a.v))
+        flops = 4.0 * d * h * sum(max(0, min(int(L), int(L) - n_q + t + 1))
+                                  for L in lens for t in range(n_q))
+
+        def run():
+            oracle.decode(q, k, v, cache_lens=lens)
+        return run, flops, (f"all {h} heads of {nb} sequences (cache lengths {list(map(int, lens))}, "
+                            f"d={d}) via oracle.decode")
     cfg = dict(spec)
     for k in ("B", "n", "d"):
         if getattr(args, k, None):
@@ -755,7 +856,7 @@ def cpu_baseline(args, calls, budget_s=10.0):
         run()
         reps += 1
         el = time.perf_counter() - t0
-        if el >= budget_s or reps >= 50:
+        if el >= budget_s or reps >= 100000:
             break
     tflops = flops * reps / el / 1e12
     return {"value": tflops, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",

@@ -82,6 +82,32 @@ attn_status attn_forward(const void *q, const void *k, const void *v, void *out,
                          tsd_stream_t stream);
 
 /*
+ * attn_decode -- one decoding step against a key/value cache ("Attention Is
+ * All You Need 해부" (sj-techlog), section "KV cache는 추론의 같은 계산을
+ * 반복하지 않게 한다"; "[논문 리뷰]Attention Is All You Need"
+ * (kimjiil.github.io), section 3.7): only the newest tokens' queries are
+ * computed; the keys and values of every position so far (theirs included)
+ * come from the cache. With L = cache_lens[b] valid rows, query t sits at
+ * position L - n_q + t and attends to the keys at positions <= its own (the
+ * causal rule aligned to the end of the cache); a query at a negative
+ * position sees no key and gets 0.
+ *   q        [B, h, n_q, d_k] bf16, device        out [B, h, n_q, d_v] bf16
+ *   k_cache  [B, h, n_max, d_k] bf16, device      v_cache [B, h, n_max, d_v]
+ *   cache_lens: device int32[B] (clamped to [0, n_max]), or NULL for L = n_max
+ *   1 <= n_q <= 8 (more -> ATTN_ERR_UNSUPPORTED); d_k == d_v in {64, 128}.
+ *   workspace: device, 16-byte aligned, >= attn_decode_workspace_bytes(...)
+ *   bytes (per-chunk partial results; scratch, caller-owned).
+ *   scale: 0 -> 1/sqrt(d_k). Cache rows at or past L are never used.
+ * Errors: as attn_forward; a short workspace -> ATTN_ERR_INVALID. Two
+ * launches (per-chunk partials, then the merge), asynchronous on `stream`.
+ */
+size_t attn_decode_workspace_bytes(int B, int h, int n_q, int n_max, int d_v);
+attn_status attn_decode(const void *q, const void *k_cache, const void *v_cache, void *out,
+                        int B, int h, int n_q, int n_max, int d_k, int d_v,
+                        const int32_t *cache_lens, float scale,
+                        void *workspace, size_t workspace_bytes, tsd_stream_t stream);
+
+/*
  * attn_forward_window -- restricted self-attention: query i considers only
  * the keys j with i - window_left <= j <= i + window_right ("[논문 리뷰]
  * Attention Is All You Need" (kimjiil.github.io), section "[4] Why

@@ -169,3 +169,31 @@ def test_attn_forward_window_rejects_bad_arguments(lib, args, expect):
 def test_attn_forward_window_empty_problem_is_a_no_op(lib):
     assert lib.attn_forward_window(FAKE, FAKE, FAKE, FAKE, 0, 1, 16, 16, 64, 64, 0, None, 3, 3,
                                    0.0, None) == tsd.ATTN_OK
+
+
+def test_attn_decode_rejects_bad_arguments(lib):
+    ws = tsd.attn_decode_workspace_bytes(1, 1, 1, 100, 64)
+    assert ws > 0
+    call = lambda *a: lib.attn_decode(*a)
+    base = [FAKE, FAKE, FAKE, FAKE, 1, 1, 1, 100, 64, 64, None, 0.0, FAKE, ws, None]
+
+    def with_(i, v):
+        args = list(base)
+        args[i] = v
+        return call(*args)
+    assert with_(6, 0) == tsd.ATTN_ERR_INVALID          # n_q = 0
+    assert with_(6, 9) == tsd.ATTN_ERR_UNSUPPORTED      # n_q > 8
+    assert with_(7, 0) == tsd.ATTN_ERR_INVALID          # empty cache shape
+    assert with_(8, 96) == tsd.ATTN_ERR_UNSUPPORTED     # head size
+    assert with_(0, None) == tsd.ATTN_ERR_INVALID       # null q
+    assert with_(1, FAKE + 4) == tsd.ATTN_ERR_INVALID   # misaligned cache
+    assert with_(10, FAKE + 2) == tsd.ATTN_ERR_INVALID  # misaligned lengths
+    assert with_(13, ws - 1) == tsd.ATTN_ERR_INVALID    # short workspace
+    assert with_(11, -1.0) == tsd.ATTN_ERR_INVALID      # negative scale
+
+
+def test_attn_decode_workspace_grows_with_chunks_queries_and_width(lib):
+    f = tsd.attn_decode_workspace_bytes
+    assert f(1, 1, 1, 256, 64) < f(1, 1, 1, 257, 64)   # a second 256-key chunk
+    assert f(2, 3, 4, 1000, 128) >= 2 * 3 * 4 * 4 * (128 + 2) * 4
+    assert f(1, 1, 0, 100, 64) == 0 and f(1, 1, 9, 100, 64) == 0

@@ -23,8 +23,8 @@ __all__ = [
     "attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_workspace_bytes",
     "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
     "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out", "mha_forward_noalloc",
-    "mha_concat_heads", "mha_forward_launches", "attn_forward_window",
-    "MHA_NOALLOC_SCRATCH_BYTES",
+    "mha_concat_heads", "mha_forward_launches", "attn_forward_window", "attn_decode",
+    "attn_decode_workspace_bytes", "MHA_NOALLOC_SCRATCH_BYTES",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = range(5)
@@ -34,7 +34,8 @@ EXPORTED_SYMBOLS = (
     "attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_workspace_bytes",
     "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
     "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out", "mha_forward_noalloc",
-    "mha_concat_heads", "mha_forward_launches", "attn_forward_window",
+    "mha_concat_heads", "mha_forward_launches", "attn_forward_window", "attn_decode",
+    "attn_decode_workspace_bytes",
 )
 
 # TSD_MHA_NOALLOC_SCRATCH_BYTES of the header: the fixed scratch of mha_forward_noalloc
@@ -89,10 +90,13 @@ def library():
     lib.attn_selftest_wait_timeout.argtypes = [i, st]
     lib.mha_forward_launches.argtypes = [i, i, i, i, i, i, i, i]
     lib.attn_forward_window.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, i, i, f, st]
+    lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i]
+    lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_decode.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp, f, vp, ctypes.c_size_t, st]
     for name in ("attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_forward",
                  "attn_get_device_status", "attn_last_cuda_error", "attn_selftest_wait_timeout",
                  "mha_project_qkv", "mha_project_out", "mha_forward_noalloc", "mha_concat_heads",
-                 "mha_forward_launches", "attn_forward_window"):
+                 "mha_forward_launches", "attn_forward_window", "attn_decode"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -134,6 +138,19 @@ def attn_forward_window(q, k, v, out, B, h, n_q, n_k, d_k, d_v, window_left, win
                                          d_k, d_v, mask_kind, _ptr(kv_lens), window_left,
                                          window_right, scale, _stream(stream)),
            "attn_forward_window")
+
+
+def attn_decode_workspace_bytes(B, h, n_q, n_max, d_v) -> int:
+    return int(library().attn_decode_workspace_bytes(B, h, n_q, n_max, d_v))
+
+
+def attn_decode(q, k_cache, v_cache, out, B, h, n_q, n_max, d_k, d_v, cache_lens=None, scale=0.0,
+                workspace=None, workspace_bytes=0, stream=None):
+    """One decoding step: the n_q newest tokens' queries against an n_max-row
+    key/value cache (cache_lens[b] valid rows, None = n_max)."""
+    _check(library().attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), B, h, n_q,
+                                 n_max, d_k, d_v, _ptr(cache_lens), scale, _ptr(workspace),
+                                 workspace_bytes, _stream(stream)), "attn_decode")
 
 
 def attn_forward_strided(q, q_sb, q_sh, q_sr, k, k_sb, k_sh, k_sr, v, v_sb, v_sh, v_sr,

@@ -532,6 +532,66 @@ attn_status mha_forward(const void* x_q, const void* x_kv, const void* w_q, cons
   return launch_out_proj(O, w_o, out, B, n_q, d_model, h, d_v, stream);
 }
 
+// Workspace of attn_decode: the chunk partials O (float) then (m, l) pairs.
+bool decode_layout(int B, int h, int n_q, int n_max, int d, size_t* o_bytes, size_t* total) {
+  if (B < 0 || h < 0 || n_q < 1 || n_q > tsd::kDecodeMaxQueries || n_max < 1 || d < 1)
+    return false;
+  const uint64_t rows = uint64_t(B) * h * tsd::decode_chunks(n_max) * n_q;
+  const uint64_t ob = align256(rows * d * 4), mb = align256(rows * 2 * 4);
+  if (ob + mb > (uint64_t(1) << 62)) return false;
+  *o_bytes = ob;
+  *total = ob + mb;
+  return true;
+}
+
+size_t attn_decode_workspace_bytes(int B, int h, int n_q, int n_max, int d_v) {
+  size_t ob = 0, total = 0;
+  return decode_layout(B, h, n_q, n_max, d_v, &ob, &total) ? total : 0;
+}
+
+attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache, void* out, int B,
+                        int h, int n_q, int n_max, int d_k, int d_v, const int32_t* cache_lens,
+                        float scale, void* workspace, size_t workspace_bytes,
+                        tsd_stream_t stream) {
+  if (B < 0 || h < 0 || n_q < 1 || n_max < 1) return ATTN_ERR_INVALID;
+  if (n_q > tsd::kDecodeMaxQueries) return ATTN_ERR_UNSUPPORTED;
+  if (B > 65535 || h > 65535 || int64_t(B) * h > INT32_MAX) return ATTN_ERR_INVALID;
+  if (!valid_scale(scale)) return ATTN_ERR_INVALID;
+  attn_status s = check_bf16_head_dims(d_k, d_v);
+  if (s != ATTN_OK) return s;
+  const void* ptrs[5] = {q, k_cache, v_cache, out, workspace};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID;
+  if (cache_lens != nullptr && (reinterpret_cast<uintptr_t>(cache_lens) & 3u))
+    return ATTN_ERR_INVALID;
+  size_t ob = 0, total = 0;
+  if (!decode_layout(B, h, n_q, n_max, d_v, &ob, &total)) return ATTN_ERR_INVALID;
+  if (workspace_bytes < total) return ATTN_ERR_INVALID;
+  if (B == 0 || h == 0) return ATTN_OK;
+  tsd::DecodeProblem p;
+  std::memset(&p, 0, sizeof(p));
+  const uint64_t dims[3] = {static_cast<uint64_t>(d_k), static_cast<uint64_t>(n_max),
+                            static_cast<uint64_t>(B) * h};
+  const int64_t strides[2] = {d_k, int64_t(n_max) * d_k};
+  const uint32_t box[3] = {64, 256, 1};
+  cudaError_t e = encode_bf16_map(&p.tm_k, k_cache, 3, dims, strides, box);
+  if (e == cudaSuccess) e = encode_bf16_map(&p.tm_v, v_cache, 3, dims, strides, box);
+  if (e != cudaSuccess) return cuda_fail(e);
+  p.q = q;
+  p.out = out;
+  p.cache_lens = cache_lens;
+  p.ws_o = static_cast<float*>(workspace);
+  p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ob);
+  p.B = B;
+  p.h = h;
+  p.n_q = n_q;
+  p.n_max = n_max;
+  p.d = d_k;
+  p.scale = resolve_scale(scale, d_k);
+  e = tsd::launch_decode(p, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
 int mha_forward_launches(int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
                          int self_attention) {
   if (B < 0 || n_q < 0 || n_k < 0 || h <= 0 || d_model < 8 || (d_model % 8) != 0 ||
@@ -599,6 +659,9 @@ attn_status attn_get_device_status(tsd_stream_t stream) {
   if (e == cudaSuccess) e = tsd::take_device_error_gemm(&g);
   if (e == cudaSuccess) e = tsd::take_device_error_f32(&f);
   if (e == cudaSuccess) e = tsd::take_device_error_fused(&m);
+  unsigned int dec = 0;
+  if (e == cudaSuccess) e = tsd::take_device_error_decode(&dec);
+  m |= dec;
   if (e != cudaSuccess) return cuda_fail(e);
   return (a | g | f | m) ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
 }

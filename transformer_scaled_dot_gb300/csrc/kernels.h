@@ -136,7 +136,26 @@ cudaError_t launch_mha_fused(const MhaFusedProblem& p, cudaStream_t stream);
 int mha_fused_out_clusters(int h, bool self);
 
 // Per-file device error words (read and cleared; see sm103.cuh).
+// One decoding step against a key/value cache: the n_q (<= 8) newest tokens'
+// queries, at positions L - n_q .. L - 1 of an L-row cache, each against the
+// keys at or before its position. Split over 256-key chunks (partials in a
+// workspace of float), then merged per (batch, head).
+constexpr int kDecodeMaxQueries = 8;
+struct DecodeProblem {
+  CUtensorMap tm_k, tm_v;      // 3-D (d, n_max, B*h) bf16, box 64 x 256 x 1, 128-byte swizzle
+  const void* q;               // [B, h, n_q, d] bf16
+  void* out;                   // [B, h, n_q, d] bf16
+  const int32_t* cache_lens;   // [B] valid rows, or null (= n_max)
+  float* ws_o;                 // [B, h, decode_chunks(n_max), n_q, d]
+  float* ws_ml;                // [B, h, decode_chunks(n_max), n_q, 2]
+  int B, h, n_q, n_max, d;
+  float scale;                 // logit factor (resolved: never 0)
+};
+int decode_chunks(int n_max);
+cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t stream);
+
 cudaError_t take_device_error_attn(unsigned int* value);
+cudaError_t take_device_error_decode(unsigned int* value);
 cudaError_t take_device_error_gemm(unsigned int* value);
 cudaError_t take_device_error_f32(unsigned int* value);
 cudaError_t take_device_error_fused(unsigned int* value);

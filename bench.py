@@ -604,7 +604,7 @@ def make_calls(tsd, wl, args, seed_offset):
         nsets = max(2, math.ceil(2.2 * L2_BYTES / per_set))
         return [MhaCall(tsd, c, nsets, seed_offset) for c in cfgs], nsets, per_set
     cfg = dict(spec)
-    for k in ("B", "n", "d"):
+    for k in ("B", "n", "d", "h"):
         if getattr(args, k, None):
             cfg[k] = getattr(args, k)
     if args.causal is not None:
@@ -819,7 +819,7 @@ def oracle_sample_runner(args):
         return run, flops, (f"all {h} heads of {nb} sequences (cache lengths {list(map(int, lens))}, "
                             f"d={d}) via oracle.decode")
     cfg = dict(spec)
-    for k in ("B", "n", "d"):
+    for k in ("B", "n", "d", "h"):
         if getattr(args, k, None):
             cfg[k] = getattr(args, k)
     if args.causal is not None:
@@ -900,7 +900,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="base_encoder_mha")
     ap.add_argument("--B", type=int, default=None)
     ap.add_argument("--n", type=int, default=None)
-    ap.add_argument("--d", type=int, default=None, choices=[64, 128])
+    ap.add_argument("--d", type=int, default=None, choices=[16, 32, 64, 128, 256])
+    ap.add_argument("--h", type=int, default=None)
     ap.add_argument("--causal", type=int, default=None, choices=[0, 1])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -119,7 +119,7 @@ def test_mha_forward_rejects_bad_arguments(lib):
     bad[10] = 100                          # d_model not a multiple of 8
     assert lib.mha_forward(*bad) == tsd.ATTN_ERR_INVALID
     bad = list(base)
-    bad[12] = bad[13] = 32                 # head size without a bf16 kernel
+    bad[12] = bad[13] = 48                 # head size without a bf16 kernel
     assert lib.mha_forward(*bad) == tsd.ATTN_ERR_UNSUPPORTED
 
 
@@ -139,7 +139,7 @@ def test_mha_concat_heads_rejects_bad_arguments(lib):
     bad[13] = tsd.ATTN_MASK_KEY_PADDING    # padding without lengths
     assert lib.mha_concat_heads(*bad) == tsd.ATTN_ERR_INVALID
     bad = list(base)
-    bad[11] = bad[12] = 32                 # head size without a bf16 kernel
+    bad[11] = bad[12] = 48                 # head size without a bf16 kernel
     assert lib.mha_concat_heads(*bad) == tsd.ATTN_ERR_UNSUPPORTED
     base[6] = 0                            # empty batch: nothing to do
     assert lib.mha_concat_heads(*base) == tsd.ATTN_OK

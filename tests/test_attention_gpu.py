@@ -58,6 +58,14 @@ CASES = [
     # more single-tile items than pipelines: every slot walks several items
     (40, 16, 100, 100, 64, MASK_KEY_PADDING, (1, 100)),
     (32, 16, 128, 128, 64, MASK_CAUSAL, None),
+    # Table 3's other head sizes: 16 and 32 through the 64-column kernels, 256
+    (2, 3, 200, 200, 16, MASK_CAUSAL, None),
+    (3, 2, 64, 64, 16, MASK_KEY_PADDING, (0, 64)),
+    (2, 2, 130, 300, 32, MASK_KEY_PADDING, (1, 300)),
+    (1, 2, 1000, 1000, 32, MASK_NONE, None),
+    (2, 2, 300, 300, 256, MASK_CAUSAL | MASK_KEY_PADDING, (50, 300)),
+    (1, 1, 128, 700, 256, MASK_NONE, None),
+    (3, 2, 77, 77, 256, MASK_KEY_PADDING, (0, 77)),
 ]
 
 
@@ -227,6 +235,8 @@ WINDOW_CASES = [
     (2, 2, 300, 128, MASK_NONE, None, 40, 40),
     (1, 2, 1000, 128, MASK_CAUSAL, None, 256, -1),
     (40, 8, 128, 64, MASK_KEY_PADDING, (1, 128), 16, 16),
+    (1, 2, 600, 256, MASK_NONE, None, 100, 100),
+    (2, 2, 500, 32, MASK_CAUSAL, None, 64, -1),
 ]
 
 

@@ -146,7 +146,8 @@ def test_mha_forward_launch_plan(tsd):
     assert plan(40, 64, 64, 128, 16, 64, 64, True) == 2      # 16 output columns per CTA: no
     assert plan(8, 1024, 1024, 1024, 16, 64, 64, True) == 3  # Transformer-big, n = 1024
     assert plan(0, 128, 128, 512, 8, 64, 64, True) == 0
-    assert plan(1, 16, 16, 512, 8, 32, 32, True) == -1
+    assert plan(1, 16, 16, 512, 16, 32, 32, True) == 3      # Table 3 head size: GEMM path
+    assert plan(1, 16, 16, 512, 8, 48, 48, True) == -1
 
 
 def test_mha_fused_output_projection_matches_two_launch_path(tsd):
@@ -177,6 +178,19 @@ def test_mha_fused_output_projection_matches_two_launch_path(tsd):
     diff = np.abs(got - two)
     # at most one bf16 step of the larger value apart
     assert np.all(diff <= np.maximum(np.abs(got), np.abs(two)) * 2.0 ** -7 + 1e-6)
+
+
+@pytest.mark.parametrize("shape", [
+    # Table 3 (A) of "[논문 리뷰]Attention Is All You Need": h x d_k = 512 at
+    # d_model = 512. B, n, h, d, mask
+    (4, 100, 16, 32, MASK_CAUSAL | MASK_KEY_PADDING),
+    (3, 150, 32, 16, MASK_KEY_PADDING),
+    (2, 200, 2, 256, MASK_CAUSAL),
+])
+def test_mha_table3_head_sizes(tsd, shape):
+    B, n, h, d, mask = shape
+    m = synthetic.mha_inputs(3500 + n + h, B, n, n, 512, h, d, d, mask, (1, n))
+    check(tsd, m, str(shape))
 
 
 def test_mha_fused_key_length_zero(tsd):

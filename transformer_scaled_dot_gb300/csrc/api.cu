@@ -159,8 +159,13 @@ attn_status check_common(int B, int h, int n_q, int n_k, int d_k, int d_v, int m
   return ATTN_OK;
 }
 
+// Head sizes of the bf16 attention kernels: 64 and 128, and Table 3's other
+// rows ("[논문 리뷰]Attention Is All You Need", section 6.2, Table 3 (A)): 16
+// and 32 run through the 64-column kernels (the tensor maps zero-fill the
+// columns past d on load and clip them on store), 256 through its own.
 attn_status check_bf16_head_dims(int d_k, int d_v) {
-  if (d_k != d_v || (d_k != 64 && d_k != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (d_k != d_v) return ATTN_ERR_UNSUPPORTED;
+  if (d_k != 16 && d_k != 32 && d_k != 64 && d_k != 128 && d_k != 256) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
 
@@ -181,7 +186,7 @@ attn_status run_attn_bf16(const void* q, int64_t q_sb, int64_t q_sh, int64_t q_s
   p.h = h;
   p.n_q = n_q;
   p.n_k = n_k;
-  p.d = d;
+  p.d = d < 64 ? 64 : d;  // 16 and 32 run through the 64-column kernels
   p.mask_kind = mask_kind;
   p.kv_lens = kv_lens;
   p.scale = resolve_scale(scale, d);
@@ -557,8 +562,7 @@ attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache,
   if (n_q > tsd::kDecodeMaxQueries) return ATTN_ERR_UNSUPPORTED;
   if (B > 65535 || h > 65535 || int64_t(B) * h > INT32_MAX) return ATTN_ERR_INVALID;
   if (!valid_scale(scale)) return ATTN_ERR_INVALID;
-  attn_status s = check_bf16_head_dims(d_k, d_v);
-  if (s != ATTN_OK) return s;
+  if (d_k != d_v || (d_k != 64 && d_k != 128)) return ATTN_ERR_UNSUPPORTED;
   const void* ptrs[5] = {q, k_cache, v_cache, out, workspace};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID;

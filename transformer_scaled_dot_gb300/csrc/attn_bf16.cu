@@ -779,7 +779,15 @@ cudaError_t launch_attn_bf16(const AttnProblem& p, const CUtensorMap& tm_q,
                   : launch_variant<128, 1, 2, 2, 2, true, 1, false, true>(p, tm_q, tm_k, tm_v,
                                                                          tm_o, stream);
     }
+    if (p.d == 256)
+      return launch_variant<256, 1, 1, 1, 1, false, 1, false, true>(p, tm_q, tm_k, tm_v, tm_o,
+                                                                    stream);
     return cudaErrorInvalidValue;
+  }
+  if (p.d == 256) {
+    // one query tile per item: S (128) + O (256) + P (64) columns of TMEM;
+    // one buffer each of Q, K, V (64 KB apiece) and rows stored directly
+    return launch_variant<256, 1, 1, 1, 1, false, 1>(p, tm_q, tm_k, tm_v, tm_o, stream);
   }
   if (p.d == 64) {
     if (!pair) return launch_variant<64, 1, 2, 2, 1, true, 2>(p, tm_q, tm_k, tm_v, tm_o, stream);

@@ -424,6 +424,18 @@ class MhaCall:
         m = self.m
         return attn_flops(m.B, m.h, m.n_q, m.n_k, m.d_k, bool(m.mask_kind & MASK_CAUSAL))
 
+    def useful_flops(self):
+        """4 d per (query, key) pair the masks allow (key padding, causal)."""
+        m = self.m
+        causal = bool(m.mask_kind & MASK_CAUSAL)
+        pairs = 0
+        for L in self.kv_effective():
+            if causal:  # query i sees keys j <= i, j < L
+                pairs += sum(min(i + 1, L) for i in range(m.n_q))
+            else:
+                pairs += m.n_q * L
+        return 4.0 * m.h * m.d_k * pairs
+
     def launches(self):
         return len(self.stage_names())
 
@@ -498,6 +510,9 @@ class AttnCall:
     def metric_flops(self):
         return self.stage_work()[0][0]
 
+    def useful_flops(self):
+        return self.metric_flops()
+
     def launches(self):
         return 1
 
@@ -571,6 +586,9 @@ class DecodeCall:
 
     def metric_flops(self):
         return self.stage_work()[0][0]
+
+    def useful_flops(self):
+        return self.metric_flops()
 
     def launches(self):
         return 2
@@ -684,6 +702,8 @@ def run_gpu_arm(args, world, rank, local):
     flops_step = sum(c.metric_flops() for c in calls)
     total_flops = dist_sum(flops_step * args.steps, world)
     value = total_flops / (ms_total_max * 1e-3) / 1e12
+    useful_value = dist_sum(sum(c.useful_flops() for c in calls) * args.steps, world) / \
+        (ms_total_max * 1e-3) / 1e12
 
     # ---------------------------------------------------------------- per-kernel timing
     # Each kernel on its own: a CUDA graph of back-to-back launches over the
@@ -765,6 +785,7 @@ def run_gpu_arm(args, world, rank, local):
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "useful_value": round(useful_value, 3),
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) / Xavier inputs of the workload's shapes)",
@@ -800,9 +821,9 @@ def oracle_sample_runner(args):
         flops = sum(attn_flops(m.B, m.h, m.n_q, m.n_k, m.d_k, bool(m.mask_kind & MASK_CAUSAL))
                     for m, _ in ms)
 
-        def run():
+        def run(nthreads=0):
             for m, f64 in ms:
-                oracle.mha(*f64, m.h, m.mask_kind, kv_lens=m.kv_lens)
+                oracle.mha(*f64, m.h, m.mask_kind, kv_lens=m.kv_lens, nthreads=nthreads)
         return run, flops, "the whole batch through oracle.mha (projections, attention, W_O)"
     if spec["kind"] == "decode":
         B, h, n_q, n_max, d = (spec[k] for k in ("B", "h", "n_q", "n_max", "d"))
@@ -814,8 +835,8 @@ def oracle_sample_runner(args):
         flops = 4.0 * d * h * sum(max(0, min(int(L), int(L) - n_q + t + 1))
                                   for L in lens for t in range(n_q))
 
-        def run():
-            oracle.decode(q, k, v, cache_lens=lens)
+        def run(nthreads=0):
+            oracle.decode(q, k, v, cache_lens=lens, nthreads=nthreads)
         return run, flops, (f"all {h} heads of {nb} sequences (cache lengths {list(map(int, lens))}, "
                             f"d={d}) via oracle.decode")
     cfg = dict(spec)
@@ -842,8 +863,8 @@ def oracle_sample_runner(args):
         keys_seen = (rows + 1).sum() if causal else len(rows) * n
     flops = 4.0 * keys_seen * d
 
-    def run():
-        oracle.attention_rows(q[rows], rows, k, v, causal=causal, window=window)
+    def run(nthreads=0):
+        oracle.attention_rows(q[rows], rows, k, v, causal=causal, window=window, nthreads=nthreads)
     return run, flops, f"{len(rows)} query rows of one head (n={n}, d={d}) via oracle.attention_rows"
 
 
@@ -859,8 +880,18 @@ def cpu_baseline(args, calls, budget_s=10.0):
         if el >= budget_s or reps >= 100000:
             break
     tflops = flops * reps / el / 1e12
+    # the same sample on one thread (the parallel figure's scaling reference)
+    reps1, t1 = 0, time.perf_counter()
+    while True:
+        run(nthreads=1)
+        reps1 += 1
+        el1 = time.perf_counter() - t1
+        if el1 >= budget_s / 3 or reps1 >= 100000:
+            break
     return {"value": tflops, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"{what}; {reps} repetitions in {el:.1f} s"}
+            "sample": f"{what}; {reps} repetitions in {el:.1f} s",
+            "single_thread": {"value": flops * reps1 / el1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                              "sample": f"the same sample, {reps1} repetitions in {el1:.1f} s"}}
 
 
 def run_reference_arm(args, world, rank):

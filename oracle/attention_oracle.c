@@ -63,6 +63,18 @@
 #define ORACLE_MASK_CAUSAL 1
 #define ORACLE_MASK_KEY_PADDING 2
 
+/* Threads of a parallel region: the caller's count, or the default team. A
+ * num_threads clause, unlike omp_set_num_threads, leaves later calls alone. */
+static int team(int nthreads)
+{
+#ifdef _OPENMP
+    return nthreads > 0 ? nthreads : omp_get_max_threads();
+#else
+    (void)nthreads;
+    return 1;
+#endif
+}
+
 static int clamp_len(int len, int n_k)
 {
     if (len < 0) return 0;
@@ -147,8 +159,7 @@ int oracle_attention_window(const double *q, const double *k, const double *v, d
     if (padding && !kv_lens) return -1;
     if ((causal || windowed) && n_q != n_k) return -1;
 #ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
-#pragma omp parallel for schedule(dynamic)
+#pragma omp parallel for schedule(dynamic) num_threads(team(nthreads))
 #endif
     for (bh = 0; bh < B * h; ++bh) {
         int b = bh / h, i;
@@ -191,8 +202,7 @@ int oracle_attention_rows_window(const double *q_rows, const int32_t *row_pos, i
     int len = kv_len < 0 ? n_k : clamp_len(kv_len, n_k);
     if (R < 0 || n_k < 0 || d_k <= 0 || d_v <= 0) return -1;
 #ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
-#pragma omp parallel
+#pragma omp parallel num_threads(team(nthreads))
 #endif
     {
         double *scores = (double *)malloc(sizeof(double) * (size_t)(n_k > 0 ? n_k : 1));
@@ -231,8 +241,7 @@ int oracle_decode(const double *q, const double *k_cache, const double *v_cache,
     int bh;
     if (B < 0 || h < 0 || n_q < 0 || n_max < 0 || d_k <= 0 || d_v <= 0) return -1;
 #ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
-#pragma omp parallel for schedule(dynamic)
+#pragma omp parallel for schedule(dynamic) num_threads(team(nthreads))
 #endif
     for (bh = 0; bh < B * h; ++bh) {
         int b = bh / h, t;
@@ -251,11 +260,13 @@ int oracle_decode(const double *q, const double *k_cache, const double *v_cache,
 }
 
 /* C[M,N] = A[M,K] B[K,N], plain triple loop (row-major). */
-static void matmul(const double *A, const double *Bm, double *C, int M, int N, int K)
+static void matmul(const double *A, const double *Bm, double *C, int M, int N, int K,
+                   int nthreads)
 {
     int i;
+    (void)nthreads;
 #ifdef _OPENMP
-#pragma omp parallel for schedule(static)
+#pragma omp parallel for schedule(static) num_threads(team(nthreads))
 #endif
     for (i = 0; i < M; ++i) {
         int j, p;
@@ -288,9 +299,6 @@ int oracle_mha(const double *x_q, const double *x_kv, const double *w_q, const d
     size_t vsz = (size_t)B * n_k * h * d_v, osz = (size_t)B * n_q * h * d_v;
     double *Q, *Kp, *Vp, *Qh, *Kh, *Vh, *Oh, *concat;
     if (B < 0 || n_q < 0 || n_k < 0 || d_model <= 0 || h <= 0 || d_k <= 0 || d_v <= 0) return -1;
-#ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
-#endif
     Q = (double *)malloc(sizeof(double) * (qsz ? qsz : 1));
     Kp = (double *)malloc(sizeof(double) * (ksz ? ksz : 1));
     Vp = (double *)malloc(sizeof(double) * (vsz ? vsz : 1));
@@ -301,9 +309,9 @@ int oracle_mha(const double *x_q, const double *x_kv, const double *w_q, const d
     concat = (double *)malloc(sizeof(double) * (osz ? osz : 1));
 
     /* projections of all positions at once */
-    matmul(x_q, w_q, Q, B * n_q, h * d_k, d_model);
-    matmul(x_kv, w_k, Kp, B * n_k, h * d_k, d_model);
-    matmul(x_kv, w_v, Vp, B * n_k, h * d_v, d_model);
+    matmul(x_q, w_q, Q, B * n_q, h * d_k, d_model, nthreads);
+    matmul(x_kv, w_k, Kp, B * n_k, h * d_k, d_model, nthreads);
+    matmul(x_kv, w_v, Vp, B * n_k, h * d_v, d_model, nthreads);
 
     /* head split: head hh takes column block hh of each projection */
     for (b = 0; b < B; ++b)
@@ -335,7 +343,7 @@ int oracle_mha(const double *x_q, const double *x_kv, const double *w_q, const d
                             Oh[(((size_t)b * h + hh) * n_q + i) * d_v + c];
         if (concat_out)
             for (size_t t = 0; t < osz; ++t) concat_out[t] = concat[t];
-        matmul(concat, w_o, out, B * n_q, d_model, h * d_v);
+        matmul(concat, w_o, out, B * n_q, d_model, h * d_v, nthreads);
     }
 
     free(Q); free(Kp); free(Vp); free(Qh); free(Kh); free(Vh); free(Oh); free(concat);

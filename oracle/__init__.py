@@ -59,6 +59,12 @@ def _load():
             lib.oracle_mha.restype = ci
             lib.oracle_decode.argtypes = [dp, dp, dp, dp, ci, ci, ci, ci, ci, ci, ip, cd, ci]
             lib.oracle_decode.restype = ci
+            lib.oracle_layernorm.argtypes = [dp, dp, dp, dp, ci, ci, cd]
+            lib.oracle_layernorm.restype = None
+            lib.oracle_ffn.argtypes = [dp, dp, dp, dp, dp, dp, ci, ci, ci, ci]
+            lib.oracle_ffn.restype = ci
+            lib.oracle_encoder_layer.argtypes = [dp] * 15 + [ci] * 7 + [ip, cd, cd, ci]
+            lib.oracle_encoder_layer.restype = ci
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ci
             _lib = lib
@@ -199,3 +205,55 @@ def mha(x_q, x_kv, w_q, w_k, w_v, w_o, h: int, mask_kind: int = MASK_NONE, kv_le
     if rc != 0:
         raise ValueError("oracle_mha rejected its arguments")
     return (out, concat) if return_concat else out
+
+
+def layernorm(x, gamma, beta, eps: float):
+    """gamma (x - mu) / sqrt(var + eps) + beta over the last axis (population variance)."""
+    x = _f64(x)
+    d = x.shape[-1]
+    gamma, beta = _f64(gamma), _f64(beta)
+    assert gamma.shape == (d,) and beta.shape == (d,)
+    out = np.empty_like(x)
+    _load().oracle_layernorm(_dp(x), _dp(gamma), _dp(beta), _dp(out), int(x.size // d), d,
+                             float(eps))
+    return out
+
+
+def ffn(x, w_1, b_1, w_2, b_2, nthreads: int = 0):
+    """FFN(x) = max(0, x W_1 + b_1) W_2 + b_2 over the last axis of x."""
+    x = _f64(x)
+    d_model = x.shape[-1]
+    w_1, b_1, w_2, b_2 = _f64(w_1), _f64(b_1), _f64(w_2), _f64(b_2)
+    d_ff = w_1.shape[1]
+    assert w_1.shape == (d_model, d_ff) and b_1.shape == (d_ff,)
+    assert w_2.shape == (d_ff, d_model) and b_2.shape == (d_model,)
+    out = np.empty_like(x)
+    rc = _load().oracle_ffn(_dp(x), _dp(w_1), _dp(b_1), _dp(w_2), _dp(b_2), _dp(out),
+                            int(x.size // d_model), d_model, d_ff, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_ffn rejected its arguments")
+    return out
+
+
+def encoder_layer(x, w_q, w_k, w_v, w_o, g_1, be_1, w_1, b_1, w_2, b_2, g_2, be_2, h: int,
+                  mask_kind: int = MASK_NONE, kv_lens=None, scale: float | None = None,
+                  eps: float = 1e-6, return_mid: bool = False, nthreads: int = 0):
+    """LayerNorm_2(y + FFN(y)) with y = LayerNorm_1(x + MultiHead(x, x)); x [B, n, d_model]."""
+    x = _f64(x)
+    B, n, d_model = x.shape
+    args = [_f64(a) for a in (w_q, w_k, w_v, w_o, g_1, be_1, w_1, b_1, w_2, b_2, g_2, be_2)]
+    d_k = args[0].shape[1] // h
+    d_ff = args[6].shape[1]
+    if scale is None or scale == 0.0:
+        scale = default_scale(d_k)
+    lens = None
+    if mask_kind & MASK_KEY_PADDING:
+        lens = np.ascontiguousarray(np.asarray(kv_lens, dtype=np.int32))
+    out = np.zeros_like(x)
+    mid = np.zeros_like(x) if return_mid else None
+    rc = _load().oracle_encoder_layer(_dp(x), *[_dp(a) for a in args], _dp(out), _dp(mid), B, n,
+                                      d_model, h, d_k, d_ff, int(mask_kind), _ip(lens),
+                                      float(scale), float(eps), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_encoder_layer rejected its arguments")
+    return (out, mid) if return_mid else out

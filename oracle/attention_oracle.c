@@ -32,6 +32,12 @@
  *     Is All You Need", section 3.7 "Inference — auto-regressive 디코딩"):
  *     with L valid cache rows the n_q new tokens sit at positions
  *     L - n_q .. L - 1, and the causal rule (key j <= query position) applies;
+ *   - the encoder sub-layers: output = LayerNorm(x + Sublayer(x)) (post-LN),
+ *     LayerNorm(x) = gamma (x - mu) / sqrt(sigma^2 + eps) + beta over one
+ *     token's features ("[논문 리뷰]Attention Is All You Need", section 3.1;
+ *     "Attention Is All You Need 해부", section "4. residual connection과
+ *     LayerNorm은 깊은 층을 학습 가능하게 한다"), and
+ *     FFN(x) = max(0, x W_1 + b_1) W_2 + b_2 ("[논문 리뷰]", section 3.3);
  *   - MultiHead(Q,K,V) = Concat(head_1..head_h) W^O,
  *     head_i = Attention(Q W_i^Q, K W_i^K, V W_i^V), with the per-head matrices
  *     being column block i of one [d_model, h*d] matrix
@@ -347,6 +353,90 @@ int oracle_mha(const double *x_q, const double *x_kv, const double *w_q, const d
     }
 
     free(Q); free(Kp); free(Vp); free(Qh); free(Kh); free(Vh); free(Oh); free(concat);
+    return rc;
+}
+
+/*
+ * LayerNorm over the last axis: out[r] = gamma * (x[r] - mu) / sqrt(var + eps)
+ * + beta, mu and var (the population variance) over the d features of row r.
+ * x may alias out.
+ */
+void oracle_layernorm(const double *x, const double *gamma, const double *beta, double *out,
+                      int rows, int d, double eps)
+{
+    int r, c;
+    for (r = 0; r < rows; ++r) {
+        const double *xr = x + (size_t)r * d;
+        double mu = 0.0, var = 0.0, inv;
+        for (c = 0; c < d; ++c) mu += xr[c];
+        mu /= d;
+        for (c = 0; c < d; ++c) var += (xr[c] - mu) * (xr[c] - mu);
+        var /= d;
+        inv = 1.0 / sqrt(var + eps);
+        for (c = 0; c < d; ++c) out[(size_t)r * d + c] = gamma[c] * (xr[c] - mu) * inv + beta[c];
+    }
+}
+
+/* FFN(x) = max(0, x W_1 + b_1) W_2 + b_2 for rows x [rows, d_model];
+ * w_1 [d_model, d_ff], w_2 [d_ff, d_model]; out [rows, d_model]. */
+int oracle_ffn(const double *x, const double *w_1, const double *b_1, const double *w_2,
+               const double *b_2, double *out, int rows, int d_model, int d_ff, int nthreads)
+{
+    int r, c;
+    double *hid;
+    if (rows < 0 || d_model <= 0 || d_ff <= 0) return -1;
+    hid = (double *)malloc(sizeof(double) * ((size_t)rows * d_ff ? (size_t)rows * d_ff : 1));
+    matmul(x, w_1, hid, rows, d_ff, d_model, nthreads);
+    for (r = 0; r < rows; ++r)
+        for (c = 0; c < d_ff; ++c) {
+            double v = hid[(size_t)r * d_ff + c] + b_1[c];
+            hid[(size_t)r * d_ff + c] = v > 0.0 ? v : 0.0;
+        }
+    matmul(hid, w_2, out, rows, d_model, d_ff, nthreads);
+    for (r = 0; r < rows; ++r)
+        for (c = 0; c < d_model; ++c) out[(size_t)r * d_model + c] += b_2[c];
+    free(hid);
+    return 0;
+}
+
+/*
+ * One encoder layer (self-attention sub-layer, then the feed-forward one,
+ * each wrapped as LayerNorm(x + Sublayer(x))):
+ *   y   = LayerNorm_1(x + MultiHead(x, x))
+ *   out = LayerNorm_2(y + FFN(y))
+ * x [B, n, d_model]; the attention weights and mask as oracle_mha; LayerNorm
+ * parameters [d_model]; FFN as oracle_ffn. y_out (nullable) receives y.
+ */
+int oracle_encoder_layer(const double *x, const double *w_q, const double *w_k,
+                         const double *w_v, const double *w_o, const double *g_1,
+                         const double *be_1, const double *w_1, const double *b_1,
+                         const double *w_2, const double *b_2, const double *g_2,
+                         const double *be_2, double *out, double *y_out, int B, int n,
+                         int d_model, int h, int d_k, int d_ff, int mask_kind,
+                         const int32_t *kv_lens, double scale, double eps, int nthreads)
+{
+    size_t rows = (size_t)B * n, t;
+    size_t sz = rows * d_model;
+    double *att, *y, *f;
+    int rc;
+    if (B < 0 || n < 0 || d_model <= 0 || h <= 0 || d_k <= 0 || d_ff <= 0) return -1;
+    att = (double *)malloc(sizeof(double) * (sz ? sz : 1));
+    y = (double *)malloc(sizeof(double) * (sz ? sz : 1));
+    f = (double *)malloc(sizeof(double) * (sz ? sz : 1));
+    rc = oracle_mha(x, x, w_q, w_k, w_v, w_o, att, NULL, B, n, n, d_model, h, d_k, d_k,
+                    mask_kind, kv_lens, scale, nthreads);
+    if (rc == 0) {
+        for (t = 0; t < sz; ++t) y[t] = x[t] + att[t];
+        oracle_layernorm(y, g_1, be_1, y, (int)rows, d_model, eps);
+        if (y_out)
+            for (t = 0; t < sz; ++t) y_out[t] = y[t];
+        rc = oracle_ffn(y, w_1, b_1, w_2, b_2, f, (int)rows, d_model, d_ff, nthreads);
+    }
+    if (rc == 0) {
+        for (t = 0; t < sz; ++t) f[t] += y[t];
+        oracle_layernorm(f, g_2, be_2, out, (int)rows, d_model, eps);
+    }
+    free(att); free(y); free(f);
     return rc;
 }
 

@@ -536,3 +536,115 @@ def test_decode_matches_torch_fp64_sdpa_with_bottom_right_causal_mask():
                                              torch.from_numpy(v[b:b + 1, :, :L]),
                                              attn_mask=allowed).numpy()
         np.testing.assert_allclose(ours[b:b + 1], ref, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- encoder sub-layers
+# "[논문 리뷰]Attention Is All You Need", sections 3.1 (output = LayerNorm(x +
+# Sublayer(x))) and 3.3 (FFN(x) = max(0, x W_1 + b_1) W_2 + b_2);
+# "Attention Is All You Need 해부", section "4. residual connection과
+# LayerNorm": LayerNorm(x) = gamma (x - mu) / sqrt(sigma^2 + eps) + beta over
+# one token's features.
+
+def test_layernorm_rows_have_zero_mean_and_the_eps_shrunk_unit_variance():
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((7, 33)) * 3.0 + 5.0
+    eps = 1e-3
+    out = oracle.layernorm(x, np.ones(33), np.zeros(33), eps)
+    np.testing.assert_allclose(out.mean(axis=1), 0.0, atol=1e-13)
+    var = x.var(axis=1)
+    np.testing.assert_allclose(out.var(axis=1), var / (var + eps), rtol=1e-12)
+
+
+def test_layernorm_constant_row_gives_beta_and_gamma_beta_are_affine():
+    rng = np.random.default_rng(42)
+    d = 16
+    gamma, beta = rng.standard_normal(d), rng.standard_normal(d)
+    const = np.full((2, d), 3.25)
+    np.testing.assert_allclose(oracle.layernorm(const, gamma, beta, 1e-6), np.broadcast_to(beta, (2, d)),
+                               atol=1e-15)
+    x = rng.standard_normal((5, d))
+    plain = oracle.layernorm(x, np.ones(d), np.zeros(d), 1e-6)
+    np.testing.assert_allclose(oracle.layernorm(x, gamma, beta, 1e-6), plain * gamma + beta,
+                               rtol=0, atol=1e-14)
+
+
+def test_ffn_with_identity_weights_is_relu_of_the_shifted_input():
+    """W_1 = W_2 = I, b_2 = 0: FFN(x) = max(0, x + b_1) (the max(0, .) of the
+    formula, not a smooth activation; an off-by-one bias or a missing ReLU fails)."""
+    rng = np.random.default_rng(43)
+    d = 12
+    x = rng.standard_normal((6, d))
+    b_1 = rng.standard_normal(d) * 0.5
+    out = oracle.ffn(x, np.eye(d), b_1, np.eye(d), np.zeros(d))
+    np.testing.assert_allclose(out, np.maximum(0.0, x + b_1), rtol=0, atol=1e-15)
+
+
+def test_ffn_and_layernorm_match_torch_fp64():
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    rng = np.random.default_rng(44)
+    x = rng.standard_normal((3, 5, 32))
+    w_1, b_1 = rng.standard_normal((32, 128)) * 0.2, rng.standard_normal(128) * 0.1
+    w_2, b_2 = rng.standard_normal((128, 32)) * 0.2, rng.standard_normal(32) * 0.1
+    t = torch.from_numpy
+    ref = F.linear(F.relu(F.linear(t(x), t(w_1.T.copy()), t(b_1))), t(w_2.T.copy()), t(b_2))
+    np.testing.assert_allclose(oracle.ffn(x, w_1, b_1, w_2, b_2), ref.numpy(), rtol=1e-12,
+                               atol=1e-12)
+    g, b = rng.standard_normal(32), rng.standard_normal(32)
+    ref = F.layer_norm(t(x), (32,), t(g), t(b), eps=1e-5)
+    np.testing.assert_allclose(oracle.layernorm(x, g, b, 1e-5), ref.numpy(), rtol=1e-12,
+                               atol=1e-12)
+
+
+def _encoder_case(seed, B=2, n=7, d_model=16, h=4, d_ff=32):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((B, n, d_model))
+    ws = [rng.standard_normal((d_model, d_model)) * 0.3 for _ in range(4)]
+    g_1, be_1 = 1 + 0.1 * rng.standard_normal(d_model), 0.1 * rng.standard_normal(d_model)
+    w_1, b_1 = rng.standard_normal((d_model, d_ff)) * 0.3, 0.1 * rng.standard_normal(d_ff)
+    w_2, b_2 = rng.standard_normal((d_ff, d_model)) * 0.3, 0.1 * rng.standard_normal(d_model)
+    g_2, be_2 = 1 + 0.1 * rng.standard_normal(d_model), 0.1 * rng.standard_normal(d_model)
+    return x, ws, (g_1, be_1, w_1, b_1, w_2, b_2, g_2, be_2), h
+
+
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_KEY_PADDING])
+def test_encoder_layer_is_two_post_ln_sublayers(mask):
+    x, ws, p, h = _encoder_case(45)
+    g_1, be_1, w_1, b_1, w_2, b_2, g_2, be_2 = p
+    lens = np.array([7, 3], dtype=np.int32)
+    out, y = oracle.encoder_layer(x, *ws, *p, h, mask, kv_lens=lens, eps=1e-6, return_mid=True)
+    att = oracle.mha(x, x, *ws, h, mask, kv_lens=lens)
+    np.testing.assert_allclose(y, oracle.layernorm(x + att, g_1, be_1, 1e-6), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(out, oracle.layernorm(y + oracle.ffn(y, w_1, b_1, w_2, b_2), g_2,
+                                                     be_2, 1e-6), rtol=0, atol=1e-13)
+
+
+def test_encoder_layer_matches_torch_transformer_encoder_layer():
+    """torch's post-LN TransformerEncoderLayer (ReLU, no dropout, zero
+    attention biases) with the same weights, in fp64."""
+    torch = pytest.importorskip("torch")
+    x, ws, p, h = _encoder_case(46)
+    g_1, be_1, w_1, b_1, w_2, b_2, g_2, be_2 = p
+    d_model, d_ff = x.shape[2], w_1.shape[1]
+    layer = torch.nn.TransformerEncoderLayer(d_model, h, d_ff, dropout=0.0, activation="relu",
+                                             layer_norm_eps=1e-6, batch_first=True,
+                                             norm_first=False, dtype=torch.float64)
+    t = torch.from_numpy
+    with torch.no_grad():
+        layer.self_attn.in_proj_weight.copy_(t(np.concatenate([w.T for w in ws[:3]], axis=0)))
+        layer.self_attn.in_proj_bias.zero_()
+        layer.self_attn.out_proj.weight.copy_(t(ws[3].T.copy()))
+        layer.self_attn.out_proj.bias.zero_()
+        layer.linear1.weight.copy_(t(w_1.T.copy()))
+        layer.linear1.bias.copy_(t(b_1))
+        layer.linear2.weight.copy_(t(w_2.T.copy()))
+        layer.linear2.bias.copy_(t(b_2))
+        layer.norm1.weight.copy_(t(g_1))
+        layer.norm1.bias.copy_(t(be_1))
+        layer.norm2.weight.copy_(t(g_2))
+        layer.norm2.bias.copy_(t(be_2))
+    layer.eval()
+    with torch.no_grad():
+        ref = layer(t(x)).numpy()
+    np.testing.assert_allclose(oracle.encoder_layer(x, *ws, *p, h, eps=1e-6), ref, rtol=1e-10,
+                               atol=1e-10)

@@ -70,6 +70,12 @@ WORKLOADS = {
                             desc="Transformer-big causal self-attention: B=8, h=16, n=1024, d=64"),
     "long": dict(kind="attn", B=4, h=16, n=4096, d=64, causal=False, seed=1004,
                  desc="long-context attention sweep point"),
+    "base_encoder_layer": dict(
+        kind="encoder", B=32, n=128, d_model=512, h=8, d_ff=2048, mask=MASK_KEY_PADDING,
+        kv_range=(64, 128), eps=1e-6, seed=1007,
+        desc="Transformer-base encoder layer, post-LN: LayerNorm(y + FFN(y)), y = LayerNorm(x "
+             "+ MultiHead(x)); B=32, n=128, d_model=512, h=8, d_ff=2048, key padding U[64,128]; "
+             "TFLOP/s over all of the layer's matrix FLOPs (projections, attention, FFN)"),
     "decode": dict(kind="decode", B=16, h=16, n_q=1, n_max=8192, d=64, len_range=(4096, 8192),
                    seed=1006,
                    desc="one decoding step against a key/value cache: B=16, h=16, d=64, one new "
@@ -527,6 +533,80 @@ class AttnCall:
         return 3 * self.a.q.nbytes, self.a.q.nbytes
 
 
+class EncoderCall:
+    """Device buffers of one encoder_layer_forward call over rotating sets."""
+
+    def __init__(self, tsd, cfg, nsets, seed_offset):
+        import torch
+        self.tsd, self.cfg = tsd, cfg
+        c = cfg
+        e = synthetic.encoder_inputs(c["seed"] + seed_offset, c["B"], c["n"], c["d_model"], c["h"],
+                                     c["d_ff"], c["mask"], c["kv_range"], add_pe=True)
+        self.e = e
+        m = e.mha
+        bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to("cuda").view(torch.bfloat16)
+        host = [m.x_q, m.w_q, m.w_k, m.w_v, m.w_o, e.ln1_gamma, e.ln1_beta, e.w_1, e.b_1, e.w_2,
+                e.b_2, e.ln2_gamma, e.ln2_beta]
+        self.wsb = tsd.encoder_layer_workspace_bytes(m.B, m.n_q, m.d_model, m.h, m.d_k, e.d_ff)
+        self.sets = []
+        for _ in range(nsets):
+            self.sets.append(dict(t=[bf(a) for a in host],
+                                  lens=torch.from_numpy(m.kv_lens).to("cuda"),
+                                  out=torch.empty((m.B, m.n_q, m.d_model), dtype=torch.bfloat16,
+                                                  device="cuda"),
+                                  ws=torch.empty(self.wsb, dtype=torch.uint8, device="cuda")))
+        self.h_x = torch.from_numpy(np.ascontiguousarray(m.x_q).view(np.int16)).pin_memory()
+        self.h_lens = torch.from_numpy(m.kv_lens).pin_memory()
+        self.h_out = torch.empty((m.B, m.n_q, m.d_model), dtype=torch.bfloat16).pin_memory()
+
+    @staticmethod
+    def set_bytes(cfg):
+        B, n, dm, ff = cfg["B"], cfg["n"], cfg["d_model"], cfg["d_ff"]
+        return 2 * (2 * B * n * dm + 4 * dm * dm + 2 * dm * ff) + B * n * (6 * dm + 2 * ff) * 2
+
+    def run(self, i, stream):
+        m, e, s = self.e.mha, self.e, self.sets[i % len(self.sets)]
+        self.tsd.encoder_layer_forward(*s["t"], s["out"], m.B, m.n_q, m.d_model, m.h, m.d_k,
+                                       e.d_ff, m.mask_kind, s["lens"], 0.0, self.cfg["eps"],
+                                       s["ws"], self.wsb, stream)
+
+    def run_stage(self, k, i, stream):
+        self.run(i, stream)
+
+    def stage_names(self):
+        return ["encoder_layer"]
+
+    def stage_work(self):
+        m, e = self.e.mha, self.e
+        rows = m.B * m.n_q
+        f = 2.0 * rows * m.d_model * (4 * m.h * m.d_k) + 4.0 * rows * m.d_model * e.d_ff
+        f += attn_flops(m.B, m.h, m.n_q, m.n_k, m.d_k, False)
+        b = 2.0 * (2 * rows * m.d_model + 4 * m.d_model * m.h * m.d_k + 2 * m.d_model * e.d_ff)
+        return [(f, b)]
+
+    def metric_flops(self):
+        return self.stage_work()[0][0]
+
+    def useful_flops(self):
+        return self.metric_flops()
+
+    def launches(self):
+        m = self.e.mha
+        return self.tsd.mha_forward_launches(m.B, m.n_q, m.n_k, m.d_model, m.h, m.d_k, m.d_v,
+                                             True) + 4
+
+    def e2e_run(self, i, stream):
+        s = self.sets[i % len(self.sets)]
+        s["t"][0].view(torch_int16()).copy_(self.h_x, non_blocking=True)
+        s["lens"].copy_(self.h_lens, non_blocking=True)
+        self.run(i, stream)
+        self.h_out.copy_(s["out"], non_blocking=True)
+
+    def e2e_bytes(self):
+        m = self.e.mha
+        return m.x_q.nbytes + m.kv_lens.nbytes, m.B * m.n_q * m.d_model * 2
+
+
 class DecodeCall:
     """Device buffers of one attn_decode call (queries, the cache, lengths,
     workspace) over rotating sets."""
@@ -611,10 +691,11 @@ def torch_int16():
 
 def make_calls(tsd, wl, args, seed_offset):
     spec = WORKLOADS[wl]
-    if spec["kind"] == "decode":
-        per_set = DecodeCall.set_bytes(spec)
+    if spec["kind"] in ("decode", "encoder"):
+        cls = DecodeCall if spec["kind"] == "decode" else EncoderCall
+        per_set = cls.set_bytes(spec)
         nsets = max(2, math.ceil(2.2 * L2_BYTES / per_set))
-        return [DecodeCall(tsd, spec, nsets, seed_offset)], nsets, per_set
+        return [cls(tsd, spec, nsets, seed_offset)], nsets, per_set
     if spec["kind"] == "mha":
         cfgs = spec["calls"]
         probe = [MhaCall(tsd, c, 1, seed_offset) for c in cfgs]
@@ -643,6 +724,9 @@ def workload_config(wl, calls, args, nsets, per_set):
     elif spec["kind"] == "decode":
         cfg.update({k: spec[k] for k in ("B", "h", "n_q", "n_max", "d")})
         cfg["len_range"] = list(spec["len_range"])
+    elif spec["kind"] == "encoder":
+        cfg.update({k: spec[k] for k in ("B", "n", "d_model", "h", "d_ff", "eps")})
+        cfg["kv_range"] = list(spec["kv_range"])
     else:
         a = calls[0].a
         cfg.update(B=a.B, h=a.h, n=a.n_q, d=a.d_k, causal=bool(a.mask_kind & MASK_CAUSAL))
@@ -825,6 +909,21 @@ def oracle_sample_runner(args):
             for m, f64 in ms:
                 oracle.mha(*f64, m.h, m.mask_kind, kv_lens=m.kv_lens, nthreads=nthreads)
         return run, flops, "the whole batch through oracle.mha (projections, attention, W_O)"
+    if spec["kind"] == "encoder":
+        nb = 4  # the first four sequences of the batch
+        e = synthetic.encoder_inputs(spec["seed"], nb, spec["n"], spec["d_model"], spec["h"],
+                                     spec["d_ff"], spec["mask"], spec["kv_range"], add_pe=True)
+        m = e.mha
+        x, _, wq, wk, wv, wo = m.as_f64()
+        params = e.params_f64()
+        rows = nb * m.n_q
+        flops = 2.0 * rows * m.d_model * 4 * m.h * m.d_k + 4.0 * rows * m.d_model * e.d_ff
+        flops += attn_flops(nb, m.h, m.n_q, m.n_k, m.d_k, False)
+
+        def run(nthreads=0):
+            oracle.encoder_layer(x, wq, wk, wv, wo, *params, m.h, m.mask_kind, kv_lens=m.kv_lens,
+                                 eps=spec["eps"], nthreads=nthreads)
+        return run, flops, f"{nb} sequences of the batch through oracle.encoder_layer"
     if spec["kind"] == "decode":
         B, h, n_q, n_max, d = (spec[k] for k in ("B", "h", "n_q", "n_max", "d"))
         nb = 2  # every head of the first two sequences

@@ -82,6 +82,43 @@ attn_status attn_forward(const void *q, const void *k, const void *v, void *out,
                          tsd_stream_t stream);
 
 /*
+ * encoder_layer_forward -- one Transformer encoder layer, both sub-layers
+ * wrapped post-LN as output = LayerNorm(x + Sublayer(x)) ("[논문 리뷰]
+ * Attention Is All You Need" (kimjiil.github.io), sections 3.1 and 3.3;
+ * LayerNorm(v) = gamma (v - mu) / sqrt(sigma^2 + eps) + beta over one token's
+ * d_model features, "Attention Is All You Need 해부" (sj-techlog), section
+ * "4. residual connection과 LayerNorm"):
+ *   y   = LayerNorm_1(x + MultiHead(x, x))            (mha_forward, self-attention)
+ *   out = LayerNorm_2(y + FFN(y)),  FFN(y) = max(0, y W_1 + b_1) W_2 + b_2
+ *   x, out   [B, n, d_model] bf16, device; d_model in {256, 512, 1024, 2048}
+ *            (else ATTN_ERR_UNSUPPORTED)
+ *   w_q, w_k, w_v, w_o: as mha_forward with d_v = d_k (d_model x h*d_k, h*d_k x d_model)
+ *   ln1_gamma, ln1_beta, ln2_gamma, ln2_beta: [d_model] bf16
+ *   w_1 [d_model, d_ff], b_1 [d_ff], w_2 [d_ff, d_model], b_2 [d_model], bf16;
+ *   d_ff a multiple of 8
+ *   mask_kind, kv_lens, scale: as mha_forward (self-attention, n_q = n_k = n)
+ *   eps: LayerNorm's epsilon (> 0; the pages do not give a value)
+ *   workspace: device, 256-byte aligned, >= encoder_layer_workspace_bytes(...)
+ *   bytes; scratch (it holds mha_forward's workspace, the attention output,
+ *   y, the FFN's hidden layer and y + FFN(y)).
+ * Errors: as mha_forward; eps <= 0 -> ATTN_ERR_INVALID. Launches: mha_forward's
+ * plus four (LayerNorm, the two FFN GEMMs with their bias / ReLU / residual
+ * epilogues, LayerNorm).
+ */
+size_t encoder_layer_workspace_bytes(int B, int n, int d_model, int h, int d_k, int d_ff);
+attn_status encoder_layer_forward(const void *x,
+                                  const void *w_q, const void *w_k, const void *w_v,
+                                  const void *w_o,
+                                  const void *ln1_gamma, const void *ln1_beta,
+                                  const void *w_1, const void *b_1,
+                                  const void *w_2, const void *b_2,
+                                  const void *ln2_gamma, const void *ln2_beta,
+                                  void *out,
+                                  int B, int n, int d_model, int h, int d_k, int d_ff,
+                                  int mask_kind, const int32_t *kv_lens, float scale, float eps,
+                                  void *workspace, size_t workspace_bytes, tsd_stream_t stream);
+
+/*
  * attn_decode -- one decoding step against a key/value cache ("Attention Is
  * All You Need 해부" (sj-techlog), section "KV cache는 추론의 같은 계산을
  * 반복하지 않게 한다"; "[논문 리뷰]Attention Is All You Need"

@@ -23,7 +23,8 @@ import numpy as np
 
 __all__ = [
     "f32_to_bf16_bits", "bf16_bits_to_f64", "bf16_bits_to_f32", "normal_bf16",
-    "positional_encoding", "xavier_uniform_bf16", "uniform_lengths",
+    "positional_encoding", "xavier_uniform_bf16", "uniform_lengths", "encoder_inputs",
+    "EncoderInputs",
     "AttentionInputs", "MhaInputs", "attention_inputs", "mha_inputs",
 ]
 
@@ -185,3 +186,41 @@ def mha_inputs(seed: int, B: int, n_q: int, n_k: int, d_model: int, h: int, d_k:
         kv_lens = uniform_lengths(rng, B, lo, hi)
     return MhaInputs(x_q, x_kv, w_q, w_k, w_v, w_o, B, n_q, n_k, d_model, h, d_k, d_v,
                      mask_kind, kv_lens, self_attention)
+
+
+@dataclasses.dataclass
+class EncoderInputs:
+    """One encoder layer's inputs (bf16 bits): the attention part as MhaInputs
+    (self-attention), LayerNorm gains/offsets and the FFN weights/biases."""
+    mha: MhaInputs
+    ln1_gamma: np.ndarray
+    ln1_beta: np.ndarray
+    w_1: np.ndarray
+    b_1: np.ndarray
+    w_2: np.ndarray
+    b_2: np.ndarray
+    ln2_gamma: np.ndarray
+    ln2_beta: np.ndarray
+    d_ff: int
+
+    def params_f64(self):
+        return [bf16_bits_to_f64(a) for a in (self.ln1_gamma, self.ln1_beta, self.w_1, self.b_1,
+                                              self.w_2, self.b_2, self.ln2_gamma, self.ln2_beta)]
+
+
+def encoder_inputs(seed: int, B: int, n: int, d_model: int, h: int, d_ff: int,
+                   mask_kind: int = MASK_NONE, kv_len_range=None, add_pe: bool = False) -> EncoderInputs:
+    """x ~ N(0,1) (+ PE), Xavier-uniform W_Q/K/V/O and W_1/W_2; biases ~ U(-0.1, 0.1);
+    LayerNorm gains ~ 1 + U(-0.1, 0.1) and offsets ~ U(-0.1, 0.1) (the pages give
+    no initialisation for these)."""
+    d_k = d_model // h
+    m = mha_inputs(seed, B, n, n, d_model, h, d_k, d_k, mask_kind, kv_len_range, add_pe=add_pe)
+    rng = np.random.default_rng(seed + 7919)
+
+    def small(k, centre=0.0):
+        return f32_to_bf16_bits((centre + rng.uniform(-0.1, 0.1, size=k)).astype(np.float32))
+
+    return EncoderInputs(m, small(d_model, 1.0), small(d_model),
+                         xavier_uniform_bf16(rng, d_model, d_ff), small(d_ff),
+                         xavier_uniform_bf16(rng, d_ff, d_model), small(d_model),
+                         small(d_model, 1.0), small(d_model), d_ff)

@@ -197,3 +197,24 @@ def test_attn_decode_workspace_grows_with_chunks_queries_and_width(lib):
     assert f(1, 1, 1, 256, 64) < f(1, 1, 1, 257, 64)   # a second 256-key chunk
     assert f(2, 3, 4, 1000, 128) >= 2 * 3 * 4 * 4 * (128 + 2) * 4
     assert f(1, 1, 0, 100, 64) == 0 and f(1, 1, 9, 100, 64) == 0
+
+
+def test_encoder_layer_rejects_bad_arguments(lib):
+    B, n, dm, h, d, ff = 2, 16, 512, 8, 64, 2048
+    wsb = tsd.encoder_layer_workspace_bytes(B, n, dm, h, d, ff)
+    assert wsb > tsd.mha_workspace_bytes(B, n, n, h, d, d)
+    # 14 tensors, B, n, d_model, h, d_k, d_ff, mask, lens, scale, eps, workspace, bytes, stream
+    base = [FAKE] * 14 + [B, n, dm, h, d, ff, 0, None, 0.0, 1e-6, FAKE, wsb, None]
+
+    def with_(i, v):
+        args = list(base)
+        args[i] = v
+        return lib.encoder_layer_forward(*args)
+    assert with_(16, 384) == tsd.ATTN_ERR_UNSUPPORTED   # d_model without a LayerNorm kernel
+    assert with_(19, 2044) == tsd.ATTN_ERR_INVALID      # d_ff not a multiple of 8
+    assert with_(23, 0.0) == tsd.ATTN_ERR_INVALID       # eps
+    assert with_(23, -1.0) == tsd.ATTN_ERR_INVALID
+    assert with_(25, wsb - 1) == tsd.ATTN_ERR_INVALID   # short workspace
+    assert with_(24, FAKE + 16) == tsd.ATTN_ERR_INVALID  # workspace not 256-byte aligned
+    assert with_(7, None) == tsd.ATTN_ERR_INVALID       # no W_1
+    assert with_(18, 96) == tsd.ATTN_ERR_UNSUPPORTED    # head size

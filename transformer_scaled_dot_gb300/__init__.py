@@ -24,7 +24,8 @@ __all__ = [
     "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
     "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out", "mha_forward_noalloc",
     "mha_concat_heads", "mha_forward_launches", "attn_forward_window", "attn_decode",
-    "attn_decode_workspace_bytes", "MHA_NOALLOC_SCRATCH_BYTES",
+    "attn_decode_workspace_bytes", "encoder_layer_forward", "encoder_layer_workspace_bytes",
+    "MHA_NOALLOC_SCRATCH_BYTES",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = range(5)
@@ -35,7 +36,7 @@ EXPORTED_SYMBOLS = (
     "mha_forward", "attn_get_device_status", "attn_last_cuda_error", "attn_status_string",
     "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out", "mha_forward_noalloc",
     "mha_concat_heads", "mha_forward_launches", "attn_forward_window", "attn_decode",
-    "attn_decode_workspace_bytes",
+    "attn_decode_workspace_bytes", "encoder_layer_forward", "encoder_layer_workspace_bytes",
 )
 
 # TSD_MHA_NOALLOC_SCRATCH_BYTES of the header: the fixed scratch of mha_forward_noalloc
@@ -93,10 +94,14 @@ def library():
     lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i]
     lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_decode.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp, f, vp, ctypes.c_size_t, st]
+    lib.encoder_layer_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    lib.encoder_layer_workspace_bytes.restype = ctypes.c_size_t
+    lib.encoder_layer_forward.argtypes = [vp] * 14 + [i] * 7 + [vp, f, f, vp, ctypes.c_size_t, st]
     for name in ("attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_forward",
                  "attn_get_device_status", "attn_last_cuda_error", "attn_selftest_wait_timeout",
                  "mha_project_qkv", "mha_project_out", "mha_forward_noalloc", "mha_concat_heads",
-                 "mha_forward_launches", "attn_forward_window", "attn_decode"):
+                 "mha_forward_launches", "attn_forward_window", "attn_decode",
+                 "encoder_layer_forward"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -151,6 +156,23 @@ def attn_decode(q, k_cache, v_cache, out, B, h, n_q, n_max, d_k, d_v, cache_lens
     _check(library().attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), B, h, n_q,
                                  n_max, d_k, d_v, _ptr(cache_lens), scale, _ptr(workspace),
                                  workspace_bytes, _stream(stream)), "attn_decode")
+
+
+def encoder_layer_workspace_bytes(B, n, d_model, h, d_k, d_ff) -> int:
+    return int(library().encoder_layer_workspace_bytes(B, n, d_model, h, d_k, d_ff))
+
+
+def encoder_layer_forward(x, w_q, w_k, w_v, w_o, ln1_gamma, ln1_beta, w_1, b_1, w_2, b_2,
+                          ln2_gamma, ln2_beta, out, B, n, d_model, h, d_k, d_ff,
+                          mask_kind=ATTN_MASK_NONE, kv_lens=None, scale=0.0, eps=1e-6,
+                          workspace=None, workspace_bytes=0, stream=None):
+    """LayerNorm_2(y + FFN(y)), y = LayerNorm_1(x + MultiHead(x, x)) (post-LN encoder layer)."""
+    ptrs = [_ptr(t) for t in (x, w_q, w_k, w_v, w_o, ln1_gamma, ln1_beta, w_1, b_1, w_2, b_2,
+                              ln2_gamma, ln2_beta, out)]
+    _check(library().encoder_layer_forward(*ptrs, B, n, d_model, h, d_k, d_ff, mask_kind,
+                                           _ptr(kv_lens), scale, eps, _ptr(workspace),
+                                           workspace_bytes, _stream(stream)),
+           "encoder_layer_forward")
 
 
 def attn_forward_strided(q, q_sb, q_sh, q_sr, k, k_sb, k_sh, k_sr, v, v_sb, v_sh, v_sr,

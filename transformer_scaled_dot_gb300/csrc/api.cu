@@ -397,6 +397,66 @@ attn_status launch_out_proj(const void* concat, const void* w_o, void* out, int 
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
+// Workspace of attn_decode: the chunk partials O (float) then (m, l) pairs.
+bool decode_layout(int B, int h, int n_q, int n_max, int d, size_t* o_bytes, size_t* total) {
+  if (B < 0 || h < 0 || n_q < 1 || n_q > tsd::kDecodeMaxQueries || n_max < 1 || d < 1)
+    return false;
+  const uint64_t rows = uint64_t(B) * h * tsd::decode_chunks(n_max) * n_q;
+  const uint64_t ob = align256(rows * d * 4), mb = align256(rows * 2 * 4);
+  if (ob + mb > (uint64_t(1) << 62)) return false;
+  *o_bytes = ob;
+  *total = ob + mb;
+  return true;
+}
+
+// Workspace of encoder_layer_forward: mha_forward's own, then the attention
+// output, y = LayerNorm_1(x + attention) in bf16 (the FFN's input) and fp32
+// (its residual), the FFN's hidden layer and z = y + FFN(y) in fp32.
+struct EncoderLayout {
+  size_t mha_bytes, a_off, y_off, y32_off, hid_off, z_off, total;
+};
+
+bool encoder_layout(int B, int n, int d_model, int h, int d_k, int d_ff, EncoderLayout* L) {
+  if (B < 0 || n < 0 || d_model <= 0 || h <= 0 || d_k <= 0 || d_ff <= 0) return false;
+  MhaLayout M;
+  if (!mha_layout(B, n, n, h, d_k, d_k, &M)) return false;
+  const uint64_t rows = uint64_t(B) * n;
+  L->mha_bytes = M.total;
+  L->a_off = align256(M.total);
+  L->y_off = L->a_off + align256(rows * d_model * 2);
+  L->y32_off = L->y_off + align256(rows * d_model * 2);
+  L->hid_off = L->y32_off + align256(rows * d_model * 4);
+  L->z_off = L->hid_off + align256(rows * uint64_t(d_ff) * 2);
+  L->total = L->z_off + align256(rows * d_model * 4);
+  return true;
+}
+
+// out = x W (+ bias, + residual, ReLU): one GEMM launch with the epilogue;
+// out is bf16, or fp32 when out_f32 (then the residual is fp32 too).
+attn_status launch_linear(const void* x, const void* w, const void* bias, const void* residual,
+                          bool relu, void* out, bool out_f32, int M, int N, int K,
+                          cudaStream_t stream) {
+  if (M == 0) return ATTN_OK;
+  tsd::GemmProblem g;
+  std::memset(&g, 0, sizeof(g));
+  g.K = K;
+  g.num_groups = 1;
+  cudaError_t e = make_gemm_group(&g.g[0], x, w, out, M, N, K);
+  if (e != cudaSuccess) return cuda_fail(e);
+  g.g[0].bias = static_cast<const uint16_t*>(bias);
+  if (out_f32) {
+    g.g[0].residual_f32 = static_cast<const float*>(residual);
+    g.g[0].c_f32 = static_cast<float*>(out);
+  } else {
+    g.g[0].residual = static_cast<const uint16_t*>(residual);
+  }
+  g.g[0].ldr = N;
+  g.g[0].relu = relu ? 1 : 0;
+  finish_gemm_problem(&g);
+  e = tsd::launch_gemm_bf16(g, stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -537,18 +597,6 @@ attn_status mha_forward(const void* x_q, const void* x_kv, const void* w_q, cons
   return launch_out_proj(O, w_o, out, B, n_q, d_model, h, d_v, stream);
 }
 
-// Workspace of attn_decode: the chunk partials O (float) then (m, l) pairs.
-bool decode_layout(int B, int h, int n_q, int n_max, int d, size_t* o_bytes, size_t* total) {
-  if (B < 0 || h < 0 || n_q < 1 || n_q > tsd::kDecodeMaxQueries || n_max < 1 || d < 1)
-    return false;
-  const uint64_t rows = uint64_t(B) * h * tsd::decode_chunks(n_max) * n_q;
-  const uint64_t ob = align256(rows * d * 4), mb = align256(rows * 2 * 4);
-  if (ob + mb > (uint64_t(1) << 62)) return false;
-  *o_bytes = ob;
-  *total = ob + mb;
-  return true;
-}
-
 size_t attn_decode_workspace_bytes(int B, int h, int n_q, int n_max, int d_v) {
   size_t ob = 0, total = 0;
   return decode_layout(B, h, n_q, n_max, d_v, &ob, &total) ? total : 0;
@@ -593,6 +641,71 @@ attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache,
   p.d = d_k;
   p.scale = resolve_scale(scale, d_k);
   e = tsd::launch_decode(p, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+size_t encoder_layer_workspace_bytes(int B, int n, int d_model, int h, int d_k, int d_ff) {
+  EncoderLayout L;
+  return encoder_layout(B, n, d_model, h, d_k, d_ff, &L) ? L.total : 0;
+}
+
+attn_status encoder_layer_forward(const void* x, const void* w_q, const void* w_k,
+                                  const void* w_v, const void* w_o, const void* ln1_gamma,
+                                  const void* ln1_beta, const void* w_1, const void* b_1,
+                                  const void* w_2, const void* b_2, const void* ln2_gamma,
+                                  const void* ln2_beta, void* out, int B, int n, int d_model,
+                                  int h, int d_k, int d_ff, int mask_kind,
+                                  const int32_t* kv_lens, float scale, float eps,
+                                  void* workspace, size_t workspace_bytes,
+                                  tsd_stream_t stream_) {
+  attn_status s = check_common(B, h, n, n, d_k, d_k, mask_kind, kv_lens, scale);
+  if (s != ATTN_OK) return s;
+  if (!(eps > 0.f) || !std::isfinite(eps)) return ATTN_ERR_INVALID;
+  if (d_model != 256 && d_model != 512 && d_model != 1024 && d_model != 2048)
+    return ATTN_ERR_UNSUPPORTED;
+  if (d_ff < 8 || (d_ff % 8) != 0) return ATTN_ERR_INVALID;
+  s = check_bf16_head_dims(d_k, d_k);
+  if (s != ATTN_OK) return s;
+  const void* ptrs[15] = {x, w_q, w_k, w_v, w_o, ln1_gamma, ln1_beta, w_1, b_1, w_2, b_2,
+                          ln2_gamma, ln2_beta, out, workspace};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID;
+  EncoderLayout L;
+  if (!encoder_layout(B, n, d_model, h, d_k, d_ff, &L)) return ATTN_ERR_INVALID;
+  if (workspace_bytes < L.total) return ATTN_ERR_INVALID;
+  const int64_t rows64 = int64_t(B) * n;
+  if (rows64 > INT32_MAX) return ATTN_ERR_INVALID;
+  const int rows = static_cast<int>(rows64);
+  if (rows == 0) return ATTN_OK;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint16_t* a = reinterpret_cast<uint16_t*>(ws + L.a_off);
+  uint16_t* y = reinterpret_cast<uint16_t*>(ws + L.y_off);
+  float* y32 = reinterpret_cast<float*>(ws + L.y32_off);
+  uint16_t* hid = reinterpret_cast<uint16_t*>(ws + L.hid_off);
+  float* z = reinterpret_cast<float*>(ws + L.z_off);
+  // 1. a = MultiHead(x, x)
+  s = mha_forward(x, x, w_q, w_k, w_v, w_o, a, B, n, n, d_model, h, d_k, d_k, mask_kind, kv_lens,
+                  scale, ws, L.mha_bytes, stream_);
+  if (s != ATTN_OK) return s;
+  // 2. y = LayerNorm_1(x + a): bf16 for the FFN's GEMM, fp32 for its residual
+  cudaError_t e = tsd::launch_add_layernorm(x, false, a,
+                                            static_cast<const uint16_t*>(ln1_gamma),
+                                            static_cast<const uint16_t*>(ln1_beta), y, y32, rows,
+                                            d_model, eps, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // 3. hid = max(0, y W_1 + b_1)
+  s = launch_linear(y, w_1, b_1, nullptr, true, hid, false, rows, d_ff, d_model, stream);
+  if (s != ATTN_OK) return s;
+  // 4. z = y + (hid W_2 + b_2), fp32
+  s = launch_linear(hid, w_2, b_2, y32, false, z, true, rows, d_model, d_ff, stream);
+  if (s != ATTN_OK) return s;
+  // 5. out = LayerNorm_2(z)
+  e = tsd::launch_add_layernorm(z, true, nullptr, static_cast<const uint16_t*>(ln2_gamma),
+                                static_cast<const uint16_t*>(ln2_beta),
+                                static_cast<uint16_t*>(out), nullptr, rows, d_model, eps,
+                                stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 

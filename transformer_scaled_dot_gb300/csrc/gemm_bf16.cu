@@ -2,7 +2,9 @@
 // tensor cores: Q = X_q W_Q, K = X_kv W_K, V = X_kv W_V in one grouped
 // launch, and Concat(head_1..head_h) W_O ("[논문 리뷰]Attention Is All You
 // Need" (kimjiil.github.io), section 3.2.2; weights in the x.W layout,
-// [d_model, h*d], no biases).
+// [d_model, h*d], no biases); and the two linear maps of the position-wise
+// feed-forward network (section 3.3), whose bias, ReLU and residual the
+// epilogue adds.
 //
 // Persistent kernel, optionally in clusters of CM CTAs stacked along M: a
 // cluster walks groups of CM vertically adjacent 128 x 128 output tiles that
@@ -66,6 +68,16 @@ struct GemmSmem {
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
+
+// acc[i] += the 8 bf16 of w (low half first)
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], uint4 w) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] += __uint_as_float(u[i] << 16);
+    acc[2 * i + 1] += __uint_as_float(u[i] & 0xffff0000u);
+  }
+}
 
 struct TileCoord {
   const GemmGroup* g;
@@ -255,12 +267,66 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&sm.acc_empty[acc]);  // the MMA warp may reuse this accumulator
+      {
+        // optional epilogue of a feed-forward layer: + bias, + residual, ReLU
+        const GemmGroup& G = *c.g;
+        if (G.bias != nullptr || G.residual != nullptr || G.residual_f32 != nullptr || G.relu) {
+          const int row = c.m0 + r;
+          const uint16_t* res_row =
+              (G.residual != nullptr && row < G.M) ? G.residual + row * G.ldr : nullptr;
+          const float* res32_row =
+              (G.residual_f32 != nullptr && row < G.M) ? G.residual_f32 + row * G.ldr : nullptr;
+#pragma unroll
+          for (int j8 = 0; j8 < kBN / 8; ++j8) {
+            const int col = c.n0 + j8 * 8;
+            float add[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (col < G.N) {
+              if (G.bias != nullptr) {
+                const uint4 w = __ldg(reinterpret_cast<const uint4*>(G.bias + col));
+                add_bf16x8(add, w);
+              }
+              if (res_row != nullptr) {
+                const uint4 w = __ldg(reinterpret_cast<const uint4*>(res_row + col));
+                add_bf16x8(add, w);
+              }
+              if (res32_row != nullptr) {
+                const float4 a = __ldg(reinterpret_cast<const float4*>(res32_row + col));
+                const float4 b = __ldg(reinterpret_cast<const float4*>(res32_row + col + 4));
+                add[0] += a.x; add[1] += a.y; add[2] += a.z; add[3] += a.w;
+                add[4] += b.x; add[5] += b.y; add[6] += b.z; add[7] += b.w;
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float x = __uint_as_float(v[j8 * 8 + i]) + add[i];
+              if (G.relu) x = fmaxf(x, 0.f);
+              v[j8 * 8 + i] = __float_as_uint(x);
+            }
+          }
+        }
+      }
 
       uint8_t* stage = sm.c[it % kCStages];
+      const bool out_f32 = c.g->c_f32 != nullptr;
+      if (out_f32) {
+        // fp32 output: each thread writes its row's columns straight out
+        const int row = c.m0 + r;
+        if (row < c.g->M) {
+          float* dst = c.g->c_f32 + static_cast<int64_t>(row) * c.g->N;
+#pragma unroll
+          for (int j4 = 0; j4 < kBN / 4; ++j4) {
+            const int col = c.n0 + j4 * 4;
+            if (col < c.g->N)
+              *reinterpret_cast<float4*>(dst + col) =
+                  make_float4(__uint_as_float(v[j4 * 4]), __uint_as_float(v[j4 * 4 + 1]),
+                              __uint_as_float(v[j4 * 4 + 2]), __uint_as_float(v[j4 * 4 + 3]));
+          }
+        }
+      }
       // 128-byte swizzle of the store's tensor map: the 16-byte chunk j of
       // row r sits at chunk position j ^ (r mod 8) of the row's 128 bytes
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int half = 0; half < 2 && !out_f32; ++half) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t* e = v + half * 64 + j * 8;
@@ -274,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       fence_proxy_async_smem();  // staged bytes visible to the TMA unit
       named_bar_sync<kEpiBarrier>(128);
       // a cluster's last row tiles may lie past M: computed on zero rows, not stored
-      if (leader && c.m0 < c.g->M) {
+      if (leader && c.m0 < c.g->M && !out_f32) {
         // the map clips rows past M and columns past N
         tma_store_2d(&c.g->tm_c, stage, c.n0, c.m0);
         if (c.n0 + 64 < c.g->N) tma_store_2d(&c.g->tm_c, stage + 16384, c.n0 + 64, c.m0);

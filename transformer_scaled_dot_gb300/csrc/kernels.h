@@ -59,6 +59,16 @@ struct GemmGroup {
   int64_t ldc;       // elements
   int M, N;
   int tiles_m, tiles_n, tile_begin;
+  // optional epilogue, in this order: + bias[col] (bf16 [N]), + residual[row,
+  // col] (bf16, or fp32 residual_f32; row stride ldr), max(0, .) when relu;
+  // with c_f32 the tile is written in fp32 there (row stride N) instead of
+  // bf16 through tm_c. N a multiple of 8 then.
+  const uint16_t* bias;
+  const uint16_t* residual;
+  const float* residual_f32;
+  int64_t ldr;
+  int relu;
+  float* c_f32;
 };
 constexpr int kMaxGemmGroups = 3;
 struct GemmProblem {
@@ -153,6 +163,14 @@ struct DecodeProblem {
 };
 int decode_chunks(int n_max);
 cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t stream);
+
+// out = LayerNorm(x + r) over rows of d_model (256, 512, 1024 or 2048)
+// features: x bf16 (or fp32 when x_f32), r bf16 or null, gamma/beta bf16,
+// out bf16 and, when out32 is not null, the same values in fp32 as well.
+cudaError_t launch_add_layernorm(const void* x, bool x_f32, const uint16_t* r,
+                                 const uint16_t* gamma, const uint16_t* beta, uint16_t* out,
+                                 float* out32, int rows, int d_model, float eps,
+                                 cudaStream_t stream);
 
 cudaError_t take_device_error_attn(unsigned int* value);
 cudaError_t take_device_error_decode(unsigned int* value);

@@ -131,7 +131,8 @@ attn_status encoder_layer_forward(const void *x,
  *   q        [B, h, n_q, d_k] bf16, device        out [B, h, n_q, d_v] bf16
  *   k_cache  [B, h, n_max, d_k] bf16, device      v_cache [B, h, n_max, d_v]
  *   cache_lens: device int32[B] (clamped to [0, n_max]), or NULL for L = n_max
- *   1 <= n_q <= 8 (more -> ATTN_ERR_UNSUPPORTED); d_k == d_v in {64, 128}.
+ *   1 <= n_q <= 8 and n_max <= 131072 (more -> ATTN_ERR_UNSUPPORTED);
+ *   d_k == d_v in {64, 128}.
  *   workspace: device, 16-byte aligned, >= attn_decode_workspace_bytes(...)
  *   bytes (per-chunk partial results; scratch, caller-owned).
  *   scale: 0 -> 1/sqrt(d_k). Cache rows at or past L are never used.

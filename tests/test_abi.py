@@ -218,3 +218,10 @@ def test_encoder_layer_rejects_bad_arguments(lib):
     assert with_(24, FAKE + 16) == tsd.ATTN_ERR_INVALID  # workspace not 256-byte aligned
     assert with_(7, None) == tsd.ATTN_ERR_INVALID       # no W_1
     assert with_(18, 96) == tsd.ATTN_ERR_UNSUPPORTED    # head size
+
+
+def test_attn_decode_caps_the_cache_length(lib):
+    ws = tsd.attn_decode_workspace_bytes(1, 1, 1, 131072, 64)
+    st = lib.attn_decode(FAKE, FAKE, FAKE, FAKE, 1, 1, 1, 131073, 64, 64, None, 0.0, FAKE,
+                         ws * 2, None)
+    assert st == tsd.ATTN_ERR_UNSUPPORTED

@@ -607,7 +607,8 @@ attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache,
                         float scale, void* workspace, size_t workspace_bytes,
                         tsd_stream_t stream) {
   if (B < 0 || h < 0 || n_q < 1 || n_max < 1) return ATTN_ERR_INVALID;
-  if (n_q > tsd::kDecodeMaxQueries) return ATTN_ERR_UNSUPPORTED;
+  if (n_q > tsd::kDecodeMaxQueries || tsd::decode_chunks(n_max) > tsd::kDecodeMaxChunks)
+    return ATTN_ERR_UNSUPPORTED;
   if (B > 65535 || h > 65535 || int64_t(B) * h > INT32_MAX) return ATTN_ERR_INVALID;
   if (!valid_scale(scale)) return ATTN_ERR_INVALID;
   if (d_k != d_v || (d_k != 64 && d_k != 128)) return ATTN_ERR_UNSUPPORTED;

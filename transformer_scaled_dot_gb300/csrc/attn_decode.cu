@@ -230,32 +230,62 @@ __global__ void __launch_bounds__(kDecThreads)
   }
 }
 
+constexpr int kMergeThreads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeArgs a) {
-  const int col = static_cast<int>(threadIdx.x);
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeArgs a) {
+  // the weights of every (chunk, query) pair go to shared memory first; then
+  // kMergeThreads / D groups of D threads (one per column) each sum a share
+  // of the chunks with several loads in flight, and the groups' sums are added
+  constexpr int kGroups = kMergeThreads / D;
+  __shared__ float w_s[kDecodeMaxChunks * kDecodeMaxQueries];
+  __shared__ float inv_l_s[kDecodeMaxQueries];
+  __shared__ float part_s[kGroups][kDecodeMaxQueries][D];
+  const int tid = static_cast<int>(threadIdx.x);
   const int hh = static_cast<int>(blockIdx.x), b = static_cast<int>(blockIdx.y);
   const int64_t bh = static_cast<int64_t>(b) * a.h + hh;
   griddep_launch_dependents();
   griddep_wait();  // the partials of the previous kernel are complete
   const int L = cache_len(a, b);
-  const int nc = (L + kChunk - 1) / kChunk;
-  for (int t = 0; t < a.n_q; ++t) {
+  const int nc = (L + kChunk - 1) / kChunk;       // <= kDecodeMaxChunks (checked on the host)
+  const float* ml = a.ws_ml + bh * a.chunks * a.n_q * 2;  // [chunk][query][m, l]
+  // per query (warp t, lanes over the chunks): m = max_c m_c,
+  // w_c = 2^(m_c - m), l = sum_c w_c l_c
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int t = warp; t < a.n_q; t += kMergeThreads / 32) {
     float m = -INFINITY;
-    for (int c = 0; c < nc; ++c) m = fmaxf(m, a.ws_ml[((bh * a.chunks + c) * a.n_q + t) * 2]);
-    float o = 0.f;
-    if (m != -INFINITY) {  // else no key is visible to this query: 0
-      float l = 0.f;
-      for (int c = 0; c < nc; ++c) {
-        const int64_t slot = (bh * a.chunks + c) * a.n_q + t;
-        const float mc = a.ws_ml[slot * 2];
-        if (mc == -INFINITY) continue;  // the chunk holds none of this query's keys
-        const float w = ex2(mc - m);
-        l = fmaf(w, a.ws_ml[slot * 2 + 1], l);
-        o = fmaf(w, a.ws_o[slot * D + col], o);
-      }
-      o = o / l;
+    for (int c = lane; c < nc; c += 32) m = fmaxf(m, ml[(c * a.n_q + t) * 2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float l = 0.f;
+    for (int c = lane; c < nc; c += 32) {
+      const float mc = ml[(c * a.n_q + t) * 2];
+      // a chunk holding none of this query's keys has m_c = -inf and weight 0
+      const float w = mc == -INFINITY ? 0.f : ex2(mc - m);
+      l = fmaf(w, ml[(c * a.n_q + t) * 2 + 1], l);
+      w_s[c * kDecodeMaxQueries + t] = w;
     }
-    a.out[(bh * a.n_q + t) * D + col] = __float2bfloat16_rn(o);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (lane == 0) inv_l_s[t] = l > 0.f ? 1.f / l : 0.f;  // no visible key: output 0
+  }
+  __syncthreads();
+  const int col = tid % D, grp = tid / D;
+  for (int t = 0; t < a.n_q; ++t) {
+    float o = 0.f;
+#pragma unroll 4
+    for (int c = grp; c < nc; c += kGroups)
+      o = fmaf(w_s[c * kDecodeMaxQueries + t], a.ws_o[((bh * a.chunks + c) * a.n_q + t) * D + col],
+               o);
+    part_s[grp][t][col] = o;
+  }
+  __syncthreads();
+  for (int i = tid; i < a.n_q * D; i += kMergeThreads) {
+    const int t = i / D, cc = i % D;
+    float o = 0.f;
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) o += part_s[g][t][cc];
+    a.out[(bh * a.n_q + t) * D + cc] = __float2bfloat16_rn(o * inv_l_s[t]);
   }
 }
 
@@ -281,7 +311,7 @@ cudaError_t launch_decode_nq(const DecodeProblem& p, cudaStream_t stream) {
   e = launch_pdl(kernel, dim3(a.chunks, p.h, p.B), dim3(kDecThreads), smem_bytes, stream,
                  p.tm_k, p.tm_v, a);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_merge_kernel<D>, dim3(p.h, p.B), dim3(D), 0, stream, a);
+  return launch_pdl(decode_merge_kernel<D>, dim3(p.h, p.B), dim3(kMergeThreads), 0, stream, a);
 }
 
 template <int D>
@@ -297,7 +327,8 @@ cudaError_t launch_decode_d(const DecodeProblem& p, cudaStream_t stream) {
 int decode_chunks(int n_max) { return (n_max + kChunk - 1) / kChunk; }
 
 cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t stream) {
-  if (p.n_q < 1 || p.n_q > kDecodeMaxQueries || p.n_max < 1 || p.B < 1 || p.h < 1)
+  if (p.n_q < 1 || p.n_q > kDecodeMaxQueries || p.n_max < 1 || p.B < 1 || p.h < 1 ||
+      decode_chunks(p.n_max) > kDecodeMaxChunks)
     return cudaErrorInvalidValue;
   if (p.d == 64) return launch_decode_d<64>(p, stream);
   if (p.d == 128) return launch_decode_d<128>(p, stream);

@@ -151,6 +151,7 @@ int mha_fused_out_clusters(int h, bool self);
 // keys at or before its position. Split over 256-key chunks (partials in a
 // workspace of float), then merged per (batch, head).
 constexpr int kDecodeMaxQueries = 8;
+constexpr int kDecodeMaxChunks = 512;  // n_max <= 512 * 256 = 131072
 struct DecodeProblem {
   CUtensorMap tm_k, tm_v;      // 3-D (d, n_max, B*h) bf16, box 64 x 256 x 1, 128-byte swizzle
   const void* q;               // [B, h, n_q, d] bf16

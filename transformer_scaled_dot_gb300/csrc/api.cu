@@ -443,12 +443,15 @@ attn_status launch_linear(const void* x, const void* w, const void* bias, const 
   g.num_groups = 1;
   cudaError_t e = make_gemm_group(&g.g[0], x, w, out, M, N, K);
   if (e != cudaSuccess) return cuda_fail(e);
+  // the kernel's epilogue modes: + bias, ReLU (bf16 out); + bias + fp32
+  // residual (fp32 out)
+  if (out_f32 ? (residual == nullptr || relu || bias == nullptr)
+              : (residual != nullptr || (bias != nullptr) != relu))
+    return ATTN_ERR_INVALID;
   g.g[0].bias = static_cast<const uint16_t*>(bias);
   if (out_f32) {
     g.g[0].residual_f32 = static_cast<const float*>(residual);
     g.g[0].c_f32 = static_cast<float*>(out);
-  } else {
-    g.g[0].residual = static_cast<const uint16_t*>(residual);
   }
   g.g[0].ldr = N;
   g.g[0].relu = relu ? 1 : 0;

@@ -100,7 +100,11 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmProblem& p, int ct, in
   return c;
 }
 
-template <int CM>
+// Epilogue modes (compile-time, so each instance holds only its own
+// registers): plain; + bias then ReLU; + bias + fp32 residual, fp32 output.
+constexpr int kEpiPlain = 0, kEpiBiasRelu = 1, kEpiBiasResF32 = 2;
+
+template <int CM, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_constant__ GemmProblem p) {
   extern __shared__ uint8_t smem_raw[];
   GemmSmem& sm = *reinterpret_cast<GemmSmem*>(
@@ -246,6 +250,47 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
     for (int ct = first; ct < p.total_tiles; ct += stride, ++it) {
       const int acc = it & 1;
       const TileCoord c = tile_coord<CM>(p, ct, rank);
+      // the group's fields once into registers (reads through the pointer
+      // into the parameter space would be repeated past every store)
+      const uint16_t* const g_bias = c.g->bias;
+      const float* const g_res32 = c.g->residual_f32;
+      float* const g_c32 = c.g->c_f32;
+      const int64_t g_ldr = c.g->ldr;
+      const int g_N = c.g->N;
+      const int row = c.m0 + r;
+      const bool row_ok = row < c.g->M;
+      // bias and residual of chunk cc (32 columns) of this thread's row
+      auto load_bias = [&](int cc, uint4 (&bw)[4]) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int col = c.n0 + cc * 32 + 8 * k;
+          bw[k] = col < g_N ? __ldg(reinterpret_cast<const uint4*>(g_bias + col))
+                            : make_uint4(0u, 0u, 0u, 0u);
+        }
+      };
+      auto load_res = [&](int cc, float4 (&rf)[8]) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int col = c.n0 + cc * 32 + 4 * k;
+          rf[k] = (col < g_N && row_ok)
+                      ? __ldg(reinterpret_cast<const float4*>(g_res32 + row * g_ldr + col))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      };
+      // the first chunk's operands (the whole tile's bias with ReLU) are
+      // loaded while the main loop runs, later chunks' during the previous
+      uint4 bias_all[EPI == kEpiBiasRelu ? kBN / 8 : 1];
+      uint4 bw_next[4];
+      float4 rf_next[EPI == kEpiBiasResF32 ? 8 : 1];
+      if constexpr (EPI == kEpiBiasRelu) {
+#pragma unroll
+        for (int cc = 0; cc < kBN / 32; ++cc)
+          load_bias(cc, *reinterpret_cast<uint4(*)[4]>(bias_all + 4 * cc));
+      }
+      if constexpr (EPI == kEpiBiasResF32) {
+        load_bias(0, bw_next);
+        load_res(0, *reinterpret_cast<float4(*)[8]>(rf_next));
+      }
       bool ok = __all_sync(
           0xffffffffu,
           mbar_wait(&sm.acc_full[acc], static_cast<uint32_t>(it >> 1) & 1u, abort_flag));
@@ -256,91 +301,81 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       ok = named_bar_and<kEpiBarrier>(128, ok);
       if (!ok) break;
       tc_fence_after();
-      uint32_t v[kBN];
+      // 32 columns at a time: TMEM -> registers, the epilogue's additions
+      // (their loads issued before the TMEM wait), then bf16 into the
+      // swizzled staging tile or fp32 straight to global memory
+      uint8_t* stage = sm.c[it % kCStages];
 #pragma unroll
       for (int cc = 0; cc < kBN / 32; ++cc) {
-        uint32_t chunk[32];
-        tmem_ld32(tmem + lane_base + acc * kAccCols + cc * 32, chunk);
+        uint32_t x[32];
+        tmem_ld32(tmem + lane_base + acc * kAccCols + cc * 32, x);
+        float add[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[cc * 32 + i] = chunk[i];
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&sm.acc_empty[acc]);  // the MMA warp may reuse this accumulator
-      {
-        // optional epilogue of a feed-forward layer: + bias, + residual, ReLU
-        const GemmGroup& G = *c.g;
-        if (G.bias != nullptr || G.residual != nullptr || G.residual_f32 != nullptr || G.relu) {
-          const int row = c.m0 + r;
-          const uint16_t* res_row =
-              (G.residual != nullptr && row < G.M) ? G.residual + row * G.ldr : nullptr;
-          const float* res32_row =
-              (G.residual_f32 != nullptr && row < G.M) ? G.residual_f32 + row * G.ldr : nullptr;
+        for (int i = 0; i < 32; ++i) add[i] = 0.f;
+        if constexpr (EPI == kEpiBiasRelu) {
 #pragma unroll
-          for (int j8 = 0; j8 < kBN / 8; ++j8) {
-            const int col = c.n0 + j8 * 8;
-            float add[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (col < G.N) {
-              if (G.bias != nullptr) {
-                const uint4 w = __ldg(reinterpret_cast<const uint4*>(G.bias + col));
-                add_bf16x8(add, w);
-              }
-              if (res_row != nullptr) {
-                const uint4 w = __ldg(reinterpret_cast<const uint4*>(res_row + col));
-                add_bf16x8(add, w);
-              }
-              if (res32_row != nullptr) {
-                const float4 a = __ldg(reinterpret_cast<const float4*>(res32_row + col));
-                const float4 b = __ldg(reinterpret_cast<const float4*>(res32_row + col + 4));
-                add[0] += a.x; add[1] += a.y; add[2] += a.z; add[3] += a.w;
-                add[4] += b.x; add[5] += b.y; add[6] += b.z; add[7] += b.w;
-              }
-            }
+          for (int k = 0; k < 4; ++k)
+            add_bf16x8(*reinterpret_cast<float(*)[8]>(add + 8 * k), bias_all[cc * 4 + k]);
+        }
+        if constexpr (EPI == kEpiBiasResF32) {
+          uint4 bw[4];
+          float4 rf[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float x = __uint_as_float(v[j8 * 8 + i]) + add[i];
-              if (G.relu) x = fmaxf(x, 0.f);
-              v[j8 * 8 + i] = __float_as_uint(x);
-            }
+          for (int k = 0; k < 4; ++k) bw[k] = bw_next[k];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) rf[k] = rf_next[k];
+          if (cc + 1 < kBN / 32) {  // the next chunk's, in flight meanwhile
+            load_bias(cc + 1, bw_next);
+            load_res(cc + 1, *reinterpret_cast<float4(*)[8]>(rf_next));
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            add_bf16x8(*reinterpret_cast<float(*)[8]>(add + 8 * k), bw[k]);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            add[4 * k] += rf[k].x;
+            add[4 * k + 1] += rf[k].y;
+            add[4 * k + 2] += rf[k].z;
+            add[4 * k + 3] += rf[k].w;
           }
         }
-      }
-
-      uint8_t* stage = sm.c[it % kCStages];
-      const bool out_f32 = c.g->c_f32 != nullptr;
-      if (out_f32) {
-        // fp32 output: each thread writes its row's columns straight out
-        const int row = c.m0 + r;
-        if (row < c.g->M) {
-          float* dst = c.g->c_f32 + static_cast<int64_t>(row) * c.g->N;
-#pragma unroll
-          for (int j4 = 0; j4 < kBN / 4; ++j4) {
-            const int col = c.n0 + j4 * 4;
-            if (col < c.g->N)
-              *reinterpret_cast<float4*>(dst + col) =
-                  make_float4(__uint_as_float(v[j4 * 4]), __uint_as_float(v[j4 * 4 + 1]),
-                              __uint_as_float(v[j4 * 4 + 2]), __uint_as_float(v[j4 * 4 + 3]));
-          }
+        tmem_wait_ld();
+        if (cc == kBN / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(&sm.acc_empty[acc]);  // the MMA warp may reuse this accumulator
         }
-      }
-      // 128-byte swizzle of the store's tensor map: the 16-byte chunk j of
-      // row r sits at chunk position j ^ (r mod 8) of the row's 128 bytes
+        float y[32];
 #pragma unroll
-      for (int half = 0; half < 2 && !out_f32; ++half) {
+        for (int i = 0; i < 32; ++i) {
+          y[i] = __uint_as_float(x[i]) + add[i];
+          if constexpr (EPI == kEpiBiasRelu) y[i] = fmaxf(y[i], 0.f);
+        }
+        if constexpr (EPI == kEpiBiasResF32) {
+          if (row_ok) {
+            float* dst = g_c32 + static_cast<int64_t>(row) * g_N + c.n0 + cc * 32;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t* e = v + half * 64 + j * 8;
-          st_shared_v4(smem_u32(stage + half * 16384 + r * 128 + ((j ^ (r & 7)) << 4)),
-                       pack_bf16x2(__uint_as_float(e[0]), __uint_as_float(e[1])),
-                       pack_bf16x2(__uint_as_float(e[2]), __uint_as_float(e[3])),
-                       pack_bf16x2(__uint_as_float(e[4]), __uint_as_float(e[5])),
-                       pack_bf16x2(__uint_as_float(e[6]), __uint_as_float(e[7])));
+            for (int k = 0; k < 8; ++k)
+              if (c.n0 + cc * 32 + 4 * k < g_N)
+                *reinterpret_cast<float4*>(dst + 4 * k) =
+                    make_float4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+          }
+        } else {
+          // 128-byte swizzle of the store's tensor map: the 16-byte chunk j of
+          // row r sits at chunk position j ^ (r mod 8) of the row's 128 bytes
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const int j = (cc & 1) * 4 + v4;
+            const float* e = y + 8 * v4;
+            st_shared_v4(smem_u32(stage + (cc >> 1) * 16384 + r * 128 + ((j ^ (r & 7)) << 4)),
+                         pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
+                         pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+          }
         }
       }
       fence_proxy_async_smem();  // staged bytes visible to the TMA unit
       named_bar_sync<kEpiBarrier>(128);
       // a cluster's last row tiles may lie past M: computed on zero rows, not stored
-      if (leader && c.m0 < c.g->M && !out_f32) {
+      if (leader && c.m0 < c.g->M && EPI != kEpiBiasResF32) {
         // the map clips rows past M and columns past N
         tma_store_2d(&c.g->tm_c, stage, c.n0, c.m0);
         if (c.n0 + 64 < c.g->N) tma_store_2d(&c.g->tm_c, stage + 16384, c.n0 + 64, c.m0);
@@ -385,9 +420,25 @@ cudaError_t launch_gemm_bf16(const GemmProblem& problem, cudaStream_t stream) {
   p.total_tiles = t;
   if (t <= 0) return cudaSuccess;
   const size_t smem_bytes = sizeof(GemmSmem) + 1024;
-  auto kernel = gemm_bf16_kernel<CM>;
-  static unsigned long long configured = 0;
-  cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured);
+  // one epilogue mode per launch (every group's fields must agree)
+  const GemmGroup& g0 = p.g[0];
+  int epi = kEpiPlain;
+  if (g0.c_f32 != nullptr) {
+    if (g0.bias == nullptr || g0.residual_f32 == nullptr || g0.relu) return cudaErrorInvalidValue;
+    epi = kEpiBiasResF32;
+  } else if (g0.bias != nullptr || g0.relu) {
+    if (g0.bias == nullptr || !g0.relu || g0.residual_f32 != nullptr) return cudaErrorInvalidValue;
+    epi = kEpiBiasRelu;
+  }
+  for (int i = 1; i < p.num_groups; ++i)
+    if (p.g[i].bias != g0.bias || p.g[i].relu != g0.relu || p.g[i].c_f32 != nullptr ||
+        p.g[i].residual_f32 != nullptr)
+      return cudaErrorInvalidValue;
+  auto kernel = epi == kEpiPlain      ? gemm_bf16_kernel<CM, kEpiPlain>
+                : epi == kEpiBiasRelu ? gemm_bf16_kernel<CM, kEpiBiasRelu>
+                                      : gemm_bf16_kernel<CM, kEpiBiasResF32>;
+  static unsigned long long configured[3] = {0, 0, 0};
+  cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured[epi]);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
@@ -404,7 +455,7 @@ cudaError_t launch_gemm_bf16(const GemmProblem& problem, cudaStream_t stream) {
   cfg.numAttrs = 2;
   // persistent: as many clusters as can be resident at once (clusters stay
   // inside one GPC, so this can be below SMs / CM)
-  static int max_clusters = 0;
+  static int max_clusters = 0;  // the same for every epilogue mode (same resources)
   if (max_clusters == 0) {
     cfg.gridDim = dim3(num_sms() / CM * CM);
     int n = 0;

@@ -59,12 +59,11 @@ struct GemmGroup {
   int64_t ldc;       // elements
   int M, N;
   int tiles_m, tiles_n, tile_begin;
-  // optional epilogue, in this order: + bias[col] (bf16 [N]), + residual[row,
-  // col] (bf16, or fp32 residual_f32; row stride ldr), max(0, .) when relu;
-  // with c_f32 the tile is written in fp32 there (row stride N) instead of
-  // bf16 through tm_c. N a multiple of 8 then.
+  // optional epilogue, one of: + bias[col] (bf16 [N]) then max(0, .) (relu
+  // set); or + bias[col] + residual_f32[row, col] (row stride ldr) written in
+  // fp32 to c_f32 (row stride N) instead of bf16 through tm_c. N a multiple
+  // of 8 then. Every group of a launch uses the same one.
   const uint16_t* bias;
-  const uint16_t* residual;
   const float* residual_f32;
   int64_t ldr;
   int relu;

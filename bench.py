@@ -125,16 +125,23 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_sha(rel):
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+def source_sha(rels):
+    """sha256 of one source file, or of several concatenated in order."""
+    h = hashlib.sha256()
+    for rel in ((rels,) if isinstance(rels, str) else rels):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
+_CSRC = "transformer_scaled_dot_gb300/csrc/"
 KERNEL_SOURCES = {
-    "attn_fwd_bf16": "transformer_scaled_dot_gb300/csrc/attn_bf16.cu",
-    "gemm_bf16": "transformer_scaled_dot_gb300/csrc/gemm_bf16.cu",
-    "mha_fused": "transformer_scaled_dot_gb300/csrc/mha_fused.cu",
-    "attn_decode": "transformer_scaled_dot_gb300/csrc/attn_decode.cu",
+    "attn_fwd_bf16": _CSRC + "attn_bf16.cu",
+    "gemm_bf16": _CSRC + "gemm_bf16.cu",
+    "mha_fused": _CSRC + "mha_fused.cu",
+    "attn_decode": _CSRC + "attn_decode.cu",
+    # the encoder layer's five launches: fused MHA, two LayerNorms, two GEMMs
+    "encoder_layer": (_CSRC + "mha_fused.cu", _CSRC + "layernorm.cu", _CSRC + "gemm_bf16.cu"),
 }
 
 

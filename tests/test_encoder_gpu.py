@@ -68,3 +68,33 @@ def test_encoder_layer_other_eps(tsd):
     x, _, wq, wk, wv, wo = m.as_f64()
     ref = oracle.encoder_layer(x, wq, wk, wv, wo, *e.params_f64(), 4, MASK_NONE, eps=1e-2)
     assert_bf16_close(got, ref, "eps 1e-2")
+
+
+@pytest.mark.parametrize("B", [1, 2, 4])
+def test_encoder_layer_small_batches_repeated(tsd, B):
+    """Small batches leave most SMs free during the first FFN GEMM, so the
+    second GEMM's CTAs start beside it, and beside the LayerNorm before it
+    (every kernel releases its dependents at entry): its epilogue must not
+    read the fp32 residual before the grid dependency has resolved. Several
+    back-to-back layers, each against the oracle."""
+    import torch
+    e = synthetic.encoder_inputs(4200 + B, B, 128, 512, 8, 2048, MASK_KEY_PADDING, (64, 128),
+                                 add_pe=True)
+    m = e.mha
+    dev = [to_dev_bf16(t) for t in (m.x_q, m.w_q, m.w_k, m.w_v, m.w_o, e.ln1_gamma, e.ln1_beta,
+                                    e.w_1, e.b_1, e.w_2, e.b_2, e.ln2_gamma, e.ln2_beta)]
+    wsb = tsd.encoder_layer_workspace_bytes(m.B, m.n_q, m.d_model, m.h, m.d_k, e.d_ff)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    lens = to_dev_i32(m.kv_lens)
+    outs = [torch.full((m.B, m.n_q, m.d_model), float("nan"), dtype=torch.bfloat16, device="cuda")
+            for _ in range(8)]
+    for out in outs:
+        tsd.encoder_layer_forward(*dev, out, m.B, m.n_q, m.d_model, m.h, m.d_k, e.d_ff,
+                                  m.mask_kind, lens, 0.0, 1e-6, ws, wsb)
+    torch.cuda.synchronize()
+    assert tsd.attn_get_device_status() == tsd.ATTN_OK
+    x, _, wq, wk, wv, wo = m.as_f64()
+    ref = oracle.encoder_layer(x, wq, wk, wv, wo, *e.params_f64(), m.h, m.mask_kind,
+                               kv_lens=m.kv_lens, eps=1e-6)
+    for i, out in enumerate(outs):
+        assert_bf16_close(to_host_f64(out), ref, f"B={B} layer {i}")

@@ -245,7 +245,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
     const int r = quarter * 32 + static_cast<int>(lane);
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const bool leader = (warp == 2 && lane == 0);  // issues the tile's TMA stores
-    if (leader) griddep_wait();
+    // Every thread that touches global memory waits for the previous grid
+    // first: the leader before its stores; with an epilogue, every thread
+    // (bias and residual may come from earlier kernels, and the fp32 output
+    // is stored directly). Kernels release their dependents at entry, so
+    // without the wait this grid can run beside a kernel two launches back
+    // when the one in between leaves SMs free.
+    if (EPI != kEpiPlain || leader) griddep_wait();
     int it = 0;
     for (int ct = first; ct < p.total_tiles; ct += stride, ++it) {
       const int acc = it & 1;

@@ -145,6 +145,23 @@ KERNEL_SOURCES = {
 }
 
 
+# the public call the end-to-end leg times, per workload kind
+E2E_API = {
+    "mha": "mha_forward_host (pinned host x, lengths and result; weights resident; "
+           "two staging workspaces in turn)",
+    "attn": "attn_forward_host / attn_forward_window_host (pinned host Q, K, V and O; "
+            "two staging workspaces in turn)",
+    "encoder": "encoder_layer_forward_host (pinned host x, lengths and result; parameters "
+               "resident; two staging workspaces in turn)",
+    "decode": "attn_decode_host (pinned host queries, cache lengths and result; caches "
+              "resident; two staging workspaces in turn)",
+}
+
+
+def spec_kind(workload):
+    return WORKLOADS[workload]["kind"] if workload in WORKLOADS else "attn"
+
+
 def profiled_traffic(kernel, workload):
     """DRAM bytes per launch from a committed ncu summary, or None when there is
     none for this kernel and workload, or the kernel source changed since."""
@@ -335,6 +352,19 @@ class MhaCall:
             torch.from_numpy(np.ascontiguousarray(m.x_kv).view(np.int16)).pin_memory()
         self.h_lens = torch.from_numpy(m.kv_lens).pin_memory() if m.kv_lens is not None else None
         self.h_out = torch.empty((m.B, m.n_q, m.d_model), dtype=torch.bfloat16).pin_memory()
+        self.h_ws = None
+
+    def host_workspaces(self):
+        """Two staging workspaces of mha_forward_host, taken in turn by the
+        end-to-end leg (allocated on first use)."""
+        import torch
+        if self.h_ws is None:
+            m = self.m
+            self.h_wsb = self.tsd.mha_host_workspace_bytes(m.B, m.n_q, m.n_k, m.d_model, m.h,
+                                                           m.d_k, m.d_v)
+            self.h_ws = [torch.empty(self.h_wsb, dtype=torch.uint8, device="cuda")
+                         for _ in range(2)]
+        return self.h_ws
 
     def bytes_per_set(self):
         m = self.m
@@ -453,15 +483,14 @@ class MhaCall:
         return len(self.stage_names())
 
     def e2e_run(self, i, stream):
-        """Host inputs -> device, mha_forward, result -> host (pinned buffers)."""
-        m, s = self.m, self.sets[i % len(self.sets)]
-        s["x_q"].view(torch_int16()).copy_(self.h_x_q, non_blocking=True)
-        if self.h_x_kv is not None:
-            s["x_kv"].view(torch_int16()).copy_(self.h_x_kv, non_blocking=True)
-        if self.h_lens is not None:
-            s["lens"].copy_(self.h_lens, non_blocking=True)
-        self.run(i, stream)
-        self.h_out.copy_(s["out"], non_blocking=True)
+        """mha_forward_host: pinned host x (and lengths) in, pinned host result
+        out, the weights resident on the device."""
+        m, s = self.m, self.sets[0]
+        ws = self.host_workspaces()[i % 2]
+        hx = self.h_x_q
+        self.tsd.mha_forward_host(hx, hx if self.h_x_kv is None else self.h_x_kv, *s["w"],
+                                  self.h_out, m.B, m.n_q, m.n_k, m.d_model, m.h, m.d_k, m.d_v,
+                                  m.mask_kind, self.h_lens, 0.0, ws, self.h_wsb, stream)
 
     def e2e_bytes(self):
         m = self.m
@@ -490,6 +519,7 @@ class AttnCall:
                       for x in (a.q, a.k, a.v)]
         self.h_out = torch.empty(a.q.shape, dtype=torch.bfloat16).pin_memory()
         self.window = cfg.get("window")
+        self.h_ws = None
 
     def bytes_per_set(self):
         return 4 * self.a.q.nbytes
@@ -530,11 +560,22 @@ class AttnCall:
         return 1
 
     def e2e_run(self, i, stream):
-        s = self.sets[i % len(self.sets)]
-        for dst, src in zip((s["q"], s["k"], s["v"]), self.h_qkv):
-            dst.view(torch_int16()).copy_(src, non_blocking=True)
-        self.run(i, stream)
-        self.h_out.copy_(s["out"], non_blocking=True)
+        """attn_forward_host (attn_forward_window_host): pinned host Q, K, V in,
+        pinned host O out, two staging workspaces in turn."""
+        import torch
+        a = self.a
+        if self.h_ws is None:
+            self.h_wsb = self.tsd.attn_host_workspace_bytes(a.B, a.h, a.n_q, a.n_k, a.d_k, a.d_v)
+            self.h_ws = [torch.empty(self.h_wsb, dtype=torch.uint8, device="cuda")
+                         for _ in range(2)]
+        ws = self.h_ws[i % 2]
+        if self.window is not None:
+            self.tsd.attn_forward_window_host(*self.h_qkv, self.h_out, a.B, a.h, a.n_q, a.n_k,
+                                              a.d_k, a.d_v, self.window[0], self.window[1],
+                                              a.mask_kind, None, 0.0, ws, self.h_wsb, stream)
+            return
+        self.tsd.attn_forward_host(*self.h_qkv, self.h_out, a.B, a.h, a.n_q, a.n_k, a.d_k, a.d_v,
+                                   a.mask_kind, None, 0.0, ws, self.h_wsb, stream)
 
     def e2e_bytes(self):
         return 3 * self.a.q.nbytes, self.a.q.nbytes
@@ -565,6 +606,7 @@ class EncoderCall:
         self.h_x = torch.from_numpy(np.ascontiguousarray(m.x_q).view(np.int16)).pin_memory()
         self.h_lens = torch.from_numpy(m.kv_lens).pin_memory()
         self.h_out = torch.empty((m.B, m.n_q, m.d_model), dtype=torch.bfloat16).pin_memory()
+        self.h_ws = None
 
     @staticmethod
     def set_bytes(cfg):
@@ -603,11 +645,19 @@ class EncoderCall:
                                              True) + 4
 
     def e2e_run(self, i, stream):
-        s = self.sets[i % len(self.sets)]
-        s["t"][0].view(torch_int16()).copy_(self.h_x, non_blocking=True)
-        s["lens"].copy_(self.h_lens, non_blocking=True)
-        self.run(i, stream)
-        self.h_out.copy_(s["out"], non_blocking=True)
+        """encoder_layer_forward_host: pinned host x and lengths in, pinned host
+        output out, the layer's parameters resident on the device."""
+        import torch
+        m, e, s = self.e.mha, self.e, self.sets[0]
+        if self.h_ws is None:
+            self.h_wsb = self.tsd.encoder_layer_host_workspace_bytes(m.B, m.n_q, m.d_model, m.h,
+                                                                     m.d_k, e.d_ff)
+            self.h_ws = [torch.empty(self.h_wsb, dtype=torch.uint8, device="cuda")
+                         for _ in range(2)]
+        self.tsd.encoder_layer_forward_host(self.h_x, *s["t"][1:], self.h_out, m.B, m.n_q,
+                                            m.d_model, m.h, m.d_k, e.d_ff, m.mask_kind,
+                                            self.h_lens, 0.0, self.cfg["eps"], self.h_ws[i % 2],
+                                            self.h_wsb, stream)
 
     def e2e_bytes(self):
         m = self.e.mha
@@ -639,6 +689,7 @@ class DecodeCall:
         self.h_q = torch.from_numpy(np.ascontiguousarray(a.q).view(np.int16)).pin_memory()
         self.h_lens = torch.from_numpy(self.lens).pin_memory()
         self.h_out = torch.empty((B, h, n_q, d), dtype=torch.bfloat16).pin_memory()
+        self.h_ws = None
 
     @staticmethod
     def set_bytes(cfg):
@@ -681,19 +732,20 @@ class DecodeCall:
         return 2
 
     def e2e_run(self, i, stream):
+        """attn_decode_host: pinned host queries and cache lengths in, pinned host
+        output out; the caches (state) resident on the device, rotating sets."""
+        import torch
+        B, h, n_q, n_max, d = self.shape
+        if self.h_ws is None:
+            self.h_wsb = self.tsd.attn_decode_host_workspace_bytes(B, h, n_q, n_max, d, d)
+            self.h_ws = [torch.empty(self.h_wsb, dtype=torch.uint8, device="cuda")
+                         for _ in range(2)]
         s = self.sets[i % len(self.sets)]
-        s["q"].view(torch_int16()).copy_(self.h_q, non_blocking=True)
-        s["lens"].copy_(self.h_lens, non_blocking=True)
-        self.run(i, stream)
-        self.h_out.copy_(s["out"], non_blocking=True)
+        self.tsd.attn_decode_host(self.h_q, s["k"], s["v"], self.h_out, B, h, n_q, n_max, d, d,
+                                  self.h_lens, 0.0, self.h_ws[i % 2], self.h_wsb, stream)
 
     def e2e_bytes(self):
         return self.a.q.nbytes + self.lens.nbytes, self.a.q.nbytes
-
-
-def torch_int16():
-    import torch
-    return torch.int16
 
 
 def make_calls(tsd, wl, args, seed_offset):
@@ -886,7 +938,8 @@ def run_gpu_arm(args, world, rank, local):
         "roofline": roof,
         "kernels": kernel_table,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 5)},
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 5),
+                "api": E2E_API[spec_kind(args.workload)]},
         "clocks": clocks,
         "gpu_launches": int(sum(c.launches() for c in calls) * args.steps),
     }

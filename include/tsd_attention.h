@@ -331,6 +331,85 @@ attn_status mha_forward_noalloc(const void *x_q, const void *x_kv,
                                 tsd_stream_t stream);
 
 /*
+ * Host-buffer entry points -- attn_forward, attn_forward_window, mha_forward,
+ * encoder_layer_forward and attn_decode with the step's inputs and result
+ * in HOST memory (the pages' operations unchanged; a deployment variant).
+ * Each call copies its host inputs into staging regions at the front of
+ * `workspace`, runs the device entry point on the staged copies on
+ * `stream`, and copies the result back to the host on `stream`. Weights,
+ * LayerNorm parameters and the key/value cache stay DEVICE pointers: they
+ * are state that lives on the GPU between steps.
+ *
+ *   *_host arguments: host memory (pinned -- cudaHostAlloc or
+ *   cudaHostRegister -- for the copies to be asynchronous; pageable memory
+ *   works and is copied synchronously). Sizes, layouts, masks and errors as
+ *   the device entry point; kv_lens / cache_lens are host int32[B] here.
+ *   workspace: device, 256-byte aligned, >= the matching
+ *   *_host_workspace_bytes(...) (0 for invalid sizes); a workspace serves
+ *   one stream at a time and only these calls.
+ *
+ * Ordering. The input copies run on a copy stream the library creates once
+ * per device (non-blocking), after the last computation that read the same
+ * workspace's staging region; the computation waits for them. The result
+ * copy is on `stream`, so once `stream` has passed the call, the result is
+ * in host memory and the host inputs may be reused. A caller that passes
+ * two workspaces in turn over consecutive calls overlaps call i+1's input
+ * copy with call i's computation and result copy. The first call with a
+ * workspace (or after the library's table of 64 workspaces evicted it)
+ * orders its copy after everything already on `stream`. Calls are
+ * serialised by a library-wide lock while they enqueue (microseconds).
+ * Errors: every argument error returns before anything is copied; a failed
+ * copy or stream operation returns ATTN_ERR_CUDA.
+ */
+size_t attn_host_workspace_bytes(int B, int h, int n_q, int n_k, int d_k, int d_v);
+attn_status attn_forward_host(const void *q_host, const void *k_host, const void *v_host,
+                              void *out_host,
+                              int B, int h, int n_q, int n_k, int d_k, int d_v,
+                              int mask_kind, const int32_t *kv_lens_host, float scale,
+                              void *workspace, size_t workspace_bytes, tsd_stream_t stream);
+
+/* attn_forward_window with host q, k, v, out; the workspace as attn_forward_host's. */
+attn_status attn_forward_window_host(const void *q_host, const void *k_host, const void *v_host,
+                                     void *out_host,
+                                     int B, int h, int n_q, int n_k, int d_k, int d_v,
+                                     int mask_kind, const int32_t *kv_lens_host,
+                                     int window_left, int window_right, float scale,
+                                     void *workspace, size_t workspace_bytes,
+                                     tsd_stream_t stream);
+
+size_t mha_host_workspace_bytes(int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v);
+/* x_kv_host == x_q_host (with n_q == n_k) is self-attention: x is copied once. */
+attn_status mha_forward_host(const void *x_q_host, const void *x_kv_host,
+                             const void *w_q, const void *w_k, const void *w_v, const void *w_o,
+                             void *out_host,
+                             int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
+                             int mask_kind, const int32_t *kv_lens_host, float scale,
+                             void *workspace, size_t workspace_bytes, tsd_stream_t stream);
+
+size_t encoder_layer_host_workspace_bytes(int B, int n, int d_model, int h, int d_k, int d_ff);
+attn_status encoder_layer_forward_host(const void *x_host,
+                                       const void *w_q, const void *w_k, const void *w_v,
+                                       const void *w_o,
+                                       const void *ln1_gamma, const void *ln1_beta,
+                                       const void *w_1, const void *b_1,
+                                       const void *w_2, const void *b_2,
+                                       const void *ln2_gamma, const void *ln2_beta,
+                                       void *out_host,
+                                       int B, int n, int d_model, int h, int d_k, int d_ff,
+                                       int mask_kind, const int32_t *kv_lens_host, float scale,
+                                       float eps, void *workspace, size_t workspace_bytes,
+                                       tsd_stream_t stream);
+
+size_t attn_decode_host_workspace_bytes(int B, int h, int n_q, int n_max, int d_k, int d_v);
+/* q_host [B, h, n_q, d_k] and out_host [B, h, n_q, d_v] on the host; the
+ * caches are device memory; cache_lens_host: host int32[B] or NULL. */
+attn_status attn_decode_host(const void *q_host, const void *k_cache, const void *v_cache,
+                             void *out_host,
+                             int B, int h, int n_q, int n_max, int d_k, int d_v,
+                             const int32_t *cache_lens_host, float scale,
+                             void *workspace, size_t workspace_bytes, tsd_stream_t stream);
+
+/*
  * attn_get_device_status -- synchronises `stream`, then reads and clears the
  * device error word the kernels set when a bounded wait runs out.
  * Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT, or ATTN_ERR_CUDA if the

@@ -225,3 +225,81 @@ def test_attn_decode_caps_the_cache_length(lib):
     st = lib.attn_decode(FAKE, FAKE, FAKE, FAKE, 1, 1, 1, 131073, 64, 64, None, 0.0, FAKE,
                          ws * 2, None)
     assert st == tsd.ATTN_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------ host-buffer entry points
+def test_host_workspace_sizes_cover_staging_and_device_workspace(lib):
+    al = lambda x: (x + 255) // 256 * 256
+    B, n, dm, h, d = 32, 128, 512, 8, 64
+    xb = B * n * dm * 2
+    assert tsd.mha_host_workspace_bytes(B, n, n, dm, h, d, d) == \
+        3 * al(xb) + al(B * 4) + tsd.mha_workspace_bytes(B, n, n, h, d, d)
+    qb = 2 * 4 * 100 * 64 * 2
+    assert tsd.attn_host_workspace_bytes(2, 4, 100, 100, 64, 64) == 4 * al(qb) + al(2 * 4)
+    assert tsd.encoder_layer_host_workspace_bytes(B, n, dm, h, d, 2048) == \
+        2 * al(xb) + al(B * 4) + tsd.encoder_layer_workspace_bytes(B, n, dm, h, d, 2048)
+    assert tsd.attn_decode_host_workspace_bytes(16, 16, 1, 8192, 64, 64) == \
+        2 * al(16 * 16 * 64 * 2) + al(16 * 4) + tsd.attn_decode_workspace_bytes(16, 16, 1, 8192, 64)
+    for bad in (tsd.mha_host_workspace_bytes(-1, n, n, dm, h, d, d),
+                tsd.attn_host_workspace_bytes(1, 1, 16, 16, 0, 64),
+                tsd.encoder_layer_host_workspace_bytes(1, 16, 0, 8, 64, 2048),
+                tsd.attn_decode_host_workspace_bytes(1, 1, 0, 128, 64, 64)):
+        assert bad == 0
+
+
+def test_host_entry_points_reject_bad_arguments_before_copying(lib):
+    # every case fails validation, so nothing reaches the CUDA runtime
+    # (none is present here; a call that got that far would say ATTN_ERR_CUDA)
+    ws = 1 << 24  # 256-byte aligned fake device address, never touched
+    big = 1 << 40
+    hx = FAKE
+    M = tsd.ATTN_MASK_KEY_PADDING
+    # attn_forward_host: null host pointer, short / misaligned workspace,
+    # padding without lengths, unsupported head size
+    assert lib.attn_forward_host(None, hx, hx, hx, 1, 1, 16, 16, 64, 64, 0, None, 0.0, ws, big,
+                                 None) == tsd.ATTN_ERR_INVALID
+    assert lib.attn_forward_host(hx, hx, hx, hx, 1, 1, 16, 16, 64, 64, 0, None, 0.0, ws, 1024,
+                                 None) == tsd.ATTN_ERR_INVALID
+    assert lib.attn_forward_host(hx, hx, hx, hx, 1, 1, 16, 16, 64, 64, 0, None, 0.0, ws + 16, big,
+                                 None) == tsd.ATTN_ERR_INVALID
+    assert lib.attn_forward_host(hx, hx, hx, hx, 1, 1, 16, 16, 64, 64, M, None, 0.0, ws, big,
+                                 None) == tsd.ATTN_ERR_INVALID
+    assert lib.attn_forward_host(hx, hx, hx, hx, 1, 1, 16, 16, 96, 96, 0, None, 0.0, ws, big,
+                                 None) == tsd.ATTN_ERR_UNSUPPORTED
+    # attn_forward_window_host: a window needs n_q == n_k; bounds below -1
+    assert lib.attn_forward_window_host(hx, hx, hx, hx, 1, 1, 16, 32, 64, 64, 0, None, 4, 4, 0.0,
+                                        ws, big, None) == tsd.ATTN_ERR_INVALID
+    assert lib.attn_forward_window_host(hx, hx, hx, hx, 1, 1, 16, 16, 64, 64, 0, None, -2, 4, 0.0,
+                                        ws, big, None) == tsd.ATTN_ERR_INVALID
+    # mha_forward_host: null weight, short workspace, causal with n_q != n_k
+    w = FAKE
+    assert lib.mha_forward_host(hx, hx, None, w, w, w, hx, 2, 16, 16, 512, 8, 64, 64, 0, None, 0.0,
+                                ws, big, None) == tsd.ATTN_ERR_INVALID
+    need = tsd.mha_host_workspace_bytes(2, 16, 16, 512, 8, 64, 64)
+    assert lib.mha_forward_host(hx, hx, w, w, w, w, hx, 2, 16, 16, 512, 8, 64, 64, 0, None, 0.0,
+                                ws, need - 1, None) == tsd.ATTN_ERR_INVALID
+    assert lib.mha_forward_host(hx, hx + 4096, w, w, w, w, hx, 2, 16, 8, 512, 8, 64, 64, 1, None,
+                                0.0, ws, big, None) == tsd.ATTN_ERR_INVALID
+    # encoder_layer_forward_host: bad eps, unsupported d_model
+    args = [hx] + [w] * 12 + [hx]
+    assert lib.encoder_layer_forward_host(*args, 2, 16, 512, 8, 64, 2048, 0, None, 0.0, 0.0, ws,
+                                          big, None) == tsd.ATTN_ERR_INVALID
+    assert lib.encoder_layer_forward_host(*args, 2, 16, 384, 8, 64, 2048, 0, None, 0.0, 1e-6, ws,
+                                          big, None) == tsd.ATTN_ERR_UNSUPPORTED
+    # attn_decode_host: null cache, too many queries
+    assert lib.attn_decode_host(hx, None, w, hx, 1, 1, 1, 128, 64, 64, None, 0.0, ws, big,
+                                None) == tsd.ATTN_ERR_INVALID
+    # the device entry point's codes: more than 8 queries, a cache past 131072 rows
+    assert lib.attn_decode_host(hx, w, w, hx, 1, 1, 9, 128, 64, 64, None, 0.0, ws, big,
+                                None) == tsd.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_decode_host(hx, w, w, hx, 1, 1, 1, 131072 + 256, 64, 64, None, 0.0, ws, big,
+                                None) == tsd.ATTN_ERR_UNSUPPORTED
+
+
+def test_host_entry_points_empty_problems_are_no_ops(lib):
+    ws = 1 << 24
+    hx = FAKE
+    assert lib.attn_forward_host(hx, hx, hx, hx, 0, 1, 16, 16, 64, 64, 0, None, 0.0, ws,
+                                 1 << 30, None) == tsd.ATTN_OK
+    assert lib.mha_forward_host(hx, hx, FAKE, FAKE, FAKE, FAKE, hx, 0, 16, 16, 512, 8, 64, 64, 0,
+                                None, 0.0, ws, 1 << 30, None) == tsd.ATTN_OK

@@ -25,7 +25,10 @@ __all__ = [
     "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out", "mha_forward_noalloc",
     "mha_concat_heads", "mha_forward_launches", "attn_forward_window", "attn_decode",
     "attn_decode_workspace_bytes", "encoder_layer_forward", "encoder_layer_workspace_bytes",
-    "MHA_NOALLOC_SCRATCH_BYTES",
+    "MHA_NOALLOC_SCRATCH_BYTES", "attn_host_workspace_bytes", "attn_forward_host",
+    "mha_host_workspace_bytes", "mha_forward_host", "encoder_layer_host_workspace_bytes",
+    "encoder_layer_forward_host", "attn_decode_host_workspace_bytes", "attn_decode_host",
+    "attn_forward_window_host",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = range(5)
@@ -37,6 +40,9 @@ EXPORTED_SYMBOLS = (
     "attn_selftest_wait_timeout", "mha_project_qkv", "mha_project_out", "mha_forward_noalloc",
     "mha_concat_heads", "mha_forward_launches", "attn_forward_window", "attn_decode",
     "attn_decode_workspace_bytes", "encoder_layer_forward", "encoder_layer_workspace_bytes",
+    "attn_host_workspace_bytes", "attn_forward_host", "mha_host_workspace_bytes",
+    "mha_forward_host", "encoder_layer_host_workspace_bytes", "encoder_layer_forward_host",
+    "attn_decode_host_workspace_bytes", "attn_decode_host", "attn_forward_window_host",
 )
 
 # TSD_MHA_NOALLOC_SCRATCH_BYTES of the header: the fixed scratch of mha_forward_noalloc
@@ -97,22 +103,38 @@ def library():
     lib.encoder_layer_workspace_bytes.argtypes = [i, i, i, i, i, i]
     lib.encoder_layer_workspace_bytes.restype = ctypes.c_size_t
     lib.encoder_layer_forward.argtypes = [vp] * 14 + [i] * 7 + [vp, f, f, vp, ctypes.c_size_t, st]
+    sz = ctypes.c_size_t
+    for name, n in (("attn_host_workspace_bytes", 6), ("mha_host_workspace_bytes", 7),
+                    ("encoder_layer_host_workspace_bytes", 6),
+                    ("attn_decode_host_workspace_bytes", 6)):
+        getattr(lib, name).argtypes = [i] * n
+        getattr(lib, name).restype = sz
+    lib.attn_forward_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, f, vp, sz, st]
+    lib.attn_forward_window_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, i, i, f, vp,
+                                             sz, st]
+    lib.mha_forward_host.argtypes = [vp] * 7 + [i] * 8 + [vp, f, vp, sz, st]
+    lib.encoder_layer_forward_host.argtypes = [vp] * 14 + [i] * 7 + [vp, f, f, vp, sz, st]
+    lib.attn_decode_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp, f, vp, sz, st]
     for name in ("attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_forward",
                  "attn_get_device_status", "attn_last_cuda_error", "attn_selftest_wait_timeout",
                  "mha_project_qkv", "mha_project_out", "mha_forward_noalloc", "mha_concat_heads",
                  "mha_forward_launches", "attn_forward_window", "attn_decode",
-                 "encoder_layer_forward"):
+                 "encoder_layer_forward", "attn_forward_host", "mha_forward_host",
+                 "encoder_layer_forward_host", "attn_decode_host", "attn_forward_window_host"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
 
 
 def _ptr(x):
+    """Address of a torch tensor (device or host), a numpy array (host), or an int."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
-    return x.data_ptr()
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return x.ctypes.data
 
 
 def _stream(s):
@@ -258,3 +280,75 @@ def attn_status_string(status: int) -> str:
 def attn_selftest_wait_timeout(limit_us: int, stream=None):
     _check(library().attn_selftest_wait_timeout(limit_us, _stream(stream)),
            "attn_selftest_wait_timeout")
+
+
+# ---------------------------------------------------------------- host buffers
+# The *_host entry points take the step's inputs and result in host memory
+# (pinned for asynchronous copies) and stage them through the workspace.
+
+def attn_host_workspace_bytes(B, h, n_q, n_k, d_k, d_v) -> int:
+    return int(library().attn_host_workspace_bytes(B, h, n_q, n_k, d_k, d_v))
+
+
+def attn_forward_host(q_host, k_host, v_host, out_host, B, h, n_q, n_k, d_k, d_v,
+                      mask_kind=ATTN_MASK_NONE, kv_lens_host=None, scale=0.0, workspace=None,
+                      workspace_bytes=0, stream=None):
+    _check(library().attn_forward_host(_ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(out_host),
+                                       B, h, n_q, n_k, d_k, d_v, mask_kind, _ptr(kv_lens_host),
+                                       scale, _ptr(workspace), workspace_bytes, _stream(stream)),
+           "attn_forward_host")
+
+
+def attn_forward_window_host(q_host, k_host, v_host, out_host, B, h, n_q, n_k, d_k, d_v,
+                             window_left, window_right, mask_kind=ATTN_MASK_NONE,
+                             kv_lens_host=None, scale=0.0, workspace=None, workspace_bytes=0,
+                             stream=None):
+    _check(library().attn_forward_window_host(_ptr(q_host), _ptr(k_host), _ptr(v_host),
+                                              _ptr(out_host), B, h, n_q, n_k, d_k, d_v, mask_kind,
+                                              _ptr(kv_lens_host), window_left, window_right,
+                                              scale, _ptr(workspace), workspace_bytes,
+                                              _stream(stream)),
+           "attn_forward_window_host")
+
+
+def mha_host_workspace_bytes(B, n_q, n_k, d_model, h, d_k, d_v) -> int:
+    return int(library().mha_host_workspace_bytes(B, n_q, n_k, d_model, h, d_k, d_v))
+
+
+def mha_forward_host(x_q_host, x_kv_host, w_q, w_k, w_v, w_o, out_host, B, n_q, n_k, d_model, h,
+                     d_k, d_v, mask_kind=ATTN_MASK_NONE, kv_lens_host=None, scale=0.0,
+                     workspace=None, workspace_bytes=0, stream=None):
+    _check(library().mha_forward_host(_ptr(x_q_host), _ptr(x_kv_host), _ptr(w_q), _ptr(w_k),
+                                      _ptr(w_v), _ptr(w_o), _ptr(out_host), B, n_q, n_k, d_model,
+                                      h, d_k, d_v, mask_kind, _ptr(kv_lens_host), scale,
+                                      _ptr(workspace), workspace_bytes, _stream(stream)),
+           "mha_forward_host")
+
+
+def encoder_layer_host_workspace_bytes(B, n, d_model, h, d_k, d_ff) -> int:
+    return int(library().encoder_layer_host_workspace_bytes(B, n, d_model, h, d_k, d_ff))
+
+
+def encoder_layer_forward_host(x_host, w_q, w_k, w_v, w_o, ln1_gamma, ln1_beta, w_1, b_1, w_2,
+                               b_2, ln2_gamma, ln2_beta, out_host, B, n, d_model, h, d_k, d_ff,
+                               mask_kind=ATTN_MASK_NONE, kv_lens_host=None, scale=0.0, eps=1e-6,
+                               workspace=None, workspace_bytes=0, stream=None):
+    ptrs = [_ptr(t) for t in (x_host, w_q, w_k, w_v, w_o, ln1_gamma, ln1_beta, w_1, b_1, w_2, b_2,
+                              ln2_gamma, ln2_beta, out_host)]
+    _check(library().encoder_layer_forward_host(*ptrs, B, n, d_model, h, d_k, d_ff, mask_kind,
+                                                _ptr(kv_lens_host), scale, eps, _ptr(workspace),
+                                                workspace_bytes, _stream(stream)),
+           "encoder_layer_forward_host")
+
+
+def attn_decode_host_workspace_bytes(B, h, n_q, n_max, d_k, d_v) -> int:
+    return int(library().attn_decode_host_workspace_bytes(B, h, n_q, n_max, d_k, d_v))
+
+
+def attn_decode_host(q_host, k_cache, v_cache, out_host, B, h, n_q, n_max, d_k, d_v,
+                     cache_lens_host=None, scale=0.0, workspace=None, workspace_bytes=0,
+                     stream=None):
+    _check(library().attn_decode_host(_ptr(q_host), _ptr(k_cache), _ptr(v_cache), _ptr(out_host),
+                                      B, h, n_q, n_max, d_k, d_v, _ptr(cache_lens_host), scale,
+                                      _ptr(workspace), workspace_bytes, _stream(stream)),
+           "attn_decode_host")

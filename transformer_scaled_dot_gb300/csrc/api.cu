@@ -10,6 +10,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include "host_stage.h"
 #include "kernels.h"
 #include "tsd_attention.h"
 
@@ -460,6 +461,146 @@ attn_status launch_linear(const void* x, const void* w, const void* bias, const 
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
+
+// The checks of each entry point, apart from its launches, so that the
+// host-buffer entry points can refuse bad arguments before copying anything.
+attn_status attn_check(const void* q, const void* k, const void* v, const void* out, int B, int h,
+                       int n_q, int n_k, int d_k, int d_v, int mask_kind, const int32_t* kv_lens,
+                       float scale) {
+  attn_status s = check_common(B, h, n_q, n_k, d_k, d_v, mask_kind, kv_lens, scale);
+  if (s != ATTN_OK) return s;
+  if (!q || !k || !v || !out) return ATTN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_INVALID;
+  return check_bf16_head_dims(d_k, d_v);
+}
+
+attn_status mha_check(const void* x_q, const void* x_kv, const void* w_q, const void* w_k,
+                      const void* w_v, const void* w_o, const void* out, int B, int n_q, int n_k,
+                      int d_model, int h, int d_k, int d_v, int mask_kind,
+                      const int32_t* kv_lens, float scale, const void* workspace,
+                      size_t workspace_bytes) {
+  attn_status s = check_common(B, h, n_q, n_k, d_k, d_v, mask_kind, kv_lens, scale);
+  if (s != ATTN_OK) return s;
+  if (h <= 0 || d_model < 8 || (d_model % 8) != 0) return ATTN_ERR_INVALID;
+  const void* ptrs[8] = {x_q, x_kv, w_q, w_k, w_v, w_o, out, workspace};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID;
+  s = check_bf16_head_dims(d_k, d_v);
+  if (s != ATTN_OK) return s;
+  MhaLayout L;
+  if (!mha_layout(B, n_q, n_k, h, d_k, d_v, &L)) return ATTN_ERR_INVALID;
+  if (workspace_bytes < L.total) return ATTN_ERR_INVALID;
+  if (int64_t(B) * n_q > INT32_MAX || int64_t(B) * n_k > INT32_MAX) return ATTN_ERR_INVALID;
+  return ATTN_OK;
+}
+
+attn_status encoder_check(const void* const* ptrs15, int B, int n, int d_model, int h, int d_k,
+                          int d_ff, int mask_kind, const int32_t* kv_lens, float scale, float eps,
+                          const void* workspace, size_t workspace_bytes) {
+  attn_status s = check_common(B, h, n, n, d_k, d_k, mask_kind, kv_lens, scale);
+  if (s != ATTN_OK) return s;
+  if (!(eps > 0.f) || !std::isfinite(eps)) return ATTN_ERR_INVALID;
+  if (d_model != 256 && d_model != 512 && d_model != 1024 && d_model != 2048)
+    return ATTN_ERR_UNSUPPORTED;
+  if (d_ff < 8 || (d_ff % 8) != 0) return ATTN_ERR_INVALID;
+  s = check_bf16_head_dims(d_k, d_k);
+  if (s != ATTN_OK) return s;
+  for (int i = 0; i < 15; ++i)
+    if (ptrs15[i] == nullptr || !aligned16(ptrs15[i])) return ATTN_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID;
+  EncoderLayout L;
+  if (!encoder_layout(B, n, d_model, h, d_k, d_ff, &L)) return ATTN_ERR_INVALID;
+  if (workspace_bytes < L.total) return ATTN_ERR_INVALID;
+  if (int64_t(B) * n > INT32_MAX) return ATTN_ERR_INVALID;
+  return ATTN_OK;
+}
+
+attn_status decode_check(const void* q, const void* k_cache, const void* v_cache, const void* out,
+                         int B, int h, int n_q, int n_max, int d_k, int d_v,
+                         const int32_t* cache_lens, float scale, const void* workspace,
+                         size_t workspace_bytes) {
+  if (B < 0 || h < 0 || n_q < 1 || n_max < 1) return ATTN_ERR_INVALID;
+  if (n_q > tsd::kDecodeMaxQueries || tsd::decode_chunks(n_max) > tsd::kDecodeMaxChunks)
+    return ATTN_ERR_UNSUPPORTED;
+  if (B > 65535 || h > 65535 || int64_t(B) * h > INT32_MAX) return ATTN_ERR_INVALID;
+  if (!valid_scale(scale)) return ATTN_ERR_INVALID;
+  if (d_k != d_v || (d_k != 64 && d_k != 128)) return ATTN_ERR_UNSUPPORTED;
+  const void* ptrs[5] = {q, k_cache, v_cache, out, workspace};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID;
+  if (cache_lens != nullptr && (reinterpret_cast<uintptr_t>(cache_lens) & 3u))
+    return ATTN_ERR_INVALID;
+  size_t ob = 0, total = 0;
+  if (!decode_layout(B, h, n_q, n_max, d_v, &ob, &total)) return ATTN_ERR_INVALID;
+  if (workspace_bytes < total) return ATTN_ERR_INVALID;
+  return ATTN_OK;
+}
+
+// Staging regions of the host-buffer entry points, 256-byte aligned, in
+// order; the device entry point's own workspace follows them.
+struct StageLayout {
+  size_t end = 0;
+  bool ok = true;
+  size_t add(uint64_t bytes) {
+    const size_t off = end;
+    if (bytes > (uint64_t(1) << 60) || end > (size_t(1) << 61)) ok = false;
+    else end += align256(bytes);
+    return off;
+  }
+};
+
+// Staging layouts of the host-buffer entry points; false for invalid sizes.
+bool attn_host_layout(int B, int h, int n_q, int n_k, int d_k, int d_v, size_t* total) {
+  if (B < 0 || h < 0 || n_q < 0 || n_k < 0 || d_k <= 0 || d_v <= 0) return false;
+  StageLayout S;
+  S.add(uint64_t(B) * h * n_q * d_k * 2);
+  S.add(uint64_t(B) * h * n_k * d_k * 2);
+  S.add(uint64_t(B) * h * n_k * d_v * 2);
+  S.add(uint64_t(B) * 4);
+  S.add(uint64_t(B) * h * n_q * d_v * 2);
+  *total = S.end;
+  return S.ok;
+}
+
+bool mha_host_layout(int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
+                     size_t* total) {
+  MhaLayout L;
+  if (d_model <= 0 || !mha_layout(B, n_q, n_k, h, d_k, d_v, &L)) return false;
+  StageLayout S;
+  S.add(uint64_t(B) * n_q * d_model * 2);
+  S.add(uint64_t(B) * n_k * d_model * 2);
+  S.add(uint64_t(B) * 4);
+  S.add(uint64_t(B) * n_q * d_model * 2);
+  S.add(L.total);
+  *total = S.end;
+  return S.ok;
+}
+
+bool encoder_host_layout(int B, int n, int d_model, int h, int d_k, int d_ff, size_t* total) {
+  EncoderLayout L;
+  if (!encoder_layout(B, n, d_model, h, d_k, d_ff, &L)) return false;
+  StageLayout S;
+  S.add(uint64_t(B) * n * d_model * 2);
+  S.add(uint64_t(B) * 4);
+  S.add(uint64_t(B) * n * d_model * 2);
+  S.add(L.total);
+  *total = S.end;
+  return S.ok;
+}
+
+bool decode_host_layout(int B, int h, int n_q, int n_max, int d_k, int d_v, size_t* total) {
+  size_t ob = 0, inner = 0;
+  if (d_k <= 0 || !decode_layout(B, h, n_q, n_max, d_v, &ob, &inner)) return false;
+  StageLayout S;
+  S.add(uint64_t(B) * h * n_q * d_k * 2);
+  S.add(uint64_t(B) * 4);
+  S.add(uint64_t(B) * h * n_q * d_v * 2);
+  S.add(inner);
+  *total = S.end;
+  return S.ok;
+}
+
 }  // namespace
 
 extern "C" {
@@ -467,11 +608,7 @@ extern "C" {
 attn_status attn_forward(const void* q, const void* k, const void* v, void* out, int B, int h,
                          int n_q, int n_k, int d_k, int d_v, int mask_kind, const int32_t* kv_lens,
                          float scale, tsd_stream_t stream) {
-  attn_status s = check_common(B, h, n_q, n_k, d_k, d_v, mask_kind, kv_lens, scale);
-  if (s != ATTN_OK) return s;
-  if (!q || !k || !v || !out) return ATTN_ERR_INVALID;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_INVALID;
-  s = check_bf16_head_dims(d_k, d_v);
+  attn_status s = attn_check(q, k, v, out, B, h, n_q, n_k, d_k, d_v, mask_kind, kv_lens, scale);
   if (s != ATTN_OK) return s;
   if (B == 0 || h == 0 || n_q == 0) return ATTN_OK;  // nothing to write
   const int64_t d = d_k;
@@ -565,21 +702,12 @@ attn_status mha_forward(const void* x_q, const void* x_kv, const void* w_q, cons
                         int d_model, int h, int d_k, int d_v, int mask_kind,
                         const int32_t* kv_lens, float scale, void* workspace,
                         size_t workspace_bytes, tsd_stream_t stream_) {
-  attn_status s = check_common(B, h, n_q, n_k, d_k, d_v, mask_kind, kv_lens, scale);
-  if (s != ATTN_OK) return s;
-  if (h <= 0 || d_model < 8 || (d_model % 8) != 0) return ATTN_ERR_INVALID;
-  const void* ptrs[8] = {x_q, x_kv, w_q, w_k, w_v, w_o, out, workspace};
-  for (const void* p : ptrs)
-    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID;
-  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID;
-  s = check_bf16_head_dims(d_k, d_v);
+  attn_status s = mha_check(x_q, x_kv, w_q, w_k, w_v, w_o, out, B, n_q, n_k, d_model, h, d_k, d_v,
+                            mask_kind, kv_lens, scale, workspace, workspace_bytes);
   if (s != ATTN_OK) return s;
   MhaLayout L;
-  if (!mha_layout(B, n_q, n_k, h, d_k, d_v, &L)) return ATTN_ERR_INVALID;
-  if (workspace_bytes < L.total) return ATTN_ERR_INVALID;
-  const int64_t Mq = int64_t(B) * n_q, Mk = int64_t(B) * n_k;
-  if (Mq > INT32_MAX || Mk > INT32_MAX) return ATTN_ERR_INVALID;
-  if (Mq == 0) return ATTN_OK;
+  mha_layout(B, n_q, n_k, h, d_k, d_v, &L);
+  if (int64_t(B) * n_q == 0) return ATTN_OK;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* Q = ws + L.q_off;
@@ -609,20 +737,11 @@ attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache,
                         int h, int n_q, int n_max, int d_k, int d_v, const int32_t* cache_lens,
                         float scale, void* workspace, size_t workspace_bytes,
                         tsd_stream_t stream) {
-  if (B < 0 || h < 0 || n_q < 1 || n_max < 1) return ATTN_ERR_INVALID;
-  if (n_q > tsd::kDecodeMaxQueries || tsd::decode_chunks(n_max) > tsd::kDecodeMaxChunks)
-    return ATTN_ERR_UNSUPPORTED;
-  if (B > 65535 || h > 65535 || int64_t(B) * h > INT32_MAX) return ATTN_ERR_INVALID;
-  if (!valid_scale(scale)) return ATTN_ERR_INVALID;
-  if (d_k != d_v || (d_k != 64 && d_k != 128)) return ATTN_ERR_UNSUPPORTED;
-  const void* ptrs[5] = {q, k_cache, v_cache, out, workspace};
-  for (const void* p : ptrs)
-    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID;
-  if (cache_lens != nullptr && (reinterpret_cast<uintptr_t>(cache_lens) & 3u))
-    return ATTN_ERR_INVALID;
+  attn_status s = decode_check(q, k_cache, v_cache, out, B, h, n_q, n_max, d_k, d_v, cache_lens,
+                               scale, workspace, workspace_bytes);
+  if (s != ATTN_OK) return s;
   size_t ob = 0, total = 0;
-  if (!decode_layout(B, h, n_q, n_max, d_v, &ob, &total)) return ATTN_ERR_INVALID;
-  if (workspace_bytes < total) return ATTN_ERR_INVALID;
+  decode_layout(B, h, n_q, n_max, d_v, &ob, &total);
   if (B == 0 || h == 0) return ATTN_OK;
   tsd::DecodeProblem p;
   std::memset(&p, 0, sizeof(p));
@@ -662,25 +781,14 @@ attn_status encoder_layer_forward(const void* x, const void* w_q, const void* w_
                                   const int32_t* kv_lens, float scale, float eps,
                                   void* workspace, size_t workspace_bytes,
                                   tsd_stream_t stream_) {
-  attn_status s = check_common(B, h, n, n, d_k, d_k, mask_kind, kv_lens, scale);
-  if (s != ATTN_OK) return s;
-  if (!(eps > 0.f) || !std::isfinite(eps)) return ATTN_ERR_INVALID;
-  if (d_model != 256 && d_model != 512 && d_model != 1024 && d_model != 2048)
-    return ATTN_ERR_UNSUPPORTED;
-  if (d_ff < 8 || (d_ff % 8) != 0) return ATTN_ERR_INVALID;
-  s = check_bf16_head_dims(d_k, d_k);
-  if (s != ATTN_OK) return s;
   const void* ptrs[15] = {x, w_q, w_k, w_v, w_o, ln1_gamma, ln1_beta, w_1, b_1, w_2, b_2,
                           ln2_gamma, ln2_beta, out, workspace};
-  for (const void* p : ptrs)
-    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID;
-  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID;
+  attn_status s = encoder_check(ptrs, B, n, d_model, h, d_k, d_ff, mask_kind, kv_lens, scale, eps,
+                                workspace, workspace_bytes);
+  if (s != ATTN_OK) return s;
   EncoderLayout L;
-  if (!encoder_layout(B, n, d_model, h, d_k, d_ff, &L)) return ATTN_ERR_INVALID;
-  if (workspace_bytes < L.total) return ATTN_ERR_INVALID;
-  const int64_t rows64 = int64_t(B) * n;
-  if (rows64 > INT32_MAX) return ATTN_ERR_INVALID;
-  const int rows = static_cast<int>(rows64);
+  encoder_layout(B, n, d_model, h, d_k, d_ff, &L);
+  const int rows = static_cast<int>(int64_t(B) * n);
   if (rows == 0) return ATTN_OK;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -805,6 +913,231 @@ attn_status attn_selftest_wait_timeout(int limit_us, tsd_stream_t stream) {
   cudaError_t e = tsd::launch_wait_timeout_selftest(static_cast<unsigned long long>(limit_us) * 1000ull,
                                                     reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+// ---------------------------------------------------------------- host buffers
+// The same operations with the step's inputs and result in host memory: the
+// inputs are copied into staging regions at the front of the workspace, the
+// device entry point runs on them (on `stream`), and the result is copied
+// back on `stream` (host_stage.h has the ordering).
+
+size_t attn_host_workspace_bytes(int B, int h, int n_q, int n_k, int d_k, int d_v) {
+  size_t t = 0;
+  return attn_host_layout(B, h, n_q, n_k, d_k, d_v, &t) ? t : 0;
+}
+
+}  // extern "C"
+
+namespace {
+
+// attn_forward_host and attn_forward_window_host (windowed: the window's
+// bounds apply, as in attn_forward_window)
+attn_status attn_host_call(const void* q_host, const void* k_host, const void* v_host,
+                           void* out_host, int B, int h, int n_q, int n_k, int d_k, int d_v,
+                           int mask_kind, const int32_t* kv_lens_host, bool windowed,
+                           int window_left, int window_right, float scale, void* workspace,
+                           size_t workspace_bytes, tsd_stream_t stream) {
+  if (!q_host || !k_host || !v_host || !out_host || !workspace) return ATTN_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID;
+  size_t need = 0;
+  if (!attn_host_layout(B, h, n_q, n_k, d_k, d_v, &need) || workspace_bytes < need)
+    return ATTN_ERR_INVALID;
+  if (windowed && (window_left < -1 || window_right < -1 ||
+                   ((window_left >= 0 || window_right >= 0) && n_q != n_k)))
+    return ATTN_ERR_INVALID;
+  StageLayout S;
+  const uint64_t qb = uint64_t(B) * h * n_q * d_k * 2, kb = uint64_t(B) * h * n_k * d_k * 2,
+                 vb = uint64_t(B) * h * n_k * d_v * 2, ob = uint64_t(B) * h * n_q * d_v * 2;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* q = ws + S.add(qb);
+  void* k = ws + S.add(kb);
+  void* v = ws + S.add(vb);
+  int32_t* lens = reinterpret_cast<int32_t*>(ws + S.add(uint64_t(B) * 4));
+  void* out = ws + S.add(ob);
+  const bool pad = (mask_kind & ATTN_MASK_KEY_PADDING) != 0 && kv_lens_host != nullptr;
+  attn_status s = attn_check(q, k, v, out, B, h, n_q, n_k, d_k, d_v, mask_kind,
+                             pad ? lens : nullptr, scale);
+  if (s != ATTN_OK) return s;
+  if (B == 0 || h == 0 || n_q == 0) return ATTN_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  tsd::HostStage hs(workspace, st);
+  hs.copy_in(q, q_host, qb);
+  hs.copy_in(k, k_host, kb);
+  hs.copy_in(v, v_host, vb);
+  if (pad) hs.copy_in(lens, kv_lens_host, size_t(B) * 4);
+  if (hs.inputs_ready() != cudaSuccess) return cuda_fail(hs.status());
+  s = windowed ? attn_forward_window(q, k, v, out, B, h, n_q, n_k, d_k, d_v, mask_kind,
+                                     pad ? lens : nullptr, window_left, window_right, scale,
+                                     stream)
+               : attn_forward(q, k, v, out, B, h, n_q, n_k, d_k, d_v, mask_kind,
+                              pad ? lens : nullptr, scale, stream);
+  hs.computed();
+  if (s != ATTN_OK) return s;
+  return hs.copy_out(out_host, out, ob) == cudaSuccess ? ATTN_OK : cuda_fail(hs.status());
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_forward_host(const void* q_host, const void* k_host, const void* v_host,
+                              void* out_host, int B, int h, int n_q, int n_k, int d_k, int d_v,
+                              int mask_kind, const int32_t* kv_lens_host, float scale,
+                              void* workspace, size_t workspace_bytes, tsd_stream_t stream) {
+  return attn_host_call(q_host, k_host, v_host, out_host, B, h, n_q, n_k, d_k, d_v, mask_kind,
+                        kv_lens_host, false, -1, -1, scale, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_forward_window_host(const void* q_host, const void* k_host, const void* v_host,
+                                     void* out_host, int B, int h, int n_q, int n_k, int d_k,
+                                     int d_v, int mask_kind, const int32_t* kv_lens_host,
+                                     int window_left, int window_right, float scale,
+                                     void* workspace, size_t workspace_bytes,
+                                     tsd_stream_t stream) {
+  return attn_host_call(q_host, k_host, v_host, out_host, B, h, n_q, n_k, d_k, d_v, mask_kind,
+                        kv_lens_host, true, window_left, window_right, scale, workspace,
+                        workspace_bytes, stream);
+}
+
+size_t mha_host_workspace_bytes(int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v) {
+  size_t t = 0;
+  return mha_host_layout(B, n_q, n_k, d_model, h, d_k, d_v, &t) ? t : 0;
+}
+
+attn_status mha_forward_host(const void* x_q_host, const void* x_kv_host, const void* w_q,
+                             const void* w_k, const void* w_v, const void* w_o, void* out_host,
+                             int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
+                             int mask_kind, const int32_t* kv_lens_host, float scale,
+                             void* workspace, size_t workspace_bytes, tsd_stream_t stream) {
+  if (!x_q_host || !x_kv_host || !out_host || !workspace) return ATTN_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID;
+  size_t need = 0;
+  if (!mha_host_layout(B, n_q, n_k, d_model, h, d_k, d_v, &need) || workspace_bytes < need)
+    return ATTN_ERR_INVALID;
+  // one host array for both (self-attention) -> one staged copy, so the
+  // device entry point sees x_kv == x_q and takes its self-attention path
+  const bool self = x_kv_host == x_q_host && n_q == n_k;
+  const uint64_t xqb = uint64_t(B) * n_q * d_model * 2, xkb = uint64_t(B) * n_k * d_model * 2;
+  StageLayout S;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* x_q = ws + S.add(xqb);
+  void* x_kv = ws + S.add(xkb);
+  if (self) x_kv = x_q;
+  int32_t* lens = reinterpret_cast<int32_t*>(ws + S.add(uint64_t(B) * 4));
+  void* out = ws + S.add(xqb);
+  const size_t inner_off = S.add(0);
+  void* inner = ws + inner_off;
+  const size_t inner_bytes = workspace_bytes - inner_off;
+  const bool pad = (mask_kind & ATTN_MASK_KEY_PADDING) != 0 && kv_lens_host != nullptr;
+  attn_status s = mha_check(x_q, x_kv, w_q, w_k, w_v, w_o, out, B, n_q, n_k, d_model, h, d_k, d_v,
+                            mask_kind, pad ? lens : nullptr, scale, inner, inner_bytes);
+  if (s != ATTN_OK) return s;
+  if (int64_t(B) * n_q == 0) return ATTN_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  tsd::HostStage hs(workspace, st);
+  hs.copy_in(x_q, x_q_host, xqb);
+  if (!self) hs.copy_in(x_kv, x_kv_host, xkb);
+  if (pad) hs.copy_in(lens, kv_lens_host, size_t(B) * 4);
+  if (hs.inputs_ready() != cudaSuccess) return cuda_fail(hs.status());
+  s = mha_forward(x_q, x_kv, w_q, w_k, w_v, w_o, out, B, n_q, n_k, d_model, h, d_k, d_v, mask_kind,
+                  pad ? lens : nullptr, scale, inner, inner_bytes, stream);
+  hs.computed();
+  if (s != ATTN_OK) return s;
+  return hs.copy_out(out_host, out, xqb) == cudaSuccess ? ATTN_OK : cuda_fail(hs.status());
+}
+
+size_t encoder_layer_host_workspace_bytes(int B, int n, int d_model, int h, int d_k, int d_ff) {
+  size_t t = 0;
+  return encoder_host_layout(B, n, d_model, h, d_k, d_ff, &t) ? t : 0;
+}
+
+attn_status encoder_layer_forward_host(const void* x_host, const void* w_q, const void* w_k,
+                                       const void* w_v, const void* w_o, const void* ln1_gamma,
+                                       const void* ln1_beta, const void* w_1, const void* b_1,
+                                       const void* w_2, const void* b_2, const void* ln2_gamma,
+                                       const void* ln2_beta, void* out_host, int B, int n,
+                                       int d_model, int h, int d_k, int d_ff, int mask_kind,
+                                       const int32_t* kv_lens_host, float scale, float eps,
+                                       void* workspace, size_t workspace_bytes,
+                                       tsd_stream_t stream) {
+  if (!x_host || !out_host || !workspace) return ATTN_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID;
+  size_t need = 0;
+  if (!encoder_host_layout(B, n, d_model, h, d_k, d_ff, &need) || workspace_bytes < need)
+    return ATTN_ERR_INVALID;
+  const uint64_t xb = uint64_t(B) * n * d_model * 2;
+  StageLayout S;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* x = ws + S.add(xb);
+  int32_t* lens = reinterpret_cast<int32_t*>(ws + S.add(uint64_t(B) * 4));
+  void* out = ws + S.add(xb);
+  const size_t inner_off = S.add(0);
+  void* inner = ws + inner_off;
+  const size_t inner_bytes = workspace_bytes - inner_off;
+  const bool pad = (mask_kind & ATTN_MASK_KEY_PADDING) != 0 && kv_lens_host != nullptr;
+  const void* ptrs[15] = {x, w_q, w_k, w_v, w_o, ln1_gamma, ln1_beta, w_1, b_1, w_2, b_2,
+                          ln2_gamma, ln2_beta, out, inner};
+  attn_status s = encoder_check(ptrs, B, n, d_model, h, d_k, d_ff, mask_kind,
+                                pad ? lens : nullptr, scale, eps, inner, inner_bytes);
+  if (s != ATTN_OK) return s;
+  if (int64_t(B) * n == 0) return ATTN_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  tsd::HostStage hs(workspace, st);
+  hs.copy_in(x, x_host, xb);
+  if (pad) hs.copy_in(lens, kv_lens_host, size_t(B) * 4);
+  if (hs.inputs_ready() != cudaSuccess) return cuda_fail(hs.status());
+  s = encoder_layer_forward(x, w_q, w_k, w_v, w_o, ln1_gamma, ln1_beta, w_1, b_1, w_2, b_2,
+                            ln2_gamma, ln2_beta, out, B, n, d_model, h, d_k, d_ff, mask_kind,
+                            pad ? lens : nullptr, scale, eps, inner, inner_bytes, stream);
+  hs.computed();
+  if (s != ATTN_OK) return s;
+  return hs.copy_out(out_host, out, xb) == cudaSuccess ? ATTN_OK : cuda_fail(hs.status());
+}
+
+size_t attn_decode_host_workspace_bytes(int B, int h, int n_q, int n_max, int d_k, int d_v) {
+  size_t t = 0;
+  return decode_host_layout(B, h, n_q, n_max, d_k, d_v, &t) ? t : 0;
+}
+
+attn_status attn_decode_host(const void* q_host, const void* k_cache, const void* v_cache,
+                             void* out_host, int B, int h, int n_q, int n_max, int d_k, int d_v,
+                             const int32_t* cache_lens_host, float scale, void* workspace,
+                             size_t workspace_bytes, tsd_stream_t stream) {
+  if (!q_host || !out_host || !workspace) return ATTN_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID;
+  size_t need = 0;
+  if (!decode_host_layout(B, h, n_q, n_max, d_k, d_v, &need)) {
+    // the device entry point's own code for these sizes (query and cache
+    // limits are ATTN_ERR_UNSUPPORTED there)
+    const attn_status s = decode_check(workspace, k_cache, v_cache, workspace, B, h, n_q, n_max,
+                                       d_k, d_v, nullptr, scale, workspace, 0);
+    return s != ATTN_OK ? s : ATTN_ERR_INVALID;
+  }
+  if (workspace_bytes < need) return ATTN_ERR_INVALID;
+  const uint64_t qb = uint64_t(B) * h * n_q * d_k * 2, ob = uint64_t(B) * h * n_q * d_v * 2;
+  StageLayout S;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* q = ws + S.add(qb);
+  int32_t* lens = reinterpret_cast<int32_t*>(ws + S.add(uint64_t(B) * 4));
+  void* out = ws + S.add(ob);
+  const size_t inner_off = S.add(0);
+  void* inner = ws + inner_off;
+  const size_t inner_bytes = workspace_bytes - inner_off;
+  const bool has_lens = cache_lens_host != nullptr;
+  attn_status s = decode_check(q, k_cache, v_cache, out, B, h, n_q, n_max, d_k, d_v,
+                               has_lens ? lens : nullptr, scale, inner, inner_bytes);
+  if (s != ATTN_OK) return s;
+  if (B == 0 || h == 0) return ATTN_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  tsd::HostStage hs(workspace, st);
+  hs.copy_in(q, q_host, qb);
+  if (has_lens) hs.copy_in(lens, cache_lens_host, size_t(B) * 4);
+  if (hs.inputs_ready() != cudaSuccess) return cuda_fail(hs.status());
+  s = attn_decode(q, k_cache, v_cache, out, B, h, n_q, n_max, d_k, d_v, has_lens ? lens : nullptr,
+                  scale, inner, inner_bytes, stream);
+  hs.computed();
+  if (s != ATTN_OK) return s;
+  return hs.copy_out(out_host, out, ob) == cudaSuccess ? ATTN_OK : cuda_fail(hs.status());
 }
 
 }  // extern "C"

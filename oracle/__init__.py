@@ -84,7 +84,12 @@ def _ip(a):
 
 
 def _f64(a):
-    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    """Values as contiguous fp64. 16-bit integer arrays are refused: those are
+    bf16 bit patterns, which must be widened to their values first."""
+    a = np.asarray(a)
+    if a.dtype in (np.uint16, np.int16):
+        raise TypeError("the oracle takes values, not 16-bit patterns: widen bf16 bits first")
+    return np.ascontiguousarray(a, dtype=np.float64)
 
 
 def default_scale(d_k: int) -> float:

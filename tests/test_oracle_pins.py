@@ -648,3 +648,12 @@ def test_encoder_layer_matches_torch_transformer_encoder_layer():
         ref = layer(t(x)).numpy()
     np.testing.assert_allclose(oracle.encoder_layer(x, *ws, *p, h, eps=1e-6), ref, rtol=1e-10,
                                atol=1e-10)
+
+
+def test_oracle_refuses_bf16_bit_patterns():
+    """A bf16 tensor's uint16 bits are not its values: the oracle refuses them."""
+    bits = np.zeros((1, 1, 4, 64), dtype=np.uint16)
+    with pytest.raises(TypeError):
+        oracle.attention(bits, bits, bits)
+    with pytest.raises(TypeError):
+        oracle.attention_rows(bits[0, 0], np.arange(4), bits[0, 0], bits[0, 0], causal=False)

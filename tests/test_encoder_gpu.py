@@ -98,3 +98,21 @@ def test_encoder_layer_small_batches_repeated(tsd, B):
                                kv_lens=m.kv_lens, eps=1e-6)
     for i, out in enumerate(outs):
         assert_bf16_close(to_host_f64(out), ref, f"B={B} layer {i}")
+
+
+@pytest.mark.parametrize("B,dm,h,ff", [(64, 1024, 16, 4096), (160, 512, 8, 2048)])
+def test_encoder_layer_several_row_tiles_per_cluster(tsd, B, dm, h, ff):
+    """Enough rows that each cluster of the second FFN GEMM (whose epilogue
+    takes the LayerNorm, a row's d_model columns over d_model / 128 CTAs)
+    walks several row tiles: the statistics slots alternate. Sequences are
+    independent, so the oracle checks a seeded sample of them."""
+    import torch
+    e = synthetic.encoder_inputs(4300 + B, B, 128, dm, h, ff, MASK_KEY_PADDING, (64, 128),
+                                 add_pe=True)
+    got = run_layer(tsd, e, 1e-6)
+    m = e.mha
+    pick = np.unique(np.concatenate([[0, B - 1], np.random.default_rng(B).choice(B, 4, False)]))
+    x, _, wq, wk, wv, wo = m.as_f64()
+    ref = oracle.encoder_layer(x[pick], wq, wk, wv, wo, *e.params_f64(), h, m.mask_kind,
+                               kv_lens=m.kv_lens[pick], eps=1e-6)
+    assert_bf16_close(got[pick], ref, f"B={B} d_model={dm}")

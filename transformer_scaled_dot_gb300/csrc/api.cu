@@ -461,6 +461,30 @@ attn_status launch_linear(const void* x, const void* w, const void* bias, const 
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
+// out = LayerNorm(x W + bias + residual32) over each row's N columns (N in
+// {128, 256, 512, 1024}): one GEMM launch whose epilogue normalises (the
+// row's columns spread over a cluster of N / 128 CTAs).
+attn_status launch_linear_ln(const void* x, const void* w, const void* bias,
+                             const float* residual32, const void* gamma, const void* beta,
+                             float eps, void* out, int M, int N, int K, cudaStream_t stream) {
+  if (M == 0) return ATTN_OK;
+  tsd::GemmProblem g;
+  std::memset(&g, 0, sizeof(g));
+  g.K = K;
+  g.num_groups = 1;
+  cudaError_t e = make_gemm_group(&g.g[0], x, w, out, M, N, K);
+  if (e != cudaSuccess) return cuda_fail(e);
+  g.g[0].bias = static_cast<const uint16_t*>(bias);
+  g.g[0].residual_f32 = residual32;
+  g.g[0].ldr = N;
+  g.g[0].ln_gamma = static_cast<const uint16_t*>(gamma);
+  g.g[0].ln_beta = static_cast<const uint16_t*>(beta);
+  g.g[0].ln_eps = eps;
+  finish_gemm_problem(&g);
+  e = tsd::launch_gemm_bf16(g, stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
 
 // The checks of each entry point, apart from its launches, so that the
 // host-buffer entry points can refuse bad arguments before copying anything.
@@ -810,6 +834,11 @@ attn_status encoder_layer_forward(const void* x, const void* w_q, const void* w_
   // 3. hid = max(0, y W_1 + b_1)
   s = launch_linear(y, w_1, b_1, nullptr, true, hid, false, rows, d_ff, d_model, stream);
   if (s != ATTN_OK) return s;
+  // 4-5. out = LayerNorm_2(y + (hid W_2 + b_2)): in the second GEMM's
+  // epilogue when a row's d_model columns fit one cluster (<= 8 x 128)
+  if (d_model <= 1024)
+    return launch_linear_ln(hid, w_2, b_2, y32, ln2_gamma, ln2_beta, eps, out, rows, d_model, d_ff,
+                            stream);
   // 4. z = y + (hid W_2 + b_2), fp32
   s = launch_linear(hid, w_2, b_2, y32, false, z, true, rows, d_model, d_ff, stream);
   if (s != ATTN_OK) return s;

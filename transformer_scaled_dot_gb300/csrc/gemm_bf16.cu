@@ -33,6 +33,20 @@
 //              while the next tile's main loop runs.
 // The head split needs no data movement: head i of Q is column block i of
 // the [B*n, h*d] result, which the attention kernel reads through strides.
+//
+// LayerNorm epilogue (the feed-forward sub-layer's "Add & Norm", section
+// 3.1: out = LayerNorm(y + FFN(y))): a row's N <= 1024 columns are spread
+// over a cluster of N / 128 CTAs along N, one 128-row tile per cluster step.
+// Each epilogue thread forms its row's v = acc + bias + residual in fp32,
+// writes v back over its accumulator, takes the mean and the centred sum of
+// squares of its 128 columns, and sends that pair to the other CTAs of the
+// cluster (st.async into a double-buffered slot, complete_tx on their
+// mbarrier); the cluster's pairs combine exactly (equal counts: the mean of
+// the means, and the sums of squares plus 128 times the squared offsets of
+// the partial means). It then re-reads v, normalises with gamma and beta,
+// and stores its bf16 row segment (256 contiguous bytes) straight to global
+// memory: the fp32 sum never goes to memory, and without a staging tile the
+// statistics slots fit beside all six stages.
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -44,9 +58,15 @@ constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kBK = kGemmBK;
 constexpr int kStages = 6;
+constexpr int kStagesLN = 6;      // LayerNorm epilogue (no staging tile: rows stored directly)
+constexpr int kMaxLnCluster = 8;  // N <= 8 x 128
 constexpr int kThreads = 192;
 constexpr int kAccCols = 128;
 constexpr int kTmemCols = 2 * kAccCols;
+// LayerNorm epilogue: one more 128-column region after the accumulators
+// holds the tile's fp32 residual, streamed in while the main loop runs
+constexpr int kResCol = 2 * kAccCols;
+constexpr int kTmemColsLN = 512;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB: one 128-row x 128-byte K atom column
 constexpr int kBBytes = kBK * kBN * 2;  // 16 KB: two 64-row (K) x 128-byte N chunks
 constexpr int kBChunk = kBK * 128;      // bytes of one 64-wide N chunk
@@ -56,12 +76,18 @@ constexpr uint32_t kEpiBarrier = 1;     // named barrier of the four epilogue wa
 constexpr unsigned long long kDrainLimitNs = 100ull * 1000ull * 1000ull;
 static_assert(kGemmClusterM >= 1 && kBK % kGemmClusterM == 0, "B rows split over the cluster");
 
-struct GemmSmem {
-  alignas(1024) uint8_t a[kStages][kABytes];
-  alignas(1024) uint8_t b[kStages][kBBytes];
-  alignas(1024) uint8_t c[kCStages][kCBytes];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+template <int ST, bool LN>
+struct GemmSmemT {
+  alignas(1024) uint8_t a[ST][kABytes];
+  alignas(1024) uint8_t b[ST][kBBytes];
+  alignas(1024) uint8_t c[LN ? 1 : kCStages][LN ? 16 : kCBytes];
+  // LayerNorm epilogue: per tile parity, per other CTA of the cluster (in
+  // rank order, skipping this one), per row: that CTA's (mean, centred sum
+  // of squares) over its 128 columns
+  float2 ln_stat[LN ? 2 : 1][LN ? kMaxLnCluster - 1 : 1][LN ? kBM : 1];
+  uint64_t ln_full[2];
+  uint64_t full[ST];
+  uint64_t empty[ST];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drained;
@@ -101,29 +127,60 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmProblem& p, int ct, in
 }
 
 // Epilogue modes (compile-time, so each instance holds only its own
-// registers): plain; + bias then ReLU; + bias + fp32 residual, fp32 output.
-constexpr int kEpiPlain = 0, kEpiBiasRelu = 1, kEpiBiasResF32 = 2;
+// registers): plain; + bias then ReLU; + bias + fp32 residual, fp32 output;
+// + bias + fp32 residual then LayerNorm over the row, bf16 output.
+constexpr int kEpiPlain = 0, kEpiBiasRelu = 1, kEpiBiasResF32 = 2, kEpiResLN = 3;
 
-template <int CM, int EPI>
+template <int EPI>
+struct GemmStages {
+  static constexpr int value = EPI == kEpiResLN ? kStagesLN : kStages;
+};
+template <int EPI>
+using GemmSmemFor = GemmSmemT<GemmStages<EPI>::value, EPI == kEpiResLN>;
+
+// CM: CTAs per cluster along M sharing B (multicast); CN: CTAs per cluster
+// along N sharing a row tile (LayerNorm epilogue only; then CM = 1).
+template <int CM, int EPI, int CN = 1>
 __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_constant__ GemmProblem p) {
+  constexpr bool LN = EPI == kEpiResLN;
+  constexpr int kSt = GemmStages<EPI>::value;
+  constexpr int CS = LN ? CN : CM;  // CTAs per cluster
+  static_assert(!LN || (CM == 1 && CN >= 1 && CN <= kMaxLnCluster), "LayerNorm clusters");
+  static_assert(LN || CN == 1, "clusters along N only for the LayerNorm epilogue");
+  using Smem = GemmSmemFor<EPI>;
   extern __shared__ uint8_t smem_raw[];
-  GemmSmem& sm = *reinterpret_cast<GemmSmem*>(
+  Smem& sm = *reinterpret_cast<Smem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = warp_id();
   const uint32_t lane = lane_id();
   const int kblocks = (p.K + kBK - 1) / kBK;
-  const int rank = CM > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int rank = CS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int mrank = CM > 1 ? rank : 0;  // position along M: which K rows of B this CTA loads
   constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CM) - 1u);
   constexpr int kBRows = kBK / CM;  // K rows of each B box this CTA loads
   // cluster tiles of this CTA's cluster: cluster id, + number of clusters, ...
-  const int first = static_cast<int>(blockIdx.x) / CM;
-  const int stride = static_cast<int>(gridDim.x) / CM;
+  const int first = static_cast<int>(blockIdx.x) / CS;
+  const int stride = static_cast<int>(gridDim.x) / CS;
+  // this CTA's output tile of cluster tile ct (LayerNorm: row tile ct,
+  // column block = rank)
+  auto coord = [&](int ct) -> TileCoord {
+    if constexpr (LN) {
+      TileCoord c;
+      c.g = &p.g[0];
+      c.m0 = ct * kBM;
+      c.n0 = rank * kBN;
+      return c;
+    } else {
+      return tile_coord<CM>(p, ct, rank);
+    }
+  };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSt; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], CM);  // released by the MMA warp of every CTA
     }
+    for (int s = 0; s < 2; ++s) mbar_init(&sm.ln_full[s], 1);
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sm.acc_full[a], 1);
       mbar_init(&sm.acc_empty[a], 128);
@@ -133,12 +190,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_alloc(&sm.tmem_base, LN ? kTmemColsLN : kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
-  // barriers of every CTA initialised before any peer multicasts into them
-  if constexpr (CM > 1) cluster_sync();
+  // barriers of every CTA initialised before any peer writes into them
+  if constexpr (CS > 1) cluster_sync();
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
@@ -163,10 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       int issued = 0;
       bool ok = true;
       for (int ct = first; ok && ct < p.total_tiles; ct += stride) {
-        const TileCoord c = tile_coord<CM>(p, ct, rank);
+        const TileCoord c = coord(ct);
         for (int kb = 0; kb < kblocks; ++kb) {
-          const int s = issued % kStages;
-          const uint32_t ph = static_cast<uint32_t>(issued / kStages) & 1u;
+          const int s = issued % kSt;
+          const uint32_t ph = static_cast<uint32_t>(issued / kSt) & 1u;
           // stage free in every CTA of the cluster (this CTA writes into all)
           if (!mbar_wait(&sm.empty[s], ph ^ 1u, abort_flag)) {
             ok = false;
@@ -176,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
           if (issued == 0) griddep_wait();
           const int k0 = kb * kBK;
           tma_load_2d(sm.a[s], &c.g->tm_a, &sm.full[s], k0, c.m0);
-          const int kr = k0 + rank * kBRows;
-          uint8_t* bdst = sm.b[s] + rank * kBRows * 128;
+          const int kr = k0 + mrank * kBRows;
+          uint8_t* bdst = sm.b[s] + mrank * kBRows * 128;
           if constexpr (CM > 1) {
             tma_load_2d_multicast(bdst, &c.g->tm_b, &sm.full[s], c.n0, kr, kClusterMask);
             tma_load_2d_multicast(bdst + kBChunk, &c.g->tm_b, &sm.full[s], c.n0 + 64, kr,
@@ -193,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       // release is still on its way here when the cluster leaves (and, after
       // an abort, no copy of this CTA is in flight).
       volatile uint32_t never = 0;
-      for (int i = max(0, issued - kStages); i < issued; ++i)
-        mbar_wait(&sm.empty[i % kStages], static_cast<uint32_t>(i / kStages) & 1u,
+      for (int i = max(0, issued - kSt); i < issued; ++i)
+        mbar_wait(&sm.empty[i % kSt], static_cast<uint32_t>(i / kSt) & 1u,
                   ok ? abort_flag : &never, kDrainLimitNs);
     }
   } else if (warp == 1) {
@@ -215,8 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * kAccCols;
         for (int kb = 0; kb < kblocks; ++kb) {
-          const int s = consumed % kStages;
-          ok = mbar_wait(&sm.full[s], static_cast<uint32_t>(consumed / kStages) & 1u, abort_flag);
+          const int s = consumed % kSt;
+          ok = mbar_wait(&sm.full[s], static_cast<uint32_t>(consumed / kSt) & 1u, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint64_t da = sdesc_advance(da0, static_cast<uint32_t>(s) * (kABytes >> 4));
@@ -255,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
     int it = 0;
     for (int ct = first; ct < p.total_tiles; ct += stride, ++it) {
       const int acc = it & 1;
-      const TileCoord c = tile_coord<CM>(p, ct, rank);
+      const TileCoord c = coord(ct);
       // the group's fields once into registers (reads through the pointer
       // into the parameter space would be repeated past every store)
       const uint16_t* const g_bias = c.g->bias;
@@ -287,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       // loaded while the main loop runs, later chunks' during the previous
       uint4 bias_all[EPI == kEpiBiasRelu ? kBN / 8 : 1];
       uint4 bw_next[4];
-      float4 rf_next[EPI == kEpiBiasResF32 ? 8 : 1];
+      float4 rf_next[(EPI == kEpiBiasResF32 || LN) ? 8 : 1];
       if constexpr (EPI == kEpiBiasRelu) {
 #pragma unroll
         for (int cc = 0; cc < kBN / 32; ++cc)
@@ -296,6 +353,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       if constexpr (EPI == kEpiBiasResF32) {
         load_bias(0, bw_next);
         load_res(0, *reinterpret_cast<float4(*)[8]>(rf_next));
+      }
+      if constexpr (LN) {
+        // The tile's residual rows -> tensor memory while the MMAs run (this
+        // warp's previous reads of the region finished with the last tile):
+        // the loads of the next 32 columns are in flight while one chunk is
+        // stored, and the epilogue later reads them back at TMEM latency.
+        const uint32_t res_addr = tmem + lane_base + kResCol;
+        load_res(0, *reinterpret_cast<float4(*)[8]>(rf_next));
+#pragma unroll
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          float4 rf[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) rf[k] = rf_next[k];
+          if (cc + 1 < kBN / 32) load_res(cc + 1, *reinterpret_cast<float4(*)[8]>(rf_next));
+          uint32_t w[32];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            w[4 * k] = __float_as_uint(rf[k].x);
+            w[4 * k + 1] = __float_as_uint(rf[k].y);
+            w[4 * k + 2] = __float_as_uint(rf[k].z);
+            w[4 * k + 3] = __float_as_uint(rf[k].w);
+          }
+          tmem_st32(res_addr + cc * 32, w);
+        }
+        tmem_wait_st();
+        load_bias(0, bw_next);
       }
       bool ok = __all_sync(
           0xffffffffu,
@@ -311,6 +394,131 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       // (their loads issued before the TMEM wait), then bf16 into the
       // swizzled staging tile or fp32 straight to global memory
       uint8_t* stage = sm.c[it % kCStages];
+      if constexpr (LN) {
+        const uint32_t acc_addr = tmem + lane_base + acc * kAccCols;
+        const uint16_t* const g_gamma = c.g->ln_gamma;
+        const uint16_t* const g_beta = c.g->ln_beta;
+        // (1) v = acc + bias + residual (fp32), written back over the
+        // accumulator; the sum of this CTA's 128 columns
+        const uint32_t res_addr = tmem + lane_base + kResCol;
+        float s1 = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          uint32_t x[32], rs[32];
+          tmem_ld32(acc_addr + cc * 32, x);
+          tmem_ld32(res_addr + cc * 32, rs);
+          uint4 bw[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) bw[k] = bw_next[k];
+          if (cc + 1 < kBN / 32) load_bias(cc + 1, bw_next);  // in flight meanwhile
+          float add[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) add[i] = 0.f;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            add_bf16x8(*reinterpret_cast<float(*)[8]>(add + 8 * k), bw[k]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float v = __uint_as_float(x[i]) + __uint_as_float(rs[i]) + add[i];
+            x[i] = __float_as_uint(v);
+            s1 += v;
+          }
+          tmem_st32(acc_addr + cc * 32, x);
+        }
+        tmem_wait_st();
+        const float mean_l = s1 * (1.f / kBN);
+        // (2) the centred sum of squares over the same columns
+        float m2 = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          uint32_t x[32];
+          tmem_ld32(acc_addr + cc * 32, x);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float d = __uint_as_float(x[i]) - mean_l;
+            m2 = fmaf(d, d, m2);
+          }
+        }
+        // (3) the pair to every other CTA of the cluster: slot (tile
+        // parity, this CTA's index among the receiver's others, row)
+        const int slot = it & 1;
+#pragma unroll
+        for (int q = 0; q < CS; ++q) {
+          if (q == rank) continue;
+          const int idx = rank < q ? rank : rank - 1;
+          st_async_f32x2(cluster_map(&sm.ln_stat[slot][idx][r], static_cast<uint32_t>(q)), mean_l,
+                         m2, cluster_map(&sm.ln_full[slot], static_cast<uint32_t>(q)));
+        }
+        if (r == 0) mbar_arrive_expect_tx(&sm.ln_full[slot], (CS - 1) * kBM * 8);
+        // gamma and beta of the first chunk while the pairs travel
+        uint4 gw[4], btw[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          gw[k] = __ldg(reinterpret_cast<const uint4*>(g_gamma + c.n0 + 8 * k));
+          btw[k] = __ldg(reinterpret_cast<const uint4*>(g_beta + c.n0 + 8 * k));
+        }
+        bool okl = __all_sync(0xffffffffu,
+                              mbar_wait_cluster(&sm.ln_full[slot], static_cast<uint32_t>(it >> 1) & 1u,
+                                                abort_flag));
+        // one decision for all four warps before the staging barrier below
+        okl = named_bar_and<kEpiBarrier>(128, okl);
+        if (!okl) break;
+        // (4) the row's mean and variance over all CS x 128 columns
+        float mean = mean_l;
+#pragma unroll
+        for (int q = 0; q < CS - 1; ++q) mean += sm.ln_stat[slot][q][r].x;
+        mean *= 1.f / CS;
+        float dm = mean_l - mean;
+        float M2 = fmaf(static_cast<float>(kBN) * dm, dm, m2);
+#pragma unroll
+        for (int q = 0; q < CS - 1; ++q) {
+          const float2 st = sm.ln_stat[slot][q][r];
+          dm = st.x - mean;
+          M2 += fmaf(static_cast<float>(kBN) * dm, dm, st.y);
+        }
+        const float rstd = rsqrtf(M2 * (1.f / (kBN * CS)) + c.g->ln_eps);
+        // (5) (v - mean) * rstd * gamma + beta -> bf16 staging tile
+#pragma unroll
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          uint32_t x[32];
+          tmem_ld32(acc_addr + cc * 32, x);
+          float g[32], bt[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) g[i] = bt[i] = 0.f;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            add_bf16x8(*reinterpret_cast<float(*)[8]>(g + 8 * k), gw[k]);
+            add_bf16x8(*reinterpret_cast<float(*)[8]>(bt + 8 * k), btw[k]);
+          }
+          if (cc + 1 < kBN / 32) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              gw[k] = __ldg(reinterpret_cast<const uint4*>(g_gamma + c.n0 + (cc + 1) * 32 + 8 * k));
+              btw[k] = __ldg(reinterpret_cast<const uint4*>(g_beta + c.n0 + (cc + 1) * 32 + 8 * k));
+            }
+          }
+          tmem_wait_ld();
+          if (cc == kBN / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(&sm.acc_empty[acc]);  // the MMA warp may reuse this accumulator
+          }
+          float y[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) y[i] = fmaf((__uint_as_float(x[i]) - mean) * rstd, g[i], bt[i]);
+          if (row_ok) {
+            uint16_t* dst = c.g->c + static_cast<int64_t>(row) * c.g->ldc + c.n0 + cc * 32;
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              const float* e = y + 8 * v4;
+              st_global_v4(dst + 8 * v4, pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
+                           pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+            }
+          }
+        }
+        continue;  // rows stored: no staging tile in this mode
+      } else {
 #pragma unroll
       for (int cc = 0; cc < kBN / 32; ++cc) {
         uint32_t x[32];
@@ -378,6 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
           }
         }
       }
+      }  // LN
       fence_proxy_async_smem();  // staged bytes visible to the TMA unit
       named_bar_sync<kEpiBarrier>(128);
       // a cluster's last row tiles may lie past M: computed on zero rows, not stored
@@ -395,10 +604,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
 
   tc_fence_before();
   // no CTA leaves while a peer may still write into its shared memory
-  if constexpr (CM > 1) cluster_sync();
+  if constexpr (CS > 1) cluster_sync();
   else __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, LN ? kTmemColsLN : kTmemCols);
 }
 
 int num_sms() {
@@ -414,7 +623,62 @@ int num_sms() {
 
 }  // namespace
 
+static_assert(sizeof(GemmSmemFor<kEpiPlain>) + 1024 <= 227 * 1024, "shared memory per CTA");
+static_assert(sizeof(GemmSmemFor<kEpiResLN>) + 1024 <= 227 * 1024, "shared memory per CTA");
+
+// The LayerNorm epilogue: one group, clusters of N / 128 CTAs along N, one
+// row tile per cluster step.
+template <int CN>
+cudaError_t launch_gemm_ln(const GemmProblem& problem, cudaStream_t stream) {
+  GemmProblem p = problem;
+  p.g[0].tile_begin = 0;
+  p.total_tiles = p.g[0].tiles_m;
+  if (p.total_tiles <= 0) return cudaSuccess;
+  auto kernel = gemm_bf16_kernel<1, kEpiResLN, CN>;
+  const size_t smem_bytes = sizeof(GemmSmemFor<kEpiResLN>) + 1024;
+  static unsigned long long configured = 0;
+  cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CN;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  static int max_clusters = 0;
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(num_sms() / CN * CN);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters = n > 0 ? n : 1;
+  }
+  const int clusters = p.total_tiles < max_clusters ? p.total_tiles : max_clusters;
+  cfg.gridDim = dim3(clusters * CN);
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 cudaError_t launch_gemm_bf16(const GemmProblem& problem, cudaStream_t stream) {
+  if (problem.g[0].ln_gamma != nullptr) {
+    const GemmGroup& g = problem.g[0];
+    if (problem.num_groups != 1 || g.bias == nullptr || g.residual_f32 == nullptr ||
+        g.ln_beta == nullptr || g.relu || g.c_f32 != nullptr || !(g.ln_eps > 0.f))
+      return cudaErrorInvalidValue;
+    switch (g.N) {
+      case 128: return launch_gemm_ln<1>(problem, stream);
+      case 256: return launch_gemm_ln<2>(problem, stream);
+      case 512: return launch_gemm_ln<4>(problem, stream);
+      case 1024: return launch_gemm_ln<8>(problem, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   constexpr int CM = kGemmClusterM;
   // tiles counted per cluster: CM row tiles x one column tile
   GemmProblem p = problem;
@@ -425,7 +689,6 @@ cudaError_t launch_gemm_bf16(const GemmProblem& problem, cudaStream_t stream) {
   }
   p.total_tiles = t;
   if (t <= 0) return cudaSuccess;
-  const size_t smem_bytes = sizeof(GemmSmem) + 1024;
   // one epilogue mode per launch (every group's fields must agree)
   const GemmGroup& g0 = p.g[0];
   int epi = kEpiPlain;
@@ -440,9 +703,12 @@ cudaError_t launch_gemm_bf16(const GemmProblem& problem, cudaStream_t stream) {
     if (p.g[i].bias != g0.bias || p.g[i].relu != g0.relu || p.g[i].c_f32 != nullptr ||
         p.g[i].residual_f32 != nullptr)
       return cudaErrorInvalidValue;
+  for (int i = 0; i < p.num_groups; ++i)
+    if (p.g[i].ln_gamma != nullptr) return cudaErrorInvalidValue;
   auto kernel = epi == kEpiPlain      ? gemm_bf16_kernel<CM, kEpiPlain>
                 : epi == kEpiBiasRelu ? gemm_bf16_kernel<CM, kEpiBiasRelu>
                                       : gemm_bf16_kernel<CM, kEpiBiasResF32>;
+  const size_t smem_bytes = sizeof(GemmSmemFor<kEpiPlain>) + 1024;  // the same for these modes
   static unsigned long long configured[3] = {0, 0, 0};
   cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured[epi]);
   if (e != cudaSuccess) return e;

@@ -61,13 +61,19 @@ struct GemmGroup {
   int tiles_m, tiles_n, tile_begin;
   // optional epilogue, one of: + bias[col] (bf16 [N]) then max(0, .) (relu
   // set); or + bias[col] + residual_f32[row, col] (row stride ldr) written in
-  // fp32 to c_f32 (row stride N) instead of bf16 through tm_c. N a multiple
-  // of 8 then. Every group of a launch uses the same one.
+  // fp32 to c_f32 (row stride N) instead of bf16 through tm_c; or (ln_gamma
+  // set, one group, N in {128, 256, 512, 1024}) + bias + residual_f32, then
+  // LayerNorm over each row's N columns with ln_gamma, ln_beta (bf16 [N])
+  // and ln_eps, bf16 through tm_c. N a multiple of 8. Every group of a launch
+  // uses the same one.
   const uint16_t* bias;
   const float* residual_f32;
   int64_t ldr;
   int relu;
   float* c_f32;
+  const uint16_t* ln_gamma;
+  const uint16_t* ln_beta;
+  float ln_eps;
 };
 constexpr int kMaxGemmGroups = 3;
 struct GemmProblem {

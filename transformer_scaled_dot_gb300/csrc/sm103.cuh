@@ -240,6 +240,18 @@ __device__ __forceinline__ void signal_remote(uint32_t cluster_word, uint32_t cl
                ::"r"(cluster_word), "r"(1u), "r"(cluster_bar)
                : "memory");
 }
+// An asynchronous 8-byte store of (a, b) into another CTA's shared memory
+// (`cluster_addr`, from cluster_map, 8-byte aligned) whose complete_tx (8
+// bytes) lands on that CTA's mbarrier `cluster_bar`: the data is visible to
+// a thread that observes the barrier's phase completing (acquire.cluster).
+__device__ __forceinline__ void st_async_f32x2(uint32_t cluster_addr, float a, float b,
+                                               uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+          cluster_addr),
+      "f"(a), "f"(b), "r"(cluster_bar)
+      : "memory");
+}
 // Whole-cluster barrier (every thread of every CTA of the cluster), with
 // release / acquire ordering of shared and global memory.
 __device__ __forceinline__ void cluster_sync() {

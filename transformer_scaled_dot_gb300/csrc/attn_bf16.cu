@@ -703,12 +703,14 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
 }
 
 int num_sms() {
-  static int n = 0;
+  static int cached = 0;  // atomic accesses: launches may come from several host threads
+  int n = __atomic_load_n(&cached, __ATOMIC_RELAXED);
   if (n == 0) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = 148;
+    __atomic_store_n(&cached, n, __ATOMIC_RELAXED);
   }
   return n;
 }

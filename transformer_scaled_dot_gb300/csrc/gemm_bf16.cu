@@ -611,12 +611,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
 }
 
 int num_sms() {
-  static int n = 0;
+  static int cached = 0;  // atomic accesses: launches may come from several host threads
+  int n = __atomic_load_n(&cached, __ATOMIC_RELAXED);
   if (n == 0) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = 148;
+    __atomic_store_n(&cached, n, __ATOMIC_RELAXED);
   }
   return n;
 }
@@ -652,13 +654,15 @@ cudaError_t launch_gemm_ln(const GemmProblem& problem, cudaStream_t stream) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  static int max_clusters = 0;
+  static int cached_clusters = 0;  // atomic accesses, as num_sms()
+  int max_clusters = __atomic_load_n(&cached_clusters, __ATOMIC_RELAXED);
   if (max_clusters == 0) {
     cfg.gridDim = dim3(num_sms() / CN * CN);
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
     if (e != cudaSuccess) return e;
     max_clusters = n > 0 ? n : 1;
+    __atomic_store_n(&cached_clusters, max_clusters, __ATOMIC_RELAXED);
   }
   const int clusters = p.total_tiles < max_clusters ? p.total_tiles : max_clusters;
   cfg.gridDim = dim3(clusters * CN);
@@ -727,13 +731,16 @@ cudaError_t launch_gemm_bf16(const GemmProblem& problem, cudaStream_t stream) {
   cfg.numAttrs = 2;
   // persistent: as many clusters as can be resident at once (clusters stay
   // inside one GPC, so this can be below SMs / CM)
-  static int max_clusters = 0;  // the same for every epilogue mode (same resources)
+  // the same for every epilogue mode (same resources); atomic accesses, as num_sms()
+  static int cached_clusters = 0;
+  int max_clusters = __atomic_load_n(&cached_clusters, __ATOMIC_RELAXED);
   if (max_clusters == 0) {
     cfg.gridDim = dim3(num_sms() / CM * CM);
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
     if (e != cudaSuccess) return e;
     max_clusters = n > 0 ? n : 1;
+    __atomic_store_n(&cached_clusters, max_clusters, __ATOMIC_RELAXED);
   }
   const int clusters = t < max_clusters ? t : max_clusters;
   cfg.gridDim = dim3(clusters * CM);

@@ -228,3 +228,33 @@ def test_mha_concat_heads_matches_oracle(tsd, shape):
     assert tsd.attn_get_device_status() == tsd.ATTN_OK
     _, ref = oracle.mha(*m.as_f64(), h, mask, kv_lens=m.kv_lens, return_concat=True)
     assert_bf16_close(to_host_f64(concat), ref, "concat heads " + str(shape))
+
+
+@pytest.mark.parametrize("B,n_q,n_k,dm,h", [
+    (16, 999, 700, 1024, 16),   # 1024-column projections: 256-column tiles, ragged rows
+    (8, 1000, 1000, 512, 8),    # 512 columns, 63 row tiles: still enough wide tiles
+    (2, 300, 77, 256, 4),       # few tiles: 128-column tiles
+])
+def test_projection_gemm_tile_widths(tsd, B, n_q, n_k, dm, h):
+    """The grouped projection GEMM (Q from x_q, K and V from x_kv) on shapes
+    that take its 256-column tiles (every N a multiple of 256 and a tile for
+    every SM) and one that keeps 128-column tiles; sampled rows of each
+    output against the exact product of the same bf16 values."""
+    import torch
+    m = synthetic.mha_inputs(3300 + n_q, B, n_q, n_k, dm, h, 64, 64, MASK_NONE,
+                             self_attention=False)
+    xq, xkv, wq, wk, wv, _ = m.as_f64()
+    dev = [to_dev_bf16(t) for t in (m.x_q, m.x_kv, m.w_q, m.w_k, m.w_v)]
+    q = torch.empty((B, n_q, h * 64), dtype=torch.bfloat16, device="cuda")
+    k = torch.empty((B, n_k, h * 64), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty((B, n_k, h * 64), dtype=torch.bfloat16, device="cuda")
+    tsd.mha_project_qkv(*dev, q, k, v, B, n_q, n_k, dm, h, 64, 64)
+    torch.cuda.synchronize()
+    assert tsd.attn_get_device_status() == tsd.ATTN_OK
+    rng = np.random.default_rng(B + n_q)
+    for name, out, x, w, n in (("Q", q, xq, wq, n_q), ("K", k, xkv, wk, n_k), ("V", v, xkv, wv, n_k)):
+        rows = np.unique(np.concatenate([[0, B * n - 1],
+                                         rng.choice(B * n, min(256, B * n), replace=False)]))
+        got = to_host_f64(out.reshape(B * n, h * 64)[torch.from_numpy(rows).cuda()])
+        ref = x.reshape(B * n, dm)[rows] @ w
+        assert_bf16_close(got, ref, f"{name} B={B} n={n} d_model={dm}")

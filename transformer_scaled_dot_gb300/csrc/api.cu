@@ -123,10 +123,20 @@ cudaError_t encode_bf16_map_uncached(CUtensorMap* map, const void* base, int ran
     estride[i] = 1;
   }
   for (int i = 0; i < rank - 1; ++i) gstride[i] = static_cast<cuuint64_t>(strides_elems[i]) * 2u;
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
-                   const_cast<void*>(base), gdim, gstride, bdim, estride,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  auto encode = [&] {
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+               const_cast<void*>(base), gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  };
+  CUresult r = encode();
+  if (r == CUDA_ERROR_INVALID_CONTEXT) {
+    // A host thread whose runtime calls so far needed no device has no
+    // current context, and the encoder is a driver call: a no-op runtime
+    // call binds the current device's primary context to the thread.
+    (void)cudaFree(nullptr);
+    r = encode();
+  }
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 

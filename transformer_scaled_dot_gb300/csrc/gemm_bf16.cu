@@ -62,13 +62,11 @@ constexpr int kStagesLN = 6;      // LayerNorm epilogue (no staging tile: rows s
 constexpr int kMaxLnCluster = 8;  // N <= 8 x 128
 constexpr int kThreads = 192;
 constexpr int kAccCols = 128;
-constexpr int kTmemCols = 2 * kAccCols;
 // LayerNorm epilogue: one more 128-column region after the accumulators
 // holds the tile's fp32 residual, streamed in while the main loop runs
 constexpr int kResCol = 2 * kAccCols;
 constexpr int kTmemColsLN = 512;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB: one 128-row x 128-byte K atom column
-constexpr int kBBytes = kBK * kBN * 2;  // 16 KB: two 64-row (K) x 128-byte N chunks
 constexpr int kBChunk = kBK * 128;      // bytes of one 64-wide N chunk
 constexpr int kCBytes = kBM * kBN * 2;  // 32 KB: one bf16 output tile (two 64-column boxes)
 constexpr int kCStages = 1;             // output staging tiles
@@ -76,10 +74,10 @@ constexpr uint32_t kEpiBarrier = 1;     // named barrier of the four epilogue wa
 constexpr unsigned long long kDrainLimitNs = 100ull * 1000ull * 1000ull;
 static_assert(kGemmClusterM >= 1 && kBK % kGemmClusterM == 0, "B rows split over the cluster");
 
-template <int ST, bool LN>
+template <int ST, bool LN, int BN>
 struct GemmSmemT {
   alignas(1024) uint8_t a[ST][kABytes];
-  alignas(1024) uint8_t b[ST][kBBytes];
+  alignas(1024) uint8_t b[ST][kBK * BN * 2];
   alignas(1024) uint8_t c[LN ? 1 : kCStages][LN ? 16 : kCBytes];
   // LayerNorm epilogue: per tile parity, per other CTA of the cluster (in
   // rank order, skipping this one), per row: that CTA's (mean, centred sum
@@ -110,8 +108,8 @@ struct TileCoord {
   int m0, n0;
 };
 
-// Cluster tile `ct` (CM row tiles x one column tile) -> this CTA's tile.
-template <int CM>
+// Cluster tile `ct` (CM row tiles x one column tile of BN columns) -> this CTA's tile.
+template <int CM, int BN>
 __device__ __forceinline__ TileCoord tile_coord(const GemmProblem& p, int ct, int rank) {
   int gi = 0;
   for (int i = 1; i < p.num_groups; ++i)
@@ -122,7 +120,7 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmProblem& p, int ct, in
   TileCoord c;
   c.g = &G;
   c.m0 = ((local % ctm) * CM + rank) * kBM;  // m fastest: neighbouring clusters share B
-  c.n0 = (local / ctm) * kBN;
+  c.n0 = (local / ctm) * BN;
   return c;
 }
 
@@ -131,23 +129,30 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmProblem& p, int ct, in
 // + bias + fp32 residual then LayerNorm over the row, bf16 output.
 constexpr int kEpiPlain = 0, kEpiBiasRelu = 1, kEpiBiasResF32 = 2, kEpiResLN = 3;
 
-template <int EPI>
+// Tile width BN = 128, or 256 (plain and bias + ReLU only): the wide tile
+// takes 1.5x the operand bytes for 2x the FLOPs of a 128-wide one, and
+// runs four stages of 48 KB.
+template <int EPI, int BN = 128>
 struct GemmStages {
-  static constexpr int value = EPI == kEpiResLN ? kStagesLN : kStages;
+  static constexpr int value = EPI == kEpiResLN ? kStagesLN : (BN == 256 ? 4 : kStages);
 };
-template <int EPI>
-using GemmSmemFor = GemmSmemT<GemmStages<EPI>::value, EPI == kEpiResLN>;
+template <int EPI, int BN = 128>
+using GemmSmemFor = GemmSmemT<GemmStages<EPI, BN>::value, EPI == kEpiResLN, BN>;
 
 // CM: CTAs per cluster along M sharing B (multicast); CN: CTAs per cluster
 // along N sharing a row tile (LayerNorm epilogue only; then CM = 1).
-template <int CM, int EPI, int CN = 1>
+template <int CM, int EPI, int CN = 1, int BN = 128>
 __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_constant__ GemmProblem p) {
   constexpr bool LN = EPI == kEpiResLN;
-  constexpr int kSt = GemmStages<EPI>::value;
+  constexpr int kSt = GemmStages<EPI, BN>::value;
   constexpr int CS = LN ? CN : CM;  // CTAs per cluster
+  constexpr int kBBytesT = kBK * BN * 2;           // one stage's B: BN / 64 chunks of 8 KB
+  constexpr int kTmemAlloc = LN ? kTmemColsLN : 2 * BN;  // two BN-column accumulators
   static_assert(!LN || (CM == 1 && CN >= 1 && CN <= kMaxLnCluster), "LayerNorm clusters");
   static_assert(LN || CN == 1, "clusters along N only for the LayerNorm epilogue");
-  using Smem = GemmSmemFor<EPI>;
+  static_assert(BN == 128 || (BN == 256 && (EPI == kEpiPlain || EPI == kEpiBiasRelu)),
+                "wide tiles: plain and bias + ReLU epilogues");
+  using Smem = GemmSmemFor<EPI, BN>;
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -171,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       c.n0 = rank * kBN;
       return c;
     } else {
-      return tile_coord<CM>(p, ct, rank);
+      return tile_coord<CM, BN>(p, ct, rank);
     }
   };
 
@@ -190,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&sm.tmem_base, LN ? kTmemColsLN : kTmemCols);
+    tmem_alloc(&sm.tmem_base, kTmemAlloc);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -229,19 +234,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sm.full[s], kABytes + kBBytes);
+          mbar_arrive_expect_tx(&sm.full[s], kABytes + kBBytesT);
           if (issued == 0) griddep_wait();
           const int k0 = kb * kBK;
           tma_load_2d(sm.a[s], &c.g->tm_a, &sm.full[s], k0, c.m0);
           const int kr = k0 + mrank * kBRows;
           uint8_t* bdst = sm.b[s] + mrank * kBRows * 128;
-          if constexpr (CM > 1) {
-            tma_load_2d_multicast(bdst, &c.g->tm_b, &sm.full[s], c.n0, kr, kClusterMask);
-            tma_load_2d_multicast(bdst + kBChunk, &c.g->tm_b, &sm.full[s], c.n0 + 64, kr,
-                                  kClusterMask);
-          } else {
-            tma_load_2d(bdst, &c.g->tm_b, &sm.full[s], c.n0, kr);
-            tma_load_2d(bdst + kBChunk, &c.g->tm_b, &sm.full[s], c.n0 + 64, kr);
+#pragma unroll
+          for (int ch = 0; ch < BN / 64; ++ch) {  // 64-column chunks of B, kBChunk apart
+            if constexpr (CM > 1)
+              tma_load_2d_multicast(bdst + ch * kBChunk, &c.g->tm_b, &sm.full[s], c.n0 + 64 * ch,
+                                    kr, kClusterMask);
+            else
+              tma_load_2d(bdst + ch * kBChunk, &c.g->tm_b, &sm.full[s], c.n0 + 64 * ch, kr);
           }
           ++issued;
         }
@@ -257,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdesc = idesc_bf16(kBM, kBN, false, true);
+      constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, false, true);
       // descriptors built once, advanced inside the start-address field
       const uint64_t da0 = sdesc_sw128(smem_u32(sm.a[0]), 16, 1024);       // K-major A
       const uint64_t db0 = sdesc_sw128(smem_u32(sm.b[0]), kBChunk, 1024);  // N-major B
@@ -270,14 +275,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
         ok = mbar_wait(&sm.acc_empty[acc], (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * kAccCols;
+        const uint32_t d_tmem = tmem + acc * BN;
         for (int kb = 0; kb < kblocks; ++kb) {
           const int s = consumed % kSt;
           ok = mbar_wait(&sm.full[s], static_cast<uint32_t>(consumed / kSt) & 1u, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint64_t da = sdesc_advance(da0, static_cast<uint32_t>(s) * (kABytes >> 4));
-          const uint64_t db = sdesc_advance(db0, static_cast<uint32_t>(s) * (kBBytes >> 4));
+          const uint64_t db = sdesc_advance(db0, static_cast<uint32_t>(s) * (kBBytesT >> 4));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             // A: K-major, 32 bytes per 16-element step inside the atom;
@@ -342,14 +347,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       };
       // the first chunk's operands (the whole tile's bias with ReLU) are
       // loaded while the main loop runs, later chunks' during the previous
-      uint4 bias_all[EPI == kEpiBiasRelu ? kBN / 8 : 1];
+      constexpr bool kBiasAll = EPI == kEpiBiasRelu && BN == 128;  // wide tiles: chunk by chunk
+      uint4 bias_all[kBiasAll ? kBN / 8 : 1];
       uint4 bw_next[4];
       float4 rf_next[(EPI == kEpiBiasResF32 || LN) ? 8 : 1];
-      if constexpr (EPI == kEpiBiasRelu) {
+      if constexpr (kBiasAll) {
 #pragma unroll
         for (int cc = 0; cc < kBN / 32; ++cc)
           load_bias(cc, *reinterpret_cast<uint4(*)[4]>(bias_all + 4 * cc));
       }
+      if constexpr (EPI == kEpiBiasRelu && !kBiasAll) load_bias(0, bw_next);
       if constexpr (EPI == kEpiBiasResF32) {
         load_bias(0, bw_next);
         load_res(0, *reinterpret_cast<float4(*)[8]>(rf_next));
@@ -520,16 +527,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
         continue;  // rows stored: no staging tile in this mode
       } else {
 #pragma unroll
-      for (int cc = 0; cc < kBN / 32; ++cc) {
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        if (BN > 128 && cc > 0 && cc % 4 == 0) {
+          // wide tile: the staged 128-column half goes out, and the staging
+          // tile is free again once its store has read it (every warp here)
+          fence_proxy_async_smem();
+          named_bar_sync<kEpiBarrier>(128);
+          if (leader && c.m0 < c.g->M) {
+            const int nh = c.n0 + (cc - 4) * 32;
+            tma_store_2d(&c.g->tm_c, stage, nh, c.m0);
+            if (nh + 64 < c.g->N) tma_store_2d(&c.g->tm_c, stage + 16384, nh + 64, c.m0);
+            bulk_commit_group();
+            bulk_wait_group_read<0>();
+          }
+          named_bar_sync<kEpiBarrier>(128);
+        }
+        const int hc = cc % 4;  // chunk within the staged 128-column half
         uint32_t x[32];
-        tmem_ld32(tmem + lane_base + acc * kAccCols + cc * 32, x);
+        tmem_ld32(tmem + lane_base + acc * BN + cc * 32, x);
         float add[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) add[i] = 0.f;
-        if constexpr (EPI == kEpiBiasRelu) {
+        if constexpr (kBiasAll) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             add_bf16x8(*reinterpret_cast<float(*)[8]>(add + 8 * k), bias_all[cc * 4 + k]);
+        } else if constexpr (EPI == kEpiBiasRelu) {
+          uint4 bw[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) bw[k] = bw_next[k];
+          if (cc + 1 < BN / 32) load_bias(cc + 1, bw_next);  // in flight meanwhile
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            add_bf16x8(*reinterpret_cast<float(*)[8]>(add + 8 * k), bw[k]);
         }
         if constexpr (EPI == kEpiBiasResF32) {
           uint4 bw[4];
@@ -554,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
           }
         }
         tmem_wait_ld();
-        if (cc == kBN / 32 - 1) {
+        if (cc == BN / 32 - 1) {
           tc_fence_before();
           mbar_arrive(&sm.acc_empty[acc]);  // the MMA warp may reuse this accumulator
         }
@@ -578,9 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
           // row r sits at chunk position j ^ (r mod 8) of the row's 128 bytes
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
-            const int j = (cc & 1) * 4 + v4;
+            const int j = (hc & 1) * 4 + v4;
             const float* e = y + 8 * v4;
-            st_shared_v4(smem_u32(stage + (cc >> 1) * 16384 + r * 128 + ((j ^ (r & 7)) << 4)),
+            st_shared_v4(smem_u32(stage + (hc >> 1) * 16384 + r * 128 + ((j ^ (r & 7)) << 4)),
                          pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
                          pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
           }
@@ -591,9 +621,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       named_bar_sync<kEpiBarrier>(128);
       // a cluster's last row tiles may lie past M: computed on zero rows, not stored
       if (leader && c.m0 < c.g->M && EPI != kEpiBiasResF32) {
-        // the map clips rows past M and columns past N
-        tma_store_2d(&c.g->tm_c, stage, c.n0, c.m0);
-        if (c.n0 + 64 < c.g->N) tma_store_2d(&c.g->tm_c, stage + 16384, c.n0 + 64, c.m0);
+        // the map clips rows past M and columns past N (the last 128-column
+        // half of a wide tile)
+        const int nh = c.n0 + BN - 128;
+        tma_store_2d(&c.g->tm_c, stage, nh, c.m0);
+        if (nh + 64 < c.g->N) tma_store_2d(&c.g->tm_c, stage + 16384, nh + 64, c.m0);
         bulk_commit_group();
       }
     }
@@ -607,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
   if constexpr (CS > 1) cluster_sync();
   else __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, LN ? kTmemColsLN : kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, kTmemAlloc);
 }
 
 int num_sms() {
@@ -626,6 +658,7 @@ int num_sms() {
 }  // namespace
 
 static_assert(sizeof(GemmSmemFor<kEpiPlain>) + 1024 <= 227 * 1024, "shared memory per CTA");
+static_assert(sizeof(GemmSmemFor<kEpiPlain, 256>) + 1024 <= 227 * 1024, "shared memory per CTA");
 static_assert(sizeof(GemmSmemFor<kEpiResLN>) + 1024 <= 227 * 1024, "shared memory per CTA");
 
 // The LayerNorm epilogue: one group, clusters of N / 128 CTAs along N, one
@@ -684,15 +717,7 @@ cudaError_t launch_gemm_bf16(const GemmProblem& problem, cudaStream_t stream) {
     }
   }
   constexpr int CM = kGemmClusterM;
-  // tiles counted per cluster: CM row tiles x one column tile
   GemmProblem p = problem;
-  int t = 0;
-  for (int i = 0; i < p.num_groups; ++i) {
-    p.g[i].tile_begin = t;
-    t += ((p.g[i].tiles_m + CM - 1) / CM) * p.g[i].tiles_n;
-  }
-  p.total_tiles = t;
-  if (t <= 0) return cudaSuccess;
   // one epilogue mode per launch (every group's fields must agree)
   const GemmGroup& g0 = p.g[0];
   int epi = kEpiPlain;
@@ -709,12 +734,43 @@ cudaError_t launch_gemm_bf16(const GemmProblem& problem, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   for (int i = 0; i < p.num_groups; ++i)
     if (p.g[i].ln_gamma != nullptr) return cudaErrorInvalidValue;
-  auto kernel = epi == kEpiPlain      ? gemm_bf16_kernel<CM, kEpiPlain>
-                : epi == kEpiBiasRelu ? gemm_bf16_kernel<CM, kEpiBiasRelu>
-                                      : gemm_bf16_kernel<CM, kEpiBiasResF32>;
-  const size_t smem_bytes = sizeof(GemmSmemFor<kEpiPlain>) + 1024;  // the same for these modes
-  static unsigned long long configured[3] = {0, 0, 0};
-  cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured[epi]);
+  // 256-column tiles (plain and bias + ReLU, every N a multiple of 256) when
+  // their waves cost less: a wide tile moves 1.5x the operand bytes of a
+  // 128-column one (the loads set the pace), so wide wins when
+  // 1.5 x (its waves) < the narrow tiles' waves over the SMs; and only with
+  // three waves or more (measured: the encoder layer's 4096 x 2048 x 512 FFN
+  // GEMM, two wide waves, was faster alone but slower inside the layer)
+  bool wide = epi == kEpiPlain || epi == kEpiBiasRelu;
+  long long wide_tiles = 0, narrow_tiles = 0;
+  for (int i = 0; i < p.num_groups; ++i) {
+    if (p.g[i].N % 256 != 0) wide = false;
+    const long long rows = (p.g[i].tiles_m + CM - 1) / CM;
+    wide_tiles += rows * (p.g[i].N / 256);
+    narrow_tiles += rows * ((p.g[i].N + 127) / 128);
+  }
+  const long long sms = num_sms();
+  const long long wide_waves = (wide_tiles + sms - 1) / sms;
+  if (wide_waves < 3 || 3 * wide_waves >= 2 * ((narrow_tiles + sms - 1) / sms)) wide = false;
+  const int bn = wide ? 256 : 128;
+  // tiles counted per cluster: CM row tiles x one column tile
+  int t = 0;
+  for (int i = 0; i < p.num_groups; ++i) {
+    p.g[i].tiles_n = (p.g[i].N + bn - 1) / bn;
+    p.g[i].tile_begin = t;
+    t += ((p.g[i].tiles_m + CM - 1) / CM) * p.g[i].tiles_n;
+  }
+  p.total_tiles = t;
+  if (t <= 0) return cudaSuccess;
+  auto kernel = wide ? (epi == kEpiPlain ? gemm_bf16_kernel<CM, kEpiPlain, 1, 256>
+                                         : gemm_bf16_kernel<CM, kEpiBiasRelu, 1, 256>)
+            : epi == kEpiPlain      ? gemm_bf16_kernel<CM, kEpiPlain>
+            : epi == kEpiBiasRelu ? gemm_bf16_kernel<CM, kEpiBiasRelu>
+                                    : gemm_bf16_kernel<CM, kEpiBiasResF32>;
+  const size_t smem_bytes =
+      (wide ? sizeof(GemmSmemFor<kEpiPlain, 256>) : sizeof(GemmSmemFor<kEpiPlain>)) + 1024;
+  static unsigned long long configured[5] = {0, 0, 0, 0, 0};
+  cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes),
+                                &configured[wide ? 3 + epi : epi]);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);

@@ -770,10 +770,11 @@ cudaError_t launch_attn_bf16(const AttnProblem& p, const CUtensorMap& tm_q,
       if (!pair)
         return launch_variant<64, 1, 2, 2, 1, true, 2, false, true>(p, tm_q, tm_k, tm_v, tm_o,
                                                                      stream);
-      return causal ? launch_variant<64, 2, 4, 4, 2, true, 1, false, true>(p, tm_q, tm_k, tm_v,
-                                                                          tm_o, stream)
-                    : launch_variant<64, 2, 4, 4, 2, true, 1, true, true>(p, tm_q, tm_k, tm_v,
-                                                                         tm_o, stream);
+      // one copy of the score load (no unmasked twin): the two window edges
+      // put masking in most of a short item's tiles, and the smaller loop
+      // measured faster (n = 16384, keys within +-256: 534 -> 588 TFLOP/s)
+      return launch_variant<64, 2, 4, 4, 2, true, 1, false, true>(p, tm_q, tm_k, tm_v, tm_o,
+                                                                  stream);
     }
     if (p.d == 128) {
       return pair ? launch_variant<128, 2, 2, 2, 1, false, 1, false, true>(p, tm_q, tm_k, tm_v,

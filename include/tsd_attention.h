@@ -386,6 +386,27 @@ attn_status mha_forward_host(const void *x_q_host, const void *x_kv_host,
                              int mask_kind, const int32_t *kv_lens_host, float scale,
                              void *workspace, size_t workspace_bytes, tsd_stream_t stream);
 
+/*
+ * mha_forward_host_async -- mha_forward_host whose result copy runs on a
+ * device-to-host stream the library creates once per device, after the
+ * computation, instead of on `stream`: consecutive calls (two workspaces in
+ * turn) then overlap call i's result copy with call i+1's computation, as a
+ * serving loop wants. A call's result is in out_host, and its host inputs
+ * may be reused, once `stream` has passed a later attn_host_join(stream).
+ * A workspace's next computation waits for the result copy that last read
+ * it. Arguments and errors as mha_forward_host.
+ */
+attn_status mha_forward_host_async(const void *x_q_host, const void *x_kv_host,
+                                   const void *w_q, const void *w_k, const void *w_v,
+                                   const void *w_o, void *out_host,
+                                   int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
+                                   int mask_kind, const int32_t *kv_lens_host, float scale,
+                                   void *workspace, size_t workspace_bytes, tsd_stream_t stream);
+
+/* attn_host_join -- `stream` waits for every result copy the asynchronous
+ * host-buffer calls issued so far on the current device (none: a no-op). */
+attn_status attn_host_join(tsd_stream_t stream);
+
 size_t encoder_layer_host_workspace_bytes(int B, int n, int d_model, int h, int d_k, int d_ff);
 attn_status encoder_layer_forward_host(const void *x_host,
                                        const void *w_q, const void *w_k, const void *w_v,

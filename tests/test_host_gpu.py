@@ -217,3 +217,27 @@ def test_attn_forward_window_host_matches_device_call(tsd):
     torch.cuda.current_stream().synchronize()
     assert tsd.attn_get_device_status() == tsd.ATTN_OK
     np.testing.assert_array_equal(hout.numpy(), bits_of_device(out_dev))
+
+
+@pytest.mark.parametrize("n_ws", [1, 2])
+def test_mha_forward_host_async_back_to_back_then_join(tsd, n_ws):
+    """Asynchronous result copies: eight calls with different inputs, no
+    host synchronisation, one join at the end; each result is its own
+    input's (a workspace's staging is not rewritten before its copy read it)."""
+    import torch
+    m = synthetic.mha_inputs(1001, 32, 128, 128, 512, 8, 64, 64, MASK_KEY_PADDING, (64, 128),
+                             add_pe=True)
+    w, wss, wsb = host_mha_setup(tsd, m, n_ws)
+    hl = pinned_i32(m.kv_lens)
+    xs = [synthetic.mha_inputs(7100 + i, 32, 128, 128, 512, 8, 64, 64).x_q for i in range(8)]
+    hxs = [pinned_bf16(x) for x in xs]
+    houts = [pinned_out((m.B, m.n_q, m.d_model)) for _ in xs]
+    for i, (hx, ho) in enumerate(zip(hxs, houts)):
+        tsd.mha_forward_host_async(hx, hx, *w, ho, m.B, m.n_q, m.n_k, m.d_model, m.h, m.d_k,
+                                   m.d_v, m.mask_kind, hl, 0.0, wss[i % n_ws], wsb)
+    tsd.attn_host_join()
+    torch.cuda.current_stream().synchronize()
+    assert tsd.attn_get_device_status() == tsd.ATTN_OK
+    for i, x in enumerate(xs):
+        np.testing.assert_array_equal(houts[i].numpy(), device_mha(tsd, m, x), err_msg=f"call {i}")
+

@@ -28,7 +28,7 @@ __all__ = [
     "MHA_NOALLOC_SCRATCH_BYTES", "attn_host_workspace_bytes", "attn_forward_host",
     "mha_host_workspace_bytes", "mha_forward_host", "encoder_layer_host_workspace_bytes",
     "encoder_layer_forward_host", "attn_decode_host_workspace_bytes", "attn_decode_host",
-    "attn_forward_window_host",
+    "attn_forward_window_host", "mha_forward_host_async", "attn_host_join",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = range(5)
@@ -43,6 +43,7 @@ EXPORTED_SYMBOLS = (
     "attn_host_workspace_bytes", "attn_forward_host", "mha_host_workspace_bytes",
     "mha_forward_host", "encoder_layer_host_workspace_bytes", "encoder_layer_forward_host",
     "attn_decode_host_workspace_bytes", "attn_decode_host", "attn_forward_window_host",
+    "mha_forward_host_async", "attn_host_join",
 )
 
 # TSD_MHA_NOALLOC_SCRATCH_BYTES of the header: the fixed scratch of mha_forward_noalloc
@@ -113,6 +114,8 @@ def library():
     lib.attn_forward_window_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, i, i, f, vp,
                                              sz, st]
     lib.mha_forward_host.argtypes = [vp] * 7 + [i] * 8 + [vp, f, vp, sz, st]
+    lib.mha_forward_host_async.argtypes = [vp] * 7 + [i] * 8 + [vp, f, vp, sz, st]
+    lib.attn_host_join.argtypes = [st]
     lib.encoder_layer_forward_host.argtypes = [vp] * 14 + [i] * 7 + [vp, f, f, vp, sz, st]
     lib.attn_decode_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp, f, vp, sz, st]
     for name in ("attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_forward",
@@ -120,7 +123,8 @@ def library():
                  "mha_project_qkv", "mha_project_out", "mha_forward_noalloc", "mha_concat_heads",
                  "mha_forward_launches", "attn_forward_window", "attn_decode",
                  "encoder_layer_forward", "attn_forward_host", "mha_forward_host",
-                 "encoder_layer_forward_host", "attn_decode_host", "attn_forward_window_host"):
+                 "encoder_layer_forward_host", "attn_decode_host", "attn_forward_window_host",
+                 "mha_forward_host_async", "attn_host_join"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -323,6 +327,23 @@ def mha_forward_host(x_q_host, x_kv_host, w_q, w_k, w_v, w_o, out_host, B, n_q, 
                                       h, d_k, d_v, mask_kind, _ptr(kv_lens_host), scale,
                                       _ptr(workspace), workspace_bytes, _stream(stream)),
            "mha_forward_host")
+
+
+def mha_forward_host_async(x_q_host, x_kv_host, w_q, w_k, w_v, w_o, out_host, B, n_q, n_k,
+                           d_model, h, d_k, d_v, mask_kind=ATTN_MASK_NONE, kv_lens_host=None,
+                           scale=0.0, workspace=None, workspace_bytes=0, stream=None):
+    """mha_forward_host with the result copy on the library's result stream:
+    out_host is complete once `stream` has passed a later attn_host_join."""
+    _check(library().mha_forward_host_async(_ptr(x_q_host), _ptr(x_kv_host), _ptr(w_q),
+                                            _ptr(w_k), _ptr(w_v), _ptr(w_o), _ptr(out_host), B,
+                                            n_q, n_k, d_model, h, d_k, d_v, mask_kind,
+                                            _ptr(kv_lens_host), scale, _ptr(workspace),
+                                            workspace_bytes, _stream(stream)),
+           "mha_forward_host_async")
+
+
+def attn_host_join(stream=None):
+    _check(library().attn_host_join(_stream(stream)), "attn_host_join")
 
 
 def encoder_layer_host_workspace_bytes(B, n, d_model, h, d_k, d_ff) -> int:

@@ -1043,11 +1043,15 @@ size_t mha_host_workspace_bytes(int B, int n_q, int n_k, int d_model, int h, int
   return mha_host_layout(B, n_q, n_k, d_model, h, d_k, d_v, &t) ? t : 0;
 }
 
-attn_status mha_forward_host(const void* x_q_host, const void* x_kv_host, const void* w_q,
-                             const void* w_k, const void* w_v, const void* w_o, void* out_host,
-                             int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
-                             int mask_kind, const int32_t* kv_lens_host, float scale,
-                             void* workspace, size_t workspace_bytes, tsd_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+attn_status mha_host_call(const void* x_q_host, const void* x_kv_host, const void* w_q,
+                          const void* w_k, const void* w_v, const void* w_o, void* out_host, int B,
+                          int n_q, int n_k, int d_model, int h, int d_k, int d_v, int mask_kind,
+                          const int32_t* kv_lens_host, float scale, void* workspace,
+                          size_t workspace_bytes, tsd_stream_t stream, bool async) {
   if (!x_q_host || !x_kv_host || !out_host || !workspace) return ATTN_ERR_INVALID;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID;
   size_t need = 0;
@@ -1082,7 +1086,40 @@ attn_status mha_forward_host(const void* x_q_host, const void* x_kv_host, const 
                   pad ? lens : nullptr, scale, inner, inner_bytes, stream);
   hs.computed();
   if (s != ATTN_OK) return s;
-  return hs.copy_out(out_host, out, xqb) == cudaSuccess ? ATTN_OK : cuda_fail(hs.status());
+  const cudaError_t e =
+      async ? hs.copy_out_async(out_host, out, xqb) : hs.copy_out(out_host, out, xqb);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(hs.status());
+}
+
+
+}  // namespace
+
+extern "C" {
+
+attn_status mha_forward_host(const void* x_q_host, const void* x_kv_host, const void* w_q,
+                             const void* w_k, const void* w_v, const void* w_o, void* out_host,
+                             int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
+                             int mask_kind, const int32_t* kv_lens_host, float scale,
+                             void* workspace, size_t workspace_bytes, tsd_stream_t stream) {
+  return mha_host_call(x_q_host, x_kv_host, w_q, w_k, w_v, w_o, out_host, B, n_q, n_k, d_model, h,
+                       d_k, d_v, mask_kind, kv_lens_host, scale, workspace, workspace_bytes, stream,
+                       false);
+}
+
+attn_status mha_forward_host_async(const void* x_q_host, const void* x_kv_host, const void* w_q,
+                                   const void* w_k, const void* w_v, const void* w_o,
+                                   void* out_host, int B, int n_q, int n_k, int d_model, int h,
+                                   int d_k, int d_v, int mask_kind, const int32_t* kv_lens_host,
+                                   float scale, void* workspace, size_t workspace_bytes,
+                                   tsd_stream_t stream) {
+  return mha_host_call(x_q_host, x_kv_host, w_q, w_k, w_v, w_o, out_host, B, n_q, n_k, d_model, h,
+                       d_k, d_v, mask_kind, kv_lens_host, scale, workspace, workspace_bytes, stream,
+                       true);
+}
+
+attn_status attn_host_join(tsd_stream_t stream) {
+  const cudaError_t e = tsd::host_join(reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
 size_t encoder_layer_host_workspace_bytes(int B, int n, int d_model, int h, int d_k, int d_ff) {

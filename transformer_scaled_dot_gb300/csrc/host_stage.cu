@@ -1,13 +1,15 @@
 // host_stage.cu -- copy streams and per-workspace events of the host-buffer
 // entry points (the ordering rules are in host_stage.h).
 //
-// State: per device one non-blocking copy stream; a table of workspaces
-// (device, base address) with two events each -- `staged` (recorded on the
-// copy stream after a call's input copies) and `computed` (recorded on the
-// caller's stream after the computation that read them). A workspace seen
-// for the first time, or again after its entry was evicted, first gets
-// `computed` recorded on the caller's stream, so its first copy waits for
-// everything the stream had before it. Streams and events live as long as
+// State: per device one non-blocking copy stream and one result stream; a
+// table of workspaces (device, base address) with three events each --
+// `staged` (recorded on the copy stream after a call's input copies),
+// `computed` (recorded on the caller's stream after the computation that
+// read them) and `out_free` (recorded on the result stream after an
+// asynchronous result copy read the workspace's result staging). A workspace
+// seen for the first time, or again after its entry was evicted, first gets
+// `computed` and `out_free` recorded on the caller's stream, so its first
+// copy waits for everything the stream had before it. Streams and events live as long as
 // the process: they are never destroyed, so nothing depends on the order of
 // static destruction against the CUDA runtime's own teardown.
 #include "host_stage.h"
@@ -26,11 +28,21 @@ struct WorkspaceSlot {
   const void* base = nullptr;
   cudaEvent_t staged = nullptr;
   cudaEvent_t computed = nullptr;
+  cudaEvent_t out_free = nullptr;  // the last asynchronous result copy has read the staging
   uint64_t last_use = 0;
 };
 
 std::mutex g_mutex;
 cudaStream_t g_copy_stream[kMaxDevices] = {};
+cudaStream_t g_result_stream[kMaxDevices] = {};
+cudaEvent_t g_join_event[kMaxDevices] = {};
+
+cudaError_t make_stream(cudaStream_t* s) {
+  if (*s != nullptr) return cudaSuccess;
+  cudaError_t e = cudaStreamCreateWithFlags(s, cudaStreamNonBlocking);
+  if (e != cudaSuccess) *s = nullptr;
+  return e;
+}
 WorkspaceSlot g_slots[kWorkspaceSlots];
 uint64_t g_use_clock = 0;
 
@@ -45,14 +57,11 @@ HostStage::HostStage(const void* workspace, cudaStream_t stream)
     err_ = cudaErrorInvalidDevice;
     return;
   }
-  if (g_copy_stream[dev] == nullptr) {
-    err_ = cudaStreamCreateWithFlags(&g_copy_stream[dev], cudaStreamNonBlocking);
-    if (err_ != cudaSuccess) {
-      g_copy_stream[dev] = nullptr;
-      return;
-    }
-  }
+  err_ = make_stream(&g_copy_stream[dev]);
+  if (err_ == cudaSuccess) err_ = make_stream(&g_result_stream[dev]);
+  if (err_ != cudaSuccess) return;
   copy_ = g_copy_stream[dev];
+  result_ = g_result_stream[dev];
   // the workspace's slot: a hit, else an empty slot, else the least recently used
   WorkspaceSlot* slot = nullptr;
   WorkspaceSlot* victim = &g_slots[0];
@@ -68,16 +77,22 @@ HostStage::HostStage(const void* workspace, cudaStream_t stream)
     slot = victim;
     if (slot->staged == nullptr || slot->device != dev) {
       // events belong to the device current at their creation
-      cudaEvent_t a = nullptr, b = nullptr;
-      err_ = cudaEventCreateWithFlags(&a, cudaEventDisableTiming);
-      if (err_ == cudaSuccess) err_ = cudaEventCreateWithFlags(&b, cudaEventDisableTiming);
-      if (err_ != cudaSuccess) return;
+      cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+      for (cudaEvent_t& x : ev)
+        if (err_ == cudaSuccess) err_ = cudaEventCreateWithFlags(&x, cudaEventDisableTiming);
+      if (err_ != cudaSuccess) {
+        for (cudaEvent_t x : ev)
+          if (x != nullptr) cudaEventDestroy(x);
+        return;
+      }
       // an evicted slot's events may still be pending in a stream; their
       // destruction is deferred by the runtime until they complete
       if (slot->staged != nullptr) cudaEventDestroy(slot->staged);
       if (slot->computed != nullptr) cudaEventDestroy(slot->computed);
-      slot->staged = a;
-      slot->computed = b;
+      if (slot->out_free != nullptr) cudaEventDestroy(slot->out_free);
+      slot->staged = ev[0];
+      slot->computed = ev[1];
+      slot->out_free = ev[2];
     }
     slot->device = dev;
     slot->base = workspace;
@@ -86,8 +101,10 @@ HostStage::HostStage(const void* workspace, cudaStream_t stream)
   slot->last_use = ++g_use_clock;
   staged_ = slot->staged;
   computed_ = slot->computed;
+  out_free_ = slot->out_free;
   if (fresh) {
     err_ = cudaEventRecord(computed_, stream_);
+    if (err_ == cudaSuccess) err_ = cudaEventRecord(out_free_, stream_);
     if (err_ != cudaSuccess) return;
   }
   // refill the staging region only after the last computation that read it
@@ -104,6 +121,9 @@ cudaError_t HostStage::inputs_ready() {
   if (err_ != cudaSuccess) return err_;
   err_ = cudaEventRecord(staged_, copy_);
   if (err_ == cudaSuccess) err_ = cudaStreamWaitEvent(stream_, staged_, 0);
+  // the computation rewrites the result staging: after the last
+  // asynchronous copy that read it
+  if (err_ == cudaSuccess) err_ = cudaStreamWaitEvent(stream_, out_free_, 0);
   return err_;
 }
 
@@ -117,6 +137,34 @@ cudaError_t HostStage::copy_out(void* dst_host, const void* src_dev, size_t byte
   if (err_ != cudaSuccess || bytes == 0) return err_;
   err_ = cudaMemcpyAsync(dst_host, src_dev, bytes, cudaMemcpyDeviceToHost, stream_);
   return err_;
+}
+
+cudaError_t HostStage::copy_out_async(void* dst_host, const void* src_dev, size_t bytes) {
+  if (err_ != cudaSuccess) return err_;
+  err_ = cudaStreamWaitEvent(result_, computed_, 0);
+  if (err_ == cudaSuccess && bytes != 0)
+    err_ = cudaMemcpyAsync(dst_host, src_dev, bytes, cudaMemcpyDeviceToHost, result_);
+  if (err_ == cudaSuccess) err_ = cudaEventRecord(out_free_, result_);
+  return err_;
+}
+
+cudaError_t host_join(cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (g_result_stream[dev] == nullptr) return cudaSuccess;  // nothing was ever issued there
+  if (g_join_event[dev] == nullptr) {
+    e = cudaEventCreateWithFlags(&g_join_event[dev], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      g_join_event[dev] = nullptr;
+      return e;
+    }
+  }
+  e = cudaEventRecord(g_join_event[dev], g_result_stream[dev]);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, g_join_event[dev], 0);
+  return e;
 }
 
 }  // namespace tsd

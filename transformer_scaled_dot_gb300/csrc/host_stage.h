@@ -9,7 +9,11 @@
 // stream. So a caller that alternates two workspaces over consecutive calls
 // gets call i+1's input copy overlapped with call i's computation and result
 // copy, while every call stays ordered on its stream: once the stream has
-// passed a call, its result is in host memory.
+// passed a call, its result is in host memory. The asynchronous variant
+// copies the result on a library-owned result stream instead, so that it
+// also overlaps the next call's computation; the result is in host memory
+// once the stream has passed a later host_join. A workspace's next
+// computation waits for the result copy that last read its staging region.
 #pragma once
 
 #include <cstddef>
@@ -37,14 +41,23 @@ class HostStage {
   cudaError_t computed();
   // device -> host on the caller's stream
   cudaError_t copy_out(void* dst_host, const void* src_dev, size_t bytes);
+  // device -> host on the library's result stream (after the computation):
+  // it overlaps the next call's computation; host_join orders it
+  cudaError_t copy_out_async(void* dst_host, const void* src_dev, size_t bytes);
 
  private:
   std::unique_lock<std::mutex> lock_;
   cudaStream_t stream_ = nullptr;
   cudaStream_t copy_ = nullptr;
+  cudaStream_t result_ = nullptr;
   cudaEvent_t staged_ = nullptr;
   cudaEvent_t computed_ = nullptr;
+  cudaEvent_t out_free_ = nullptr;
   cudaError_t err_ = cudaSuccess;
 };
+
+// `stream` waits for every result copy issued so far (copy_out_async) on
+// the current device.
+cudaError_t host_join(cudaStream_t stream);
 
 }  // namespace tsd

@@ -194,7 +194,7 @@ def test_attn_decode_rejects_bad_arguments(lib):
 
 def test_attn_decode_workspace_grows_with_chunks_queries_and_width(lib):
     f = tsd.attn_decode_workspace_bytes
-    assert f(1, 1, 1, 256, 64) < f(1, 1, 1, 257, 64)   # a second 256-key chunk
+    assert f(1, 1, 1, 128, 64) < f(1, 1, 1, 129, 64)   # a second 128-key chunk
     assert f(2, 3, 4, 1000, 128) >= 2 * 3 * 4 * 4 * (128 + 2) * 4
     assert f(1, 1, 0, 100, 64) == 0 and f(1, 1, 9, 100, 64) == 0
 

@@ -25,6 +25,9 @@ def tsd():
 
 def decode_inputs(seed, B, h, n_q, n_max, d, lens):
     a = synthetic.attention_inputs(seed, B, h, n_q, n_max, d, d)
+    if isinstance(lens, str):  # "ragged": seeded lengths in [0, n_max], some empty
+        lens = np.random.default_rng(seed).integers(0, n_max + 1, size=B)
+        lens[::7] = 0
     return a.q, a.k, a.v, (None if lens is None else np.asarray(lens, dtype=np.int32))
 
 
@@ -60,6 +63,13 @@ CASES = [
     (2, 2, 8, 1100, 128, [9, 1100]),
     (1, 2, 2, 5000, 128, None),
     (3, 2, 2, 400, 64, [0, 400, 2]),                   # an empty cache gives zeros
+    # the persistent partial kernel deals the chunks out in contiguous ranges:
+    # ranges that cross batches with empty caches between them, more batches
+    # than threads in its prefix sum, more chunks than CTAs, fewer than CTAs
+    (7, 3, 1, 2000, 64, [2000, 0, 0, 5, 1999, 256, 257]),
+    (300, 1, 1, 300, 64, "ragged"),
+    (5, 16, 2, 4096, 128, [4096, 1, 4000, 129, 2222]),
+    (9, 20, 1, 8192, 64, [8192, 0, 7000, 300, 8191, 0, 4097, 256, 6000]),
 ]
 
 

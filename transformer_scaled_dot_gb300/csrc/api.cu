@@ -782,7 +782,7 @@ attn_status attn_decode(const void* q, const void* k_cache, const void* v_cache,
   const uint64_t dims[3] = {static_cast<uint64_t>(d_k), static_cast<uint64_t>(n_max),
                             static_cast<uint64_t>(B) * h};
   const int64_t strides[2] = {d_k, int64_t(n_max) * d_k};
-  const uint32_t box[3] = {64, 256, 1};
+  const uint32_t box[3] = {64, 128, 1};
   cudaError_t e = encode_bf16_map(&p.tm_k, k_cache, 3, dims, strides, box);
   if (e == cudaSuccess) e = encode_bf16_map(&p.tm_v, v_cache, 3, dims, strides, box);
   if (e != cudaSuccess) return cuda_fail(e);

@@ -10,8 +10,10 @@
 // The step is bound by reading the cache (4 d bytes per key, 2 n_q d
 // multiply-adds per key), so it runs on the FMA pipes, split over the keys:
 //
-//   decode_partial   one CTA per (batch, head, 256-key chunk): the chunk's K
-//                    and V by TMA (128-byte swizzle, one box per 64 columns),
+//   decode_partial   one CTA per (batch, head, 128-key chunk): the chunk's K
+//                    and V by TMA (128-byte swizzle, one box per 64 columns;
+//                    32 KB at d = 64, so six CTAs share an SM and their loads
+//                    and arithmetic overlap),
 //                    a thread per key for the n_q scores (q broadcast from
 //                    shared memory), the chunk's max and sum per query in
 //                    fp32, P in shared memory, then O_chunk = P V with
@@ -20,6 +22,8 @@
 //                    and O_chunk (fp32) to the workspace
 //   decode_merge     one CTA per (batch, head): m = max_c m_c,
 //                    out = sum_c 2^(m_c - m) O_c / sum_c 2^(m_c - m) l_c, bf16
+//                    (the O_c loads of a thread issued together, so the merge
+//                    costs a few dependent L2 round trips)
 //
 // Chunks at or past L are neither computed nor read; keys at or past L in
 // the last chunk are masked before they can reach a sum (the cache past L
@@ -33,8 +37,8 @@ namespace tsd {
 
 namespace {
 
-constexpr int kChunk = 256;    // keys per CTA (one per thread in the score phase)
-constexpr int kDecThreads = 256;
+constexpr int kChunk = 128;    // keys per CTA (one per thread in the score phase)
+constexpr int kDecThreads = 128;
 constexpr unsigned long long kDrainLimitNs = 100ull * 1000ull * 1000ull;
 
 template <int D, int NQ>
@@ -231,23 +235,33 @@ __global__ void __launch_bounds__(kDecThreads)
 }
 
 constexpr int kMergeThreads = 256;
+constexpr int kMergeBatch = 16;  // chunk partials loaded per thread before they are summed
+
+// shared memory of the merge: the weights [chunks][n_q], 1 / l [n_q] and the
+// groups' sums [kMergeThreads / D][n_q][D]
+size_t merge_smem_bytes(int chunks, int n_q, int d) {
+  return (static_cast<size_t>(chunks) * n_q + n_q + static_cast<size_t>(kMergeThreads / d) * n_q * d) *
+         sizeof(float);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeArgs a) {
   // the weights of every (chunk, query) pair go to shared memory first; then
   // kMergeThreads / D groups of D threads (one per column) each sum a share
-  // of the chunks with several loads in flight, and the groups' sums are added
+  // of the chunks, kMergeBatch loads in flight per thread, and the groups'
+  // sums are added
   constexpr int kGroups = kMergeThreads / D;
-  __shared__ float w_s[kDecodeMaxChunks * kDecodeMaxQueries];
-  __shared__ float inv_l_s[kDecodeMaxQueries];
-  __shared__ float part_s[kGroups][kDecodeMaxQueries][D];
+  extern __shared__ float merge_smem[];
+  float* w_s = merge_smem;                  // [chunks][n_q]
+  float* inv_l_s = w_s + a.chunks * a.n_q;  // [n_q]
+  float* part_s = inv_l_s + a.n_q;          // [kGroups][n_q][D]
   const int tid = static_cast<int>(threadIdx.x);
   const int hh = static_cast<int>(blockIdx.x), b = static_cast<int>(blockIdx.y);
   const int64_t bh = static_cast<int64_t>(b) * a.h + hh;
   griddep_launch_dependents();
   griddep_wait();  // the partials of the previous kernel are complete
   const int L = cache_len(a, b);
-  const int nc = (L + kChunk - 1) / kChunk;       // <= kDecodeMaxChunks (checked on the host)
+  const int nc = (L + kChunk - 1) / kChunk;       // <= a.chunks
   const float* ml = a.ws_ml + bh * a.chunks * a.n_q * 2;  // [chunk][query][m, l]
   // per query (warp t, lanes over the chunks): m = max_c m_c,
   // w_c = 2^(m_c - m), l = sum_c w_c l_c
@@ -263,7 +277,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
       // a chunk holding none of this query's keys has m_c = -inf and weight 0
       const float w = mc == -INFINITY ? 0.f : ex2(mc - m);
       l = fmaf(w, ml[(c * a.n_q + t) * 2 + 1], l);
-      w_s[c * kDecodeMaxQueries + t] = w;
+      w_s[c * a.n_q + t] = w;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
@@ -271,20 +285,30 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   }
   __syncthreads();
   const int col = tid % D, grp = tid / D;
+  const float* o_bh = a.ws_o + bh * a.chunks * a.n_q * D;  // [chunk][query][D]
   for (int t = 0; t < a.n_q; ++t) {
     float o = 0.f;
-#pragma unroll 4
-    for (int c = grp; c < nc; c += kGroups)
-      o = fmaf(w_s[c * kDecodeMaxQueries + t], a.ws_o[((bh * a.chunks + c) * a.n_q + t) * D + col],
-               o);
-    part_s[grp][t][col] = o;
+    for (int c0 = grp; c0 < nc; c0 += kMergeBatch * kGroups) {
+      float v[kMergeBatch];
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const int c = c0 + u * kGroups;
+        v[u] = c < nc ? o_bh[(c * a.n_q + t) * D + col] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const int c = c0 + u * kGroups;
+        if (c < nc) o = fmaf(w_s[c * a.n_q + t], v[u], o);
+      }
+    }
+    part_s[(grp * a.n_q + t) * D + col] = o;
   }
   __syncthreads();
   for (int i = tid; i < a.n_q * D; i += kMergeThreads) {
     const int t = i / D, cc = i % D;
     float o = 0.f;
 #pragma unroll
-    for (int g = 0; g < kGroups; ++g) o += part_s[g][t][cc];
+    for (int g = 0; g < kGroups; ++g) o += part_s[(g * a.n_q + t) * D + cc];
     a.out[(bh * a.n_q + t) * D + cc] = __float2bfloat16_rn(o * inv_l_s[t]);
   }
 }
@@ -311,7 +335,8 @@ cudaError_t launch_decode_nq(const DecodeProblem& p, cudaStream_t stream) {
   e = launch_pdl(kernel, dim3(a.chunks, p.h, p.B), dim3(kDecThreads), smem_bytes, stream,
                  p.tm_k, p.tm_v, a);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_merge_kernel<D>, dim3(p.h, p.B), dim3(kMergeThreads), 0, stream, a);
+  return launch_pdl(decode_merge_kernel<D>, dim3(p.h, p.B), dim3(kMergeThreads),
+                    merge_smem_bytes(a.chunks, p.n_q, D), stream, a);
 }
 
 template <int D>

@@ -153,12 +153,12 @@ int mha_fused_out_clusters(int h, bool self);
 // Per-file device error words (read and cleared; see sm103.cuh).
 // One decoding step against a key/value cache: the n_q (<= 8) newest tokens'
 // queries, at positions L - n_q .. L - 1 of an L-row cache, each against the
-// keys at or before its position. Split over 256-key chunks (partials in a
+// keys at or before its position. Split over 128-key chunks (partials in a
 // workspace of float), then merged per (batch, head).
 constexpr int kDecodeMaxQueries = 8;
-constexpr int kDecodeMaxChunks = 512;  // n_max <= 512 * 256 = 131072
+constexpr int kDecodeMaxChunks = 1024;  // n_max <= 1024 * 128 = 131072
 struct DecodeProblem {
-  CUtensorMap tm_k, tm_v;      // 3-D (d, n_max, B*h) bf16, box 64 x 256 x 1, 128-byte swizzle
+  CUtensorMap tm_k, tm_v;      // 3-D (d, n_max, B*h) bf16, box 64 x 128 x 1, 128-byte swizzle
   const void* q;               // [B, h, n_q, d] bf16
   void* out;                   // [B, h, n_q, d] bf16
   const int32_t* cache_lens;   // [B] valid rows, or null (= n_max)

@@ -106,8 +106,10 @@ __global__ void __launch_bounds__(kDecThreads)
     tma_prefetch_desc(&tm_v);
   }
   __syncthreads();
-  griddep_launch_dependents();
   griddep_wait();  // the cache, the queries and the lengths may come from the previous kernel
+  // after the wait: the merge starts once every CTA of this grid is past it,
+  // so whatever came before this grid is complete when the merge starts
+  griddep_launch_dependents();
 
   const int L = cache_len(a, b);
   const int c0 = c * kChunk;
@@ -258,16 +260,30 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   const int tid = static_cast<int>(threadIdx.x);
   const int hh = static_cast<int>(blockIdx.x), b = static_cast<int>(blockIdx.y);
   const int64_t bh = static_cast<int64_t>(b) * a.h + hh;
-  griddep_launch_dependents();
-  griddep_wait();  // the partials of the previous kernel are complete
+  // the lengths before the wait: the partial grid triggers this launch only
+  // after its own dependency wait, so the kernel that wrote them (if any) is
+  // complete; the partials themselves are read after the wait
   const int L = cache_len(a, b);
   const int nc = (L + kChunk - 1) / kChunk;       // <= a.chunks
+  const int col = tid % D, grp = tid / D;
+  const float* o_bh = a.ws_o + bh * a.chunks * a.n_q * D;  // [chunk][query][D]
+  griddep_launch_dependents();
+  griddep_wait();  // the partials of the previous kernel are complete
+  // the first query's first batch of chunk partials is in flight while the
+  // weights are computed
+  float v0[kMergeBatch];
+#pragma unroll
+  for (int u = 0; u < kMergeBatch; ++u) {
+    const int c = grp + u * kGroups;
+    v0[u] = c < nc ? o_bh[c * a.n_q * D + col] : 0.f;
+  }
   const float* ml = a.ws_ml + bh * a.chunks * a.n_q * 2;  // [chunk][query][m, l]
   // per query (warp t, lanes over the chunks): m = max_c m_c,
   // w_c = 2^(m_c - m), l = sum_c w_c l_c
   const int warp = tid >> 5, lane = tid & 31;
   for (int t = warp; t < a.n_q; t += kMergeThreads / 32) {
     float m = -INFINITY;
+#pragma unroll 4
     for (int c = lane; c < nc; c += 32) m = fmaxf(m, ml[(c * a.n_q + t) * 2]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -284,8 +300,6 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     if (lane == 0) inv_l_s[t] = l > 0.f ? 1.f / l : 0.f;  // no visible key: output 0
   }
   __syncthreads();
-  const int col = tid % D, grp = tid / D;
-  const float* o_bh = a.ws_o + bh * a.chunks * a.n_q * D;  // [chunk][query][D]
   for (int t = 0; t < a.n_q; ++t) {
     float o = 0.f;
     for (int c0 = grp; c0 < nc; c0 += kMergeBatch * kGroups) {
@@ -293,7 +307,8 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
 #pragma unroll
       for (int u = 0; u < kMergeBatch; ++u) {
         const int c = c0 + u * kGroups;
-        v[u] = c < nc ? o_bh[(c * a.n_q + t) * D + col] : 0.f;
+        if (t == 0 && c0 == grp) v[u] = v0[u];
+        else v[u] = c < nc ? o_bh[(c * a.n_q + t) * D + col] : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < kMergeBatch; ++u) {

@@ -154,8 +154,9 @@ E2E_API = {
             "two staging workspaces in turn)",
     "encoder": "encoder_layer_forward_host (pinned host x, lengths and result; parameters "
                "resident; two staging workspaces in turn)",
-    "decode": "attn_decode_host (pinned host queries, cache lengths and result; caches "
-              "resident; two staging workspaces in turn)",
+    "decode": "attn_decode_host_async + attn_host_join (pinned host queries, cache lengths "
+              "and result; caches resident; two staging workspaces in turn; each result copy "
+              "overlaps the next step, all joined before the closing event)",
 }
 
 
@@ -744,8 +745,9 @@ class DecodeCall:
         return 2
 
     def e2e_run(self, i, stream):
-        """attn_decode_host: pinned host queries and cache lengths in, pinned host
-        output out; the caches (state) resident on the device, rotating sets."""
+        """attn_decode_host_async: pinned host queries and cache lengths in,
+        pinned host output out; the caches (state) resident on the device,
+        rotating sets; e2e_finish joins the result copies."""
         import torch
         B, h, n_q, n_max, d = self.shape
         if self.h_ws is None:
@@ -753,11 +755,11 @@ class DecodeCall:
             self.h_ws = [torch.empty(self.h_wsb, dtype=torch.uint8, device="cuda")
                          for _ in range(2)]
         s = self.sets[i % len(self.sets)]
-        self.tsd.attn_decode_host(self.h_q, s["k"], s["v"], self.h_out, B, h, n_q, n_max, d, d,
-                                  self.h_lens, 0.0, self.h_ws[i % 2], self.h_wsb, stream)
+        self.tsd.attn_decode_host_async(self.h_q, s["k"], s["v"], self.h_out, B, h, n_q, n_max, d,
+                                        d, self.h_lens, 0.0, self.h_ws[i % 2], self.h_wsb, stream)
 
     def e2e_finish(self, stream):
-        pass  # results copied on `stream`
+        self.tsd.attn_host_join(stream)
 
     def e2e_bytes(self):
         return self.a.q.nbytes + self.lens.nbytes, self.a.q.nbytes

@@ -429,6 +429,15 @@ attn_status attn_decode_host(const void *q_host, const void *k_cache, const void
                              int B, int h, int n_q, int n_max, int d_k, int d_v,
                              const int32_t *cache_lens_host, float scale,
                              void *workspace, size_t workspace_bytes, tsd_stream_t stream);
+/* attn_decode_host_async -- attn_decode_host whose result copy runs on the
+ * library's device-to-host stream, as mha_forward_host_async: out_host is
+ * complete, and may be reused, once `stream` has passed a later
+ * attn_host_join(stream). Arguments and errors as attn_decode_host. */
+attn_status attn_decode_host_async(const void *q_host, const void *k_cache,
+                                   const void *v_cache, void *out_host,
+                                   int B, int h, int n_q, int n_max, int d_k, int d_v,
+                                   const int32_t *cache_lens_host, float scale,
+                                   void *workspace, size_t workspace_bytes, tsd_stream_t stream);
 
 /*
  * attn_get_device_status -- synchronises `stream`, then reads and clears the

@@ -294,6 +294,11 @@ def test_host_entry_points_reject_bad_arguments_before_copying(lib):
                                 None) == tsd.ATTN_ERR_UNSUPPORTED
     assert lib.attn_decode_host(hx, w, w, hx, 1, 1, 1, 131072 + 256, 64, 64, None, 0.0, ws, big,
                                 None) == tsd.ATTN_ERR_UNSUPPORTED
+    # the asynchronous variant refuses the same arguments with the same codes
+    assert lib.attn_decode_host_async(hx, None, w, hx, 1, 1, 1, 128, 64, 64, None, 0.0, ws, big,
+                                      None) == tsd.ATTN_ERR_INVALID
+    assert lib.attn_decode_host_async(hx, w, w, hx, 1, 1, 9, 128, 64, 64, None, 0.0, ws, big,
+                                      None) == tsd.ATTN_ERR_UNSUPPORTED
 
 
 def test_host_entry_points_empty_problems_are_no_ops(lib):

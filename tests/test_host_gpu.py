@@ -241,3 +241,35 @@ def test_mha_forward_host_async_back_to_back_then_join(tsd, n_ws):
     for i, x in enumerate(xs):
         np.testing.assert_array_equal(houts[i].numpy(), device_mha(tsd, m, x), err_msg=f"call {i}")
 
+
+
+def test_attn_decode_host_async_back_to_back_then_join(tsd):
+    """Six decoding steps with different queries and lengths through two
+    workspaces, no host synchronisation, one join: each result equals its own
+    step's device call."""
+    import torch
+    B, h, n_q, n_max, d = 4, 8, 1, 2048, 64
+    a = synthetic.attention_inputs(5160, B, h, n_q, n_max, d, d)
+    kc, vc = to_dev_bf16(a.k), to_dev_bf16(a.v)
+    hwsb = tsd.attn_decode_host_workspace_bytes(B, h, n_q, n_max, d, d)
+    hws = [torch.empty(hwsb, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    rng = np.random.default_rng(5161)
+    steps = [(synthetic.attention_inputs(5170 + i, B, h, n_q, 1, d, d).q,
+              rng.integers(0, n_max + 1, size=B).astype(np.int32)) for i in range(6)]
+    hq = [pinned_bf16(q) for q, _ in steps]
+    hl = [pinned_i32(l) for _, l in steps]
+    houts = [pinned_out((B, h, n_q, d)) for _ in steps]
+    for i in range(len(steps)):
+        tsd.attn_decode_host_async(hq[i], kc, vc, houts[i], B, h, n_q, n_max, d, d, hl[i], 0.0,
+                                   hws[i % 2], hwsb)
+    tsd.attn_host_join()
+    torch.cuda.current_stream().synchronize()
+    assert tsd.attn_get_device_status() == tsd.ATTN_OK
+    wsb = tsd.attn_decode_workspace_bytes(B, h, n_q, n_max, d)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    for i, (q, lens) in enumerate(steps):
+        out_dev = torch.empty((B, h, n_q, d), dtype=torch.bfloat16, device="cuda")
+        tsd.attn_decode(to_dev_bf16(q), kc, vc, out_dev, B, h, n_q, n_max, d, d, to_dev_i32(lens),
+                        0.0, ws, wsb)
+        np.testing.assert_array_equal(houts[i].numpy(), bits_of_device(out_dev),
+                                      err_msg=f"step {i}")

@@ -29,6 +29,7 @@ __all__ = [
     "mha_host_workspace_bytes", "mha_forward_host", "encoder_layer_host_workspace_bytes",
     "encoder_layer_forward_host", "attn_decode_host_workspace_bytes", "attn_decode_host",
     "attn_forward_window_host", "mha_forward_host_async", "attn_host_join",
+    "attn_decode_host_async",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = range(5)
@@ -43,7 +44,7 @@ EXPORTED_SYMBOLS = (
     "attn_host_workspace_bytes", "attn_forward_host", "mha_host_workspace_bytes",
     "mha_forward_host", "encoder_layer_host_workspace_bytes", "encoder_layer_forward_host",
     "attn_decode_host_workspace_bytes", "attn_decode_host", "attn_forward_window_host",
-    "mha_forward_host_async", "attn_host_join",
+    "mha_forward_host_async", "attn_host_join", "attn_decode_host_async",
 )
 
 # TSD_MHA_NOALLOC_SCRATCH_BYTES of the header: the fixed scratch of mha_forward_noalloc
@@ -118,13 +119,14 @@ def library():
     lib.attn_host_join.argtypes = [st]
     lib.encoder_layer_forward_host.argtypes = [vp] * 14 + [i] * 7 + [vp, f, f, vp, sz, st]
     lib.attn_decode_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp, f, vp, sz, st]
+    lib.attn_decode_host_async.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp, f, vp, sz, st]
     for name in ("attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_forward",
                  "attn_get_device_status", "attn_last_cuda_error", "attn_selftest_wait_timeout",
                  "mha_project_qkv", "mha_project_out", "mha_forward_noalloc", "mha_concat_heads",
                  "mha_forward_launches", "attn_forward_window", "attn_decode",
                  "encoder_layer_forward", "attn_forward_host", "mha_forward_host",
                  "encoder_layer_forward_host", "attn_decode_host", "attn_forward_window_host",
-                 "mha_forward_host_async", "attn_host_join"):
+                 "mha_forward_host_async", "attn_host_join", "attn_decode_host_async"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -373,3 +375,15 @@ def attn_decode_host(q_host, k_cache, v_cache, out_host, B, h, n_q, n_max, d_k, 
                                       B, h, n_q, n_max, d_k, d_v, _ptr(cache_lens_host), scale,
                                       _ptr(workspace), workspace_bytes, _stream(stream)),
            "attn_decode_host")
+
+
+def attn_decode_host_async(q_host, k_cache, v_cache, out_host, B, h, n_q, n_max, d_k, d_v,
+                           cache_lens_host=None, scale=0.0, workspace=None, workspace_bytes=0,
+                           stream=None):
+    """attn_decode_host with the result copy on the library's result stream:
+    out_host is complete once `stream` has passed a later attn_host_join."""
+    _check(library().attn_decode_host_async(_ptr(q_host), _ptr(k_cache), _ptr(v_cache),
+                                            _ptr(out_host), B, h, n_q, n_max, d_k, d_v,
+                                            _ptr(cache_lens_host), scale, _ptr(workspace),
+                                            workspace_bytes, _stream(stream)),
+           "attn_decode_host_async")

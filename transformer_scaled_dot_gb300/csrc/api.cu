@@ -1175,10 +1175,14 @@ size_t attn_decode_host_workspace_bytes(int B, int h, int n_q, int n_max, int d_
   return decode_host_layout(B, h, n_q, n_max, d_k, d_v, &t) ? t : 0;
 }
 
-attn_status attn_decode_host(const void* q_host, const void* k_cache, const void* v_cache,
+}  // extern "C"
+
+namespace {
+
+attn_status decode_host_call(const void* q_host, const void* k_cache, const void* v_cache,
                              void* out_host, int B, int h, int n_q, int n_max, int d_k, int d_v,
                              const int32_t* cache_lens_host, float scale, void* workspace,
-                             size_t workspace_bytes, tsd_stream_t stream) {
+                             size_t workspace_bytes, tsd_stream_t stream, bool async) {
   if (!q_host || !out_host || !workspace) return ATTN_ERR_INVALID;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID;
   size_t need = 0;
@@ -1213,7 +1217,28 @@ attn_status attn_decode_host(const void* q_host, const void* k_cache, const void
                   scale, inner, inner_bytes, stream);
   hs.computed();
   if (s != ATTN_OK) return s;
-  return hs.copy_out(out_host, out, ob) == cudaSuccess ? ATTN_OK : cuda_fail(hs.status());
+  const cudaError_t e = async ? hs.copy_out_async(out_host, out, ob) : hs.copy_out(out_host, out, ob);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(hs.status());
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_decode_host(const void* q_host, const void* k_cache, const void* v_cache,
+                             void* out_host, int B, int h, int n_q, int n_max, int d_k, int d_v,
+                             const int32_t* cache_lens_host, float scale, void* workspace,
+                             size_t workspace_bytes, tsd_stream_t stream) {
+  return decode_host_call(q_host, k_cache, v_cache, out_host, B, h, n_q, n_max, d_k, d_v,
+                          cache_lens_host, scale, workspace, workspace_bytes, stream, false);
+}
+
+attn_status attn_decode_host_async(const void* q_host, const void* k_cache, const void* v_cache,
+                                   void* out_host, int B, int h, int n_q, int n_max, int d_k,
+                                   int d_v, const int32_t* cache_lens_host, float scale,
+                                   void* workspace, size_t workspace_bytes, tsd_stream_t stream) {
+  return decode_host_call(q_host, k_cache, v_cache, out_host, B, h, n_q, n_max, d_k, d_v,
+                          cache_lens_host, scale, workspace, workspace_bytes, stream, true);
 }
 
 }  // extern "C"

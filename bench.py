@@ -152,8 +152,9 @@ E2E_API = {
            "next call, all joined before the closing event)",
     "attn": "attn_forward_host / attn_forward_window_host (pinned host Q, K, V and O; "
             "two staging workspaces in turn)",
-    "encoder": "encoder_layer_forward_host (pinned host x, lengths and result; parameters "
-               "resident; two staging workspaces in turn)",
+    "encoder": "encoder_layer_forward_host_async + attn_host_join (pinned host x, lengths and "
+               "result; parameters resident; two staging workspaces in turn; each result copy "
+               "overlaps the next layer, all joined before the closing event)",
     "decode": "attn_decode_host_async + attn_host_join (pinned host queries, cache lengths "
               "and result; caches resident; two staging workspaces in turn; each result copy "
               "overlaps the next step, all joined before the closing event)",
@@ -655,8 +656,9 @@ class EncoderCall:
                                              True) + 4
 
     def e2e_run(self, i, stream):
-        """encoder_layer_forward_host: pinned host x and lengths in, pinned host
-        output out, the layer's parameters resident on the device."""
+        """encoder_layer_forward_host_async: pinned host x and lengths in, pinned
+        host output out, the layer's parameters resident on the device;
+        e2e_finish joins the result copies."""
         import torch
         m, e, s = self.e.mha, self.e, self.sets[0]
         if self.h_ws is None:
@@ -664,13 +666,13 @@ class EncoderCall:
                                                                      m.d_k, e.d_ff)
             self.h_ws = [torch.empty(self.h_wsb, dtype=torch.uint8, device="cuda")
                          for _ in range(2)]
-        self.tsd.encoder_layer_forward_host(self.h_x, *s["t"][1:], self.h_out, m.B, m.n_q,
-                                            m.d_model, m.h, m.d_k, e.d_ff, m.mask_kind,
-                                            self.h_lens, 0.0, self.cfg["eps"], self.h_ws[i % 2],
-                                            self.h_wsb, stream)
+        self.tsd.encoder_layer_forward_host_async(self.h_x, *s["t"][1:], self.h_out, m.B, m.n_q,
+                                                  m.d_model, m.h, m.d_k, e.d_ff, m.mask_kind,
+                                                  self.h_lens, 0.0, self.cfg["eps"],
+                                                  self.h_ws[i % 2], self.h_wsb, stream)
 
     def e2e_finish(self, stream):
-        pass  # results copied on `stream`
+        self.tsd.attn_host_join(stream)
 
     def e2e_bytes(self):
         m = self.e.mha

@@ -420,6 +420,23 @@ attn_status encoder_layer_forward_host(const void *x_host,
                                        int mask_kind, const int32_t *kv_lens_host, float scale,
                                        float eps, void *workspace, size_t workspace_bytes,
                                        tsd_stream_t stream);
+/* encoder_layer_forward_host_async -- encoder_layer_forward_host whose
+ * result copy runs on the library's device-to-host stream, as
+ * mha_forward_host_async: out_host is complete, and may be reused, once
+ * `stream` has passed a later attn_host_join(stream). Arguments and errors as
+ * encoder_layer_forward_host. */
+attn_status encoder_layer_forward_host_async(const void *x_host,
+                                             const void *w_q, const void *w_k, const void *w_v,
+                                             const void *w_o,
+                                             const void *ln1_gamma, const void *ln1_beta,
+                                             const void *w_1, const void *b_1,
+                                             const void *w_2, const void *b_2,
+                                             const void *ln2_gamma, const void *ln2_beta,
+                                             void *out_host,
+                                             int B, int n, int d_model, int h, int d_k, int d_ff,
+                                             int mask_kind, const int32_t *kv_lens_host,
+                                             float scale, float eps, void *workspace,
+                                             size_t workspace_bytes, tsd_stream_t stream);
 
 size_t attn_decode_host_workspace_bytes(int B, int h, int n_q, int n_max, int d_k, int d_v);
 /* q_host [B, h, n_q, d_k] and out_host [B, h, n_q, d_v] on the host; the

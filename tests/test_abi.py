@@ -286,6 +286,10 @@ def test_host_entry_points_reject_bad_arguments_before_copying(lib):
                                           big, None) == tsd.ATTN_ERR_INVALID
     assert lib.encoder_layer_forward_host(*args, 2, 16, 384, 8, 64, 2048, 0, None, 0.0, 1e-6, ws,
                                           big, None) == tsd.ATTN_ERR_UNSUPPORTED
+    assert lib.encoder_layer_forward_host_async(*args, 2, 16, 512, 8, 64, 2048, 0, None, 0.0, 0.0,
+                                                ws, big, None) == tsd.ATTN_ERR_INVALID
+    assert lib.encoder_layer_forward_host_async(*args, 2, 16, 384, 8, 64, 2048, 0, None, 0.0,
+                                                1e-6, ws, big, None) == tsd.ATTN_ERR_UNSUPPORTED
     # attn_decode_host: null cache, too many queries
     assert lib.attn_decode_host(hx, None, w, hx, 1, 1, 1, 128, 64, 64, None, 0.0, ws, big,
                                 None) == tsd.ATTN_ERR_INVALID

@@ -273,3 +273,36 @@ def test_attn_decode_host_async_back_to_back_then_join(tsd):
                         0.0, ws, wsb)
         np.testing.assert_array_equal(houts[i].numpy(), bits_of_device(out_dev),
                                       err_msg=f"step {i}")
+
+
+def test_encoder_layer_forward_host_async_back_to_back_then_join(tsd):
+    """Four layers with different inputs through two workspaces, no host
+    synchronisation, one join: each result equals its own device call."""
+    import torch
+    e = synthetic.encoder_inputs(5180, 4, 128, 512, 8, 2048, MASK_KEY_PADDING, (64, 128),
+                                 add_pe=True)
+    m = e.mha
+    params = [to_dev_bf16(t) for t in (m.w_q, m.w_k, m.w_v, m.w_o, e.ln1_gamma, e.ln1_beta, e.w_1,
+                                       e.b_1, e.w_2, e.b_2, e.ln2_gamma, e.ln2_beta)]
+    hwsb = tsd.encoder_layer_host_workspace_bytes(m.B, m.n_q, m.d_model, m.h, m.d_k, e.d_ff)
+    hws = [torch.empty(hwsb, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    xs = [synthetic.encoder_inputs(5181 + i, 4, 128, 512, 8, 2048).mha.x_q for i in range(4)]
+    hxs = [pinned_bf16(x) for x in xs]
+    hl = pinned_i32(m.kv_lens)
+    houts = [pinned_out((m.B, m.n_q, m.d_model)) for _ in xs]
+    for i in range(len(xs)):
+        tsd.encoder_layer_forward_host_async(hxs[i], *params, houts[i], m.B, m.n_q, m.d_model, m.h,
+                                             m.d_k, e.d_ff, m.mask_kind, hl, 0.0, 1e-6,
+                                             hws[i % 2], hwsb)
+    tsd.attn_host_join()
+    torch.cuda.current_stream().synchronize()
+    assert tsd.attn_get_device_status() == tsd.ATTN_OK
+    wsb = tsd.encoder_layer_workspace_bytes(m.B, m.n_q, m.d_model, m.h, m.d_k, e.d_ff)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    dl = to_dev_i32(m.kv_lens)
+    for i, x in enumerate(xs):
+        out_dev = torch.empty((m.B, m.n_q, m.d_model), dtype=torch.bfloat16, device="cuda")
+        tsd.encoder_layer_forward(to_dev_bf16(x), *params, out_dev, m.B, m.n_q, m.d_model, m.h,
+                                  m.d_k, e.d_ff, m.mask_kind, dl, 0.0, 1e-6, ws, wsb)
+        np.testing.assert_array_equal(houts[i].numpy(), bits_of_device(out_dev),
+                                      err_msg=f"layer {i}")

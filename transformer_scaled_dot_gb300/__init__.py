@@ -29,7 +29,7 @@ __all__ = [
     "mha_host_workspace_bytes", "mha_forward_host", "encoder_layer_host_workspace_bytes",
     "encoder_layer_forward_host", "attn_decode_host_workspace_bytes", "attn_decode_host",
     "attn_forward_window_host", "mha_forward_host_async", "attn_host_join",
-    "attn_decode_host_async",
+    "attn_decode_host_async", "encoder_layer_forward_host_async",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = range(5)
@@ -45,6 +45,7 @@ EXPORTED_SYMBOLS = (
     "mha_forward_host", "encoder_layer_host_workspace_bytes", "encoder_layer_forward_host",
     "attn_decode_host_workspace_bytes", "attn_decode_host", "attn_forward_window_host",
     "mha_forward_host_async", "attn_host_join", "attn_decode_host_async",
+    "encoder_layer_forward_host_async",
 )
 
 # TSD_MHA_NOALLOC_SCRATCH_BYTES of the header: the fixed scratch of mha_forward_noalloc
@@ -118,6 +119,7 @@ def library():
     lib.mha_forward_host_async.argtypes = [vp] * 7 + [i] * 8 + [vp, f, vp, sz, st]
     lib.attn_host_join.argtypes = [st]
     lib.encoder_layer_forward_host.argtypes = [vp] * 14 + [i] * 7 + [vp, f, f, vp, sz, st]
+    lib.encoder_layer_forward_host_async.argtypes = lib.encoder_layer_forward_host.argtypes
     lib.attn_decode_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp, f, vp, sz, st]
     lib.attn_decode_host_async.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp, f, vp, sz, st]
     for name in ("attn_forward", "attn_forward_strided", "attn_forward_f32", "mha_forward",
@@ -126,7 +128,8 @@ def library():
                  "mha_forward_launches", "attn_forward_window", "attn_decode",
                  "encoder_layer_forward", "attn_forward_host", "mha_forward_host",
                  "encoder_layer_forward_host", "attn_decode_host", "attn_forward_window_host",
-                 "mha_forward_host_async", "attn_host_join", "attn_decode_host_async"):
+                 "mha_forward_host_async", "attn_host_join", "attn_decode_host_async",
+                 "encoder_layer_forward_host_async"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -362,6 +365,22 @@ def encoder_layer_forward_host(x_host, w_q, w_k, w_v, w_o, ln1_gamma, ln1_beta, 
                                                 _ptr(kv_lens_host), scale, eps, _ptr(workspace),
                                                 workspace_bytes, _stream(stream)),
            "encoder_layer_forward_host")
+
+
+def encoder_layer_forward_host_async(x_host, w_q, w_k, w_v, w_o, ln1_gamma, ln1_beta, w_1, b_1,
+                                     w_2, b_2, ln2_gamma, ln2_beta, out_host, B, n, d_model, h,
+                                     d_k, d_ff, mask_kind=ATTN_MASK_NONE, kv_lens_host=None,
+                                     scale=0.0, eps=1e-6, workspace=None, workspace_bytes=0,
+                                     stream=None):
+    """encoder_layer_forward_host with the result copy on the library's result
+    stream: out_host is complete once `stream` has passed a later attn_host_join."""
+    ptrs = [_ptr(t) for t in (x_host, w_q, w_k, w_v, w_o, ln1_gamma, ln1_beta, w_1, b_1, w_2, b_2,
+                              ln2_gamma, ln2_beta, out_host)]
+    _check(library().encoder_layer_forward_host_async(*ptrs, B, n, d_model, h, d_k, d_ff,
+                                                      mask_kind, _ptr(kv_lens_host), scale, eps,
+                                                      _ptr(workspace), workspace_bytes,
+                                                      _stream(stream)),
+           "encoder_layer_forward_host_async")
 
 
 def attn_decode_host_workspace_bytes(B, h, n_q, n_max, d_k, d_v) -> int:

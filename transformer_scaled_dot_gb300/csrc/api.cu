@@ -1127,15 +1127,19 @@ size_t encoder_layer_host_workspace_bytes(int B, int n, int d_model, int h, int 
   return encoder_host_layout(B, n, d_model, h, d_k, d_ff, &t) ? t : 0;
 }
 
-attn_status encoder_layer_forward_host(const void* x_host, const void* w_q, const void* w_k,
-                                       const void* w_v, const void* w_o, const void* ln1_gamma,
-                                       const void* ln1_beta, const void* w_1, const void* b_1,
-                                       const void* w_2, const void* b_2, const void* ln2_gamma,
-                                       const void* ln2_beta, void* out_host, int B, int n,
-                                       int d_model, int h, int d_k, int d_ff, int mask_kind,
-                                       const int32_t* kv_lens_host, float scale, float eps,
-                                       void* workspace, size_t workspace_bytes,
-                                       tsd_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+attn_status encoder_host_call(const void* x_host, const void* w_q, const void* w_k,
+                              const void* w_v, const void* w_o, const void* ln1_gamma,
+                              const void* ln1_beta, const void* w_1, const void* b_1,
+                              const void* w_2, const void* b_2, const void* ln2_gamma,
+                              const void* ln2_beta, void* out_host, int B, int n, int d_model,
+                              int h, int d_k, int d_ff, int mask_kind,
+                              const int32_t* kv_lens_host, float scale, float eps,
+                              void* workspace, size_t workspace_bytes, tsd_stream_t stream,
+                              bool async) {
   if (!x_host || !out_host || !workspace) return ATTN_ERR_INVALID;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID;
   size_t need = 0;
@@ -1167,7 +1171,38 @@ attn_status encoder_layer_forward_host(const void* x_host, const void* w_q, cons
                             pad ? lens : nullptr, scale, eps, inner, inner_bytes, stream);
   hs.computed();
   if (s != ATTN_OK) return s;
-  return hs.copy_out(out_host, out, xb) == cudaSuccess ? ATTN_OK : cuda_fail(hs.status());
+  const cudaError_t e = async ? hs.copy_out_async(out_host, out, xb) : hs.copy_out(out_host, out, xb);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(hs.status());
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status encoder_layer_forward_host(const void* x_host, const void* w_q, const void* w_k,
+                                       const void* w_v, const void* w_o, const void* ln1_gamma,
+                                       const void* ln1_beta, const void* w_1, const void* b_1,
+                                       const void* w_2, const void* b_2, const void* ln2_gamma,
+                                       const void* ln2_beta, void* out_host, int B, int n,
+                                       int d_model, int h, int d_k, int d_ff, int mask_kind,
+                                       const int32_t* kv_lens_host, float scale, float eps,
+                                       void* workspace, size_t workspace_bytes,
+                                       tsd_stream_t stream) {
+  return encoder_host_call(x_host, w_q, w_k, w_v, w_o, ln1_gamma, ln1_beta, w_1, b_1, w_2, b_2,
+                           ln2_gamma, ln2_beta, out_host, B, n, d_model, h, d_k, d_ff, mask_kind,
+                           kv_lens_host, scale, eps, workspace, workspace_bytes, stream, false);
+}
+
+attn_status encoder_layer_forward_host_async(
+    const void* x_host, const void* w_q, const void* w_k, const void* w_v, const void* w_o,
+    const void* ln1_gamma, const void* ln1_beta, const void* w_1, const void* b_1,
+    const void* w_2, const void* b_2, const void* ln2_gamma, const void* ln2_beta,
+    void* out_host, int B, int n, int d_model, int h, int d_k, int d_ff, int mask_kind,
+    const int32_t* kv_lens_host, float scale, float eps, void* workspace,
+    size_t workspace_bytes, tsd_stream_t stream) {
+  return encoder_host_call(x_host, w_q, w_k, w_v, w_o, ln1_gamma, ln1_beta, w_1, b_1, w_2, b_2,
+                           ln2_gamma, ln2_beta, out_host, B, n, d_model, h, d_k, d_ff, mask_kind,
+                           kv_lens_host, scale, eps, workspace, workspace_bytes, stream, true);
 }
 
 size_t attn_decode_host_workspace_bytes(int B, int h, int n_q, int n_max, int d_k, int d_v) {

@@ -70,6 +70,9 @@ CASES = [
     (300, 1, 1, 300, 64, "ragged"),
     (5, 16, 2, 4096, 128, [4096, 1, 4000, 129, 2222]),
     (9, 20, 1, 8192, 64, [8192, 0, 7000, 300, 8191, 0, 4097, 256, 6000]),
+    # the largest cache (131072 rows: 1024 chunks, the merge's largest weight table)
+    (2, 1, 8, 131072, 64, [131072, 100001]),
+    (1, 1, 8, 131072, 128, None),
 ]
 
 

@@ -68,8 +68,11 @@ enum {
  *   k    [B, h, n_k, d_k]  bf16, device, 16-byte aligned
  *   v    [B, h, n_k, d_v]  bf16, device, 16-byte aligned
  *   out  [B, h, n_q, d_v]  bf16, device, 16-byte aligned, written in full
- *   d_k == d_v, and d_k in {64, 128}         else ATTN_ERR_UNSUPPORTED
- *   B, h >= 1; n_q, n_k >= 1                 else ATTN_ERR_INVALID
+ *   d_k == d_v, and d_k in {16, 32, 64, 128, 256}   else ATTN_ERR_UNSUPPORTED
+ *     (16, 32 and 256 are the head sizes of Table 3 (A), "[논문 리뷰]Attention
+ *     Is All You Need" (kimjiil.github.io), section 6.2; 64 is the base model's)
+ *   B, h, n_q, n_k >= 0                      else ATTN_ERR_INVALID
+ *     (a zero size launches nothing; n_k = 0 writes all-zero output rows)
  *   mask_kind: OR of ATTN_MASK_* bits; CAUSAL needs n_q == n_k
  *   kv_lens: device int32[B]; required with ATTN_MASK_KEY_PADDING, ignored otherwise
  *   scale: the logit factor; 0 selects 1/sqrt(d_k) (eq. (1))

@@ -48,6 +48,9 @@ FAKE = 1 << 20  # 16-byte aligned, never dereferenced: every call below fails va
 @pytest.mark.parametrize("args,expect", [
     # (B, h, n_q, n_k, d_k, d_v, mask, kv_lens, scale)
     ((1, 1, 16, 16, 96, 96, 0, None, 0.0), tsd.ATTN_ERR_UNSUPPORTED),
+    ((1, 1, 16, 16, 48, 48, 0, None, 0.0), tsd.ATTN_ERR_UNSUPPORTED),  # not a Table 3 (A) size
+    ((1, 1, 16, 16, 8, 8, 0, None, 0.0), tsd.ATTN_ERR_UNSUPPORTED),
+    ((1, 1, 16, 16, 512, 512, 0, None, 0.0), tsd.ATTN_ERR_UNSUPPORTED),
     ((1, 1, 16, 16, 64, 128, 0, None, 0.0), tsd.ATTN_ERR_UNSUPPORTED),
     ((-1, 1, 16, 16, 64, 64, 0, None, 0.0), tsd.ATTN_ERR_INVALID),
     ((1, 1, 16, 8, 64, 64, 1, None, 0.0), tsd.ATTN_ERR_INVALID),      # causal, n_q != n_k

@@ -45,7 +45,7 @@ def test_replica_reduction_gloo_world2():
 def test_defaults_and_flops():
     import bench
     a = bench.parse_args([])
-    assert a.gpus == 1 and a.workload == "base_encoder_mha" and a.warmup >= 3
+    assert a.gpus == 1 and a.workload == "long" and a.warmup >= 3 and a.min_seconds >= 2.0
     assert bench.attn_flops(1, 16, 4096, 4096, 64, False) == 4 * 16 * 4096 * 4096 * 64
     assert bench.attn_flops(1, 16, 4096, 4096, 64, True) == 2 * 16 * 4096 * 4096 * 64
 

@@ -243,6 +243,29 @@ def test_mha_forward_host_async_back_to_back_then_join(tsd, n_ws):
 
 
 
+def test_mha_forward_host_async_across_workspace_table_eviction(tsd):
+    """More workspaces than the library's table of 64 holds, used in turn
+    with no host synchronisation: workspace 0 comes back after 65 others have
+    evicted its entry, while its first asynchronous result copy may still be
+    pending. Every result is its own input's."""
+    import torch
+    m = synthetic.mha_inputs(1002, 2, 64, 64, 128, 2, 64, 64, MASK_KEY_PADDING, (16, 64))
+    n_ws, n_calls = 66, 70
+    w, wss, wsb = host_mha_setup(tsd, m, n_ws)
+    hl = pinned_i32(m.kv_lens)
+    xs = [synthetic.mha_inputs(7200 + i, 2, 64, 64, 128, 2, 64, 64).x_q for i in range(n_calls)]
+    hxs = [pinned_bf16(x) for x in xs]
+    houts = [pinned_out((m.B, m.n_q, m.d_model)) for _ in xs]
+    for i, (hx, ho) in enumerate(zip(hxs, houts)):
+        tsd.mha_forward_host_async(hx, hx, *w, ho, m.B, m.n_q, m.n_k, m.d_model, m.h, m.d_k,
+                                   m.d_v, m.mask_kind, hl, 0.0, wss[i % n_ws], wsb)
+    tsd.attn_host_join()
+    torch.cuda.current_stream().synchronize()
+    assert tsd.attn_get_device_status() == tsd.ATTN_OK
+    for i, x in enumerate(xs):
+        np.testing.assert_array_equal(houts[i].numpy(), device_mha(tsd, m, x), err_msg=f"call {i}")
+
+
 def test_attn_decode_host_async_back_to_back_then_join(tsd):
     """Six decoding steps with different queries and lengths through two
     workspaces, no host synchronisation, one join: each result equals its own

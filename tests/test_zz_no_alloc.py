@@ -63,6 +63,17 @@ def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row(tsd):
     assert_bf16_close(got, ref, "third call")
 
 
+def test_noalloc_three_launch_path_uses_every_scratch_region(tsd):
+    """Sequences longer than the fused kernel's 128 rows take the projection
+    GEMM, the attention kernel and the output GEMM, so Q, K, V and the merged
+    heads all live in the scratch array; two calls in a row."""
+    assert tsd.mha_forward_launches(2, 512, 512, 512, 8, 64, 64, True) == 3
+    for seed in (4004, 4005):
+        m = synthetic.mha_inputs(seed, 2, 512, 512, 512, 8, 64, 64, MASK_KEY_PADDING, (256, 512))
+        got, ref = _both(tsd, m)
+        assert_bf16_close(got, ref, f"seed {seed}")
+
+
 def test_noalloc_refuses_sizes_beyond_its_scratch(tsd):
     lib = tsd.library()
     B, n, dm, h, d = 64, 1024, 512, 8, 64

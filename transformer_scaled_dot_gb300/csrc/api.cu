@@ -241,8 +241,8 @@ cudaError_t make_gemm_group(tsd::GemmGroup* g, const void* a, const void* b, voi
   if (e != cudaSuccess) return e;
   const uint64_t bdims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K)};
   const int64_t bstr[1] = {N};
-  // 64 N columns x the K rows one CTA of a cluster loads (and multicasts)
-  const uint32_t bbox[2] = {64, static_cast<uint32_t>(tsd::kGemmBK / tsd::kGemmClusterM)};
+  // 64 N columns x the K rows of one pipeline stage
+  const uint32_t bbox[2] = {64, static_cast<uint32_t>(tsd::kGemmBK)};
   e = encode_bf16_map(&g->tm_b, b, 2, bdims, bstr, bbox);
   if (e != cudaSuccess) return e;
   const uint64_t cdims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};

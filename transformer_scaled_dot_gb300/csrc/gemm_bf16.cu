@@ -6,24 +6,17 @@
 // feed-forward network (section 3.3), whose bias, ReLU and residual the
 // epilogue adds.
 //
-// Persistent kernel, optionally in clusters of CM CTAs stacked along M: a
-// cluster walks groups of CM vertically adjacent 128 x 128 output tiles that
-// share their B (weight) tile, each B tile then read from L2 once per cluster.
-// The projections are bound by L2 -> SM traffic, not by the tensor cores, but
-// what limits them is the bytes each SM receives, which multicast does not
-// reduce (kGemmClusterM = 2 measured slower than 1 on the MHA shapes, the
-// pair waiting on each other's stage releases). Per CTA (C = A B, fp32
-// accumulation in tensor memory):
-//   warp 0     TMA producer: per 64-deep K block, its own A box (64 K x 128 M,
-//              K-major) and 1/CM of the K rows of the two B boxes (64 N each,
-//              N-major), multicast to every CTA of the cluster; kStages deep
+// Persistent kernel, one CTA per SM walking 128 x BN output tiles (m
+// fastest, so CTAs working at the same time share their B (weight) tile in
+// L2). The projections are bound by L2 -> SM traffic, not by the tensor
+// cores. Per CTA (C = A B, fp32 accumulation in tensor memory):
+//   warp 0     TMA producer: per 64-deep K block, the A box (64 K x 128 M,
+//              K-major) and the B boxes (64 N each, N-major); kStages deep
 //              (as many bytes in flight as shared memory allows: the loads,
 //              not the MMAs, set the pace), running ahead across tiles
 //   warp 1     MMA issuer (one thread), 4 MMAs per K block, whose completion
-//              frees the stage in every CTA of the cluster (each stage holds
-//              bytes written by all of them); owns the TMEM allocation: two
-//              128-column accumulators, so the epilogue of one tile overlaps
-//              the main loop of the next
+//              frees the stage; owns the TMEM allocation: two accumulators,
+//              so the epilogue of one tile overlaps the main loop of the next
 //   warps 2-5  epilogue: one thread per output row (TMEM lane) reads its
 //              accumulator row, releases the accumulator, converts to bf16
 //              into a 128-byte-swizzled staging tile in shared memory, and
@@ -72,7 +65,6 @@ constexpr int kCBytes = kBM * kBN * 2;  // 32 KB: one bf16 output tile (two 64-c
 constexpr int kCStages = 1;             // output staging tiles
 constexpr uint32_t kEpiBarrier = 1;     // named barrier of the four epilogue warps
 constexpr unsigned long long kDrainLimitNs = 100ull * 1000ull * 1000ull;
-static_assert(kGemmClusterM >= 1 && kBK % kGemmClusterM == 0, "B rows split over the cluster");
 
 template <int ST, bool LN, int BN>
 struct GemmSmemT {
@@ -108,19 +100,18 @@ struct TileCoord {
   int m0, n0;
 };
 
-// Cluster tile `ct` (CM row tiles x one column tile of BN columns) -> this CTA's tile.
-template <int CM, int BN>
-__device__ __forceinline__ TileCoord tile_coord(const GemmProblem& p, int ct, int rank) {
+// Tile `ct` (over every group's 128 x BN tiles) -> its group and origin.
+template <int BN>
+__device__ __forceinline__ TileCoord tile_coord(const GemmProblem& p, int ct) {
   int gi = 0;
   for (int i = 1; i < p.num_groups; ++i)
     if (ct >= p.g[i].tile_begin) gi = i;
   const GemmGroup& G = p.g[gi];
   const int local = ct - G.tile_begin;
-  const int ctm = (G.tiles_m + CM - 1) / CM;
   TileCoord c;
   c.g = &G;
-  c.m0 = ((local % ctm) * CM + rank) * kBM;  // m fastest: neighbouring clusters share B
-  c.n0 = (local / ctm) * BN;
+  c.m0 = (local % G.tiles_m) * kBM;  // m fastest: neighbouring CTAs share B
+  c.n0 = (local / G.tiles_m) * BN;
   return c;
 }
 
@@ -139,16 +130,15 @@ struct GemmStages {
 template <int EPI, int BN = 128>
 using GemmSmemFor = GemmSmemT<GemmStages<EPI, BN>::value, EPI == kEpiResLN, BN>;
 
-// CM: CTAs per cluster along M sharing B (multicast); CN: CTAs per cluster
-// along N sharing a row tile (LayerNorm epilogue only; then CM = 1).
-template <int CM, int EPI, int CN = 1, int BN = 128>
+// CN: CTAs per cluster along N sharing a row tile (LayerNorm epilogue only).
+template <int EPI, int CN = 1, int BN = 128>
 __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_constant__ GemmProblem p) {
   constexpr bool LN = EPI == kEpiResLN;
   constexpr int kSt = GemmStages<EPI, BN>::value;
-  constexpr int CS = LN ? CN : CM;  // CTAs per cluster
+  constexpr int CS = CN;  // CTAs per cluster
   constexpr int kBBytesT = kBK * BN * 2;           // one stage's B: BN / 64 chunks of 8 KB
   constexpr int kTmemAlloc = LN ? kTmemColsLN : 2 * BN;  // two BN-column accumulators
-  static_assert(!LN || (CM == 1 && CN >= 1 && CN <= kMaxLnCluster), "LayerNorm clusters");
+  static_assert(!LN || (CN >= 1 && CN <= kMaxLnCluster), "LayerNorm clusters");
   static_assert(LN || CN == 1, "clusters along N only for the LayerNorm epilogue");
   static_assert(BN == 128 || (BN == 256 && (EPI == kEpiPlain || EPI == kEpiBiasRelu)),
                 "wide tiles: plain and bias + ReLU epilogues");
@@ -160,9 +150,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
   const uint32_t lane = lane_id();
   const int kblocks = (p.K + kBK - 1) / kBK;
   const int rank = CS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int mrank = CM > 1 ? rank : 0;  // position along M: which K rows of B this CTA loads
-  constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CM) - 1u);
-  constexpr int kBRows = kBK / CM;  // K rows of each B box this CTA loads
   // cluster tiles of this CTA's cluster: cluster id, + number of clusters, ...
   const int first = static_cast<int>(blockIdx.x) / CS;
   const int stride = static_cast<int>(gridDim.x) / CS;
@@ -176,14 +163,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
       c.n0 = rank * kBN;
       return c;
     } else {
-      return tile_coord<CM, BN>(p, ct, rank);
+      return tile_coord<BN>(p, ct);
     }
   };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSt; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], CM);  // released by the MMA warp of every CTA
+      mbar_init(&sm.empty[s], 1);  // released by the MMA warp's commit
     }
     for (int s = 0; s < 2; ++s) mbar_init(&sm.ln_full[s], 1);
     for (int a = 0; a < 2; ++a) {
@@ -229,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
         for (int kb = 0; kb < kblocks; ++kb) {
           const int s = issued % kSt;
           const uint32_t ph = static_cast<uint32_t>(issued / kSt) & 1u;
-          // stage free in every CTA of the cluster (this CTA writes into all)
+          // stage released by the MMAs that read it
           if (!mbar_wait(&sm.empty[s], ph ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -238,22 +225,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
           if (issued == 0) griddep_wait();
           const int k0 = kb * kBK;
           tma_load_2d(sm.a[s], &c.g->tm_a, &sm.full[s], k0, c.m0);
-          const int kr = k0 + mrank * kBRows;
-          uint8_t* bdst = sm.b[s] + mrank * kBRows * 128;
 #pragma unroll
-          for (int ch = 0; ch < BN / 64; ++ch) {  // 64-column chunks of B, kBChunk apart
-            if constexpr (CM > 1)
-              tma_load_2d_multicast(bdst + ch * kBChunk, &c.g->tm_b, &sm.full[s], c.n0 + 64 * ch,
-                                    kr, kClusterMask);
-            else
-              tma_load_2d(bdst + ch * kBChunk, &c.g->tm_b, &sm.full[s], c.n0 + 64 * ch, kr);
-          }
+          for (int ch = 0; ch < BN / 64; ++ch)  // 64-column chunks of B, kBChunk apart
+            tma_load_2d(sm.b[s] + ch * kBChunk, &c.g->tm_b, &sm.full[s], c.n0 + 64 * ch, k0);
           ++issued;
         }
       }
-      // Every stage this CTA wrote has been released by all CTAs: no peer's
-      // release is still on its way here when the cluster leaves (and, after
-      // an abort, no copy of this CTA is in flight).
+      // Every stage written has been released: no MMA still reads it when the
+      // CTA leaves (and, after an abort, no copy of this CTA is in flight).
       volatile uint32_t never = 0;
       for (int i = max(0, issued - kSt); i < issued; ++i)
         mbar_wait(&sm.empty[i % kSt], static_cast<uint32_t>(i / kSt) & 1u,
@@ -290,8 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
             mma_bf16_ss(d_tmem, sdesc_advance(da, kk * (32 >> 4)), sdesc_advance(db, kk * (2048 >> 4)),
                         kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          if constexpr (CM > 1) mma_commit_multicast(&sm.empty[s], kClusterMask);
-          else mma_commit(&sm.empty[s]);
+          mma_commit(&sm.empty[s]);
           ++consumed;
         }
         if (ok) mma_commit(&sm.acc_full[acc]);
@@ -669,7 +647,7 @@ cudaError_t launch_gemm_ln(const GemmProblem& problem, cudaStream_t stream) {
   p.g[0].tile_begin = 0;
   p.total_tiles = p.g[0].tiles_m;
   if (p.total_tiles <= 0) return cudaSuccess;
-  auto kernel = gemm_bf16_kernel<1, kEpiResLN, CN>;
+  auto kernel = gemm_bf16_kernel<kEpiResLN, CN>;
   const size_t smem_bytes = sizeof(GemmSmemFor<kEpiResLN>) + 1024;
   static unsigned long long configured = 0;
   cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured);
@@ -716,7 +694,6 @@ cudaError_t launch_gemm_bf16(const GemmProblem& problem, cudaStream_t stream) {
       default: return cudaErrorInvalidValue;
     }
   }
-  constexpr int CM = kGemmClusterM;
   GemmProblem p = problem;
   // one epilogue mode per launch (every group's fields must agree)
   const GemmGroup& g0 = p.g[0];
@@ -744,7 +721,7 @@ cudaError_t launch_gemm_bf16(const GemmProblem& problem, cudaStream_t stream) {
   long long wide_tiles = 0, narrow_tiles = 0;
   for (int i = 0; i < p.num_groups; ++i) {
     if (p.g[i].N % 256 != 0) wide = false;
-    const long long rows = (p.g[i].tiles_m + CM - 1) / CM;
+    const long long rows = p.g[i].tiles_m;
     wide_tiles += rows * (p.g[i].N / 256);
     narrow_tiles += rows * ((p.g[i].N + 127) / 128);
   }
@@ -752,20 +729,19 @@ cudaError_t launch_gemm_bf16(const GemmProblem& problem, cudaStream_t stream) {
   const long long wide_waves = (wide_tiles + sms - 1) / sms;
   if (wide_waves < 3 || 3 * wide_waves >= 2 * ((narrow_tiles + sms - 1) / sms)) wide = false;
   const int bn = wide ? 256 : 128;
-  // tiles counted per cluster: CM row tiles x one column tile
   int t = 0;
   for (int i = 0; i < p.num_groups; ++i) {
     p.g[i].tiles_n = (p.g[i].N + bn - 1) / bn;
     p.g[i].tile_begin = t;
-    t += ((p.g[i].tiles_m + CM - 1) / CM) * p.g[i].tiles_n;
+    t += p.g[i].tiles_m * p.g[i].tiles_n;
   }
   p.total_tiles = t;
   if (t <= 0) return cudaSuccess;
-  auto kernel = wide ? (epi == kEpiPlain ? gemm_bf16_kernel<CM, kEpiPlain, 1, 256>
-                                         : gemm_bf16_kernel<CM, kEpiBiasRelu, 1, 256>)
-            : epi == kEpiPlain      ? gemm_bf16_kernel<CM, kEpiPlain>
-            : epi == kEpiBiasRelu ? gemm_bf16_kernel<CM, kEpiBiasRelu>
-                                    : gemm_bf16_kernel<CM, kEpiBiasResF32>;
+  auto kernel = wide ? (epi == kEpiPlain ? gemm_bf16_kernel<kEpiPlain, 1, 256>
+                                         : gemm_bf16_kernel<kEpiBiasRelu, 1, 256>)
+            : epi == kEpiPlain      ? gemm_bf16_kernel<kEpiPlain>
+            : epi == kEpiBiasRelu ? gemm_bf16_kernel<kEpiBiasRelu>
+                                    : gemm_bf16_kernel<kEpiBiasResF32>;
   const size_t smem_bytes =
       (wide ? sizeof(GemmSmemFor<kEpiPlain, 256>) : sizeof(GemmSmemFor<kEpiPlain>)) + 1024;
   static unsigned long long configured[5] = {0, 0, 0, 0, 0};
@@ -776,30 +752,14 @@ cudaError_t launch_gemm_bf16(const GemmProblem& problem, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = CM;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  // persistent: as many clusters as can be resident at once (clusters stay
-  // inside one GPC, so this can be below SMs / CM)
-  // the same for every epilogue mode (same resources); atomic accesses, as num_sms()
-  static int cached_clusters = 0;
-  int max_clusters = __atomic_load_n(&cached_clusters, __ATOMIC_RELAXED);
-  if (max_clusters == 0) {
-    cfg.gridDim = dim3(num_sms() / CM * CM);
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
-    if (e != cudaSuccess) return e;
-    max_clusters = n > 0 ? n : 1;
-    __atomic_store_n(&cached_clusters, max_clusters, __ATOMIC_RELAXED);
-  }
-  const int clusters = t < max_clusters ? t : max_clusters;
-  cfg.gridDim = dim3(clusters * CM);
+  cfg.numAttrs = 1;
+  // persistent: one CTA per SM (the tensor-memory allocation keeps a second
+  // CTA off the SM)
+  cfg.gridDim = dim3(static_cast<unsigned>(t < sms ? t : sms));
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 

@@ -8,8 +8,12 @@
 // read them) and `out_free` (recorded on the result stream after an
 // asynchronous result copy read the workspace's result staging). A workspace
 // seen for the first time, or again after its entry was evicted, first gets
-// `computed` and `out_free` recorded on the caller's stream, so its first
-// copy waits for everything the stream had before it. Streams and events live as long as
+// `computed` and `out_free` recorded on the caller's stream, after that
+// stream has been made to wait for every result copy issued so far on the
+// result stream (one of them may still read this workspace from a use before
+// its entry was evicted), so its first copy waits for everything the stream
+// had before it and its first computation for every earlier result copy.
+// Streams and events live as long as
 // the process: they are never destroyed, so nothing depends on the order of
 // static destruction against the CUDA runtime's own teardown.
 #include "host_stage.h"
@@ -45,6 +49,22 @@ cudaError_t make_stream(cudaStream_t* s) {
 }
 WorkspaceSlot g_slots[kWorkspaceSlots];
 uint64_t g_use_clock = 0;
+
+// `stream` waits for everything issued so far on the device's result stream.
+// Caller holds g_mutex.
+cudaError_t join_result_locked(int dev, cudaStream_t stream) {
+  if (g_result_stream[dev] == nullptr) return cudaSuccess;  // nothing was ever issued there
+  if (g_join_event[dev] == nullptr) {
+    cudaError_t e = cudaEventCreateWithFlags(&g_join_event[dev], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      g_join_event[dev] = nullptr;
+      return e;
+    }
+  }
+  cudaError_t e = cudaEventRecord(g_join_event[dev], g_result_stream[dev]);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, g_join_event[dev], 0);
+  return e;
+}
 
 }  // namespace
 
@@ -103,7 +123,11 @@ HostStage::HostStage(const void* workspace, cudaStream_t stream)
   computed_ = slot->computed;
   out_free_ = slot->out_free;
   if (fresh) {
-    err_ = cudaEventRecord(computed_, stream_);
+    // a result copy from this workspace's earlier use (before its entry was
+    // evicted, or under another slot's events) may still be reading its
+    // result staging: the caller's stream waits for all of them first
+    err_ = join_result_locked(dev, stream_);
+    if (err_ == cudaSuccess) err_ = cudaEventRecord(computed_, stream_);
     if (err_ == cudaSuccess) err_ = cudaEventRecord(out_free_, stream_);
     if (err_ != cudaSuccess) return;
   }
@@ -154,17 +178,7 @@ cudaError_t host_join(cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (g_result_stream[dev] == nullptr) return cudaSuccess;  // nothing was ever issued there
-  if (g_join_event[dev] == nullptr) {
-    e = cudaEventCreateWithFlags(&g_join_event[dev], cudaEventDisableTiming);
-    if (e != cudaSuccess) {
-      g_join_event[dev] = nullptr;
-      return e;
-    }
-  }
-  e = cudaEventRecord(g_join_event[dev], g_result_stream[dev]);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, g_join_event[dev], 0);
-  return e;
+  return join_result_locked(dev, stream);
 }
 
 }  // namespace tsd

@@ -45,15 +45,14 @@ struct AttnF32Problem {
 cudaError_t launch_attn_f32(const AttnF32Problem& p, cudaStream_t stream);
 
 // Projection GEMM geometry shared with the host-side tensor maps.
-constexpr int kGemmBK = 64;       // K rows per pipeline stage
-constexpr int kGemmClusterM = 1;  // CTAs per cluster (along M) sharing each B tile
+constexpr int kGemmBK = 64;  // K rows per pipeline stage
 
 // Grouped bf16 GEMM C_g[M_g, N_g] = A_g[M_g, K] * B_g[K, N_g] (fp32 accumulate,
 // bf16 out). A is K-major (row-major [M, K]); B is N-major (row-major [K, N],
 // the x.W weight layout). Up to 3 groups share K and run in one launch.
 struct GemmGroup {
   CUtensorMap tm_a;  // 2-D (K, M), box 64 x 128
-  CUtensorMap tm_b;  // 2-D (N, K), box 64 x (kGemmBK / kGemmClusterM)
+  CUtensorMap tm_b;  // 2-D (N, K), box 64 x kGemmBK
   CUtensorMap tm_c;  // 2-D (N, M), box 64 x 128 (TMA store of the output tile)
   uint16_t* c;
   int64_t ldc;       // elements

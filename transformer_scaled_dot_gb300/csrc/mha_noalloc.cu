@@ -20,6 +20,7 @@
 // head row).
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "tsd_attention.h"
@@ -30,25 +31,62 @@ static __device__ __align__(256) unsigned char g_mha_scratch[TSD_MHA_NOALLOC_SCR
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchEntry {
+  unsigned long long ctx_id = 0;  // the context the address belongs to (0: none yet)
+  void* ptr = nullptr;
+};
+ScratchEntry g_scratch[kMaxDevices];
 
-// Device address of g_mha_scratch on the current device. The host-side
-// symbol is only a stand-in, so the address is looked up once per device
-// (with that device current) and cached.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Driver calls reached through the runtime (the library does not link libcuda).
+template <typename F>
+F driver_fn(const char* name, int version) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<F>(p);
+}
+
+// Unique id of the calling thread's current context (ids are never reused
+// within a process, unlike context handles), or 0 if it has none.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 4000);
+  static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_mha_scratch in the current context. The host-side
+// symbol is only a stand-in, so the address is looked up with the device
+// current and cached per device, keyed by the context's id: after a
+// cudaDeviceReset, or with another context current, the lookup runs again.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  unsigned long long id = current_context_id();
+  if (id == 0 || g_scratch[dev].ctx_id != id) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_mha_scratch);
+    e = cudaGetSymbolAddress(&p, g_mha_scratch);  // binds the primary context if none is current
     if (e != cudaSuccess) return e;
     if (p == nullptr) return cudaErrorInvalidSymbol;
-    g_scratch_ptr[dev] = p;
+    if (id == 0) id = current_context_id();
+    g_scratch[dev].ctx_id = id;  // 0 if the id is unavailable: looked up on every call
+    g_scratch[dev].ptr = p;
+    *out = p;
+    return cudaSuccess;
   }
-  *out = g_scratch_ptr[dev];
+  *out = g_scratch[dev].ptr;
   return cudaSuccess;
 }
 

@@ -203,19 +203,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// The same box delivered to the shared memory of every CTA in `cta_mask`
-// (same offsets), each destination's mbarrier at `bar`'s offset receiving
-// the bytes written there. Cluster launches only; this GPU's own memory.
-__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map,
-                                                      uint64_t* bar, int c0, int c1,
-                                                      uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask)
-      : "memory");
-}
-
 // ------------------------------------------------------------------ clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -411,16 +398,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-
-// As mma_commit, but the arrival lands on the mbarrier at `bar`'s offset in
-// every CTA of `cta_mask` (cluster launches).
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 

@@ -70,6 +70,18 @@ WORKLOADS = {
                      desc="Transformer-big self-attention: B=8, h=16, n=1024, d_k=d_v=64"),
     "big_self_causal": dict(kind="attn", B=8, h=16, n=1024, d=64, causal=True, seed=1003,
                             desc="Transformer-big causal self-attention: B=8, h=16, n=1024, d=64"),
+    "base_encoder_attn": dict(
+        kind="attn", B=32, h=8, n=128, d=64, causal=False, padding=True, kv_range=(64, 128),
+        seed=1001,
+        desc="Transformer-base encoder self-attention alone (attn_forward, no projections): "
+             "B=32, h=8, n=128, d_k=d_v=64, key padding kv_len~U[64,128]; bytes counted with K/V "
+             "to kv_len"),
+    "base_cross_attn": dict(
+        kind="attn", B=32, h=8, n=128, n_k=160, d=64, causal=False, padding=True,
+        kv_range=(80, 160), seed=1012,
+        desc="Transformer-base decoder cross-attention alone (attn_forward): B=32, h=8, n_q=128, "
+             "n_k=160, d_k=d_v=64, source padding kv_len~U[80,160]; bytes counted with K/V to "
+             "kv_len"),
     "long": dict(kind="attn", B=4, h=16, n=4096, d=64, causal=False, seed=1004,
                  desc="long-context self-attention with Transformer-big heads: B=4, h=16, "
                       "n=4096, d_k=d_v=64, non-causal, Q/K/V~N(0,1) (the O(n^2 d) row of "
@@ -518,23 +530,33 @@ class AttnCall:
         import torch
         self.tsd, self.cfg = tsd, cfg
         c = cfg
-        mask = MASK_CAUSAL if c["causal"] else MASK_NONE
-        self.a = synthetic.attention_inputs(c["seed"] + seed_offset, c["B"], c["h"], c["n"], c["n"],
-                                            c["d"], c["d"], mask)
+        mask = (MASK_CAUSAL if c["causal"] else MASK_NONE) | \
+            (MASK_KEY_PADDING if c.get("padding") else MASK_NONE)
+        self.a = synthetic.attention_inputs(c["seed"] + seed_offset, c["B"], c["h"], c["n"],
+                                            c.get("n_k", c["n"]), c["d"], c["d"], mask,
+                                            c.get("kv_range"))
         a = self.a
         bf = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to("cuda").view(torch.bfloat16)
         self.sets = []
         for i in range(nsets):
             q, k, v = (bf(x) for x in (a.q, a.k, a.v))
-            self.sets.append(dict(q=q, k=k, v=v, out=torch.empty_like(q)))
+            lens = torch.from_numpy(a.kv_lens).to("cuda") if a.kv_lens is not None else None
+            self.sets.append(dict(q=q, k=k, v=v, lens=lens, out=torch.empty_like(q)))
         self.h_qkv = [torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory()
                       for x in (a.q, a.k, a.v)]
+        self.h_lens = torch.from_numpy(a.kv_lens).pin_memory() if a.kv_lens is not None else None
         self.h_out = torch.empty(a.q.shape, dtype=torch.bfloat16).pin_memory()
         self.window = cfg.get("window")
         self.h_ws = None
 
     def bytes_per_set(self):
-        return 4 * self.a.q.nbytes
+        return 2 * self.a.q.nbytes + self.a.k.nbytes + self.a.v.nbytes
+
+    def kv_effective(self):
+        a = self.a
+        if a.kv_lens is None:
+            return [a.n_k] * a.B
+        return [int(min(max(x, 0), a.n_k)) for x in a.kv_lens]
 
     def run(self, i, stream):
         a, s = self.a, self.sets[i % len(self.sets)]
@@ -544,7 +566,7 @@ class AttnCall:
                                          a.mask_kind, None, 0.0, stream)
             return
         self.tsd.attn_forward(s["q"], s["k"], s["v"], s["out"], a.B, a.h, a.n_q, a.n_k, a.d_k,
-                              a.d_v, a.mask_kind, None, 0.0, stream)
+                              a.d_v, a.mask_kind, s["lens"], 0.0, stream)
 
     def run_stage(self, k, i, stream):
         self.run(i, stream)
@@ -559,14 +581,19 @@ class AttnCall:
             f = 4.0 * a.B * a.h * a.d_k * window_pairs(a.n_q, *self.window, causal)
         else:
             f = attn_flops(a.B, a.h, a.n_q, a.n_k, a.d_k, causal)
-        b = 2.0 * a.B * a.h * (a.n_q * a.d_k + a.n_k * (a.d_k + a.d_v) + a.n_q * a.d_v)
+        # K/V bytes to each sequence's key length (key tiles past it are never loaded)
+        b = 2.0 * a.h * sum(a.n_q * a.d_k + kv * (a.d_k + a.d_v) + a.n_q * a.d_v
+                            for kv in self.kv_effective())
         return [(f, b)]
 
     def metric_flops(self):
         return self.stage_work()[0][0]
 
     def useful_flops(self):
-        return self.metric_flops()
+        a = self.a
+        if a.kv_lens is None:
+            return self.metric_flops()
+        return 4.0 * a.h * a.d_k * a.n_q * sum(self.kv_effective())
 
     def launches(self):
         return 1
@@ -587,13 +614,15 @@ class AttnCall:
                                               a.mask_kind, None, 0.0, ws, self.h_wsb, stream)
             return
         self.tsd.attn_forward_host(*self.h_qkv, self.h_out, a.B, a.h, a.n_q, a.n_k, a.d_k, a.d_v,
-                                   a.mask_kind, None, 0.0, ws, self.h_wsb, stream)
+                                   a.mask_kind, self.h_lens, 0.0, ws, self.h_wsb, stream)
 
     def e2e_finish(self, stream):
         pass  # results copied on `stream`
 
     def e2e_bytes(self):
-        return 3 * self.a.q.nbytes, self.a.q.nbytes
+        a = self.a
+        lens = 0 if a.kv_lens is None else a.kv_lens.nbytes
+        return a.q.nbytes + a.k.nbytes + a.v.nbytes + lens, a.q.nbytes
 
 
 class EncoderCall:
@@ -790,7 +819,7 @@ def make_calls(tsd, wl, args, seed_offset):
             cfg[k] = getattr(args, k)
     if args.causal is not None:
         cfg["causal"] = bool(args.causal)
-    per_set = 4 * cfg["B"] * cfg["h"] * cfg["n"] * cfg["d"] * 2
+    per_set = 2 * cfg["B"] * cfg["h"] * (2 * cfg["n"] + 2 * cfg.get("n_k", cfg["n"])) * cfg["d"]
     nsets = max(2, math.ceil(2.2 * L2_BYTES / per_set))
     return [AttnCall(tsd, cfg, nsets, seed_offset)], nsets, per_set
 
@@ -812,6 +841,10 @@ def workload_config(wl, calls, args, nsets, per_set):
     else:
         a = calls[0].a
         cfg.update(B=a.B, h=a.h, n=a.n_q, d=a.d_k, causal=bool(a.mask_kind & MASK_CAUSAL))
+        if a.n_k != a.n_q:
+            cfg["n_k"] = a.n_k
+        if a.kv_lens is not None:
+            cfg["key_padding"] = {"kv_range": list(WORKLOADS[wl]["kv_range"])}
         if calls[0].window is not None:
             cfg["window"] = {"left": calls[0].window[0], "right": calls[0].window[1]}
     cfg["l2"] = f"{nsets} rotating input sets of {per_set / 2**20:.1f} MiB (total > L2)"
@@ -1049,6 +1082,17 @@ def oracle_sample_runner(args):
     if args.causal is not None:
         cfg["causal"] = bool(args.causal)
     n, d, causal = cfg["n"], cfg["d"], cfg["causal"]
+    if cfg.get("padding"):  # short padded shapes: every head of the first sequences
+        nb = 4
+        a = synthetic.attention_inputs(cfg["seed"], nb, cfg["h"], n, cfg.get("n_k", n), d, d,
+                                       MASK_KEY_PADDING, cfg["kv_range"])
+        q, k, v = a.as_f64()
+        flops = attn_flops(nb, a.h, a.n_q, a.n_k, d, False)
+
+        def run(nthreads=0):
+            oracle.attention(q, k, v, MASK_KEY_PADDING, kv_lens=a.kv_lens, nthreads=nthreads)
+        return run, flops, (f"all {a.h} heads of {nb} sequences (n_q={a.n_q}, n_k={a.n_k}, kv_lens "
+                            f"{list(map(int, a.kv_lens))}) via oracle.attention")
     window = cfg.get("window")
     rng = np.random.default_rng(cfg["seed"])
     # one head of the workload, a seeded subset of its query rows

@@ -66,6 +66,11 @@ CASES = [
     (2, 2, 300, 300, 256, MASK_CAUSAL | MASK_KEY_PADDING, (50, 300)),
     (1, 1, 128, 700, 256, MASK_NONE, None),
     (3, 2, 77, 77, 256, MASK_KEY_PADDING, (0, 77)),
+    # 160 paired items over 152 SMs: the last partial round runs as single
+    # query tiles (16 of them), including ragged blocks past n_q
+    (5, 16, 500, 500, 64, MASK_NONE, None),
+    (5, 16, 500, 500, 64, MASK_KEY_PADDING, (1, 500)),
+    (5, 16, 300, 300, 128, MASK_NONE, None),
 ]
 
 
@@ -237,6 +242,9 @@ WINDOW_CASES = [
     (40, 8, 128, 64, MASK_KEY_PADDING, (1, 128), 16, 16),
     (1, 2, 600, 256, MASK_NONE, None, 100, 100),
     (2, 2, 500, 32, MASK_CAUSAL, None, 64, -1),
+    # 160 paired items: the last partial round as single query tiles
+    (5, 16, 500, 64, MASK_NONE, None, 100, 50),
+    (5, 16, 300, 128, MASK_KEY_PADDING, (1, 300), 60, 130),
 ]
 
 

@@ -126,6 +126,7 @@ struct AttnArgs {
   uint16_t* out;
   int64_t o_sb, o_sh, o_sr;
   int win_left, win_right;  // restricted window (WIN): keys [i - left, i + right]; < 0: no bound
+  int tail_start;  // items from here on are single query tiles, two per query block
 };
 
 constexpr unsigned long long kDrainLimitNs = 100ull * 1000ull * 1000ull;  // 0.1 s
@@ -137,6 +138,7 @@ struct Item {
   int lo0, lo1;  // 0 unless a restricted window cuts the keys before the query
   int lo_spec;   // first key tile through the rings (known before the key length)
   int min_load;  // 1 if the key set is not empty by its shape (n_k > 0)
+  bool single;   // one query tile of a block (tile 1 of the item is idle)
   __device__ int nt(int t) const { return t == 0 ? nt0 : nt1; }
   __device__ int lo(int t) const { return t == 0 ? lo0 : lo1; }
   __device__ int nt_all() const { return nt0 > nt1 ? nt0 : nt1; }
@@ -157,8 +159,9 @@ __device__ __forceinline__ int window_lo_tile(const AttnArgs& a, int row0) {
   return k0 > 0 ? k0 / kRows : 0;
 }
 
-// Batch, head and first query row of item w (no memory access).
-template <int NQT, bool WIN>
+// Batch, head and first query row of item w (no memory access). TS: the
+// instance splits the last partial round of paired items into single tiles.
+template <int NQT, bool WIN, bool TS>
 __device__ __forceinline__ Item item_coords(const AttnArgs& a, int w) {
   const bool causal = (a.mask_kind & kMaskCausal) != 0;
   const int bh_count = a.B * a.h;
@@ -167,13 +170,16 @@ __device__ __forceinline__ Item item_coords(const AttnArgs& a, int w) {
     qblk = a.n_qblocks - 1 - w / bh_count;
     bh = w % bh_count;
   } else {       // a head's query blocks together, so its K/V stays in L2
-    bh = w / a.n_qblocks;
-    qblk = w % a.n_qblocks;
+    // past tail_start a query block is two items of one tile each
+    const int bw = (!TS || w < a.tail_start) ? w : a.tail_start + ((w - a.tail_start) >> 1);
+    bh = bw / a.n_qblocks;
+    qblk = bw % a.n_qblocks;
   }
   Item it;
   it.b = bh / a.h;
   it.hh = bh % a.h;
-  it.q0 = qblk * NQT * kRows;
+  it.single = TS && !causal && w >= a.tail_start;
+  it.q0 = qblk * NQT * kRows + (it.single && ((w - a.tail_start) & 1) ? kRows : 0);
   it.kv_eff = 0;
   it.nt0 = it.nt1 = 0;
   it.lo_spec = window_lo_tile<WIN>(a, it.q0);
@@ -184,10 +190,10 @@ __device__ __forceinline__ Item item_coords(const AttnArgs& a, int w) {
 }
 
 // The key range of an item (reads the key length).
-template <int NQT, bool WIN>
+template <int NQT, bool WIN, bool TS>
 __device__ __forceinline__ Item item_at(const AttnArgs& a, int w) {
   const bool causal = (a.mask_kind & kMaskCausal) != 0;
-  Item it = item_coords<NQT, WIN>(a, w);
+  Item it = item_coords<NQT, WIN, TS>(a, w);
   int kv_eff = a.n_k;
   if (a.mask_kind & kMaskKeyPadding) {
     const int len = a.kv_lens[it.b];
@@ -204,11 +210,11 @@ __device__ __forceinline__ Item item_at(const AttnArgs& a, int w) {
     return n;
   };
   it.nt0 = tiles_for(0);
-  it.nt1 = NQT > 1 ? tiles_for(1) : 0;
+  it.nt1 = (NQT > 1 && !it.single) ? tiles_for(1) : 0;
   return it;
 }
 
-template <int D, int NQT, int NK, int NV, int QB, bool STO, int SL, bool MS, bool WIN>
+template <int D, int NQT, int NK, int NV, int QB, bool STO, int SL, bool MS, bool WIN, bool TS>
 __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -323,7 +329,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
         for (int i = 0, w = item_index(0); ok && w < args.num_items; w = item_index(++i)) {
           // Q and the first key tile do not depend on the key length: both
           // are on their way before it is read
-          const Item at = item_coords<NQT, WIN>(args, w);
+          const Item at = item_coords<NQT, WIN, TS>(args, w);
           const int qs = qn % QB;
           ok = mbar_wait(&sm.q_empty[qs], (static_cast<uint32_t>(qn / QB) & 1u) ^ 1u, abort_flag);
           if (!ok) break;
@@ -335,7 +341,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
                           at.q0 + t * kRows, at.hh, at.b);
           ++qn;
           if (at.min_load > 0) ok = load_k(at, at.lo_spec);
-          const int n_load = item_at<NQT, WIN>(args, w).n_load();
+          const int n_load = item_at<NQT, WIN, TS>(args, w).n_load();
           // keys run one tile ahead of values, the order the MMAs consume them
           for (int jj = 0; ok && jj < n_load; ++jj) {
             if (jj + 1 < n_load) ok = load_k(at, at.lo_spec + jj + 1);
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
         bool ok = true;
         griddep_wait();  // the key lengths may come from the previous kernel
         for (int i = 0, w = item_index(0); ok && w < args.num_items; w = item_index(++i)) {
-          const Item it = item_at<NQT, WIN>(args, w);
+          const Item it = item_at<NQT, WIN, TS>(args, w);
           const int n_load = it.n_load();
           const int qs = qc % QB;
           ok = mbar_wait(&sm.q_full[qs], static_cast<uint32_t>(qc / QB) & 1u, abort_flag);
@@ -436,7 +442,7 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
         bool ok = true;
         griddep_wait();
         for (int i = 0, w = item_index(0); ok && w < args.num_items; w = item_index(++i)) {
-          const Item it = item_at<NQT, WIN>(args, w);
+          const Item it = item_at<NQT, WIN, TS>(args, w);
           const int n_load = it.n_load();
           for (int jj = 0; ok && jj < n_load; ++jj) {
             const int j = it.lo_spec + jj;  // key tile
@@ -491,7 +497,8 @@ __global__ void __launch_bounds__(AttnShape<D, NQT, SL>::kThreads, 1)
     bool ok = true;
     griddep_wait();
     for (int i = 0, w = item_index(0); ok && w < args.num_items; w = item_index(++i)) {
-      const Item it = item_at<NQT, WIN>(args, w);
+      const Item it = item_at<NQT, WIN, TS>(args, w);
+      if (TS && t == 1 && it.single) continue;  // a single-tile item: no rows for tile 1
       const int ntt = it.nt(t);
       const int lot = it.lo(t);                // key tiles [lot, ntt) of this query tile
       const bool has_tiles = ntt > lot;
@@ -716,13 +723,13 @@ int num_sms() {
 }
 
 template <int D, int NQT, int NK, int NV, int QB, bool STO, int SL, bool MS = false,
-          bool WIN = false>
+          bool WIN = false, bool TS = false>
 cudaError_t launch_variant(const AttnProblem& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                            const CUtensorMap& tm_v, const CUtensorMap& tm_o, cudaStream_t stream) {
   using Smem = AttnSmem<D, NQT, NK, NV, QB, STO>;
   using Shape = AttnShape<D, NQT, SL>;
   const size_t smem_bytes = SL * sizeof(Smem) + 1024;  // + alignment slack
-  auto kernel = attn_fwd_bf16_kernel<D, NQT, NK, NV, QB, STO, SL, MS, WIN>;
+  auto kernel = attn_fwd_bf16_kernel<D, NQT, NK, NV, QB, STO, SL, MS, WIN, TS>;
   static unsigned long long configured = 0;
   cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured);
   if (e != cudaSuccess) return e;
@@ -736,6 +743,23 @@ cudaError_t launch_variant(const AttnProblem& p, const CUtensorMap& tm_q, const 
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffLL - (1LL << 20)) return cudaErrorInvalidValue;  // item indices fit int
   a.num_items = static_cast<int>(items);
+  // Quantisation tail: when the last round of paired items over the grid is
+  // partial and its blocks, split into single query tiles, still fit in one
+  // round, those blocks run as single tiles (about half an item's time each),
+  // so the last round ends sooner (measured: B=8 h=16 n=1024 d=64 823 -> 849
+  // TFLOP/s; d=128 B=2 n=4096 1100 -> 1142). Non-causal instances only:
+  // causal items are already taken longest first, and the causal instance
+  // measured slower with the split's code compiled in even when unused.
+  a.tail_start = 0x7fffffff;
+  if (TS && NQT == 2 && SL == 1 && !(p.mask_kind & kMaskCausal)) {
+    const long long G = items < num_sms() ? items : num_sms();
+    const long long full = items / G * G;
+    const long long tail = items - full;
+    if (full > 0 && tail > 0 && 2 * tail <= G) {
+      a.tail_start = static_cast<int>(full);
+      a.num_items = static_cast<int>(full + 2 * tail);
+    }
+  }
   a.mask_kind = p.mask_kind;
   a.kv_lens = p.kv_lens;
   a.scale_log2 = p.scale * 1.4426950408889634f;
@@ -773,12 +797,12 @@ cudaError_t launch_attn_bf16(const AttnProblem& p, const CUtensorMap& tm_q,
       // one copy of the score load (no unmasked twin): the two window edges
       // put masking in most of a short item's tiles, and the smaller loop
       // measured faster (n = 16384, keys within +-256: 534 -> 588 TFLOP/s)
-      return launch_variant<64, 2, 4, 4, 2, true, 1, false, true>(p, tm_q, tm_k, tm_v, tm_o,
-                                                                  stream);
+      return launch_variant<64, 2, 4, 4, 2, true, 1, false, true, true>(p, tm_q, tm_k, tm_v, tm_o,
+                                                                        stream);
     }
     if (p.d == 128) {
-      return pair ? launch_variant<128, 2, 2, 2, 1, false, 1, false, true>(p, tm_q, tm_k, tm_v,
-                                                                          tm_o, stream)
+      return pair ? launch_variant<128, 2, 2, 2, 1, false, 1, false, true, true>(p, tm_q, tm_k,
+                                                                                tm_v, tm_o, stream)
                   : launch_variant<128, 1, 2, 2, 2, true, 1, false, true>(p, tm_q, tm_k, tm_v,
                                                                          tm_o, stream);
     }
@@ -796,9 +820,13 @@ cudaError_t launch_attn_bf16(const AttnProblem& p, const CUtensorMap& tm_q,
     if (!pair) return launch_variant<64, 1, 2, 2, 1, true, 2>(p, tm_q, tm_k, tm_v, tm_o, stream);
     return causal
                ? launch_variant<64, 2, 4, 4, 2, true, 1, false>(p, tm_q, tm_k, tm_v, tm_o, stream)
-               : launch_variant<64, 2, 4, 4, 2, true, 1, true>(p, tm_q, tm_k, tm_v, tm_o, stream);
+               : launch_variant<64, 2, 4, 4, 2, true, 1, true, false, true>(p, tm_q, tm_k, tm_v, tm_o,
+                                                                         stream);
   }
   if (p.d == 128) {
+    if (pair && !causal)
+      return launch_variant<128, 2, 2, 2, 1, false, 1, false, false, true>(p, tm_q, tm_k, tm_v,
+                                                                          tm_o, stream);
     return pair ? launch_variant<128, 2, 2, 2, 1, false, 1>(p, tm_q, tm_k, tm_v, tm_o, stream)
                 : launch_variant<128, 1, 2, 2, 2, true, 1>(p, tm_q, tm_k, tm_v, tm_o, stream);
   }

@@ -155,6 +155,7 @@ KERNEL_SOURCES = {
     "attn_fwd_bf16": _CSRC + "attn_bf16.cu",
     "gemm_bf16": _CSRC + "gemm_bf16.cu",
     "mha_fused": _CSRC + "mha_fused.cu",
+    "mha_cross": _CSRC + "mha_cross.cu",
     "attn_decode": _CSRC + "attn_decode.cu",
     # the encoder layer's five launches: fused MHA, two LayerNorms, two GEMMs
     "encoder_layer": (_CSRC + "mha_fused.cu", _CSRC + "layernorm.cu", _CSRC + "gemm_bf16.cu"),
@@ -445,10 +446,13 @@ class MhaCall:
                                      stream)
 
     def stage_names(self):
+        m = self.m
+        # cross-attention over one or two source key tiles has its own kernel
+        fused = "mha_cross" if (not m.self_attention and m.n_k > 128) else "mha_fused"
         if self.n_launches() == 1:
-            return ["mha_fused"]
+            return [fused]
         if self.fused():
-            return ["mha_fused", "gemm_bf16"]
+            return [fused, "gemm_bf16"]
         return ["gemm_bf16", "attn_fwd_bf16", "gemm_bf16"]
 
     def stage_work(self):

@@ -142,7 +142,9 @@ def test_mha_forward_launch_plan(tsd):
     """The launch counts mha_forward reports for the workload shapes."""
     plan = tsd.mha_forward_launches
     assert plan(32, 128, 128, 512, 8, 64, 64, True) == 1     # Transformer-base self-attention
-    assert plan(32, 128, 160, 512, 8, 64, 64, False) == 3    # decoder cross-attention, n_k > 128
+    assert plan(32, 128, 160, 512, 8, 64, 64, False) == 1    # decoder cross-attention, n_k = 160
+    assert plan(32, 128, 257, 512, 8, 64, 64, False) == 3    # source past two key tiles
+    assert plan(2, 50, 150, 512, 32, 64, 64, False) == 2     # 16 output columns per CTA: no W_O
     assert plan(40, 64, 64, 128, 16, 64, 64, True) == 2      # 16 output columns per CTA: no
     assert plan(8, 1024, 1024, 1024, 16, 64, 64, True) == 3  # Transformer-big, n = 1024
     assert plan(0, 128, 128, 512, 8, 64, 64, True) == 0
@@ -258,3 +260,49 @@ def test_projection_gemm_tile_widths(tsd, B, n_q, n_k, dm, h):
         got = to_host_f64(out.reshape(B * n, h * 64)[torch.from_numpy(rows).cuda()])
         ref = x.reshape(B * n, dm)[rows] @ w
         assert_bf16_close(got, ref, f"{name} B={B} n={n} d_model={dm}")
+
+
+@pytest.mark.parametrize("shape", [
+    # B, n_q, n_k, d_model, h, mask, kv_len_range
+    (3, 100, 200, 256, 4, MASK_KEY_PADDING, (0, 200)),    # lengths on both sides of 128, and 0
+    (2, 128, 256, 512, 8, MASK_NONE, None),              # both key tiles full
+    (4, 17, 129, 128, 2, MASK_KEY_PADDING, (100, 129)),  # one head pair: no peers
+    (2, 64, 180, 1024, 16, MASK_KEY_PADDING, (1, 180)),  # clusters of 8, 128 columns each
+    (48, 128, 160, 512, 8, MASK_KEY_PADDING, (80, 160)), # more batch entries than clusters fit
+])
+def test_mha_cross_attention_two_key_tiles_one_launch(tsd, shape):
+    """Cross-attention with 128 < n_k <= 256 source rows: projections, the
+    online softmax over both key tiles and W_O in one launch."""
+    B, n_q, n_k, dm, h, mask, rng = shape
+    assert tsd.mha_forward_launches(B, n_q, n_k, dm, h, 64, 64, False) == 1
+    m = synthetic.mha_inputs(3400 + B + n_q + n_k + dm, B, n_q, n_k, dm, h, 64, 64, mask, rng,
+                             self_attention=False)
+    check(tsd, m, str(shape))
+
+
+def test_mha_cross_attention_two_key_tiles_without_output_projection(tsd):
+    """32 heads (16 head pairs: no cluster of that size) take the same kernel
+    up to the merged heads, then the W_O GEMM; mha_concat_heads on the same
+    sizes gives the merged heads the oracle's per-head attention gives."""
+    import torch
+    B, n_q, n_k, dm, h = 2, 50, 150, 512, 32
+    assert tsd.mha_forward_launches(B, n_q, n_k, dm, h, 64, 64, False) == 2
+    m = synthetic.mha_inputs(3500, B, n_q, n_k, dm, h, 64, 64, MASK_KEY_PADDING, (1, n_k),
+                             self_attention=False)
+    check(tsd, m, "cross, 32 heads")
+    x_q, x_kv = to_dev_bf16(m.x_q), to_dev_bf16(m.x_kv)
+    w = [to_dev_bf16(t) for t in (m.w_q, m.w_k, m.w_v)]
+    concat = torch.full((B, n_q, h * 64), float("nan"), dtype=torch.bfloat16, device="cuda")
+    wsb = tsd.mha_workspace_bytes(B, n_q, n_k, h, 64, 64)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    tsd.mha_concat_heads(x_q, x_kv, *w, concat, B, n_q, n_k, dm, h, 64, 64, m.mask_kind,
+                         to_dev_i32(m.kv_lens), 0.0, ws, wsb)
+    torch.cuda.synchronize()
+    assert tsd.attn_get_device_status() == tsd.ATTN_OK
+    xq, xkv, wq, wk, wv, _ = m.as_f64()
+    q = (xq @ wq).reshape(B, n_q, h, 64).transpose(0, 2, 1, 3)
+    k = (xkv @ wk).reshape(B, n_k, h, 64).transpose(0, 2, 1, 3)
+    v = (xkv @ wv).reshape(B, n_k, h, 64).transpose(0, 2, 1, 3)
+    heads = oracle.attention(q, k, v, MASK_KEY_PADDING, kv_lens=m.kv_lens)
+    ref = heads.transpose(0, 2, 1, 3).reshape(B, n_q, h * 64)
+    assert_bf16_close(to_host_f64(concat), ref, "cross concat heads")

@@ -18,8 +18,8 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libtsd_attention.so")
 
-SOURCES = ["attn_bf16.cu", "gemm_bf16.cu", "mha_fused.cu", "attn_decode.cu", "layernorm.cu",
-           "attn_f32.cu", "api.cu", "mha_noalloc.cu", "host_stage.cu"]
+SOURCES = ["attn_bf16.cu", "gemm_bf16.cu", "mha_fused.cu", "mha_cross.cu", "attn_decode.cu",
+           "layernorm.cu", "attn_f32.cu", "api.cu", "mha_noalloc.cu", "host_stage.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I", INCLUDE, "-I", CSRC]

@@ -319,6 +319,21 @@ bool fused_out_eligible(bool self, int d_model, int h) {
   return tsd::mha_fused_out_clusters(h, self) > 0;
 }
 
+// Cross-attention (x_kv is not x_q) whose source is one to two key tiles
+// long: projections and attention in one launch (mha_cross.cu).
+bool cross_eligible(bool self, int n_q, int n_k, int d_model, int h, int d_k, int d_v) {
+  return !self && d_k == 64 && d_v == 64 && n_q >= 1 && n_q <= 128 && n_k > 128 &&
+         n_k <= 256 && h % 2 == 0 && d_model >= 64 && d_model % 64 == 0;
+}
+// ... and W_O in the same launch (the clusters of the fused kernel's OUT rule).
+bool cross_out_eligible(int d_model, int h) {
+  const int C = h / 2;
+  if (C < 1 || C > 8 || d_model % C != 0) return false;
+  const int n_slice = d_model / C;
+  if (n_slice != 64 && n_slice != 128) return false;
+  return tsd::mha_cross_out_clusters(h) > 0;
+}
+
 // Q/K/V projections + attention of every (batch, head pair) -> the merged
 // heads, [B, n_q, h*64], in `concat`; with `w_o` also out = concat W_O in
 // the same launch (`concat` is then scratch).
@@ -369,7 +384,7 @@ attn_status launch_fused_core(const void* x_q, const void* x_kv, const void* w_q
   p.mask_kind = mask_kind;
   p.kv_lens = kv_lens;
   p.scale = resolve_scale(scale, 64);
-  e = tsd::launch_mha_fused(p, stream);
+  e = (!p.self && n_k > 128) ? tsd::launch_mha_cross(p, stream) : tsd::launch_mha_fused(p, stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
@@ -381,7 +396,8 @@ attn_status concat_heads(const void* x_q, const void* x_kv, const void* w_q, con
                          const void* w_v, void* concat, void* Q, void* K, void* V, int B, int n_q,
                          int n_k, int d_model, int h, int d_k, int d_v, int mask_kind,
                          const int32_t* kv_lens, float scale, cudaStream_t stream) {
-  if (fused_eligible(n_q, n_k, d_model, h, d_k, d_v))
+  if (fused_eligible(n_q, n_k, d_model, h, d_k, d_v) ||
+      cross_eligible(x_q == x_kv && n_q == n_k, n_q, n_k, d_model, h, d_k, d_v))
     return launch_fused_core(x_q, x_kv, w_q, w_k, w_v, concat, B, n_q, n_k, d_model, h,
                              mask_kind, kv_lens, scale, stream);
   const int hdk = h * d_k, hdv = h * d_v;
@@ -754,6 +770,11 @@ attn_status mha_forward(const void* x_q, const void* x_kv, const void* w_q, cons
       fused_out_eligible(x_q == x_kv && n_q == n_k, d_model, h))
     return launch_fused_core(x_q, x_kv, w_q, w_k, w_v, O, B, n_q, n_k, d_model, h, mask_kind,
                              kv_lens, scale, stream, w_o, out);
+  // Cross-attention over one or two source key tiles: the same, in mha_cross.cu
+  if (cross_eligible(x_q == x_kv && n_q == n_k, n_q, n_k, d_model, h, d_k, d_v) &&
+      cross_out_eligible(d_model, h))
+    return launch_fused_core(x_q, x_kv, w_q, w_k, w_v, O, B, n_q, n_k, d_model, h, mask_kind,
+                             kv_lens, scale, stream, w_o, out);
   // 1-2. Concat(head_1..head_h) into the workspace's last region
   s = concat_heads(x_q, x_kv, w_q, w_k, w_v, O, Q, K, V, B, n_q, n_k, d_model, h, d_k, d_v,
                    mask_kind, kv_lens, scale, stream);
@@ -866,8 +887,11 @@ int mha_forward_launches(int B, int n_q, int n_k, int d_model, int h, int d_k, i
       check_bf16_head_dims(d_k, d_v) != ATTN_OK)
     return -1;
   if (int64_t(B) * n_q == 0) return 0;
+  const bool self = self_attention != 0 && n_q == n_k;
+  if (cross_eligible(self, n_q, n_k, d_model, h, d_k, d_v))
+    return cross_out_eligible(d_model, h) ? 1 : 2;
   if (!fused_eligible(n_q, n_k, d_model, h, d_k, d_v)) return 3;
-  return fused_out_eligible(self_attention != 0 && n_q == n_k, d_model, h) ? 1 : 2;
+  return fused_out_eligible(self, d_model, h) ? 1 : 2;
 }
 
 attn_status mha_concat_heads(const void* x_q, const void* x_kv, const void* w_q, const void* w_k,
@@ -927,6 +951,9 @@ attn_status attn_get_device_status(tsd_stream_t stream) {
   if (e == cudaSuccess) e = tsd::take_device_error_gemm(&g);
   if (e == cudaSuccess) e = tsd::take_device_error_f32(&f);
   if (e == cudaSuccess) e = tsd::take_device_error_fused(&m);
+  unsigned int cr = 0;
+  if (e == cudaSuccess) e = tsd::take_device_error_cross(&cr);
+  m |= cr;
   unsigned int dec = 0;
   if (e == cudaSuccess) e = tsd::take_device_error_decode(&dec);
   m |= dec;

@@ -148,6 +148,13 @@ cudaError_t launch_mha_fused(const MhaFusedProblem& p, cudaStream_t stream);
 // Clusters of h/2 output-projecting CTAs that fit on the device at once (0:
 // the output projection cannot be fused).
 int mha_fused_out_clusters(int h, bool self);
+// Cross-attention (x_kv is not x_q) with 128 < n_k <= 256 source rows, n_q <=
+// 128, d_k = d_v = 64, h even, d_model a multiple of 64: the same problem
+// description and outputs as launch_mha_fused, in one launch (the K|V
+// projection of both key tiles first, then Q, then the online softmax over
+// the key tiles).
+cudaError_t launch_mha_cross(const MhaFusedProblem& p, cudaStream_t stream);
+int mha_cross_out_clusters(int h);
 
 // Per-file device error words (read and cleared; see sm103.cuh).
 // One decoding step against a key/value cache: the n_q (<= 8) newest tokens'
@@ -182,6 +189,7 @@ cudaError_t take_device_error_decode(unsigned int* value);
 cudaError_t take_device_error_gemm(unsigned int* value);
 cudaError_t take_device_error_f32(unsigned int* value);
 cudaError_t take_device_error_fused(unsigned int* value);
+cudaError_t take_device_error_cross(unsigned int* value);
 
 // Failure-detection self test: a bounded wait on a barrier nobody arrives on.
 cudaError_t launch_wait_timeout_selftest(unsigned long long limit_ns, cudaStream_t stream);

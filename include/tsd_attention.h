@@ -225,7 +225,7 @@ size_t mha_workspace_bytes(int B, int n_q, int n_k, int h, int d_k, int d_v);
  *   are scratch (short sequences -- n_q, n_k <= 128, d_k = d_v = 64, h even,
  *   d_model a multiple of 64 -- are projected and attended in one kernel
  *   and never write them; so is cross-attention, x_kv != x_q, with
- *   n_q <= 128 and 128 < n_k <= 256 source rows, the encoder-decoder
+ *   n_q <= 128 and 128 < n_k <= 192 source rows, the encoder-decoder
  *   attention of section 3.2.3 at the Transformer-base lengths). With
  *   thread-block clusters in flight, the
  *   merged-heads region is how the CTAs of one batch entry share their
@@ -245,7 +245,7 @@ attn_status mha_forward(const void *x_q, const void *x_kv,
  * sizes on the current device (a planning query: no launch, no allocation;
  * it may ask the runtime how many thread-block clusters fit):
  *   1  short sequences, W_O applied in the same kernel (n_q, n_k <= 128, or
- *      cross-attention with n_q <= 128 and n_k <= 256; d_k = d_v = 64, h even,
+ *      cross-attention with n_q <= 128 and n_k <= 192; d_k = d_v = 64, h even,
  *      h/2 <= 8, d_model / (h/2) = 64 or 128, and a cluster of h/2 CTAs fits
  *      on the device);
  *   2  short sequences, then the W_O GEMM;

@@ -143,7 +143,7 @@ def test_mha_forward_launch_plan(tsd):
     plan = tsd.mha_forward_launches
     assert plan(32, 128, 128, 512, 8, 64, 64, True) == 1     # Transformer-base self-attention
     assert plan(32, 128, 160, 512, 8, 64, 64, False) == 1    # decoder cross-attention, n_k = 160
-    assert plan(32, 128, 257, 512, 8, 64, 64, False) == 3    # source past two key tiles
+    assert plan(32, 128, 193, 512, 8, 64, 64, False) == 3    # source past a tile and a 64-row tail
     assert plan(2, 50, 150, 512, 32, 64, 64, False) == 2     # 16 output columns per CTA: no W_O
     assert plan(40, 64, 64, 128, 16, 64, 64, True) == 2      # 16 output columns per CTA: no
     assert plan(8, 1024, 1024, 1024, 16, 64, 64, True) == 3  # Transformer-big, n = 1024
@@ -264,15 +264,17 @@ def test_projection_gemm_tile_widths(tsd, B, n_q, n_k, dm, h):
 
 @pytest.mark.parametrize("shape", [
     # B, n_q, n_k, d_model, h, mask, kv_len_range
-    (3, 100, 200, 256, 4, MASK_KEY_PADDING, (0, 200)),    # lengths on both sides of 128, and 0
-    (2, 128, 256, 512, 8, MASK_NONE, None),              # both key tiles full
+    (3, 100, 190, 256, 4, MASK_KEY_PADDING, (0, 190)),    # lengths on both sides of 128, and 0
+    (2, 128, 192, 512, 8, MASK_NONE, None),              # the whole tail
     (4, 17, 129, 128, 2, MASK_KEY_PADDING, (100, 129)),  # one head pair: no peers
     (2, 64, 180, 1024, 16, MASK_KEY_PADDING, (1, 180)),  # clusters of 8, 128 columns each
     (48, 128, 160, 512, 8, MASK_KEY_PADDING, (80, 160)), # more batch entries than clusters fit
+    (3, 128, 160, 512, 8, MASK_NONE, None),
 ])
 def test_mha_cross_attention_two_key_tiles_one_launch(tsd, shape):
-    """Cross-attention with 128 < n_k <= 256 source rows: projections, the
-    online softmax over both key tiles and W_O in one launch."""
+    """Cross-attention with 128 < n_k <= 192 source rows: the projections
+    (the rows past 128 transposed), the online softmax over the first key
+    tile and the tail, and W_O in one launch."""
     B, n_q, n_k, dm, h, mask, rng = shape
     assert tsd.mha_forward_launches(B, n_q, n_k, dm, h, 64, 64, False) == 1
     m = synthetic.mha_inputs(3400 + B + n_q + n_k + dm, B, n_q, n_k, dm, h, 64, 64, mask, rng,

@@ -319,11 +319,11 @@ bool fused_out_eligible(bool self, int d_model, int h) {
   return tsd::mha_fused_out_clusters(h, self) > 0;
 }
 
-// Cross-attention (x_kv is not x_q) whose source is one to two key tiles
-// long: projections and attention in one launch (mha_cross.cu).
+// Cross-attention (x_kv is not x_q) whose source is one key tile and a tail
+// of up to 64 rows: projections and attention in one launch (mha_cross.cu).
 bool cross_eligible(bool self, int n_q, int n_k, int d_model, int h, int d_k, int d_v) {
   return !self && d_k == 64 && d_v == 64 && n_q >= 1 && n_q <= 128 && n_k > 128 &&
-         n_k <= 256 && h % 2 == 0 && d_model >= 64 && d_model % 64 == 0;
+         n_k <= 192 && h % 2 == 0 && d_model >= 64 && d_model % 64 == 0;
 }
 // ... and W_O in the same launch (the clusters of the fused kernel's OUT rule).
 bool cross_out_eligible(int d_model, int h) {
@@ -356,6 +356,9 @@ attn_status launch_fused_core(const void* x_q, const void* x_kv, const void* w_q
                                   static_cast<uint64_t>(B)};
     const int64_t xkv_str[2] = {d_model, int64_t(n_k) * d_model};
     e = encode_bf16_map(&p.tm_xkv, x_kv, 3, xkv_dims, xkv_str, xbox);
+    const uint32_t tbox[3] = {64, 64, 1};  // the source's rows past 128, 64 at a time
+    if (e == cudaSuccess && n_k > 128)
+      e = encode_bf16_map(&p.tm_xkv_tail, x_kv, 3, xkv_dims, xkv_str, tbox);
   } else {
     p.tm_xkv = p.tm_xq;
   }

@@ -133,6 +133,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 struct MhaFusedProblem {
   CUtensorMap tm_xq;   // 3-D (d_model, n_q, B), box 64 x 128 x 1
   CUtensorMap tm_xkv;  // 3-D (d_model, n_k, B) (unused when self)
+  CUtensorMap tm_xkv_tail;  // the same tensor, box 64 x 64 x 1 (cross-attention past 128 keys)
   CUtensorMap tm_wq, tm_wk, tm_wv;  // 2-D (h*64, d_model), box 64 x 64
   CUtensorMap tm_o;    // 3-D (h*64, n_q, B), box 64 x 128 x 1 (TMA store, and load with out)
   CUtensorMap tm_wo;   // 2-D (d_model, h*64), box 64 x 64 (out only)
@@ -148,11 +149,11 @@ cudaError_t launch_mha_fused(const MhaFusedProblem& p, cudaStream_t stream);
 // Clusters of h/2 output-projecting CTAs that fit on the device at once (0:
 // the output projection cannot be fused).
 int mha_fused_out_clusters(int h, bool self);
-// Cross-attention (x_kv is not x_q) with 128 < n_k <= 256 source rows, n_q <=
+// Cross-attention (x_kv is not x_q) with 128 < n_k <= 192 source rows, n_q <=
 // 128, d_k = d_v = 64, h even, d_model a multiple of 64: the same problem
-// description and outputs as launch_mha_fused, in one launch (the K|V
-// projection of both key tiles first, then Q, then the online softmax over
-// the key tiles).
+// description and outputs as launch_mha_fused, in one launch (the source's
+// rows past 128 projected transposed, then the online softmax over the first
+// key tile and that tail).
 cudaError_t launch_mha_cross(const MhaFusedProblem& p, cudaStream_t stream);
 int mha_cross_out_clusters(int h);
 

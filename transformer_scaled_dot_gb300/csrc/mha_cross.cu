@@ -1,7 +1,7 @@
 // mha_cross.cu -- encoder-decoder (cross) multi-head attention in one kernel
-// when the source is longer than one key tile: n_q <= 128 target rows,
-// 128 < n_k <= 256 source rows, d_k = d_v = 64. The queries come from the
-// decoder's rows, the keys and values from the encoder output
+// when the source is a little longer than one key tile: n_q <= 128 target
+// rows, 128 < n_k <= 192 source rows, d_k = d_v = 64. The queries come from
+// the decoder's rows, the keys and values from the encoder output
 // ("[논문 리뷰]Attention Is All You Need" (kimjiil.github.io), section 3.2.3,
 // the encoder-decoder attention row; heads per sections 3.2.1-3.2.2,
 // head_i = Attention(X_q W_i^Q, X_kv W_i^K, X_kv W_i^V), weights in the x.W
@@ -11,45 +11,38 @@
 // A CTA owns one work item, (batch b, heads 2p and 2p+1), as the fused
 // short-sequence kernel does; with the output projection the h/2 CTAs of a
 // batch entry form a cluster and exchange their merged heads through L2 (the
-// same protocol as in mha_fused.cu). What differs is the order of the
-// projections. Q of both heads (2 x 64 fp32 columns) and K|V of both heads
-// for two 128-row key tiles (4 x 128 columns) would need 640 of the 512
-// tensor-memory columns, so:
-//   Q pass   Q of both heads into columns [0, 128), its operands streamed
-//            through the whole ring (six 32 KB stages); the head warpgroups
-//            turn the rows into bf16 Q tiles in the epilogue's staging
-//            buffers, which are idle until the epilogue
-//   KV pass  K|V of both heads for key rows [0, 128) and [128, 256) (rows past
-//            n_k are zero: the tensor map clips them) into all 512 columns,
-//            through three 64 KB stages, each loaded as soon as the two Q
-//            stages under it have been consumed; the head warpgroups turn
-//            them into bf16 K and V tiles in the first 128 KB of the ring
-// Each operand crosses from L2 once, with the ring's 192 KB in flight (the
-// L2 -> SM rate grows with the bytes in flight: with two 64 KB stages for K|V
-// and two 32 KB ones for Q the two passes took 9.6 us, one after the other).
-// The attention then takes each head over its one or two key tiles with the
-// online softmax (running max and sum in fp32).
+// same protocol as in mha_fused.cu). What is new is the source's tail, key
+// rows [128, n_k): its K|V projection is taken transposed,
+//   T_e = [W_K | W_V]_e^T X_kv[128 : 192]^T    (128 features x 64 keys),
+// the weight slice as an MN-major A operand and the 64 tail rows of X_kv as
+// the B operand. A 128-row key tile would need 128 more accumulator columns
+// per head than the 64 this takes (Q, K|V of the first key tile and the tail
+// of both heads fill exactly the 512 tensor-memory columns), and would
+// multiply mostly zero rows: at n_k = 160 the tail holds 32 keys. Everything
+// is projected in one pass over d_model. A tail accumulator row is one
+// feature over the 64 tail keys; written out as rows of 64 keys it is at once
+// the MN-major B operand of S = Q K_T^T (N = keys) and the K-major B operand
+// of O += P_T V_T (K = keys).
 //
 //   warp 0      TMA producer
-//   warp 1      MMA issuer (one thread): the Q pass, the KV pass, S = Q K^T
-//               and O += P V per key tile, and (OUT) the output projection
+//   warp 1      MMA issuer (one thread): the projections, S and O += P V for
+//               the first key tile and the tail, and (OUT) the output
+//               projection
 //   warps 4..7  head 2p, warps 8..11 head 2p+1, one thread per row (= TMEM
-//               lane): the Q row, then its K/V rows, to bf16 tiles; the
-//               softmax of its query row; O / l -> bf16 -> staging -> TMA store
+//               lane): the Q, K and V rows and one tail feature row to bf16
+//               tiles; the online softmax of its query row over the two key
+//               tiles; O / l -> bf16 -> staging -> TMA store
 //
-// Shared memory (ring, 192 KB):
-//   Q pass stage s (32 KB: X_q slice, W_Q slices of both heads) at 32 s KB;
-//   KV pass stage p (64 KB: X_kv rows [0,128) and [128,256) of one 64-wide
-//   slice of d_model, the W_K, W_V slices of both heads) at 64 p KB, over Q
-//   stages 2p and 2p+1; then the K/V tiles, tile (e, m, kv) at
-//   16 KB x (4e + 2m + kv), in [0, 128) KB; the Q tiles in o[e]
-//   OUT: the peers' merged tiles in [0, 96) KB and W_O chunks in a late ring
-//   [96, 160) KB (free once the attention MMAs are done) and an early ring
-//   [160, 192) KB for the CTA's own two heads' chunks (free once the KV pass
-//   is done)
-// Tensor memory (512 columns): Q_e at 64e; then K|V of (head e, key tile m)
-// at 128 (2e + m); then S_e at 128e, P_e (bf16) at 256 + 64e, O_e at
-// 384 + 64e; (OUT) the output columns at [0, n_slice).
+// Shared memory: a ring of two 88 KB stages (X_q, X_kv rows [0, 128) and
+// [128, 192) of one 64-wide slice of d_model, and the W_Q, W_K, W_V slices
+// of both heads); then the K/V tiles in [0, 96) KB (K_e and V_e of the first
+// key tile, 16 KB each, and the tail tiles K_T,e and V_T,e, 64 rows x 64 keys,
+// 8 KB each), the Q tiles in the epilogue's staging buffers. OUT: the peers'
+// merged tiles in [0, 96) KB once the attention MMAs are done; W_O chunks in
+// [96, 176) KB, free as soon as the projections are done.
+// Tensor memory (512 columns): Q_e at 64e, K|V_e at 128 + 128e, T_e at
+// 384 + 64e; then S_e at 128e, P_e (bf16) at 256 + 64e, O_e at 384 + 64e;
+// (OUT) the output columns at [0, n_slice).
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -59,7 +52,9 @@ namespace {
 
 constexpr int kRows = 128;              // query rows and key rows per tile
 constexpr int kD = 64;                  // d_k = d_v
+constexpr int kTail = 64;               // tail keys: n_k <= kRows + kTail
 constexpr int kTile = kRows * kD * 2;   // 16 KB: a 128 x 64 bf16 tile
+constexpr int kTailTile = kTail * kD * 2;  // 8 KB: a 64 x 64 bf16 tile
 constexpr int kWChunk = 64 * kD * 2;    // 8 KB: 64 rows of d_model x 64 columns of one weight
 constexpr int kThreads = 384;           // 4 control warps + 2 head warpgroups
 constexpr uint32_t kLaunchRegs = 65536 / kThreads / 8 * 8;  // 168
@@ -69,44 +64,50 @@ static_assert(kCtrlRegs * 128 + kHeadRegs * 256 <= kLaunchRegs * kThreads, "regi
 constexpr unsigned long long kDrainLimitNs = 100ull * 1000ull * 1000ull;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-constexpr int kKvStage = 2 * kTile + 4 * kWChunk;  // 64 KB
-constexpr int kKvStages = 3;
-constexpr int kQStage = kTile + 2 * kWChunk;       // 32 KB
-constexpr int kQStages = 6;
-constexpr int kRingBytes = kKvStages * kKvStage;   // 192 KB
-static_assert(kQStages * kQStage == kRingBytes && 2 * kQStage == kKvStage, "KV stage p over Q stages 2p, 2p+1");
-constexpr int kSlot = 16384;     // a merged-heads tile, or 64 rows of W_O x <= 128 columns
-constexpr int kOSlots = 6;       // peers' merged tiles, [0, 96) KB
-constexpr int kWoLate = 4;       // [96, 160) KB
-constexpr int kWoEarly = 2;      // [160, 192) KB
-constexpr int kWoLateBase = kOSlots * kSlot;
-constexpr int kWoEarlyBase = kWoLateBase + kWoLate * kSlot;
+// one stage: X_q | X_kv rows [0,128) | X_kv rows [128,192) | W_Q0 W_Q1 | W_K0 W_V0 | W_K1 W_V1
+constexpr int kXkvOff = kTile;
+constexpr int kXtOff = 2 * kTile;
+constexpr int kWOff = 2 * kTile + kTailTile;
+constexpr int kStage = kWOff + 6 * kWChunk;  // 88 KB
+constexpr int kStages = 2;
+constexpr int kRingBytes = kStages * kStage;  // 176 KB
+__host__ __device__ constexpr int wq_chunk(int e) { return e; }
+__host__ __device__ constexpr int wk_chunk(int e) { return 2 + 2 * e; }  // W_V_e follows
+// K/V tiles after the projections
+__host__ __device__ constexpr int k0_off(int e) { return 2 * e * kTile; }
+__host__ __device__ constexpr int v0_off(int e) { return (2 * e + 1) * kTile; }
+__host__ __device__ constexpr int kt_off(int e) { return 4 * kTile + 2 * e * kTailTile; }
+__host__ __device__ constexpr int vt_off(int e) { return 4 * kTile + (2 * e + 1) * kTailTile; }
+constexpr int kTilesEnd = 4 * kTile + 4 * kTailTile;  // 96 KB
+// output projection (OUT)
+constexpr int kSlot = 16384;  // a merged-heads tile, or 64 rows of W_O x <= 128 columns
+constexpr int kOSlots = 6;    // peers' merged tiles, [0, 96) KB
+constexpr int kWoSlots = 5;   // W_O chunks, [96, 176) KB
+constexpr int kWoBase = kOSlots * kSlot;
 constexpr int kMaxCluster = 8;
-static_assert(kWoEarlyBase + kWoEarly * kSlot == kRingBytes, "OUT layout fills the ring");
-static_assert(kWoEarlyBase >= 8 * kTile, "early W_O slots clear of the K/V tiles");
+static_assert(kTilesEnd == kWoBase, "K/V tiles end where the W_O ring starts");
+static_assert(kWoBase + kWoSlots * kSlot <= kRingBytes, "W_O ring inside the stages");
 
-__host__ __device__ constexpr uint32_t kv_col(int e, int m) { return static_cast<uint32_t>((2 * e + m) * 128); }
 __host__ __device__ constexpr uint32_t q_col(int e) { return static_cast<uint32_t>(64 * e); }
+__host__ __device__ constexpr uint32_t kv_col(int e) { return static_cast<uint32_t>(128 + 128 * e); }
+__host__ __device__ constexpr uint32_t t_col(int e) { return static_cast<uint32_t>(384 + 64 * e); }
 __host__ __device__ constexpr uint32_t s_col(int e) { return static_cast<uint32_t>(128 * e); }
 __host__ __device__ constexpr uint32_t p_col(int e) { return static_cast<uint32_t>(256 + 64 * e); }
 __host__ __device__ constexpr uint32_t o_col(int e) { return static_cast<uint32_t>(384 + 64 * e); }
-__host__ __device__ constexpr int kv_tile(int e, int m, int kv) { return 4 * e + 2 * m + kv; }
 
 struct CrossSmem {
   alignas(1024) uint8_t ring[kRingBytes];
-  alignas(1024) uint8_t o[2][kTile];  // epilogue staging, one per head
-  uint64_t kv_full[kKvStages], kv_empty[kKvStages];
-  uint64_t q_full[kQStages], q_empty[kQStages];
-  uint64_t kv_done, q_done;        // KV pass / Q pass MMAs complete
-  uint64_t kv_conv[2], q_conv[2];  // head e's accumulator rows turned into tiles
+  alignas(1024) uint8_t o[2][kTile];  // the Q tiles, then the epilogue's staging, one per head
+  uint64_t full[kStages], empty[kStages];
+  uint64_t proj_done;  // every projection MMA of the item has completed
+  uint64_t conv[2];    // head e's Q, K, V and tail rows turned into tiles (128 arrivals)
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
   uint64_t qkv_free;   // every MMA reading the item's Q/K/V tiles has completed
   uint64_t tmem_free;  // every head thread's reads of the item's tensor memory are done
   uint64_t drained;
   // output projection (OUT)
   uint64_t o_full[kOSlots], o_empty[kOSlots];
-  uint64_t wl_full[kWoLate], wl_empty[kWoLate];
-  uint64_t we_full[kWoEarly], we_empty[kWoEarly];
+  uint64_t wo_full[kWoSlots], wo_empty[kWoSlots];
   uint64_t o_staged;   // this CTA's two merged tiles are in o[] (256 arrivals)
   uint64_t out_done;   // every out-projection MMA of the item has completed
   uint64_t o_ready[2][kMaxCluster - 1];
@@ -132,13 +133,14 @@ __device__ __forceinline__ int key_limit(const CrossArgs& a, int b) {
   }
   return kv_eff;
 }
-// Key tiles the attention takes (the second only when keys past 128 are visible).
+// Key tiles the attention takes (the tail only when keys past 128 are visible).
 __device__ __forceinline__ int key_tiles(int kv_eff) { return kv_eff > kRows ? 2 : 1; }
 
 template <bool OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     mha_cross_kernel(const __grid_constant__ CUtensorMap tm_xq,
                      const __grid_constant__ CUtensorMap tm_xkv,
+                     const __grid_constant__ CUtensorMap tm_xkv_tail,
                      const __grid_constant__ CUtensorMap tm_wq,
                      const __grid_constant__ CUtensorMap tm_wk,
                      const __grid_constant__ CUtensorMap tm_wv,
@@ -154,19 +156,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int stride = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kKvStages; ++s) {
-      mbar_init(&sm.kv_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
     }
-    for (int s = 0; s < kQStages; ++s) {
-      mbar_init(&sm.q_full[s], 1);
-      mbar_init(&sm.q_empty[s], 1);
-    }
-    mbar_init(&sm.kv_done, 1);
-    mbar_init(&sm.q_done, 1);
+    mbar_init(&sm.proj_done, 1);
     for (int e = 0; e < 2; ++e) {
-      mbar_init(&sm.kv_conv[e], 128);
-      mbar_init(&sm.q_conv[e], 128);
+      mbar_init(&sm.conv[e], 128);
       mbar_init(&sm.s_full[e], 1);
       mbar_init(&sm.s_free[e], 128);
       mbar_init(&sm.p_full[e], 128);
@@ -180,13 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sm.o_full[i], 1);
         mbar_init(&sm.o_empty[i], 1);
       }
-      for (int i = 0; i < kWoLate; ++i) {
-        mbar_init(&sm.wl_full[i], 1);
-        mbar_init(&sm.wl_empty[i], 1);
-      }
-      for (int i = 0; i < kWoEarly; ++i) {
-        mbar_init(&sm.we_full[i], 1);
-        mbar_init(&sm.we_empty[i], 1);
+      for (int i = 0; i < kWoSlots; ++i) {
+        mbar_init(&sm.wo_full[i], 1);
+        mbar_init(&sm.wo_empty[i], 1);
       }
       mbar_init(&sm.o_staged, 256);
       mbar_init(&sm.out_done, 1);
@@ -211,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_xq);
     tma_prefetch_desc(&tm_xkv);
+    tma_prefetch_desc(&tm_xkv_tail);
     tma_prefetch_desc(&tm_wq);
     tma_prefetch_desc(&tm_wk);
     tma_prefetch_desc(&tm_wv);
@@ -228,61 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_decrease<kCtrlRegs>();
     if (warp == 0 && lane == 0) {
       // ------------------------------------------------------------ producer
-      int ui = 0, wl_cnt = 0, o_cnt = 0, armed = -1;
-      int uq[kQStages] = {0, 0, 0, 0, 0, 0};  // loads issued into each Q stage so far
-      int ukv[kKvStages] = {0, 0, 0};         // ... and into each KV stage
-      int we_item[kWoEarly] = {-1, -1};  // item whose W_O chunk each early slot was last loaded for
+      int issued = 0, ui = 0, wo_cnt = 0, o_cnt = 0, armed = -1;
       bool ok = true;
-      bool waited = false;
-      auto first_load = [&]() {
-        if (!waited) {
-          griddep_wait();
-          waited = true;
-        }
-      };
-      // Q pass k-block kb of head pair h0/2 into Q stage kb % kQStages
-      auto load_q = [&](int b, int h0, int kb) -> bool {
-        const int st = kb % kQStages;
-        if (!mbar_wait(&sm.q_empty[st], (static_cast<uint32_t>(uq[st]) & 1u) ^ 1u, abort_flag))
-          return false;
-        mbar_arrive_expect_tx(&sm.q_full[st], kQStage);
-        first_load();
-        const int k0 = kb * 64;
-        uint8_t* dst = sm.ring + st * kQStage;
-        tma_load_3d(dst, &tm_xq, &sm.q_full[st], k0, 0, b);
-        for (int e = 0; e < 2; ++e)
-          tma_load_2d(dst + kTile + e * kWChunk, &tm_wq, &sm.q_full[st], (h0 + e) * kD, k0);
-        ++uq[st];
-        return true;
-      };
-      // KV pass k-block kb into KV stage (kb + 1) % kKvStages: the stage over
-      // the Q stages consumed first (stage 0 lies under the last Q k-blocks)
-      auto load_kv = [&](int b, int h0, int kb) -> bool {
-        const int st = (kb + 1) % kKvStages;
-        if (kb < kKvStages) {
-          // first use in this item: the two Q stages under it have been read
-          for (int qs = 2 * st; qs < 2 * st + 2; ++qs)
-            if (uq[qs] > 0 &&
-                !mbar_wait(&sm.q_empty[qs], static_cast<uint32_t>(uq[qs] - 1) & 1u, abort_flag))
-              return false;
-        }
-        if (!mbar_wait(&sm.kv_empty[st], (static_cast<uint32_t>(ukv[st]) & 1u) ^ 1u, abort_flag))
-          return false;
-        mbar_arrive_expect_tx(&sm.kv_full[st], kKvStage);
-        first_load();
-        const int k0 = kb * 64;
-        uint8_t* dst = sm.ring + st * kKvStage;
-        tma_load_3d(dst, &tm_xkv, &sm.kv_full[st], k0, 0, b);
-        tma_load_3d(dst + kTile, &tm_xkv, &sm.kv_full[st], k0, kRows, b);  // rows past n_k: zeros
-        uint8_t* w = dst + 2 * kTile;
-        for (int e = 0; e < 2; ++e) {
-          const int col = (h0 + e) * kD;
-          tma_load_2d(w + (2 * e) * kWChunk, &tm_wk, &sm.kv_full[st], col, k0);
-          tma_load_2d(w + (2 * e + 1) * kWChunk, &tm_wv, &sm.kv_full[st], col, k0);
-        }
-        ++ukv[st];
-        return true;
-      };
       for (int u = first; ok && u < args.num_units; u += stride, ++ui) {
         const int b = u / args.head_pairs;
         const int pair = u % args.head_pairs;
@@ -299,32 +239,57 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&sm.o_ready[ui & 1][i], 8);
           armed = ui;
         }
-        for (int kb = 0; ok && kb < args.kblocks; ++kb) ok = load_q(b, h0, kb);
-        for (int kb = 0; ok && kb < args.kblocks; ++kb) ok = load_kv(b, h0, kb);
+        for (int kb = 0; kb < args.kblocks; ++kb) {
+          const int s = issued % kStages;
+          ok = mbar_wait(&sm.empty[s], (static_cast<uint32_t>(issued / kStages) & 1u) ^ 1u,
+                         abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&sm.full[s], kStage);
+          if (issued == 0) griddep_wait();
+          const int k0 = kb * 64;
+          uint8_t* st = sm.ring + s * kStage;
+          tma_load_3d(st, &tm_xq, &sm.full[s], k0, 0, b);
+          tma_load_3d(st + kXkvOff, &tm_xkv, &sm.full[s], k0, 0, b);
+          tma_load_3d(st + kXtOff, &tm_xkv_tail, &sm.full[s], k0, kRows, b);  // rows past n_k: zeros
+          uint8_t* w = st + kWOff;
+          for (int e = 0; e < 2; ++e) {
+            const int col = (h0 + e) * kD;
+            tma_load_2d(w + wq_chunk(e) * kWChunk, &tm_wq, &sm.full[s], col, k0);
+            tma_load_2d(w + wk_chunk(e) * kWChunk, &tm_wk, &sm.full[s], col, k0);
+            tma_load_2d(w + (wk_chunk(e) + 1) * kWChunk, &tm_wv, &sm.full[s], col, k0);
+          }
+          ++issued;
+        }
         if constexpr (OUT) {
           if (!ok) break;
           const int C = args.head_pairs;
           // chunk j of the output projection: head 2 ((pair + j/2) mod C) + j%2
+          // (this CTA's own two heads first)
           auto head_of = [&](int j) { return 2 * ((pair + (j >> 1)) % C) + (j & 1); };
-          auto wo_box = [&](uint8_t* dst, uint64_t* bar, int j) {
-            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(args.n_slice) * 128u);
+          auto issue_wo = [&](int j) -> bool {  // W_O rows of head j, this CTA's columns
+            const int s = wo_cnt % kWoSlots;
+            if (!mbar_wait(&sm.wo_empty[s], (static_cast<uint32_t>(wo_cnt / kWoSlots) & 1u) ^ 1u,
+                           abort_flag))
+              return false;
+            uint8_t* dst = sm.ring + kWoBase + s * kSlot;
+            mbar_arrive_expect_tx(&sm.wo_full[s], static_cast<uint32_t>(args.n_slice) * 128u);
             for (int c = 0; c < args.n_slice; c += 64)
-              tma_load_2d(dst + c * 128, &tm_wo, bar, pair * args.n_slice + c, head_of(j) * kD);
+              tma_load_2d(dst + c * 128, &tm_wo, &sm.wo_full[s], pair * args.n_slice + c,
+                          head_of(j) * kD);
+            ++wo_cnt;
+            return true;
           };
           const uint32_t ph = static_cast<uint32_t>(ui) & 1u;
-          // the own heads' W_O chunks once the KV pass has read its stages
-          // (the early slots are the upper half of the last one)
-          ok = mbar_wait(&sm.kv_done, ph, abort_flag);
-          for (int j = 0; ok && j < kWoEarly && j < args.h; ++j) {
-            ok = mbar_wait(&sm.we_empty[j], ph ^ 1u, abort_flag);
-            if (!ok) break;
-            wo_box(sm.ring + kWoEarlyBase + j * kSlot, &sm.we_full[j], j);
-            we_item[j] = ui;
-          }
-          // the peers' merged tiles and the other W_O chunks into the K/V and
-          // Q tiles' place, once those are consumed
+          // W_O's first chunks while the attention runs: the stages are free
+          // once every projection MMA has completed
+          ok = mbar_wait(&sm.proj_done, ph, abort_flag);
+          int wj = 0;
+          for (; ok && wj < args.h && wj < kWoSlots; ++wj) ok = issue_wo(wj);
+          // then the peers' merged tiles, into the K/V tiles' place once those
+          // are consumed, each peer's as soon as it has stored them, with the
+          // rest of W_O as its slots free up
           ok = ok && mbar_wait(&sm.qkv_free, ph, abort_flag);
-          for (int j = kWoEarly; ok && j < args.h; ++j) {
+          for (int j = 2; ok && j < args.h; ++j) {
             if ((j & 1) == 0) {
               ok = mbar_wait_cluster(&sm.o_ready[ui & 1][(j >> 1) - 1],
                                      static_cast<uint32_t>(ui >> 1) & 1u, abort_flag);
@@ -338,37 +303,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&sm.o_full[os], kTile);
             tma_load_3d(sm.ring + os * kSlot, &tm_o, &sm.o_full[os], head_of(j) * kD, 0, b);
             ++o_cnt;
-            const int ws = wl_cnt % kWoLate;
-            ok = mbar_wait(&sm.wl_empty[ws], (static_cast<uint32_t>(wl_cnt / kWoLate) & 1u) ^ 1u,
-                           abort_flag);
-            if (!ok) break;
-            wo_box(sm.ring + kWoLateBase + ws * kSlot, &sm.wl_full[ws], j);
-            ++wl_cnt;
+            while (ok && wj <= j + kWoSlots - 2 && wj < args.h) ok = issue_wo(wj++);
           }
+          while (ok && wj < args.h) ok = issue_wo(wj++);
         }
       }
       if (!ok) {
         // wait (bounded) for this thread's copies still in flight
         volatile uint32_t never = 0;
-        for (int st = 0; st < kKvStages; ++st)
-          if (ukv[st] > 0)
-            mbar_wait(&sm.kv_full[st], static_cast<uint32_t>(ukv[st] - 1) & 1u, &never,
-                      kDrainLimitNs);
-        for (int st = 0; st < kQStages; ++st)
-          if (uq[st] > 0)
-            mbar_wait(&sm.q_full[st], static_cast<uint32_t>(uq[st] - 1) & 1u, &never, kDrainLimitNs);
+        for (int i = max(0, issued - kStages); i < issued; ++i)
+          mbar_wait(&sm.full[i % kStages], static_cast<uint32_t>(i / kStages) & 1u, &never,
+                    kDrainLimitNs);
         if constexpr (OUT) {
-          for (int i = max(0, wl_cnt - kWoLate); i < wl_cnt; ++i)
-            mbar_wait(&sm.wl_full[i % kWoLate], static_cast<uint32_t>(i / kWoLate) & 1u, &never,
+          for (int i = max(0, wo_cnt - kWoSlots); i < wo_cnt; ++i)
+            mbar_wait(&sm.wo_full[i % kWoSlots], static_cast<uint32_t>(i / kWoSlots) & 1u, &never,
                       kDrainLimitNs);
           for (int i = max(0, o_cnt - kOSlots); i < o_cnt; ++i)
             mbar_wait(&sm.o_full[i % kOSlots], static_cast<uint32_t>(i / kOSlots) & 1u, &never,
                       kDrainLimitNs);
-          // the early slots' last loads
-          for (int j = 0; j < kWoEarly; ++j)
-            if (we_item[j] >= 0)
-              mbar_wait(&sm.we_full[j], static_cast<uint32_t>(we_item[j]) & 1u, &never,
-                        kDrainLimitNs);
         }
       }
       if constexpr (OUT) {
@@ -376,32 +328,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (at once after a normal run; bounded when a peer gave up)
         volatile uint32_t never = 0;
         if (armed >= 0)
-          for (int s = 0; s < args.head_pairs - 1; ++s)
-            mbar_wait(&sm.o_ready[armed & 1][s], static_cast<uint32_t>(armed >> 1) & 1u, &never,
+          for (int i = 0; i < args.head_pairs - 1; ++i)
+            mbar_wait(&sm.o_ready[armed & 1][i], static_cast<uint32_t>(armed >> 1) & 1u, &never,
                       ok ? kDrainLimitNs : 3 * kWaitLimitNs);
       }
     } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t kIdescKV = idesc_bf16(kRows, 2 * kD, false, true);
       constexpr uint32_t kIdescQ = idesc_bf16(kRows, kD, false, true);
+      constexpr uint32_t kIdescKV = idesc_bf16(kRows, 2 * kD, false, true);
+      // tail: A = [W_K | W_V]^T (M = 128 features, MN-major), B = X_kv tail (N = 64 keys, K-major)
+      constexpr uint32_t kIdescT = idesc_bf16(kRows, kTail, true, false);
       constexpr uint32_t kIdescS = idesc_bf16(kRows, kRows, false, false);
-      constexpr uint32_t kIdescPV = idesc_bf16(kRows, kD, false, true);
+      constexpr uint32_t kIdescST = idesc_bf16(kRows, kTail, false, true);  // B = K_T, MN-major
+      constexpr uint32_t kIdescPV = idesc_bf16(kRows, kD, false, true);     // B = V, N-major
+      constexpr uint32_t kIdescPVT = idesc_bf16(kRows, kD, false, false);   // B = V_T, K-major
       constexpr uint32_t kIdescOut128 = idesc_bf16(kRows, 128, false, true);
       constexpr uint32_t kIdescOut64 = idesc_bf16(kRows, 64, false, true);
       const uint32_t ring0 = smem_u32(sm.ring);
-      // X: K-major, rows of 128 bytes; weights: N-major 64-column chunks 8 KB apart
-      const uint64_t dkv0 = sdesc_sw128(ring0, 16, 1024);
-      const uint64_t dkvw0 = sdesc_sw128(ring0 + 2 * kTile, kWChunk, 1024);
-      const uint64_t dq0 = sdesc_sw128(ring0, 16, 1024);
-      const uint64_t dqw0 = sdesc_sw128(ring0 + kTile, kWChunk, 1024);
-      // Q and K tiles K-major (head dimension contiguous); V tiles N-major
-      const uint64_t dt0 = sdesc_sw128(ring0, 16, 1024);
-      const uint64_t dv0 = sdesc_sw128(ring0, kTile, 1024);
-      constexpr uint32_t kTileStep = kTile >> 4;
+      // X: K-major, rows of 128 bytes; weights: 64-column chunks 8 KB apart
+      const uint64_t dx0 = sdesc_sw128(ring0, 16, 1024);
+      const uint64_t dw0 = sdesc_sw128(ring0 + kWOff, kWChunk, 1024);
+      constexpr uint32_t kStageStep = kStage >> 4;
       constexpr uint32_t kWStep = kWChunk >> 4;
-      int ui = 0, o_used = 0, wl_used = 0;
-      int uq[kQStages] = {0, 0, 0, 0, 0, 0};  // each stage's loads consumed so far
-      int ukv[kKvStages] = {0, 0, 0};
+      int consumed = 0, ui = 0, o_used = 0, wo_used = 0;
       int c[2] = {0, 0};  // S / P tiles per head so far (phase counters)
       bool ok = true;
       griddep_wait();  // the key lengths may come from the previous kernel
@@ -414,79 +363,75 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         tc_fence_after();
-        // ---- Q pass: Q_e = X_q W_Q (head e) into columns [64 e, 64 e + 64)
+        // ---- projections: Q_e = X_q W_Q, [K|V]_e = X_kv[0:128] [W_K | W_V],
+        // T_e = [W_K | W_V]^T X_kv[128:192]^T (head e)
         for (int kb = 0; ok && kb < args.kblocks; ++kb) {
-          const int st = kb % kQStages;
-          ok = mbar_wait(&sm.q_full[st], static_cast<uint32_t>(uq[st]) & 1u, abort_flag);
+          const int s = consumed % kStages;
+          ok = mbar_wait(&sm.full[s], static_cast<uint32_t>(consumed / kStages) & 1u, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t so = static_cast<uint32_t>(st * kQStage) >> 4;
-          const uint64_t dx = sdesc_advance(dq0, so);
-          const uint64_t dw = sdesc_advance(dqw0, so);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t acc_flag = (kb > 0 || kk > 0) ? 1u : 0u;
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-              mma_bf16_ss(tmem + q_col(e), sdesc_advance(dx, kk * (32 >> 4)),
-                          sdesc_advance(dw, e * kWStep + kk * (2048 >> 4)), kIdescQ, acc_flag);
-          }
-          mma_commit(&sm.q_empty[st]);
-          ++uq[st];
-        }
-        if (!ok) break;
-        mma_commit(&sm.q_done);
-        // ---- KV pass: KV_{e,m} = X_kv[rows of tile m] [W_K | W_V] (head e),
-        // into every column, once both heads have read their Q rows
-        ok = mbar_wait(&sm.q_conv[0], ph, abort_flag) && mbar_wait(&sm.q_conv[1], ph, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        for (int kb = 0; ok && kb < args.kblocks; ++kb) {
-          const int st = (kb + 1) % kKvStages;
-          ok = mbar_wait(&sm.kv_full[st], static_cast<uint32_t>(ukv[st]) & 1u, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t so = static_cast<uint32_t>(st * kKvStage) >> 4;
-          const uint64_t dx = sdesc_advance(dkv0, so);
-          const uint64_t dw = sdesc_advance(dkvw0, so);
+          const uint64_t dx = sdesc_advance(dx0, static_cast<uint32_t>(s) * kStageStep);
+          const uint64_t dw = sdesc_advance(dw0, static_cast<uint32_t>(s) * kStageStep);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t acc_flag = (kb > 0 || kk > 0) ? 1u : 0u;
             const uint32_t aoff = kk * (32 >> 4);    // 16 elements along d_model
             const uint32_t woff = kk * (2048 >> 4);  // 16 rows of the weight slice
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
-#pragma unroll
-              for (int m = 0; m < 2; ++m)
-                mma_bf16_ss(tmem + kv_col(e, m), sdesc_advance(dx, m * kTileStep + aoff),
-                            sdesc_advance(dw, 2 * e * kWStep + woff), kIdescKV, acc_flag);
+            for (int e = 0; e < 2; ++e) {
+              mma_bf16_ss(tmem + q_col(e), sdesc_advance(dx, aoff),
+                          sdesc_advance(dw, wq_chunk(e) * kWStep + woff), kIdescQ, acc_flag);
+              const uint64_t wkv = sdesc_advance(dw, wk_chunk(e) * kWStep + woff);
+              mma_bf16_ss(tmem + kv_col(e), sdesc_advance(dx, (kXkvOff >> 4) + aoff), wkv,
+                          kIdescKV, acc_flag);
+              mma_bf16_ss(tmem + t_col(e), wkv, sdesc_advance(dx, (kXtOff >> 4) + aoff), kIdescT,
+                          acc_flag);
+            }
           }
-          mma_commit(&sm.kv_empty[st]);
-          ++ukv[st];
+          mma_commit(&sm.empty[s]);
+          ++consumed;
         }
         if (!ok) break;
-        mma_commit(&sm.kv_done);
+        mma_commit(&sm.proj_done);
         // ---- attention, once every Q/K/V tile is written and every
         // accumulator under S, P and O has been read
-        ok = mbar_wait(&sm.kv_conv[0], ph, abort_flag) && mbar_wait(&sm.kv_conv[1], ph, abort_flag);
+        ok = mbar_wait(&sm.conv[0], ph, abort_flag) && mbar_wait(&sm.conv[1], ph, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const int nkt = key_tiles(key_limit(args, b));
         auto issue_s = [&](int e, int m) {
-          const uint64_t a = sdesc_sw128(smem_u32(sm.o[e]), 16, 1024);  // Q tile (K-major)
-          const uint64_t bk = sdesc_advance(dt0, static_cast<uint32_t>(kv_tile(e, m, 0)) * kTileStep);
+          const uint64_t a = sdesc_sw128(smem_u32(sm.o[e]), 16, 1024);  // Q tile, K-major
+          if (m == 0) {
+            const uint64_t bk = sdesc_sw128(ring0 + k0_off(e), 16, 1024);  // K tile, K-major
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            mma_bf16_ss(tmem + s_col(e), sdesc_advance(a, kk * 2), sdesc_advance(bk, kk * 2),
-                        kIdescS, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_bf16_ss(tmem + s_col(e), sdesc_advance(a, kk * 2), sdesc_advance(bk, kk * 2),
+                          kIdescS, kk > 0 ? 1u : 0u);
+          } else {
+            // K_T: rows = head dimension, 64 keys each (MN-major, N = keys)
+            const uint64_t bk = sdesc_sw128(ring0 + kt_off(e), kTailTile, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_bf16_ss(tmem + s_col(e), sdesc_advance(a, kk * 2),
+                          sdesc_advance(bk, kk * (2048 >> 4)), kIdescST, kk > 0 ? 1u : 0u);
+          }
           mma_commit(&sm.s_full[e]);
         };
         auto issue_pv = [&](int e, int m) {
-          const uint64_t bv = sdesc_advance(dv0, static_cast<uint32_t>(kv_tile(e, m, 1)) * kTileStep);
+          if (m == 0) {
+            const uint64_t bv = sdesc_sw128(ring0 + v0_off(e), kTile, 1024);  // V, N-major
 #pragma unroll
-          for (int kk = 0; kk < kRows / 16; ++kk)
-            mma_bf16_ts(tmem + o_col(e), tmem + p_col(e) + kk * 8,
-                        sdesc_advance(bv, kk * (2048 >> 4)), kIdescPV, (m > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kRows / 16; ++kk)
+              mma_bf16_ts(tmem + o_col(e), tmem + p_col(e) + kk * 8,
+                          sdesc_advance(bv, kk * (2048 >> 4)), kIdescPV, kk > 0 ? 1u : 0u);
+          } else {
+            // V_T: rows = head dimension, 64 keys each (K-major, K = keys)
+            const uint64_t bv = sdesc_sw128(ring0 + vt_off(e), 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kTail / 16; ++kk)
+              mma_bf16_ts(tmem + o_col(e), tmem + p_col(e) + kk * 8, sdesc_advance(bv, kk * 2),
+                          kIdescPVT, 1u);
+          }
           mma_commit(&sm.pv_done[e]);
         };
         for (int e = 0; e < 2; ++e) issue_s(e, 0);
@@ -498,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok && nkt == 2) {
           for (int e = 0; ok && e < 2; ++e) {
-            // S_e of the second key tile overwrites the first, once it is read
+            // S_e of the tail overwrites the first key tile's, once it is read
             ok = mbar_wait(&sm.s_free[e], static_cast<uint32_t>(c[e]) & 1u, abort_flag);
             if (!ok) break;
             tc_fence_after();
@@ -523,37 +468,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t idesc_out = args.n_slice == 128 ? kIdescOut128 : kIdescOut64;
           for (int j = 0; ok && j < args.h; ++j) {
-            uint64_t a, bw;
+            uint64_t a;
             int os = -1;
-            if (j < kWoEarly) {  // this CTA's own heads, still in the epilogue's staging tiles
+            if (j < 2) {  // this CTA's own heads, still in the epilogue's staging tiles
               a = sdesc_sw128(smem_u32(sm.o[j]), 16, 1024);
-              ok = mbar_wait(&sm.we_full[j], ph, abort_flag);
-              bw = sdesc_sw128(ring0 + kWoEarlyBase + j * kSlot, kWChunk, 1024);
             } else {
               os = o_used % kOSlots;
               ok = mbar_wait(&sm.o_full[os], static_cast<uint32_t>(o_used / kOSlots) & 1u,
                              abort_flag);
               ++o_used;
               a = sdesc_sw128(ring0 + os * kSlot, 16, 1024);
-              const int ws = wl_used % kWoLate;
-              ok = ok && mbar_wait(&sm.wl_full[ws], static_cast<uint32_t>(wl_used / kWoLate) & 1u,
-                                   abort_flag);
-              ++wl_used;
-              bw = sdesc_sw128(ring0 + kWoLateBase + ws * kSlot, kWChunk, 1024);
             }
+            const int ws = wo_used % kWoSlots;
+            ok = ok && mbar_wait(&sm.wo_full[ws], static_cast<uint32_t>(wo_used / kWoSlots) & 1u,
+                                 abort_flag);
+            ++wo_used;
             if (!ok) break;
             tc_fence_after();
             // W_O chunk: 64 rows x n_slice columns as 64-column blocks 8 KB apart
+            const uint64_t bw = sdesc_sw128(ring0 + kWoBase + ws * kSlot, kWChunk, 1024);
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
               mma_bf16_ss(tmem, sdesc_advance(a, kk * 2), sdesc_advance(bw, kk * (2048 >> 4)),
                           idesc_out, (j > 0 || kk > 0) ? 1u : 0u);
-            if (j < kWoEarly) {
-              mma_commit(&sm.we_empty[j]);
-            } else {
-              mma_commit(&sm.wl_empty[(wl_used - 1) % kWoLate]);
-              mma_commit(&sm.o_empty[os]);
-            }
+            mma_commit(&sm.wo_empty[ws]);
+            if (os >= 0) mma_commit(&sm.o_empty[os]);
           }
           if (!ok) break;
           mma_commit(&sm.out_done);
@@ -569,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_increase<kHeadRegs>();
     const int e = (warp - 4) >> 2;      // head of the pair
     const int quarter = warp & 3;       // TMEM lane quarter of this warp
-    const int r = quarter * 32 + static_cast<int>(lane);  // row: query (and key) index in a tile
+    const int r = quarter * 32 + static_cast<int>(lane);  // row: query (and key, feature) index
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t taddr = tmem + lane_base;
     const bool leader = (quarter == 0 && lane == 0);  // issues the TMA stores
@@ -580,10 +519,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     griddep_wait();  // the key lengths may come from the previous kernel
     int ui = 0;
-    // accumulator row (64 fp32 columns from `col`) -> bf16 row r of a
-    // 128-byte-swizzled tile
-    auto convert = [&](uint32_t col, uint8_t* tile) {
-      uint8_t* row = tile + r * 128;
+    // 64 fp32 accumulator columns from `col` -> one bf16 row of 128 bytes at
+    // `row` (row index `ri` within a 128-byte-swizzled tile)
+    auto convert = [&](uint32_t col, uint8_t* row, int ri) {
       uint32_t v[64];
       tmem_ld32(taddr + col, *reinterpret_cast<uint32_t(*)[32]>(v));
       tmem_ld32(taddr + col + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
@@ -591,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 8; ++j) {  // 16-byte chunk j of the 128-byte row
         const uint32_t* x = v + 8 * j;
-        st_shared_v4(smem_u32(row + ((j ^ (r & 7)) << 4)),
+        st_shared_v4(smem_u32(row + ((j ^ (ri & 7)) << 4)),
                      pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
                      pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
                      pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
@@ -607,33 +545,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ph = static_cast<uint32_t>(ui) & 1u;
       // A failed wait is carried to the warpgroup's barrier below, where all
       // four warps stop together (none is left waiting at it).
-      bool okw = __all_sync(0xffffffffu, mbar_wait(&sm.q_done, ph, abort_flag));
-      // ---- (1) this row of Q -> bf16 tile in the staging buffer o[e], once
-      // the previous item's stores from it have read it
+      bool okw = __all_sync(0xffffffffu, mbar_wait(&sm.proj_done, ph, abort_flag));
+      // ---- (1) this row of Q, K, V and of the tail -> bf16 tiles, once the
+      // previous item's stores from the staging buffer have read it
       if (leader) bulk_wait_group_read<0>();
       okw = e == 0 ? named_bar_and<1>(128, okw) : named_bar_and<2>(128, okw);
       if (okw) {
         tc_fence_after();
-        convert(q_col(e), sm.o[e]);
-        fence_proxy_async_smem();  // the tile is read by the tensor cores
-        tc_fence_before();         // and the KV pass overwrites the accumulator just read
-        mbar_arrive(&sm.q_conv[e]);
+        convert(q_col(e), sm.o[e] + r * 128, r);
+        convert(kv_col(e), ring + k0_off(e) + r * 128, r);
+        convert(kv_col(e) + kD, ring + v0_off(e) + r * 128, r);
+        // tail feature r: K_T row r (r < 64), else V_T row r - 64; 64 keys
+        const int fr = r & 63;
+        convert(t_col(e), ring + (r < 64 ? kt_off(e) : vt_off(e)) + fr * 128, fr);
+        fence_proxy_async_smem();  // the tiles are read by the tensor cores
+        tc_fence_before();         // and S, P and O overwrite the accumulators just read
+        mbar_arrive(&sm.conv[e]);
       }
-      // ---- (2) this row of K and V for both key tiles -> bf16 tiles
-      okw = okw && __all_sync(0xffffffffu, mbar_wait(&sm.kv_done, ph, abort_flag));
-      if (okw) {
-        tc_fence_after();
-        for (int m = 0; m < 2; ++m) {
-          convert(kv_col(e, m), ring + kv_tile(e, m, 0) * kTile);
-          convert(kv_col(e, m) + kD, ring + kv_tile(e, m, 1) * kTile);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();         // S, P and O overwrite the accumulators just read
-        mbar_arrive(&sm.kv_conv[e]);
-      }
-      // ---- (3) online softmax over the key tiles; P goes where head 1's
-      // first K|V accumulator was (read once kv_conv[1] has completed)
-      okw = okw && __all_sync(0xffffffffu, mbar_wait(&sm.kv_conv[1], ph, abort_flag));
+      // ---- (2) online softmax over the first key tile and the tail
       float m_used = -INFINITY;
       float l = 0.f;
       for (int m = 0; okw && m < nkt; ++m, ++c) {
@@ -651,8 +580,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(&sm.s_free[e]);  // the next key tile's S may overwrite it
-        const int lim = kv_eff - m * kRows;  // keys >= lim of this tile are masked
+        mbar_arrive(&sm.s_free[e]);  // the tail's S may overwrite it
+        // keys >= lim of this tile are masked (the tail's S has 64 columns:
+        // the rest of the row is the first tile's and always masked)
+        const int lim = m == 0 ? kv_eff : min(kv_eff - kRows, kTail);
         if (lim < kRows) {
 #pragma unroll
           for (int x = 0; x < kRows; ++x)
@@ -690,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         f2_unpack(fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3])), r0, r1);
         const float rowsum = r0 + r1;
         if (m > 0) {
-          // P V of the previous key tile has finished: O is stable, P is free
+          // P V of the first key tile has finished: O is stable, P is free
           okw = __all_sync(0xffffffffu, mbar_wait(&sm.pv_done[e], static_cast<uint32_t>(c - 1) & 1u,
                                                   abort_flag));
           if (!okw) break;
@@ -721,10 +652,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&sm.p_full[e]);
       }
-      // ---- (4) epilogue: O / l -> bf16 -> staging -> TMA store
+      // ---- (3) epilogue: O / l -> bf16 -> staging -> TMA store (the Q tile
+      // there has been read: its last S MMA completed before the last s_full)
       okw = okw && __all_sync(0xffffffffu, mbar_wait(&sm.pv_done[e], static_cast<uint32_t>(c - 1) & 1u,
                                                      abort_flag));
-      if (leader) bulk_wait_group_read<0>();  // the staging tile's previous store has read it
       ok = e == 0 ? named_bar_and<1>(128, okw) : named_bar_and<2>(128, okw);
       if (!ok) break;
       tc_fence_after();
@@ -772,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if constexpr (OUT) {
-        // ---- (5) out[:, N pair + 64 e : + 64] (fp32 in TMEM) -> bf16 ->
+        // ---- (4) out[:, N pair + 64 e : + 64] (fp32 in TMEM) -> bf16 ->
         // staging -> TMA store
         okw = __all_sync(0xffffffffu, mbar_wait(&sm.out_done, ph, abort_flag));
         if (leader) bulk_wait_group_read<0>();  // the merged tile's store has read the staging tile
@@ -917,8 +848,8 @@ cudaError_t launch_cross(const MhaFusedProblem& p, cudaStream_t stream) {
     grid = (p.B < max_clusters ? p.B : max_clusters) * C;
   }
   cfg.gridDim = dim3(grid);
-  return cudaLaunchKernelEx(&cfg, kernel, p.tm_xq, p.tm_xkv, p.tm_wq, p.tm_wk, p.tm_wv, p.tm_o,
-                            p.tm_wo, p.tm_out, a);
+  return cudaLaunchKernelEx(&cfg, kernel, p.tm_xq, p.tm_xkv, p.tm_xkv_tail, p.tm_wq, p.tm_wk,
+                            p.tm_wv, p.tm_o, p.tm_wo, p.tm_out, a);
 }
 
 }  // namespace
@@ -933,7 +864,7 @@ int mha_cross_out_clusters(int h) {
 
 cudaError_t launch_mha_cross(const MhaFusedProblem& p, cudaStream_t stream) {
   if (p.self || p.h % 2 != 0 || p.d_model % 64 != 0 || p.d_model <= 0 || p.n_q < 1 ||
-      p.n_q > kRows || p.n_k <= kRows || p.n_k > 2 * kRows)
+      p.n_q > kRows || p.n_k <= kRows || p.n_k > kRows + kTail)
     return cudaErrorInvalidValue;
   if (p.out) {
     const int C = p.h / 2;

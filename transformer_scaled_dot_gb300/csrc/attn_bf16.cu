@@ -748,8 +748,9 @@ cudaError_t launch_variant(const AttnProblem& p, const CUtensorMap& tm_q, const 
   // round, those blocks run as single tiles (about half an item's time each),
   // so the last round ends sooner (measured: B=8 h=16 n=1024 d=64 823 -> 849
   // TFLOP/s; d=128 B=2 n=4096 1100 -> 1142). Non-causal instances only:
-  // causal items are already taken longest first, and the causal instance
-  // measured slower with the split's code compiled in even when unused.
+  // causal items are already taken longest first, and the causal and window
+  // instances measured slower with the split's code compiled in (window
+  // n=16384 +-256: 589 -> 545 TFLOP/s, its 4096 items leave no tail worth it).
   a.tail_start = 0x7fffffff;
   if (TS && NQT == 2 && SL == 1 && !(p.mask_kind & kMaskCausal)) {
     const long long G = items < num_sms() ? items : num_sms();
@@ -797,12 +798,12 @@ cudaError_t launch_attn_bf16(const AttnProblem& p, const CUtensorMap& tm_q,
       // one copy of the score load (no unmasked twin): the two window edges
       // put masking in most of a short item's tiles, and the smaller loop
       // measured faster (n = 16384, keys within +-256: 534 -> 588 TFLOP/s)
-      return launch_variant<64, 2, 4, 4, 2, true, 1, false, true, true>(p, tm_q, tm_k, tm_v, tm_o,
-                                                                        stream);
+      return launch_variant<64, 2, 4, 4, 2, true, 1, false, true>(p, tm_q, tm_k, tm_v, tm_o,
+                                                                  stream);
     }
     if (p.d == 128) {
-      return pair ? launch_variant<128, 2, 2, 2, 1, false, 1, false, true, true>(p, tm_q, tm_k,
-                                                                                tm_v, tm_o, stream)
+      return pair ? launch_variant<128, 2, 2, 2, 1, false, 1, false, true>(p, tm_q, tm_k, tm_v,
+                                                                          tm_o, stream)
                   : launch_variant<128, 1, 2, 2, 2, true, 1, false, true>(p, tm_q, tm_k, tm_v,
                                                                          tm_o, stream);
     }

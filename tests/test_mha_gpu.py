@@ -308,3 +308,44 @@ def test_mha_cross_attention_two_key_tiles_without_output_projection(tsd):
     heads = oracle.attention(q, k, v, MASK_KEY_PADDING, kv_lens=m.kv_lens)
     ref = heads.transpose(0, 2, 1, 3).reshape(B, n_q, h * 64)
     assert_bf16_close(to_host_f64(concat), ref, "cross concat heads")
+
+
+def test_mha_cross_attention_one_launch_matches_two_launch_path_and_repeats(tsd):
+    """The cross-attention kernel with W_O (one launch) against the same
+    kernel up to the merged heads followed by the W_O GEMM: the merged heads
+    are identical, out differs only by fp32 summation order; a second call is
+    bit-identical to the first, and the bytes around `out` stay untouched."""
+    import torch
+    B, n_q, n_k, dm, h = 32, 128, 160, 512, 8
+    m = synthetic.mha_inputs(3600, B, n_q, n_k, dm, h, 64, 64, MASK_KEY_PADDING, (80, n_k),
+                             self_attention=False)
+    x_q, x_kv = to_dev_bf16(m.x_q), to_dev_bf16(m.x_kv)
+    w = [to_dev_bf16(t) for t in (m.w_q, m.w_k, m.w_v, m.w_o)]
+    lens = to_dev_i32(m.kv_lens)
+    wsb = tsd.mha_workspace_bytes(B, n_q, n_k, h, 64, 64)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    guard = 4096
+    buf = torch.full((2 * guard + B * n_q * dm,), 12345, dtype=torch.int16, device="cuda")
+    out = buf[guard:guard + B * n_q * dm].view(torch.bfloat16).view(B, n_q, dm)
+    runs = []
+    for _ in range(2):
+        tsd.mha_forward(x_q, x_kv, *w, out, B, n_q, n_k, dm, h, 64, 64, m.mask_kind, lens, 0.0,
+                        ws, wsb)
+        torch.cuda.synchronize()
+        runs.append(out.clone())
+    assert tsd.attn_get_device_status() == tsd.ATTN_OK
+    assert torch.equal(runs[0], runs[1])
+    assert torch.all(buf[:guard] == 12345) and torch.all(buf[-guard:] == 12345)
+    off = wsb - B * n_q * h * 64 * 2
+    merged = ws[off:].view(torch.bfloat16).view(B, n_q, h * 64).clone()
+    concat = torch.empty((B, n_q, h * 64), dtype=torch.bfloat16, device="cuda")
+    out2 = torch.empty((B, n_q, dm), dtype=torch.bfloat16, device="cuda")
+    ws2 = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    tsd.mha_concat_heads(x_q, x_kv, *w[:3], concat, B, n_q, n_k, dm, h, 64, 64, m.mask_kind, lens,
+                         0.0, ws2, wsb)
+    tsd.mha_project_out(concat, w[3], out2, B, n_q, dm, h, 64)
+    torch.cuda.synchronize()
+    assert tsd.attn_get_device_status() == tsd.ATTN_OK
+    assert torch.equal(merged, concat)
+    got, two = to_host_f64(runs[0]), to_host_f64(out2)
+    assert np.all(np.abs(got - two) <= np.maximum(np.abs(got), np.abs(two)) * 2.0 ** -7 + 1e-6)

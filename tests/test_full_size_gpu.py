@@ -72,6 +72,7 @@ def test_transformer_big_self_attention_every_row(tsd, causal):
     (2, 8192, 128, False),
     (2, 8192, 128, True),
     (1, 16384, 64, True),
+    (1, 8200, 64, True),     # causal past 8192 rows (the unmasked-twin instance), ragged tail
     (4, 16384, 64, False),   # the largest d = 64 point of the sweep
     (1, 2048, 128, False),
 ])

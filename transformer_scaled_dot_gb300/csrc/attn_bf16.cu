@@ -819,10 +819,15 @@ cudaError_t launch_attn_bf16(const AttnProblem& p, const CUtensorMap& tm_q,
   }
   if (p.d == 64) {
     if (!pair) return launch_variant<64, 1, 2, 2, 1, true, 2>(p, tm_q, tm_k, tm_v, tm_o, stream);
-    return causal
-               ? launch_variant<64, 2, 4, 4, 2, true, 1, false>(p, tm_q, tm_k, tm_v, tm_o, stream)
-               : launch_variant<64, 2, 4, 4, 2, true, 1, true, false, true>(p, tm_q, tm_k, tm_v, tm_o,
-                                                                         stream);
+    if (!causal)
+      return launch_variant<64, 2, 4, 4, 2, true, 1, true, false, true>(p, tm_q, tm_k, tm_v, tm_o,
+                                                                       stream);
+    // causal: the unmasked score-load twin pays once the items are long
+    // (measured, TFLOP/s without / with it: n = 1024 601 / 575, 2048 825 /
+    // 801, 4096 1060 / 1056, 8192 1146 / 1166, 16384 1195 / 1233)
+    return p.n_q >= 8192
+               ? launch_variant<64, 2, 4, 4, 2, true, 1, true>(p, tm_q, tm_k, tm_v, tm_o, stream)
+               : launch_variant<64, 2, 4, 4, 2, true, 1, false>(p, tm_q, tm_k, tm_v, tm_o, stream);
   }
   if (p.d == 128) {
     if (pair && !causal)

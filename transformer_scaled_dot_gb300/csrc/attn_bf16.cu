@@ -731,7 +731,8 @@ cudaError_t launch_variant(const AttnProblem& p, const CUtensorMap& tm_q, const 
   const size_t smem_bytes = SL * sizeof(Smem) + 1024;  // + alignment slack
   auto kernel = attn_fwd_bf16_kernel<D, NQT, NK, NV, QB, STO, SL, MS, WIN, TS>;
   static unsigned long long configured = 0;
-  cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured);
+  cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured,
+                                Shape::kRegSplit ? static_cast<int>(Shape::kLaunchRegs) : 0);
   if (e != cudaSuccess) return e;
   AttnArgs a;
   a.B = p.B;

@@ -89,13 +89,24 @@ cudaError_t launch_gemm_bf16(const GemmProblem& p, cudaStream_t stream);
 // attributes belong to the device's context, and setting them on every
 // launch costs host time comparable to a short kernel. `done` holds one bit
 // per device ordinal (ordinals past 63 set them every time).
+// A kernel whose warpgroups move registers between them (setmaxnreg) passes
+// the per-thread count its split assumes at launch (`split_regs`): were the
+// kernel built with fewer, an increase could wait forever for registers no
+// one releases, so the launch is refused instead.
 template <typename Kernel>
-inline cudaError_t set_smem_once(Kernel kernel, int bytes, unsigned long long* done) {
+inline cudaError_t set_smem_once(Kernel kernel, int bytes, unsigned long long* done,
+                                 int split_regs = 0) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
   if (bit != 0ull && (__atomic_load_n(done, __ATOMIC_ACQUIRE) & bit) != 0ull) return cudaSuccess;
+  if (split_regs > 0) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < split_regs) return cudaErrorInvalidConfiguration;
+  }
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,

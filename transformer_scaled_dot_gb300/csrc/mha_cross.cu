@@ -782,7 +782,9 @@ int cross_out_max_clusters(int C) {
   const size_t smem_bytes = sizeof(CrossSmem) + 1024;
   auto kernel = mha_cross_kernel<true>;
   static unsigned long long configured = 0;
-  if (set_smem_once(kernel, static_cast<int>(smem_bytes), &configured) != cudaSuccess) return 0;
+  if (set_smem_once(kernel, static_cast<int>(smem_bytes), &configured,
+                    static_cast<int>(kLaunchRegs)) != cudaSuccess)
+    return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms() / C * C);
   cfg.blockDim = dim3(kThreads);
@@ -808,7 +810,8 @@ cudaError_t launch_cross(const MhaFusedProblem& p, cudaStream_t stream) {
   const size_t smem_bytes = sizeof(CrossSmem) + 1024;  // + alignment slack
   auto kernel = mha_cross_kernel<OUT>;
   static unsigned long long configured = 0;
-  cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured);
+  cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured,
+                                static_cast<int>(kLaunchRegs));
   if (e != cudaSuccess) return e;
   CrossArgs a;
   a.h = p.h;

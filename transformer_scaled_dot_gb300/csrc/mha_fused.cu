@@ -698,7 +698,9 @@ int fused_out_max_clusters(int C) {
   const size_t smem_bytes = sizeof(Smem) + 1024;
   auto kernel = mha_fused_kernel<SELF, true>;
   static unsigned long long configured = 0;
-  if (set_smem_once(kernel, static_cast<int>(smem_bytes), &configured) != cudaSuccess) return 0;
+  if (set_smem_once(kernel, static_cast<int>(smem_bytes), &configured,
+                    static_cast<int>(kLaunchRegs)) != cudaSuccess)
+    return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms() / C * C);
   cfg.blockDim = dim3(kThreads);
@@ -725,7 +727,8 @@ cudaError_t launch_fused(const MhaFusedProblem& p, cudaStream_t stream) {
   const size_t smem_bytes = sizeof(Smem) + 1024;  // + alignment slack
   auto kernel = mha_fused_kernel<SELF, OUT>;
   static unsigned long long configured = 0;
-  cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured);
+  cudaError_t e = set_smem_once(kernel, static_cast<int>(smem_bytes), &configured,
+                                static_cast<int>(kLaunchRegs));
   if (e != cudaSuccess) return e;
   FusedArgs a;
   a.h = p.h;

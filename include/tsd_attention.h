@@ -27,7 +27,11 @@
  *    no allowed key (kv_len = 0) produces an all-zero output row.
  *  - Kernels never trap or assert. Every wait inside a kernel is bounded;
  *    a kernel that gives up sets a device error word and exits cleanly,
- *    which attn_get_device_status() reports.
+ *    which attn_get_device_status() reports. A kernel whose warp groups
+ *    trade registers is not launched when the build gave it fewer registers
+ *    per thread than that trade assumes (ATTN_ERR_CUDA,
+ *    cudaErrorInvalidConfiguration): it could otherwise wait for registers
+ *    that are never released.
  */
 #ifndef TSD_ATTENTION_H
 #define TSD_ATTENTION_H

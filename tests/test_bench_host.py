@@ -63,3 +63,15 @@ def test_reference_arm_reports_the_oracle(monkeypatch):
 def test_profiled_traffic_requires_matching_source(tmp_path, monkeypatch):
     import bench
     assert bench.profiled_traffic("attn_fwd_bf16", "no_such_workload") is None
+
+
+def test_overridden_shape_takes_no_committed_traffic():
+    """A committed ncu summary describes its workload's own launch: --n, --d,
+    --B, --h or --causal that change the shape leave `traffic` null."""
+    import bench
+    assert not bench.config_overridden(bench.parse_args([]))
+    assert not bench.config_overridden(bench.parse_args(["--n", "4096", "--causal", "0"]))
+    for extra in (["--causal", "1"], ["--n", "8192"], ["--d", "128"], ["--B", "2"], ["--h", "8"]):
+        assert bench.config_overridden(bench.parse_args(extra)), extra
+    assert bench.config_overridden(bench.parse_args(["--workload", "big_self", "--causal", "1"]))
+    assert not bench.config_overridden(bench.parse_args(["--workload", "big_self_causal"]))

@@ -54,6 +54,7 @@ constexpr int kStages = 6;
 constexpr int kStagesLN = 6;      // LayerNorm epilogue (no staging tile: rows stored directly)
 constexpr int kMaxLnCluster = 8;  // N <= 8 x 128
 constexpr int kThreads = 192;
+constexpr bool kPrefetchL2 = true;  // a share of the first tiles' weights into L2 before the wait
 constexpr int kAccCols = 128;
 // LayerNorm epilogue: one more 128-column region after the accumulators
 // holds the tile's fp32 residual, streamed in while the main loop runs
@@ -211,6 +212,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
     if (lane == 0) {
       int issued = 0;
       bool ok = true;
+      if (kPrefetchL2 && first < p.total_tiles) {
+        // While the previous kernel finishes, this CTA prefetches into L2 its
+        // share of its first tile's B operand (the weights, from DRAM): the
+        // CTAs whose first tiles share a column block split its K blocks by
+        // their row-tile index. A, usually the previous kernel's output, is
+        // left to the loads after the wait.
+        const TileCoord c = coord(first);
+        const int tm = c.g->tiles_m > 0 ? c.g->tiles_m : 1;
+        for (int kb = c.m0 / kBM; kb < kblocks; kb += tm) {
+#pragma unroll
+          for (int ch = 0; ch < BN / 64; ++ch)
+            tma_prefetch_l2_2d(&c.g->tm_b, c.n0 + 64 * ch, kb * kBK);
+        }
+      }
       for (int ct = first; ok && ct < p.total_tiles; ct += stride) {
         const TileCoord c = coord(ct);
         for (int kb = 0; kb < kblocks; ++kb) {

@@ -63,6 +63,7 @@ constexpr uint32_t kHeadRegs = (kLaunchRegs * kThreads - kCtrlRegs * 128) / 256 
 static_assert(kCtrlRegs * 128 + kHeadRegs * 256 <= kLaunchRegs * kThreads, "register split");
 constexpr unsigned long long kDrainLimitNs = 100ull * 1000ull * 1000ull;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr bool kPrefetchL2 = true;  // a share of the first wave's operands into L2 before the wait
 
 // one stage: X_q | X_kv rows [0,128) | X_kv rows [128,192) | W_Q0 W_Q1 | W_K0 W_V0 | W_K1 W_V1
 constexpr int kXkvOff = kTile;
@@ -223,6 +224,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------------ producer
       int issued = 0, ui = 0, wo_cnt = 0, o_cnt = 0, armed = -1;
       bool ok = true;
+      if (kPrefetchL2 && first < args.num_units) {
+        // While the previous kernel finishes, this CTA prefetches into L2 its
+        // share of the data the first wave of CTAs reads: 1/C of its batch
+        // entry's X_q and X_kv rows (the C CTAs of a batch entry split them),
+        // and, CTA b of each head pair, one 64-row block of the pair's W_Q,
+        // W_K, W_V slices and of its W_O columns; the loads after the wait
+        // find them there. A prefetch only reads into L2, the point of
+        // coherence.
+        const int C = args.head_pairs;
+        const int b = first / C;
+        const int pair = first % C;
+        for (int kb = pair; kb < args.kblocks; kb += C) {
+          tma_prefetch_l2_3d(&tm_xq, kb * 64, 0, b);
+          tma_prefetch_l2_3d(&tm_xkv, kb * 64, 0, b);
+          tma_prefetch_l2_3d(&tm_xkv_tail, kb * 64, kRows, b);
+        }
+        if (b < args.kblocks) {
+          for (int e = 0; e < 2; ++e) {
+            const int col = (2 * pair + e) * kD;
+            tma_prefetch_l2_2d(&tm_wq, col, b * 64);
+            tma_prefetch_l2_2d(&tm_wk, col, b * 64);
+            tma_prefetch_l2_2d(&tm_wv, col, b * 64);
+          }
+        }
+        if constexpr (OUT) {
+          if (b < 2 * C)
+            for (int c = 0; c < args.n_slice; c += 64)
+              tma_prefetch_l2_2d(&tm_wo, pair * args.n_slice + c, b * kD);
+        }
+      }
       for (int u = first; ok && u < args.num_units; u += stride, ++ui) {
         const int b = u / args.head_pairs;
         const int pair = u % args.head_pairs;
